@@ -1,0 +1,245 @@
+/*
+ * KDA oracle: a plain, sequential, double-precision CPU statement of the
+ * Kimi Delta Attention forward and of its input prologue.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path and must never be used as a
+ * fallback for it.
+ *
+ * What is computed (per sequence n and head h, tokens t in order):
+ *
+ *     S <- Diag(exp(g_t)) S                      channel-wise decay: row c of S
+ *                                                 (key channel c) is scaled by
+ *                                                 exp(g_t[c])
+ *     S <- S - beta_t k_t (k_t^T S) + beta_t k_t v_t^T      delta-rule update
+ *     o_t = scale * S^T q_t                      read-out from the updated state
+ *
+ * with S a K x V matrix, S_0 the caller's initial state (or zero) and the final
+ * S returned as the final state.  Sources:
+ *   - "ISEEKYAN/k3" README (page 1): KDA is a recurrence computed by the K3
+ *     primitive, with a bounded CPU recurrence as the correctness path.
+ *   - "NeMo AutoModel draft_kimi_k3" (page 2), module description: positional
+ *     information reaches attention through the interleaved KDA recurrence.
+ *   - "kimi-k3-mlx" review (page 3), section "The A_log shape mismatch ...":
+ *     the gate g has shape (B,T,96,128) and A_log has 128 entries broadcast on
+ *     the trailing head_dim axis, so the decay is per channel and shared by all
+ *     heads; dt_bias has 96*128 entries.
+ *   - "kimi-k3-mlx" review, section "Attention is 93 layers ...": short
+ *     convolution with kernel size 4 on q, k and v, low-rank forget gate,
+ *     gate_lower_bound = -5.0, 96 heads of head_dim 128.
+ * The update order (decay, then delta rule, then read-out) and the recurrence
+ * itself are the project's statement of the method; the pages name KDA but do
+ * not print its equations.
+ *
+ * Layouts (all row-major, element counts not bytes):
+ *   q, k, g   [Ttot, H, K]      v, o  [Ttot, H, V]      beta [Ttot, H]
+ *   states    [N, H, K, V]      cu_seqlens [N + 1], cu_seqlens[0] = 0,
+ *                               cu_seqlens[N] = Ttot, non-decreasing.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Recurrence                                                                 */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *s0;
+    const int64_t *cu;
+    int64_t N, H, K, V;
+    double scale;
+    double *o, *sT;
+    int tid, nthreads;
+    int status;
+} rec_job;
+
+/* One (sequence, head) chain, token by token. */
+static void run_chain(const rec_job *j, int64_t n, int64_t h, double *S, double *kS)
+{
+    const int64_t H = j->H, K = j->K, V = j->V;
+    if (j->s0)
+        memcpy(S, j->s0 + ((n * H + h) * K) * V, sizeof(double) * K * V);
+    else
+        memset(S, 0, sizeof(double) * K * V);
+
+    for (int64_t t = j->cu[n]; t < j->cu[n + 1]; ++t) {
+        const double *qt = j->q + (t * H + h) * K;
+        const double *kt = j->k + (t * H + h) * K;
+        const double *gt = j->g + (t * H + h) * K;
+        const double *vt = j->v + (t * H + h) * V;
+        const double bt = j->beta[t * H + h];
+
+        /* S <- Diag(exp(g_t)) S : key channel c scales row c. */
+        for (int64_t c = 0; c < K; ++c) {
+            const double a = exp(gt[c]);
+            for (int64_t x = 0; x < V; ++x) S[c * V + x] *= a;
+        }
+        /* kS = k_t^T S  (a row vector of length V). */
+        for (int64_t x = 0; x < V; ++x) kS[x] = 0.0;
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t x = 0; x < V; ++x) kS[x] += kt[c] * S[c * V + x];
+        /* S <- S - beta k (k^T S) + beta k v^T. */
+        for (int64_t c = 0; c < K; ++c)
+            for (int64_t x = 0; x < V; ++x)
+                S[c * V + x] = S[c * V + x] - bt * kt[c] * kS[x] + bt * kt[c] * vt[x];
+        /* o_t = scale * S^T q_t. */
+        double *ot = j->o + (t * H + h) * V;
+        for (int64_t x = 0; x < V; ++x) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < K; ++c) acc += S[c * V + x] * qt[c];
+            ot[x] = j->scale * acc;
+        }
+    }
+    if (j->sT) memcpy(j->sT + ((n * H + h) * K) * V, S, sizeof(double) * K * V);
+}
+
+static void *rec_worker(void *arg)
+{
+    rec_job *j = (rec_job *)arg;
+    double *S = (double *)malloc(sizeof(double) * j->K * j->V);
+    double *kS = (double *)malloc(sizeof(double) * j->V);
+    if (!S || !kS) {
+        j->status = -2;
+        free(S);
+        free(kS);
+        return NULL;
+    }
+    const int64_t items = j->N * j->H;
+    for (int64_t it = j->tid; it < items; it += j->nthreads) run_chain(j, it / j->H, it % j->H, S, kS);
+    free(S);
+    free(kS);
+    return NULL;
+}
+
+static int spawn(void *(*fn)(void *), void *jobs, size_t job_size, int nthreads)
+{
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return -2;
+    int started = 0, rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, fn, (char *)jobs + job_size * (size_t)i) != 0) {
+            rc = -3;
+            break;
+        }
+        ++started;
+    }
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return rc;
+}
+
+/*
+ * Returns 0 on success, -1 on invalid arguments, -2 on allocation failure,
+ * -3 if a thread could not be started.
+ */
+int kda_oracle_forward(const double *q, const double *k, const double *v, const double *g,
+                       const double *beta, const double *initial_state, const int64_t *cu_seqlens,
+                       int64_t N, int64_t H, int64_t K, int64_t V, double scale, double *o,
+                       double *final_state, int nthreads)
+{
+    if (!q || !k || !v || !g || !beta || !cu_seqlens || !o || N < 0 || H <= 0 || K <= 0 || V <= 0)
+        return -1;
+    if (cu_seqlens[0] != 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > N * H && N * H > 0) nthreads = (int)(N * H);
+
+    rec_job *jobs = (rec_job *)calloc((size_t)nthreads, sizeof(rec_job));
+    if (!jobs) return -2;
+    for (int i = 0; i < nthreads; ++i) {
+        rec_job j = {q, k, v, g, beta, initial_state, cu_seqlens, N, H, K, V,
+                     scale, o, final_state, i, nthreads, 0};
+        jobs[i] = j;
+    }
+    int rc = spawn(rec_worker, jobs, sizeof(rec_job), nthreads);
+    for (int i = 0; i < nthreads && rc == 0; ++i)
+        if (jobs[i].status) rc = jobs[i].status;
+    free(jobs);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Prologue: short convolution, L2 normalisation, forget gate                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Causal depthwise convolution of width W over the token axis, restarted at
+ * every sequence boundary ("kimi-k3-mlx" review, section "Attention is 93
+ * layers ...": a short convolution with kernel size 4 on q, k and v).
+ *
+ *     y[t, c] = sum_{j=0}^{W-1} w[c, j] * x[t - (W-1) + j, c]
+ *
+ * where x[s, c] = 0 for s before the start of t's sequence, so tap w[c, W-1]
+ * multiplies the current token.  act = 0: no activation; act = 1: y*sigmoid(y).
+ * x, y: [Ttot, C]; w: [C, W].
+ */
+int kda_oracle_short_conv(const double *x, const double *w, const int64_t *cu_seqlens, int64_t N,
+                          int64_t C, int64_t W, int act, double *y)
+{
+    if (!x || !w || !cu_seqlens || !y || C <= 0 || W <= 0 || (act != 0 && act != 1)) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        const int64_t b = cu_seqlens[n], e = cu_seqlens[n + 1];
+        for (int64_t t = b; t < e; ++t) {
+            for (int64_t c = 0; c < C; ++c) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < W; ++j) {
+                    const int64_t s = t - (W - 1) + j;
+                    if (s >= b) acc += w[c * W + j] * x[s * C + c];
+                }
+                if (act == 1) acc = acc / (1.0 + exp(-acc));
+                y[t * C + c] = acc;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Per-row L2 normalisation: x <- x / sqrt(sum_c x_c^2 + eps), rows of length D.
+ */
+int kda_oracle_l2norm(double *x, int64_t rows, int64_t D, double eps)
+{
+    if (!x || rows < 0 || D <= 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t c = 0; c < D; ++c) ss += x[r * D + c] * x[r * D + c];
+        const double inv = 1.0 / sqrt(ss + eps);
+        for (int64_t c = 0; c < D; ++c) x[r * D + c] *= inv;
+    }
+    return 0;
+}
+
+static double softplus(double z)
+{
+    /* log(1 + e^z) without overflow. */
+    if (z > 0.0) return z + log1p(exp(-z));
+    return log1p(exp(z));
+}
+
+/*
+ * Per-channel forget gate ("kimi-k3-mlx" review, sections "The A_log shape
+ * mismatch ..." and "Attention is 93 layers ..."):
+ *
+ *     g[t, h, c] = max(lower_bound, -exp(A_log[c]) * softplus(x[t, h, c] + dt_bias[h*K + c]))
+ *
+ * A_log has K entries broadcast on the channel axis and shared by all heads;
+ * dt_bias has H*K entries.  x, g: [Ttot, H, K].
+ */
+int kda_oracle_gate(const double *x, const double *A_log, const double *dt_bias, int64_t Ttot,
+                    int64_t H, int64_t K, double lower_bound, double *g)
+{
+    if (!x || !A_log || !dt_bias || !g || Ttot < 0 || H <= 0 || K <= 0) return -1;
+    for (int64_t t = 0; t < Ttot; ++t)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t c = 0; c < K; ++c) {
+                const int64_t i = (t * H + h) * K + c;
+                const double val = -exp(A_log[c]) * softplus(x[i] + dt_bias[h * K + c]);
+                g[i] = val > lower_bound ? val : lower_bound;
+            }
+    return 0;
+}

@@ -1,0 +1,349 @@
+"""Pins for the fp64 CPU oracle: closed forms, invariants, brute force, special
+cases that reduce to textbook formulas or library routines, and a hand-worked
+fixture.  None of these calls the CUDA path; none needs a GPU.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped decay, a
+wrong sign in the delta rule, decay on the wrong axis, read-out before the
+update, q and k swapped) fails at least one of them; test_oracle_mutations.py
+plants those slips in copies of the oracle and checks that they are caught.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(rng, T, H, K, V, unit_k=False, g_zero=False, beta=None):
+    q = rng.standard_normal((T, H, K))
+    k = rng.standard_normal((T, H, K))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, V))
+    g = np.zeros((T, H, K)) if g_zero else np.maximum(-5.0, -np.logaddexp(0.0, rng.standard_normal((T, H, K))))
+    b = rng.uniform(0.05, 1.0, (T, H)) if beta is None else np.full((T, H), float(beta))
+    return q, k, v, g, b
+
+
+# ---------------------------------------------------------------- closed form
+def test_closed_form_single_token():
+    """T=1, S0=0: S1 = beta k v^T and o = scale * beta (q.k) v (post-update read-out)."""
+    rng = np.random.default_rng(11)
+    for K, V in ((5, 3), (64, 64), (128, 128)):
+        q, k, v, g, b = _rand(rng, 1, 3, K, V)
+        scale = K ** -0.5
+        o, s = oracle.kda_forward(q, k, v, g, b, scale=scale)
+        for h in range(3):
+            qk = float(q[0, h] @ k[0, h])
+            np.testing.assert_allclose(o[0, h], scale * b[0, h] * qk * v[0, h], rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(s[0, h], b[0, h] * np.outer(k[0, h], v[0, h]), rtol=1e-13, atol=1e-15)
+        assert np.abs(o).max() > 0  # a pre-update read-out would give exactly zero
+
+
+def test_default_scale_is_inverse_sqrt_head_dim():
+    rng = np.random.default_rng(12)
+    q, k, v, g, b = _rand(rng, 3, 1, 64, 8)
+    o1, _ = oracle.kda_forward(q, k, v, g, b)
+    o2, _ = oracle.kda_forward(q, k, v, g, b, scale=0.125)
+    np.testing.assert_array_equal(o1, o2)
+
+
+# ---------------------------------------------------------------- invariants
+def test_delta_rule_overwrites_value_under_key():
+    """g=0, beta=1, |k|=1: after the step S^T k = v for any prior state."""
+    rng = np.random.default_rng(13)
+    K, V, H = 16, 7, 2
+    for _ in range(5):
+        q, k, v, g, b = _rand(rng, 1, H, K, V, unit_k=True, g_zero=True, beta=1.0)
+        s0 = rng.standard_normal((1, H, K, V))
+        _, s = oracle.kda_forward(q, k, v, g, b, initial_state=s0)
+        for h in range(H):
+            np.testing.assert_allclose(s[0, h].T @ k[0, h], v[0, h], rtol=1e-12, atol=1e-12)
+
+
+def test_beta_zero_is_pure_channelwise_decay():
+    """beta=0: S_T = Diag(exp(sum_t g_t)) S0 and o_t = scale (Diag(e^{G_t}) S0)^T q_t."""
+    rng = np.random.default_rng(14)
+    T, H, K, V = 9, 2, 6, 5
+    q, k, v, g, b = _rand(rng, T, H, K, V, beta=0.0)
+    s0 = rng.standard_normal((1, H, K, V))
+    o, s = oracle.kda_forward(q, k, v, g, b, scale=0.3, initial_state=s0)
+    G = np.cumsum(g, axis=0)
+    for h in range(H):
+        np.testing.assert_allclose(s[0, h], np.exp(G[-1, h])[:, None] * s0[0, h], rtol=1e-12)
+        for t in range(T):
+            want = 0.3 * (np.exp(G[t, h])[:, None] * s0[0, h]).T @ q[t, h]
+            np.testing.assert_allclose(o[t, h], want, rtol=1e-11, atol=1e-14)
+
+
+def _transition(k, g, b):
+    K = k.shape[0]
+    return (np.eye(K) - b * np.outer(k, k)) @ np.diag(np.exp(g))
+
+
+def test_brute_force_transition_products():
+    """S_t = M_t...M_1 S0 + sum_j (M_t...M_{j+1}) beta_j k_j v_j^T, M_j = (I - beta_j k_j k_j^T) Diag(e^{g_j})."""
+    rng = np.random.default_rng(15)
+    T, H, K, V = 7, 2, 4, 3
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    scale = 0.7
+    o, s = oracle.kda_forward(q, k, v, g, b, scale=scale, initial_state=s0)
+    for h in range(H):
+        for t in range(T):
+            # S_t by the explicit product formula
+            St = np.eye(K)
+            for j in range(t + 1):
+                St = _transition(k[j, h], g[j, h], b[j, h]) @ St
+            St = St @ s0[0, h]
+            for j in range(t + 1):
+                P = np.eye(K)
+                for i in range(j + 1, t + 1):
+                    P = _transition(k[i, h], g[i, h], b[i, h]) @ P
+                St = St + P @ (b[j, h] * np.outer(k[j, h], v[j, h]))
+            np.testing.assert_allclose(o[t, h], scale * St.T @ q[t, h], rtol=1e-11, atol=1e-13)
+            if t == T - 1:
+                np.testing.assert_allclose(s[0, h], St, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------- special cases
+def test_scalar_decay_is_gated_delta_rule():
+    """g equal across channels: the gated delta rule S_t = a_t (I - b k k^T) S_{t-1} + b k v^T."""
+    rng = np.random.default_rng(16)
+    T, K, V = 12, 8, 5
+    q, k, v, _, b = _rand(rng, T, 1, K, V)
+    a = rng.uniform(0.2, 1.0, T)
+    g = np.repeat(np.log(a)[:, None, None], K, axis=2)
+    o, s = oracle.kda_forward(q, k, v, g, b, scale=1.0)
+    S = np.zeros((K, V))
+    for t in range(T):
+        kt = k[t, 0]
+        S = a[t] * (np.eye(K) - b[t, 0] * np.outer(kt, kt)) @ S + b[t, 0] * np.outer(kt, v[t, 0])
+        np.testing.assert_allclose(o[t, 0], S.T @ q[t, 0], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(s[0, 0], S, rtol=1e-11, atol=1e-13)
+
+
+def test_plain_delta_rule_and_constant_state():
+    rng = np.random.default_rng(17)
+    T, K, V = 10, 6, 4
+    q, k, v, g, b = _rand(rng, T, 1, K, V, g_zero=True)
+    s0 = rng.standard_normal((1, 1, K, V))
+    o, s = oracle.kda_forward(q, k, v, g, b, scale=1.0, initial_state=s0)
+    S = s0[0, 0].copy()
+    for t in range(T):  # Widrow-Hoff / delta rule: S += beta k (v - S^T k)^T
+        S = S + b[t, 0] * np.outer(k[t, 0], v[t, 0] - S.T @ k[t, 0])
+    np.testing.assert_allclose(s[0, 0], S, rtol=1e-11, atol=1e-12)
+    # beta = 0 and g = 0: the state never changes and o_t = S0^T q_t
+    o2, s2 = oracle.kda_forward(q, k, v, g, np.zeros_like(b), scale=1.0, initial_state=s0)
+    np.testing.assert_array_equal(s2, s0)
+    np.testing.assert_allclose(o2[:, 0], q[:, 0] @ s0[0, 0], rtol=1e-13)
+
+
+def test_joint_linearity_in_values_and_initial_state():
+    rng = np.random.default_rng(18)
+    T, H, K, V = 8, 2, 5, 4
+    q, k, v1, g, b = _rand(rng, T, H, K, V)
+    v2 = rng.standard_normal(v1.shape)
+    s1 = rng.standard_normal((1, H, K, V))
+    s2 = rng.standard_normal((1, H, K, V))
+    a1, a2 = 0.7, -1.9
+    oa, sa = oracle.kda_forward(q, k, v1, g, b, initial_state=s1)
+    ob, sb = oracle.kda_forward(q, k, v2, g, b, initial_state=s2)
+    oc, sc = oracle.kda_forward(q, k, a1 * v1 + a2 * v2, g, b, initial_state=a1 * s1 + a2 * s2)
+    np.testing.assert_allclose(oc, a1 * oa + a2 * ob, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(sc, a1 * sa + a2 * sb, rtol=1e-10, atol=1e-12)
+
+
+def test_householder_norm_invariants():
+    """beta=2, |k|=1, g=0, v=0: each step is a reflection, so ||S||_F is kept;
+    beta in (0,1], g<=0, v=0: ||S||_F never grows."""
+    rng = np.random.default_rng(19)
+    T, K, V = 20, 6, 3
+    q, k, v, g, b = _rand(rng, T, 1, K, V, unit_k=True, g_zero=True, beta=2.0)
+    s0 = rng.standard_normal((1, 1, K, V))
+    for t in range(1, T + 1):
+        _, s = oracle.kda_forward(q[:t], k[:t], 0 * v[:t], g[:t], b[:t], initial_state=s0)
+        assert abs(np.linalg.norm(s) - np.linalg.norm(s0)) < 1e-12 * np.linalg.norm(s0)
+    q, k, v, g, b = _rand(rng, T, 1, K, V, unit_k=True)
+    prev = np.linalg.norm(s0)
+    for t in range(1, T + 1):
+        _, s = oracle.kda_forward(q[:t], k[:t], 0 * v[:t], g[:t], b[:t], initial_state=s0)
+        cur = np.linalg.norm(s)
+        assert cur <= prev * (1 + 1e-13)
+        prev = cur
+
+
+def test_padding_tokens_leave_state_unchanged():
+    rng = np.random.default_rng(20)
+    T, P, H, K, V = 5, 4, 2, 6, 5
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    o, s = oracle.kda_forward(q, k, v, g, b, initial_state=s0)
+    pad = lambda a: np.concatenate([a, np.zeros((P,) + a.shape[1:])], axis=0)  # noqa: E731
+    op, sp = oracle.kda_forward(pad(q), pad(k), pad(v), pad(g), pad(b), initial_state=s0)
+    np.testing.assert_array_equal(sp, s)
+    np.testing.assert_array_equal(op[:T], o)
+    assert not op[T:].any()
+
+
+def test_varlen_equals_separate_sequences():
+    rng = np.random.default_rng(21)
+    lens = [3, 0, 9, 1, 6]
+    H, K, V = 2, 5, 4
+    T = sum(lens)
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((len(lens), H, K, V))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, s = oracle.kda_forward(q, k, v, g, b, initial_state=s0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        a, e = cu[n], cu[n + 1]
+        on, sn = oracle.kda_forward(q[a:e], k[a:e], v[a:e], g[a:e], b[a:e], initial_state=s0[n:n + 1])
+        np.testing.assert_array_equal(o[a:e], on)
+        np.testing.assert_array_equal(s[n], sn[0])
+    # an empty sequence returns its initial state
+    np.testing.assert_array_equal(s[1], s0[1])
+
+
+def test_decay_axis_is_key_channel_and_heads_are_independent():
+    """Per-channel decay acts on rows (key channels) of S; permuting heads permutes outputs."""
+    rng = np.random.default_rng(22)
+    T, H, K, V = 6, 3, 8, 5
+    q, k, v, _, b = _rand(rng, T, H, K, V)
+    A = rng.uniform(-1, 1, K)  # one value per channel, shared by all heads
+    g = -np.exp(A)[None, None, :] * rng.uniform(0.1, 1.0, (T, H, 1))
+    s0 = rng.standard_normal((1, H, K, V))
+    o, s = oracle.kda_forward(q, k, v, g, np.zeros_like(b), initial_state=s0)
+    decay = np.exp(g.sum(0))  # [H, K]
+    for h in range(H):
+        np.testing.assert_allclose(s[0, h], decay[h][:, None] * s0[0, h], rtol=1e-12)
+    perm = [2, 0, 1]
+    o1, s1 = oracle.kda_forward(q, k, v, g, b, initial_state=s0)
+    o2, s2 = oracle.kda_forward(q[:, perm], k[:, perm], v[:, perm], g[:, perm], b[:, perm],
+                                initial_state=s0[:, perm])
+    np.testing.assert_array_equal(o2, o1[:, perm])
+    np.testing.assert_array_equal(s2, s1[:, perm])
+
+
+# ---------------------------------------------------------------- golden fixture
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, *nums = line.split()
+                vals[key] = np.array([float(x) for x in nums])
+    return vals
+
+
+def test_hand_worked_fixture():
+    gv = _read_golden("kda_hand_worked_t2.txt")
+    st = lambda a, b: np.stack([gv[a], gv[b]])[:, None, :]  # noqa: E731  [T=2, H=1, D]
+    beta = np.array([[gv["beta1"][0]], [gv["beta2"][0]]])
+    o, s = oracle.kda_forward(st("q1", "q2"), st("k1", "k2"), st("v1", "v2"), st("g1", "g2"), beta,
+                              scale=float(gv["scale"][0]))
+    np.testing.assert_allclose(o[0, 0], gv["o1"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(o[1, 0], gv["o2"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(s[0, 0].ravel(), gv["S2"], rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- prologue pins
+def test_short_conv_matches_numpy_convolve_with_restarts():
+    rng = np.random.default_rng(30)
+    lens = [5, 1, 8, 3]
+    C, W = 7, 4
+    x = rng.standard_normal((sum(lens), C))
+    w = rng.standard_normal((C, W))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    y = oracle.short_conv(x, w, cu_seqlens=cu)
+    for n in range(len(lens)):
+        a, e = cu[n], cu[n + 1]
+        for c in range(C):
+            # causal: tap W-1 multiplies the current token, tap 0 the token W-1 steps back
+            want = np.convolve(x[a:e, c], w[c, ::-1])[: e - a]
+            np.testing.assert_allclose(y[a:e, c], want, rtol=1e-13, atol=1e-14)
+    ys = oracle.short_conv(x, w, cu_seqlens=cu, act=1)
+    np.testing.assert_allclose(ys, y * (0.5 * (1 + np.tanh(0.5 * y))), rtol=1e-12, atol=1e-14)
+
+
+def test_short_conv_one_hot_tap_is_identity():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((2, 11, 6))
+    w = np.zeros((6, 4))
+    w[:, 3] = 1.0
+    np.testing.assert_array_equal(oracle.short_conv(x, w), x)
+    w = np.zeros((6, 4))
+    w[:, 2] = 1.0  # one-token delay, zero at the start of each of the 2 sequences
+    y = oracle.short_conv(x, w)
+    np.testing.assert_array_equal(y[:, 1:], x[:, :-1])
+    assert not y[:, 0].any()
+
+
+def test_l2norm_matches_linalg_norm():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((5, 3, 128)) * 3.0
+    y = oracle.l2norm(x, eps=0.0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(y, x / np.linalg.norm(x, axis=-1, keepdims=True), rtol=1e-14)
+    y = oracle.l2norm(x, eps=1e-6)
+    np.testing.assert_allclose(y, x / np.sqrt(np.linalg.norm(x, axis=-1, keepdims=True) ** 2 + 1e-6),
+                               rtol=1e-13)
+
+
+def test_gate_special_cases():
+    rng = np.random.default_rng(33)
+    T, H, K = 7, 3, 16
+    x = rng.standard_normal((T, H, K)) * 3
+    zero_bias = np.zeros(H * K)
+    # A_log = 0, dt_bias = 0: g = max(-5, -softplus(x)), softplus from numpy.logaddexp
+    g = oracle.gate(x, np.zeros(K), zero_bias)
+    np.testing.assert_allclose(g, np.maximum(-5.0, -np.logaddexp(0.0, x)), rtol=1e-14)
+    assert g.max() <= 0.0
+    # large inputs hit the lower bound exactly
+    g = oracle.gate(np.full((1, H, K), 50.0), np.zeros(K), zero_bias)
+    assert np.all(g == -5.0)
+    # A_log = ln(a_c) per channel, shared across heads: g = max(-5, -a_c softplus(x))
+    a = rng.uniform(0.2, 2.0, K)
+    g = oracle.gate(x, np.log(a), zero_bias)
+    np.testing.assert_allclose(g, np.maximum(-5.0, -a[None, None, :] * np.logaddexp(0.0, x)), rtol=1e-13)
+    # dt_bias is indexed [h*K + c]: a bias on head 1 alone changes only head 1
+    db = np.zeros(H * K)
+    db[K:2 * K] = rng.uniform(-1, 1, K)
+    g0 = oracle.gate(x, np.zeros(K), zero_bias)
+    g1 = oracle.gate(x, np.zeros(K), db)
+    np.testing.assert_array_equal(g1[:, [0, 2]], g0[:, [0, 2]])
+    np.testing.assert_allclose(g1[:, 1], np.maximum(-5.0, -np.logaddexp(0.0, x[:, 1] + db[K:2 * K])),
+                               rtol=1e-14)
+
+
+def test_prologue_composition():
+    rng = np.random.default_rng(34)
+    B, T, H, K, V = 1, 9, 2, 8, 4
+    qr, kr, gx = (rng.standard_normal((B, T, H, K)) for _ in range(3))
+    vr = rng.standard_normal((B, T, H, V))
+    wq, wk = rng.standard_normal((H * K, 4)), rng.standard_normal((H * K, 4))
+    wv = rng.standard_normal((H * V, 4))
+    A, db = rng.uniform(-1, 1, K), rng.uniform(-1, 1, H * K)
+    q, k, v, g = oracle.prologue(qr, kr, vr, gx, (wq, wk, wv), A, db)
+    for h in range(H):
+        conv = np.stack([np.convolve(qr[0, :, h, c], wq[h * K + c, ::-1])[:T] for c in range(K)], -1)
+        want = conv / np.sqrt(np.sum(conv * conv, axis=-1, keepdims=True) + 1e-6)
+        np.testing.assert_allclose(q[0, :, h], want, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(np.linalg.norm(q, axis=-1), 1.0, rtol=1e-5)
+    np.testing.assert_allclose(np.linalg.norm(k, axis=-1), 1.0, rtol=1e-5)
+    np.testing.assert_allclose(v.reshape(T, H * V), oracle.short_conv(vr.reshape(T, H * V), wv), rtol=0)
+    np.testing.assert_allclose(g, oracle.gate(gx, A, db), rtol=0)
+    assert np.all((g <= 0) & (g >= -5))
+
+
+@pytest.mark.parametrize("nthreads", [1, 3])
+def test_thread_count_does_not_change_results(nthreads):
+    rng = np.random.default_rng(40)
+    q, k, v, g, b = _rand(rng, 17, 5, 8, 6)
+    o1, s1 = oracle.kda_forward(q, k, v, g, b, nthreads=1)
+    o2, s2 = oracle.kda_forward(q, k, v, g, b, nthreads=nthreads)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
