@@ -1,0 +1,378 @@
+"""KDA forward benchmark on GB300: chunked prefill tokens/s (H=96, K=V=128) with
+the decode steps/s beside it, each as a fraction of its HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  The headline ``value`` is whole-job prefill
+throughput on the 4096-token, 96-head workload with inputs resident in HBM;
+``e2e`` is the same metric through the public call with pinned host buffers
+and the host<->device copies inside the timed region; ``decode`` is the
+256-sequence single-token step repeated 64 times.  Each rank is an independent
+replica (the sequences and heads of KDA are independent problems), so the job
+processes N times the work and ``scaling`` is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (H=96,K=V=128) + decode steps/s, % of roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def prefill_bytes(T_tokens: int, H: int, K: int, V: int, N: int, in_bytes: int, reads_state: bool) -> int:
+    """Algorithmic HBM bytes of one chunked prefill: q, k, g [T,H,K] + v [T,H,V] + beta [T,H]
+    read once, o [T,H,V] fp32 written once, final state [N,H,K,V] fp32 written once (and the
+    initial state read once when given)."""
+    per_token = H * ((3 * K + V) * in_bytes + in_bytes + V * 4)
+    states = N * H * K * V * 4 * (2 if reads_state else 1)
+    return T_tokens * per_token + states
+
+
+def decode_bytes(N: int, H: int, K: int, V: int, in_bytes: int) -> int:
+    """One decode step: the fp32 state read and written once, plus q, k, g, v, beta and o."""
+    return 2 * N * H * K * V * 4 + N * H * ((3 * K + V) * in_bytes + in_bytes + V * 4)
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kimi_delta_attention_chunk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(kernel)
+    if not rec or rec.get("source_sha") != source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for t, r in self.rows if self.t0 is None or (self.t0 - 0.1 <= t <= (self.t1 or t) + 0.1)]
+        if not rows:
+            rows = [r for _, r in self.rows]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_prefill_rate(H: int, T: int, heads: int, seed: int = 1):
+    """Oracle tokens/s on `heads` of the H heads of a T-token prefill (scaled to all H)."""
+    import oracle
+    from kimi_delta_attention_chunk_gb300 import synth
+    inp = synth.direct_inputs(T, heads, 128, 128, torch.bfloat16, seed=seed)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"], nthreads=threads)
+    dt = time.perf_counter() - t0
+    return T * heads / H / dt, dt, threads
+
+
+def cpu_baseline(H: int, T: int, budget_s: float = 12.0):
+    # calibrate on 2 heads, then size the sample to about budget_s seconds
+    rate1, dt1, threads = oracle_prefill_rate(H, T, 2)
+    per_head = dt1 / 2
+    heads = int(max(2, min(H, budget_s / max(per_head, 1e-6))))
+    rate, dt, threads = oracle_prefill_rate(H, T, heads)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{T} tokens x {heads} of {H} heads (K=V=128, bf16 inputs upcast to fp64), "
+                      f"{dt:.1f} s; rate scaled to all {H} heads"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    H, T = 96, 4096
+    heads = 4
+    for _ in range(args.warmup):
+        oracle_prefill_rate(H, T, heads)
+    rates, total = [], 0.0
+    for _ in range(args.steps):
+        r, dt, threads = oracle_prefill_rate(H, T, heads)
+        rates.append(r)
+        total += dt
+    value = sum(rates) / len(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill B=1 T=4096 H=96 K=V=128 bf16 inputs, zero initial state",
+                       "sample": f"{T} tokens x {heads} of {H} heads per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{T} tokens x {heads} of {H} heads per step, rate scaled to {H} heads"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU legs
+def time_launches(fn, steps: int, stream):
+    """Run fn() `steps` times; return (total ms, per-launch ms list) from CUDA events on `stream`."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in ev]
+
+
+def run_ours(args, world, rank, local):
+    import kimi_delta_attention_chunk_gb300 as kda
+    from kimi_delta_attention_chunk_gb300 import synth
+
+    kda.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    w = synth.WORKLOADS["prefill"]
+    H, K, V, T = w.H, w.K, w.V, w.T
+    host = synth.direct_inputs(T, H, K, V, w.dtype, w.seed + 1000 * rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    o = torch.empty((1, T, H, V), dtype=torch.float32, device=dev)
+    sT = torch.empty((1, H, K, V), dtype=torch.float32, device=dev)
+
+    def prefill():
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"], o=o, final_state=sT)
+
+    for _ in range(max(3, args.warmup)):
+        prefill()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    total_ms, per = time_launches(prefill, args.steps, stream)
+    clocks.mark("t1")
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    tokens_per_step = T * world
+    value = tokens_per_step / (ms_step * 1e-3)
+    kernel_ms = sum(per) / len(per)
+    pbytes = prefill_bytes(T, H, K, V, 1, 2, reads_state=False)
+    achieved = pbytes / (kernel_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public call: pinned host in, host out
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    o_host = torch.empty_like(o, device="cpu").pin_memory()
+    s_host = torch.empty_like(sT, device="cpu").pin_memory()
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "g", "beta"))
+    d2h = o_host.numel() * 4 + s_host.numel() * 4
+
+    def e2e_step():
+        for k in ("q", "k", "v", "g", "beta"):
+            d[k].copy_(pin[k], non_blocking=True)
+        prefill()
+        o_host.copy_(o, non_blocking=True)
+        s_host.copy_(sT, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms, _ = time_launches(e2e_step, args.steps, stream)
+    e2e_ms = max_over_ranks(e2e_ms, world) / args.steps
+    e2e = {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+    del pin, o_host, s_host
+
+    # ---- decode: 256 sequences x 64 steps
+    dw = synth.WORKLOADS["decode"]
+    dec = synth.decode_inputs(dw.B, dw.H, dw.K, dw.V, dw.decode_steps, dw.dtype, dw.seed + 1000 * rank)
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dec.items()}
+    state = dd["state"].clone()
+    od = torch.empty((dw.B, dw.H, dw.V), dtype=torch.float32, device=dev)
+    steps = dw.decode_steps
+    qs = [dd["q"][i] for i in range(steps)]
+    ks = [dd["k"][i] for i in range(steps)]
+    vs = [dd["v"][i] for i in range(steps)]
+    gs = [dd["g"][i] for i in range(steps)]
+    bs = [dd["beta"][i] for i in range(steps)]
+    it = [0]
+
+    def dstep():
+        i = it[0] % steps
+        it[0] += 1
+        kda.recurrent_step(qs[i], ks[i], vs[i], gs[i], bs[i], state, scale=dd["scale"], o=od)
+
+    for _ in range(max(3, args.warmup)):
+        dstep()
+    torch.cuda.synchronize()
+    barrier(world)
+    dsteps = steps * max(1, args.steps // 10)
+    dec_ms, dper = time_launches(dstep, dsteps, stream)
+    dec_ms = max_over_ranks(dec_ms, world) / dsteps
+    dker = sum(dper) / len(dper)
+    dbytes = decode_bytes(dw.B, dw.H, dw.K, dw.V, 2)
+    dach = dbytes / (dker * 1e-3) / 1e9
+    decode = {"value": world / (dec_ms * 1e-3), "unit": "steps/s", "tokens_per_s": world * dw.B / (dec_ms * 1e-3),
+              "ms_per_step": dec_ms, "workload": "decode N=256 H=96 K=V=128 bf16, fp32 state in place, 64 steps",
+              "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s", "frac": dach / hbm,
+                           "traffic": recorded_traffic("decode_step_kernel"), "algorithmic_bytes": dbytes,
+                           "peak_kind": peak_kind}}
+    del dd, state, qs, ks, vs, gs, bs
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B=1 T=4096 H=96 K=V=128 bf16 inputs, fp32 state and output, "
+                               "zero initial state", "parallelism": f"replicas x{world}",
+                   "l2": "inputs (611 MB per step) larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": recorded_traffic("chunk_prefill"), "algorithmic_bytes": pbytes,
+                     "kernel_ms": kernel_ms, "peak_kind": peak_kind},
+        "clocks": clk, "e2e": e2e, "gpu_launches": args.steps,
+        "decode": decode,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(H, T)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * kda.h -- C ABI of libkda.so, the GB300 (sm_103a) Kimi Delta Attention forward.
+ *
+ * KDA is a gated delta-rule linear-attention recurrence with per-channel decay
+ * (the K3 text backbone's KDA layers; "kimi-k3-mlx" review, sections "The A_log
+ * shape mismatch ..." and "Attention is 93 layers ..."; "ISEEKYAN/k3" README,
+ * which names the chunked KDA forward and a recurrent path as the operator's
+ * compute paths).  Per sequence n and head h, over the tokens t of the sequence:
+ *
+ *     S <- Diag(exp(g_t)) S                              (row c = key channel c)
+ *     S <- S - beta_t k_t (k_t^T S) + beta_t k_t v_t^T
+ *     o_t = scale * S^T q_t
+ *
+ * S is a K x V fp32 matrix.  The gate g is a log-decay in [-5, 0] (the K3
+ * gate_lower_bound is -5.0).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    allocates no memory and keeps no state between calls, so calls from
+ *    different host threads are safe.
+ *  - Layouts are row-major and token-major, as the K3 gate tensor (B, T, 96, 128):
+ *        q, k, g [B, T, H, K]    v [B, T, H, V]    beta [B, T, H]
+ *        o [B, T, H, V]          states [N, H, K, V] (V contiguous, fp32)
+ *  - in_dtype selects the element type of q, k, v, g, beta (KDA_BF16 or
+ *    KDA_F32); o_dtype that of o.  States are always fp32.
+ *  - Supported head sizes: K, V in {64, 128}.  Anything else returns
+ *    KDA_ERR_UNSUPPORTED; nothing falls back to another implementation.
+ *  - q, k, v, g, o and the state tensors must be 16-byte aligned; beta and
+ *    cu_seqlens need only the alignment of their element type.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously; the call returns before the
+ *    GPU finishes.
+ *  - Errors found on the host return before anything is enqueued, so no
+ *    output is touched.  A failed launch returns KDA_ERR_CUDA.
+ *  - g outside [-5, 0] is a precondition violation: results are then
+ *    unspecified (the in-chunk decay products are only kept in range by the
+ *    bound), but no memory outside the given tensors is accessed.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, inconsistent B/N */
+    KDA_ERR_UNSUPPORTED = 2, /* head size or dtype outside the supported set */
+    KDA_ERR_WORKSPACE = 3,   /* reserved */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_RANGE = 5,       /* reserved for input-range checks */
+    KDA_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+KDA_API const char *kda_status_string(kda_status status);
+
+/* Version of this ABI; bumped on any incompatible change. */
+KDA_API int kda_abi_version(void);
+
+/*
+ * kda_chunk_fwd -- chunked prefill.
+ *
+ * Computes the recurrence above for N independent sequences with a chunked
+ * (64-token) algorithm: in-chunk gated products A = K K^T and P = Q K^T with
+ * cumulative per-channel decay, a UT transform of the decayed keys, and the
+ * state carried from chunk to chunk on chip.  Results equal the token-by-token
+ * recurrence up to rounding.
+ *
+ *  q, k, g, v, beta   inputs as laid out above, element type in_dtype.
+ *  scale              read-out scale; scale <= 0 selects K^-0.5.
+ *  initial_state      [N, H, K, V] fp32 state before the first token of each
+ *                     sequence, or NULL for zeros.  Read only.
+ *  cu_seqlens         NULL: B sequences of T tokens each (N must equal B).
+ *                     Non-NULL: device int32 [N+1] offsets of N sequences packed
+ *                     along the token axis of a B == 1 batch; cu_seqlens[0] = 0,
+ *                     non-decreasing, cu_seqlens[N] = T.  The kernel clamps
+ *                     offsets into [0, T] and treats a decreasing pair as an
+ *                     empty sequence, so malformed offsets never cause an
+ *                     out-of-bounds access (but leave tokens unwritten).
+ *  B, T, H, K, V, N   sizes; T = 0 or N = 0 is valid (nothing but the final
+ *                     state is written).
+ *  o                  [B, T, H, V] output, element type o_dtype.
+ *  final_state        [N, H, K, V] fp32 state after each sequence's last token,
+ *                     or NULL to skip.  May alias initial_state exactly (the
+ *                     state is then updated in place); no other overlap is
+ *                     allowed.
+ */
+KDA_API kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
+                         const void *beta, kda_dtype in_dtype, float scale,
+                         const float *initial_state, const int32_t *cu_seqlens,
+                         int B, int T, int H, int K, int V, int N,
+                         void *o, kda_dtype o_dtype, float *final_state, void *stream);
+
+/*
+ * kda_chunk_fwd_fused -- chunked prefill with the input prologue fused into
+ * the tile loads ("kimi-k3-mlx" review, section "Attention is 93 layers ...":
+ * short convolution of kernel size 4 on q, k and v, per-channel forget gate
+ * with gate_lower_bound; section "The A_log shape mismatch ...": A_log has K
+ * entries shared by all heads, dt_bias has H*K entries).  Per token:
+ *
+ *     q = l2norm(conv4(q_raw; conv_q)),  k = l2norm(conv4(k_raw; conv_k)),
+ *     v = conv4(v_raw; conv_v),
+ *     g[t,h,c] = max(lower_bound, -exp(A_log[c]) * softplus(gate_x[t,h,c] + dt_bias[h*K+c]))
+ *
+ * conv4 is causal and depthwise: y[t,ch] = sum_{j=0..3} w[ch][j] * x[t-3+j, ch],
+ * with zero history before the first token of each sequence (tap 3 multiplies
+ * the current token); conv_act = 0 for none, 1 for SiLU after the convolution.
+ * l2norm(x) = x / sqrt(sum_c x_c^2 + l2_eps) over the K channels of one head.
+ *
+ *  q_raw, k_raw, gate_x [B, T, H, K], v_raw [B, T, H, V], beta [B, T, H]:
+ *                     element type in_dtype.
+ *  conv_q, conv_k     fp32 [H*K][4];  conv_v fp32 [H*V][4]  (channel = h*D + c).
+ *  A_log fp32 [K];  dt_bias fp32 [H*K].
+ *  Everything else as for kda_chunk_fwd.
+ */
+KDA_API kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, const void *v_raw,
+                               const void *gate_x, const void *beta, kda_dtype in_dtype,
+                               const float *conv_q, const float *conv_k, const float *conv_v,
+                               int conv_act, const float *A_log, const float *dt_bias,
+                               float lower_bound, float l2_eps, float scale,
+                               const float *initial_state, const int32_t *cu_seqlens,
+                               int B, int T, int H, int K, int V, int N,
+                               void *o, kda_dtype o_dtype, float *final_state, void *stream);
+
+/*
+ * kda_recurrent_step -- one decode token for each of N sequences.
+ *
+ * Applies one step of the recurrence to the fp32 state in place, streaming it
+ * through HBM once (read, update, write):
+ *
+ *     a = S_old^T (k * exp(g)),  b = S_old^T (q * exp(g))
+ *     delta = beta (v - a),      o = scale (b + (q . k) delta)
+ *     S_new = Diag(exp(g)) S_old + k delta^T
+ *
+ * which equals decay, delta update and read-out of the recurrence above.
+ *
+ *  q, k, g [N, H, K], v [N, H, V], beta [N, H]: element type in_dtype.
+ *  state   [N, H, K, V] fp32, read and written in place.
+ *  o       [N, H, V], element type o_dtype.
+ */
+KDA_API kda_status kda_recurrent_step(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, kda_dtype in_dtype, float scale, float *state,
+                              int N, int H, int K, int V, void *o, kda_dtype o_dtype,
+                              void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,1 +1,17 @@
-"""GB300-native Kimi Delta Attention (KDA) forward."""
+"""GB300-native Kimi Delta Attention (KDA) forward.
+
+The compute lives in ``libkda.so`` (CUDA for sm_103a behind the C ABI declared
+in ``include/kda.h``); :mod:`.kda` is a thin ctypes binding that marshals
+torch tensors and the current stream into those calls.  Importing the package
+does not load the library; the first call does, and fails loudly if the
+library is missing.
+"""
+from .kda import (  # noqa: F401
+    KDAError,
+    SIGNATURES,
+    chunk_fwd,
+    chunk_fwd_fused,
+    library_path,
+    load_library,
+    recurrent_step,
+)

@@ -1,0 +1,151 @@
+// C-ABI entry points of libkda.so (declared in include/kda.h): argument
+// validation on the host, then one kernel launch on the caller's stream.
+#include <math.h>
+
+#include "kda_chunk.h"
+#include "kda_common.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+bool head_size_ok(int d) { return d == 64 || d == 128; }
+bool dtype_ok(kda_dtype d) { return d == KDA_F32 || d == KDA_BF16; }
+
+// Sizes: all non-negative, element counts representable in int64 and
+// per-sequence token offsets in int32 (the kernels index tokens with int64).
+kda_status check_sizes(int B, int T, int H, int K, int V, int N) {
+    if (B < 0 || T < 0 || H <= 0 || N < 0) return KDA_ERR_INVALID_ARG;
+    if (!head_size_ok(K) || !head_size_ok(V)) return KDA_ERR_UNSUPPORTED;
+    const double elems = (double)B * (double)T * (double)H * (double)(K > V ? K : V);
+    if (elems > 9.0e18) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+float resolve_scale(float scale, int K) { return scale > 0.f ? scale : 1.0f / sqrtf((float)K); }
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+kda_status check_common(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, kda_dtype in_dtype, const float* initial_state,
+                        const int32_t* cu_seqlens, int B, int T, int H, int K, int V, int N,
+                        const void* o, kda_dtype o_dtype, const float* final_state) {
+    kda_status s = check_sizes(B, T, H, K, V, N);
+    if (s != KDA_OK) return s;
+    if (!dtype_ok(in_dtype) || !dtype_ok(o_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (cu_seqlens != nullptr) {
+        if (B != 1) return KDA_ERR_INVALID_ARG;
+    } else if (N != B) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, o, initial_state, final_state};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t esz = in_dtype == KDA_BF16 ? 2 : 4;
+    if (beta && ((uintptr_t)beta % esz)) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && ((uintptr_t)cu_seqlens % 4)) return KDA_ERR_INVALID_ARG;
+    if (final_state && initial_state && final_state != initial_state) {
+        // Partial overlap of the two state tensors is not allowed.
+        const char* a = (const char*)initial_state;
+        const char* b = (const char*)final_state;
+        const size_t bytes = (size_t)N * H * K * V * sizeof(float);
+        if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head size or dtype not supported";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+        case KDA_ERR_RANGE: return "KDA_ERR_RANGE: input out of range";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: device-side wait gave up";
+    }
+    return "unknown kda_status";
+}
+
+int kda_abi_version(void) { return kAbiVersion; }
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
+                         const void* beta, kda_dtype in_dtype, float scale,
+                         const float* initial_state, const int32_t* cu_seqlens, int B, int T,
+                         int H, int K, int V, int N, void* o, kda_dtype o_dtype,
+                         float* final_state, void* stream) {
+    kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H,
+                                K, V, N, o, o_dtype, final_state);
+    if (s != KDA_OK) return s;
+    kda::ChunkParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.scale = resolve_scale(scale, K);
+    p.initial_state = initial_state;
+    p.cu_seqlens = cu_seqlens;
+    p.B = B; p.T = T; p.H = H; p.N = N;
+    p.o = o;
+    p.final_state = final_state;
+    cudaStream_t st = (cudaStream_t)stream;
+    return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, false, p, st));
+}
+
+kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v_raw,
+                               const void* gate_x, const void* beta, kda_dtype in_dtype,
+                               const float* conv_q, const float* conv_k, const float* conv_v,
+                               int conv_act, const float* A_log, const float* dt_bias,
+                               float lower_bound, float l2_eps, float scale,
+                               const float* initial_state, const int32_t* cu_seqlens, int B,
+                               int T, int H, int K, int V, int N, void* o, kda_dtype o_dtype,
+                               float* final_state, void* stream) {
+    kda_status s = check_common(q_raw, k_raw, v_raw, gate_x, beta, in_dtype, initial_state,
+                                cu_seqlens, B, T, H, K, V, N, o, o_dtype, final_state);
+    if (s != KDA_OK) return s;
+    if (conv_act != 0 && conv_act != 1) return KDA_ERR_INVALID_ARG;
+    if (!(l2_eps >= 0.f) || !(lower_bound <= 0.f) || isnan(lower_bound)) return KDA_ERR_INVALID_ARG;
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens && (!conv_q || !conv_k || !conv_v || !A_log || !dt_bias)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {conv_q, conv_k, conv_v, A_log, dt_bias};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    kda::ChunkParams p{};
+    p.q = q_raw; p.k = k_raw; p.v = v_raw; p.g = gate_x; p.beta = beta;
+    p.scale = resolve_scale(scale, K);
+    p.initial_state = initial_state;
+    p.cu_seqlens = cu_seqlens;
+    p.B = B; p.T = T; p.H = H; p.N = N;
+    p.o = o;
+    p.final_state = final_state;
+    p.conv_q = conv_q; p.conv_k = conv_k; p.conv_v = conv_v;
+    p.conv_act = conv_act;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.lower_bound = lower_bound;
+    p.l2_eps = l2_eps;
+    cudaStream_t st = (cudaStream_t)stream;
+    return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, true, p, st));
+}
+
+kda_status kda_recurrent_step(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, kda_dtype in_dtype, float scale, float* state,
+                              int N, int H, int K, int V, void* o, kda_dtype o_dtype,
+                              void* stream) {
+    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (!head_size_ok(K) || !head_size_ok(V)) return KDA_ERR_UNSUPPORTED;
+    if (!dtype_ok(in_dtype) || !dtype_ok(o_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !o) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, state, o};
+    for (const void* p : ptrs)
+        if (!kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if ((uintptr_t)beta % (in_dtype == KDA_BF16 ? 2 : 4)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    return from_cuda(kda::decode_step(in_dtype, o_dtype, K, V, q, k, v, g, beta,
+                                      resolve_scale(scale, K), state, N, H, o, st));
+}
+
+}  // extern "C"

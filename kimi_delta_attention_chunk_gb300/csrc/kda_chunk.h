@@ -1,0 +1,45 @@
+// Parameters and launchers of the KDA prefill and decode kernels (internal to
+// libkda.so; the public surface is include/kda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+struct ChunkParams {
+    // Direct inputs, or the raw prologue inputs (q_raw, k_raw, v_raw, gate_x).
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    float scale;
+    const float* initial_state;
+    const int32_t* cu_seqlens;
+    int B, T, H, N;
+    void* o;
+    float* final_state;
+    // Prologue (only read by the fused variants).
+    const float* conv_q;
+    const float* conv_k;
+    const float* conv_v;
+    int conv_act;
+    const float* A_log;
+    const float* dt_bias;
+    float lower_bound;
+    float l2_eps;
+};
+
+// CUDA-core fp32 chunk kernel (any supported K/V, fp32 or bf16 inputs).
+cudaError_t chunk_simt(kda_dtype in_dt, kda_dtype out_dt, int K, int V, bool prologue,
+                       const ChunkParams& p, cudaStream_t st);
+
+// Single-token decode.
+cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const void* q,
+                        const void* k, const void* v, const void* g, const void* beta,
+                        float scale, float* state, int N, int H, void* o, cudaStream_t st);
+
+}  // namespace kda

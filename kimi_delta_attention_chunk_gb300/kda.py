@@ -1,0 +1,167 @@
+"""Thin ctypes binding of libkda.so (C ABI in include/kda.h).
+
+Marshalling only: every function checks that the tensors live on the current
+CUDA device, picks the dtype codes, and forwards raw device pointers, sizes and
+the current CUDA stream to the library.  All arithmetic runs in the library's
+kernels; there is no CPU or PyTorch fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libkda.so"
+_lock = threading.Lock()
+_lib = None
+
+KDA_F32, KDA_BF16 = 0, 1
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_WORKSPACE",
+           4: "KDA_ERR_CUDA", 5: "KDA_ERR_RANGE", 6: "KDA_ERR_TIMEOUT"}
+
+# (name, restype, argtypes) of every exported symbol of include/kda.h
+_vp, _fp, _i32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_i, _f = ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "kda_status_string": (ctypes.c_char_p, [_i]),
+    "kda_abi_version": (_i, []),
+    "kda_chunk_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
+                           _vp, _i, _fp, _vp]),
+    "kda_chunk_fwd_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _fp, _fp, _f, _f,
+                                 _f, _fp, _i32p, _i, _i, _i, _i, _i, _i, _vp, _i, _fp, _vp]),
+    "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
+                                _vp]),
+}
+
+
+class KDAError(RuntimeError):
+    """A libkda.so call returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("KDA_LIBRARY", os.path.join(_PKG, _LIB_NAME))
+
+
+def load_library():
+    """Load libkda.so (built by ``build.py``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(f"{path} is missing: build it with "
+                                  "`python -m kimi_delta_attention_chunk_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libkda must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkda must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise KDAError(fn, status)
+
+
+def chunk_fwd(q, k, v, g, beta, scale: float | None = None, initial_state=None, cu_seqlens=None,
+              output_final_state: bool = True, o_dtype=torch.float32, o=None, final_state=None):
+    """Chunked KDA prefill.  q, k, g: [B,T,H,K]; v: [B,T,H,V]; beta: [B,T,H].
+
+    Returns (o [B,T,H,V] in ``o_dtype``, final_state [N,H,K,V] fp32 or None).
+    ``cu_seqlens`` (int32 [N+1], on the device) packs N sequences into B == 1.
+    ``final_state`` may be the ``initial_state`` tensor itself (in-place update).
+    """
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=o_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q),
+                           float(scale or 0.0), _ptr(initial_state), _ptr(cu_seqlens),
+                           B, T, H, K, V, N, _ptr(o), _dt(o), _ptr(final_state), _stream(q.device))
+    _check("kda_chunk_fwd", st)
+    return o, final_state
+
+
+def chunk_fwd_fused(q_raw, k_raw, v_raw, gate_x, beta, conv_w, A_log, dt_bias,
+                    scale: float | None = None, initial_state=None, cu_seqlens=None,
+                    lower_bound: float = -5.0, l2_eps: float = 1e-6, conv_act: int = 0,
+                    output_final_state: bool = True, o_dtype=torch.float32, o=None,
+                    final_state=None):
+    """Chunked prefill with the fused prologue (short conv, L2-norm, gate).
+
+    conv_w: a sequence (conv_q [H*K,4], conv_k [H*K,4], conv_v [H*V,4]) of fp32
+    tensors, or one [3, H*D, 4] tensor whose leading rows are used.
+    """
+    lib = load_library()
+    B, T, H, K = q_raw.shape
+    V = v_raw.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if isinstance(conv_w, torch.Tensor):
+        cq = conv_w[0, : H * K].contiguous()
+        ck = conv_w[1, : H * K].contiguous()
+        cv = conv_w[2, : H * V].contiguous()
+    else:
+        cq, ck, cv = (w.contiguous() for w in conv_w)
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=o_dtype, device=q_raw.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q_raw.device)
+    st = lib.kda_chunk_fwd_fused(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(gate_x), _ptr(beta),
+                                 _dt(q_raw), _ptr(cq), _ptr(ck), _ptr(cv), int(conv_act), _ptr(A_log),
+                                 _ptr(dt_bias), float(lower_bound), float(l2_eps), float(scale or 0.0),
+                                 _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(o),
+                                 _dt(o), _ptr(final_state), _stream(q_raw.device))
+    _check("kda_chunk_fwd_fused", st)
+    return o, final_state
+
+
+def recurrent_step(q, k, v, g, beta, state, scale: float | None = None, o_dtype=torch.float32, o=None):
+    """One decode token per sequence; ``state`` [N,H,K,V] fp32 is updated in place.
+
+    q, k, g: [N,H,K]; v: [N,H,V]; beta: [N,H].  Returns o [N,H,V].
+    """
+    lib = load_library()
+    N, H, K = q.shape
+    V = v.shape[-1]
+    if o is None:
+        o = torch.empty((N, H, V), dtype=o_dtype, device=q.device)
+    st = lib.kda_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q),
+                                float(scale or 0.0), _ptr(state), N, H, K, V, _ptr(o), _dt(o),
+                                _stream(q.device))
+    _check("kda_recurrent_step", st)
+    return o

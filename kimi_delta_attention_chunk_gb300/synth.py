@@ -6,8 +6,9 @@ CUDA path and the CPU oracle are fed from here, and neither is imported here.
 
 Every draw comes from ``numpy.random.Generator(PCG64(seed))`` in a fixed order
 (q, k, v, gate pre-activation, beta pre-activation, initial state, conv weights,
-A_log, dt_bias), in float32, block by block over tokens so that the 65536-token
-workload stays within a few GB of host memory.  Each tensor is rounded once
+A_log, dt_bias), in float32 (beta in float64), block by block over tokens so
+that the 65536-token workload stays within a few GB of host memory; the shaping
+transforms run in float32 torch CPU ops.  Each tensor is rounded once
 (round-to-nearest-even) to its storage dtype; the oracle reads exactly the
 rounded values.
 
@@ -78,32 +79,32 @@ def _to(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
 def _normal(rng, shape, dtype, std=1.0, unit_rows=False) -> torch.Tensor:
     """N(0, std^2) draws in token blocks; optionally each last-axis row scaled to unit norm."""
     out = torch.empty(shape, dtype=dtype)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1) if len(shape) > 1 else out.view(-1, 1)
     rows = flat.shape[0]
     for b in range(0, rows, TOKEN_BLOCK):
         e = min(rows, b + TOKEN_BLOCK)
-        x = rng.standard_normal((e - b,) + tuple(shape[1:]), dtype=np.float32)
+        x = torch.from_numpy(rng.standard_normal((e - b,) + tuple(shape[1:]), dtype=np.float32))
         if std != 1.0:
-            x *= np.float32(std)
+            x *= std
         if unit_rows:
-            x64 = x.astype(np.float64)
-            x = (x64 / np.sqrt(np.sum(x64 * x64, axis=-1, keepdims=True))).astype(np.float32)
-        flat[b:e] = _to(x, dtype).reshape(e - b, -1)
+            x = x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+        flat[b:e] = x.to(dtype).reshape(e - b, -1)
     return out
 
 
 def _beta(rng, shape, dtype) -> torch.Tensor:
-    z = rng.standard_normal(shape).astype(np.float64)
-    return _to(1.0 / (1.0 + np.exp(-z)), dtype)
+    z = torch.from_numpy(rng.standard_normal(shape))
+    return torch.sigmoid(z).to(dtype)
 
 
 def _log_decay(rng, shape, dtype) -> torch.Tensor:
     out = torch.empty(shape, dtype=dtype)
     for b in range(0, shape[0], TOKEN_BLOCK):
         e = min(shape[0], b + TOKEN_BLOCK)
-        z = rng.standard_normal((e - b,) + tuple(shape[1:]), dtype=np.float32).astype(np.float64)
-        sp = np.logaddexp(0.0, z)
-        out[b:e] = _to(np.maximum(GATE_LOWER_BOUND, -sp), dtype)
+        z = torch.from_numpy(rng.standard_normal((e - b,) + tuple(shape[1:]), dtype=np.float32))
+        out[b:e] = torch.clamp(-torch.nn.functional.softplus(z), min=GATE_LOWER_BOUND).to(dtype)
     return out
 
 

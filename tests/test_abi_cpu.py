@@ -1,0 +1,110 @@
+"""The C ABI on the host: libkda.so builds, loads and exports every symbol that
+include/kda.h declares; host-side argument checks reject bad calls before any
+GPU work.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import kimi_delta_attention_chunk_gb300 as kda
+from kimi_delta_attention_chunk_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+INVALID_ARG, UNSUPPORTED = 1, 2
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"KDA_API[^;(]*?\b(kda_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load_library()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("kda_chunk_fwd", "kda_chunk_fwd_fused", "kda_recurrent_step", "kda_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert sorted(kda.SIGNATURES) == declared_symbols()
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kda_abi_version() >= 1
+    for s in range(7):
+        assert lib.kda_status_string(s)
+    assert lib.kda_status_string(99) == b"unknown kda_status"
+
+
+# Fake, 16-byte aligned, never-dereferenced addresses: every call below must be
+# rejected on the host before anything is launched.
+P = ctypes.c_void_p(0x10000)
+Pm = ctypes.c_void_p(0x10008)  # misaligned
+
+
+def chunk(lib, *, q=P, k=P, v=P, g=P, beta=P, dt=1, s0=None, cu=None, B=1, T=64, H=2, K=128, V=128,
+          N=1, o=P, odt=0, sT=None):
+    return lib.kda_chunk_fwd(q, k, v, g, beta, dt, 0.0, s0, cu, B, T, H, K, V, N, o, odt, sT, None)
+
+
+def test_chunk_rejects_bad_arguments(lib):
+    assert chunk(lib, K=96) == UNSUPPORTED
+    assert chunk(lib, V=32) == UNSUPPORTED
+    assert chunk(lib, dt=7) == UNSUPPORTED
+    assert chunk(lib, odt=3) == UNSUPPORTED
+    assert chunk(lib, q=None) == INVALID_ARG
+    assert chunk(lib, o=None) == INVALID_ARG
+    assert chunk(lib, k=Pm) == INVALID_ARG
+    assert chunk(lib, T=-1) == INVALID_ARG
+    assert chunk(lib, H=0) == INVALID_ARG
+    assert chunk(lib, B=2, N=1) == INVALID_ARG          # N must equal B without cu_seqlens
+    assert chunk(lib, B=2, N=3, cu=P) == INVALID_ARG    # packed sequences need B == 1
+    assert chunk(lib, s0=ctypes.c_void_p(0x100000), sT=ctypes.c_void_p(0x100000 + 4096)) == INVALID_ARG
+
+
+def test_fused_rejects_bad_arguments(lib):
+    def fused(**kw):
+        a = dict(conv_act=0, lb=-5.0, eps=1e-6, cq=P, ck=P, cv=P, A=P, db=P, K=128)
+        a.update(kw)
+        return lib.kda_chunk_fwd_fused(P, P, P, P, P, 1, a["cq"], a["ck"], a["cv"], a["conv_act"], a["A"],
+                                       a["db"], a["lb"], a["eps"], 0.0, None, None, 1, 64, 2, a["K"], 128, 1,
+                                       P, 0, None, None)
+    assert fused(conv_act=2) == INVALID_ARG
+    assert fused(lb=1.0) == INVALID_ARG
+    assert fused(eps=-1.0) == INVALID_ARG
+    assert fused(A=None) == INVALID_ARG
+    assert fused(cv=Pm) == INVALID_ARG
+    assert fused(K=80) == UNSUPPORTED
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def step(**kw):
+        a = dict(q=P, st=P, N=4, H=2, K=128, V=128, dt=1)
+        a.update(kw)
+        return lib.kda_recurrent_step(a["q"], P, P, P, P, a["dt"], 0.0, a["st"], a["N"], a["H"], a["K"],
+                                      a["V"], P, 0, None)
+    assert step(K=100) == UNSUPPORTED
+    assert step(dt=5) == UNSUPPORTED
+    assert step(st=None) == INVALID_ARG
+    assert step(q=Pm) == INVALID_ARG
+    assert step(N=-1) == INVALID_ARG
+    assert step(N=0, q=None) == 0   # nothing to do
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    x = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
+    b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.chunk_fwd(x, x, x, x, b)
