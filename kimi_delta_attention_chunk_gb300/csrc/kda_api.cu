@@ -92,6 +92,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
     p.o = o;
     p.final_state = final_state;
     cudaStream_t st = (cudaStream_t)stream;
+    if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc(o_dtype, p, st));
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, false, p, st));
 }
 

@@ -37,6 +37,10 @@ struct ChunkParams {
 cudaError_t chunk_simt(kda_dtype in_dt, kda_dtype out_dt, int K, int V, bool prologue,
                        const ChunkParams& p, cudaStream_t st);
 
+// Tensor-core chunk kernel (bf16 inputs, K = V = 128).
+bool chunk_tc_supported(kda_dtype in_dt, int K, int V);
+cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+
 // Single-token decode.
 cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const void* q,
                         const void* k, const void* v, const void* g, const void* beta,
