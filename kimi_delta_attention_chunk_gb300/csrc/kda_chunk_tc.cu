@@ -6,9 +6,10 @@
 // cumulative log-decay per key channel; all products below are the chunk
 // algebra of the recurrence, see kda_chunk_simt.cu):
 //
-//   A, P   gated in-chunk products, per 16-token row block R with the decay
-//          reference at the block start:  D_R[j, r] = Rt_R[j] . L_R[r]
-//          (tcgen05, M = 64, N = 32: 16 rows of k and 16 of q)
+//   A, P   gated in-chunk products, per 32-token row block R with the decay
+//          reference at the block centre (so every factor is within e^{+-80}):
+//          D_R[i, j] = L_R[i] . Rt_R[j]   (tcgen05, M = 64: 32 rows of k and 32
+//          rows of q, N = 32 (R+1))
 //   T      = (I + Diag(beta) A)^{-1}, 16x16 block forward substitution (CUDA cores)
 //   W^T    = (k e^G)^T (T Diag(beta))^T,   U~^T = v^T (T Diag(beta))^T     (tcgen05)
 //   U^T    = U~^T - S^T W^T                                              (tcgen05, negated A)
@@ -19,9 +20,9 @@
 // split x = hi + lo into two bf16 values and multiplied as hi*hi + hi*lo +
 // lo*hi (about 16 significant bits); W and the correction W S use one bf16
 // term; v is exact in bf16.  Decay factors are running products of e^{g}
-// over exactly the tokens they span (values <= 1, or reciprocals of such
-// within one 16-token block, <= e^80 since g >= -5), so nothing overflows and
-// nothing cancels.
+// over exactly the tokens they span, built from per-16-token-block prefix
+// products (each >= e^-80 since g >= -5, so ratios inside a block are safe)
+// and block totals; nothing overflows and nothing cancels.
 //
 // Sources: "ISEEKYAN/k3" README (chunked KDA forward as the compute path);
 // "kimi-k3-mlx" review, "The A_log shape mismatch ..." (per-channel decay) and
@@ -40,24 +41,29 @@ constexpr int D = 128;  // K = V
 constexpr int NT = 256;
 
 // ---- shared memory map (bytes) ----------------------------------------------
-constexpr uint32_t SM_STG = 0;            // 64 KB: q | k | v | g tiles, [64 rows][128] bf16
-constexpr uint32_t SM_Q = SM_STG;
-constexpr uint32_t SM_K = SM_STG + 16384;
-constexpr uint32_t SM_V = SM_STG + 32768;
-constexpr uint32_t SM_G = SM_STG + 49152;
-constexpr uint32_t SM_QT = 65536;         // 32 KB: (q e^G) hi | lo, B operand [64 r][128 c]
-constexpr uint32_t SM_KB = 98304;         // 32 KB: (k e^{G_C-G})^T hi | lo, B operand [128 c][64 j]
-constexpr uint32_t SM_X = 131072;         // 48 KB union:
-constexpr uint32_t SM_RT = SM_X;          //   A/P phase: Rt_R hi | lo, A operand [64 j][128 c]
-constexpr uint32_t SM_LQ = SM_X + 32768;  //               L_R hi | lo, B operand [32][128 c]
-constexpr uint32_t SM_TB = SM_X;          //   later: (T Diag(beta)) hi | lo, B operand [64 r][64 j]
-constexpr uint32_t SM_PB = SM_X + 16384;  //          P hi | lo, B operand [64 r][64 j]
-constexpr uint32_t SM_WB = SM_X + 32768;  //          W hi, B operand [64 r][128 c]
-constexpr uint32_t SM_AF = 180224;        // 16 KB fp32 [64][64]: Diag(beta) A   (or e^g, first half)
-constexpr uint32_t SM_TF = 196608;        // 16 KB fp32 [64][64]: T               (or e^g, second half)
-constexpr uint32_t SM_E = SM_AF;          // 32 KB fp32 [64][128]: e^g during the build
-constexpr uint32_t SM_SMALL = 212992;     // beta[64], eGC[128], barriers, tmem base
-constexpr uint32_t SM_TOTAL = SM_SMALL + 1024;
+constexpr uint32_t SM_STG = 0;            // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
+constexpr uint32_t SM_OPA = 65536;        // 64 KB, A/P phase: L_R hi|lo (A op [64 i][128 c]), Rt_R hi|lo (B op)
+constexpr uint32_t SM_LA = SM_OPA;        //   then (q e^G) hi|lo (B op [64 r][128 c], K-major)
+constexpr uint32_t SM_RB = SM_OPA + 32768;//   and (k e^{G_C-G}) hi|lo (B op, MN-major: n = c, k = j)
+constexpr uint32_t SM_QT = SM_OPA;
+constexpr uint32_t SM_KB = SM_OPA + 32768;
+constexpr uint32_t SM_OPB = 131072;       // 48 KB:
+constexpr uint32_t SM_TB = SM_OPB;        //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
+constexpr uint32_t SM_PB = SM_OPB + 16384;//   P hi|lo, B op [64 r][64 j] K-major
+constexpr uint32_t SM_WB = SM_OPB + 32768;//   W hi, B op MN-major (n = r, k = c)
+constexpr uint32_t SM_PRE = 180224;       // fp32 [64][PRE_LD] in-block prefix products of e^g,
+constexpr int PRE_LD = 132;               //   later Diag(beta) A and T as fp32 [64][MAT_LD] each
+constexpr int MAT_LD = 68;
+constexpr uint32_t SM_AF = SM_PRE;
+constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
+constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
+constexpr uint32_t SM_TOT = SM_SMALL;     // fp32 [4][128] block totals of e^g
+constexpr uint32_t SM_BETA = SM_SMALL + 2048;   // fp32 [64]
+constexpr uint32_t SM_EGC = SM_BETA + 256;      // fp32 [128] e^{G_C}
+constexpr uint32_t SM_BAR = SM_EGC + 512;       // barriers, tmem base
+constexpr uint32_t SM_TOTAL = SM_BAR + 64;
+static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
+static_assert(SM_TOTAL + 1024 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
 constexpr uint32_t TM_S = 0;      // S^T fp32 [128 x][128 c]
@@ -70,7 +76,7 @@ constexpr uint32_t TM_KTH = TM_UH;
 constexpr uint32_t TM_KTL = TM_UL;
 constexpr uint32_t TM_AU = 352;   // U^T accumulator fp32 [128 x][64 r]
 constexpr uint32_t TM_AO = 416;   // O^T accumulator fp32 [128 x][64 r]   (alias: W^T [128 c][64 r])
-constexpr uint32_t TM_AP = 352;   // A/P accumulators, 4 x 32 columns, M = 64 layout (alias AU, AO)
+constexpr uint32_t TM_AP = 352;   // A/P accumulators (M = 64 layout): R=0 32 cols, R=1 64 cols
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t kWaitIter = 1u << 26;
@@ -82,11 +88,15 @@ __global__ void __launch_bounds__(NT, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
                 const ChunkParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte-swizzled TMA tiles need a 1024-byte aligned base
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float* beta_s = reinterpret_cast<float*>(smem + SM_SMALL);        // [64]
-    float* egc_s = beta_s + 64;                                       // [128]
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_SMALL + 1024 - 64);
+    float* beta_s = reinterpret_cast<float*>(smem + SM_BETA);   // [64]
+    float* egc_s = reinterpret_cast<float*>(smem + SM_EGC);     // [128]
+    float* tot_s = reinterpret_cast<float*>(smem + SM_TOT);     // [4][128]
+    float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
     int* flag_s = reinterpret_cast<int*>(bar_tma + 3);
@@ -130,9 +140,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         tc::bar_init_fence();
         *flag_s = 0;
     }
-    // zero the A/P right-factor operand once (rows beyond a block are never
-    // refreshed; they only reach accumulator rows that are not read)
-    for (int i = tid; i < 32768 / 16; i += NT) reinterpret_cast<uint4*>(smem + SM_RT)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
@@ -145,10 +152,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 
     auto issue_tma = [&](int64_t t0) {
         tc::bar_expect_tx(bar_tma, 4u * 16384u);
-        tc::tma_load_3d(smem + SM_Q, &mq, 0, h, (int)t0, bar_tma);
-        tc::tma_load_3d(smem + SM_K, &mk, 0, h, (int)t0, bar_tma);
-        tc::tma_load_3d(smem + SM_V, &mv, 0, h, (int)t0, bar_tma);
-        tc::tma_load_3d(smem + SM_G, &mg, 0, h, (int)t0, bar_tma);
+        const CUtensorMap* maps[4] = {&mq, &mk, &mv, &mg};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, h, (int)t0, bar_tma);
     };
     // Wait for the MMAs committed so far; all threads.
     auto mma_sync = [&]() {
@@ -185,10 +194,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         tc::tmem_st_wait();
     }
 
-    const uint32_t id_ap = tc::idesc_bf16(64, 32);
     const uint32_t id_n64 = tc::idesc_bf16(128, 64);
-    const uint32_t id_n64_neg = tc::idesc_bf16(128, 64, true);
-    const uint32_t id_n128 = tc::idesc_bf16(128, 128);
+    const uint32_t id_n64_neg_bmn = tc::idesc_bf16(128, 64, true, true);
+    const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
     const float scale = p.scale;
     TOut* __restrict__ o = reinterpret_cast<TOut*>(p.o);
     const __nv_bfloat16* __restrict__ beta_g = reinterpret_cast<const __nv_bfloat16*>(p.beta);
@@ -196,24 +204,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     // S hi/lo from the fp32 state in TMEM (lane x; warpgroup splits columns).
     auto s_epilogue = [&]() {
         const int cbeg = (warp >> 2) * 64;
-        for (int c0 = cbeg; c0 < cbeg + 64; c0 += 32) {
-            uint32_t a[16], b[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + c0, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + c0 + 16, b);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int cc = cbeg + 32 * half;
+            uint32_t a[32];
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, a + 16);
             tc::tmem_ld_wait();
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float x0 = __uint_as_float(i < 8 ? a[2 * i] : b[2 * i - 16]);
-                const float x1 = __uint_as_float(i < 8 ? a[2 * i + 1] : b[2 * i - 15]);
                 __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(x0, h0, l0);
-                tc::split_bf16(x1, h1, l1);
+                tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
+                tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
                 hi[i] = tc::pack_bf16(h0, h1);
                 lo[i] = tc::pack_bf16(l0, l1);
             }
-            tc::tmem_st16(tm + lane_base(warp) + TM_SH + c0 / 2, hi);
-            tc::tmem_st16(tm + lane_base(warp) + TM_SL + c0 / 2, lo);
+            tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
+            tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
         }
         tc::tmem_st_wait();
     };
@@ -228,128 +236,213 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         failed = __syncthreads_or(!ok);
         if (failed) break;
 
-        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + SM_Q);
-        const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(smem + SM_K);
-        const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(smem + SM_V);
-        const __nv_bfloat16* gs = reinterpret_cast<const __nv_bfloat16*>(smem + SM_G);
-        float* E = reinterpret_cast<float*>(smem + SM_E);  // [64][128]
-
-        // ---- build: decay factors and the chunk operands ------------------------
-        if (tid < 128) {
-            const int c = tid;
-            float gp = 1.f;
-            uint32_t kth[16], ktl[16];
-            for (int r = 0; r < C; ++r) {
-                const bool in = r < L;
-                const float e = in ? __expf(__bfloat162float(gs[r * D + c])) : 1.f;
-                E[r * D + c] = e;
-                gp *= e;
-                const float qv = in ? __bfloat162float(qs[r * D + c]) : 0.f;
-                const float kv = in ? __bfloat162float(ks[r * D + c]) : 0.f;
-                __nv_bfloat16 hi, lo;
-                tc::split_bf16(qv * gp, hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_QT + tc::kmaj(r, c, D)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_QT + 16384 + tc::kmaj(r, c, D)) = lo;
-                // (k e^G)^T: lane c, column pair r/2 of TMEM (flushed every 32 rows)
-                __nv_bfloat16 kh, kl;
-                tc::split_bf16(kv * gp, kh, kl);
-                const int slot = (r & 31) >> 1;
-                if ((r & 1) == 0) {
-                    kth[slot] = (uint32_t)__bfloat16_as_ushort(kh);
-                    ktl[slot] = (uint32_t)__bfloat16_as_ushort(kl);
-                } else {
-                    kth[slot] |= (uint32_t)__bfloat16_as_ushort(kh) << 16;
-                    ktl[slot] |= (uint32_t)__bfloat16_as_ushort(kl) << 16;
-                }
-                if ((r & 31) == 31) {
-                    tc::tmem_st16(tm + lane_base(warp) + TM_KTH + (r >> 5) * 16, kth);
-                    tc::tmem_st16(tm + lane_base(warp) + TM_KTL + (r >> 5) * 16, ktl);
-                }
-            }
-            egc_s[c] = gp;
-            // (k e^{G_C - G})^T: suffix products, row c of a [128 c][64 j] operand
-            float sfx = 1.f;
-            for (int j = C - 1; j >= 0; --j) {
-                const float kv = j < L ? __bfloat162float(ks[j * D + c]) : 0.f;
-                __nv_bfloat16 hi, lo;
-                tc::split_bf16(kv * sfx, hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_KB + tc::kmaj(c, j, C)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_KB + 16384 + tc::kmaj(c, j, C)) = lo;
-                sfx *= E[j * D + c];
-            }
-        } else {
-            // v^T into TMEM: lane x, bf16 pairs of consecutive tokens
-            const int x = tid - 128;
-            for (int j0 = 0; j0 < C; j0 += 32) {
-                uint32_t w[16];
+        const uint8_t* qs = smem + SM_STG;
+        const uint8_t* ks = smem + SM_STG + 16384;
+        const uint8_t* vs = smem + SM_STG + 32768;
+        const uint8_t* gs = smem + SM_STG + 49152;
+        auto ld_bf = [&](const uint8_t* t, int r, int c) {
+            return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(t + tc::swz128(r, c)));
+        };
+        // 8 consecutive channels [c, c+8) of row r as floats (0 for rows >= L)
+        auto ld8 = [&](const uint8_t* t, int r, int c, float* x) {
+            if (r < L) {
+                tc::unpack8(*reinterpret_cast<const uint4*>(t + tc::swz128(r, c)), x);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = j0 + 2 * i;
-                    const __nv_bfloat16 a = j < L ? vs[j * D + x] : __float2bfloat16(0.f);
-                    const __nv_bfloat16 b = j + 1 < L ? vs[(j + 1) * D + x] : __float2bfloat16(0.f);
-                    w[i] = tc::pack_bf16(a, b);
-                }
-                tc::tmem_st16(tm + lane_base(warp) + TM_VT + j0 / 2, w);
+                for (int i = 0; i < 8; ++i) x[i] = 0.f;
             }
-            if (x < C) beta_s[x] = x < L ? __bfloat162float(beta_g[(c0 + x) * H + h]) : 0.f;
+        };
+        auto ld_pre8 = [&](int r, int c, float* x) {
+            const float4 a = *reinterpret_cast<const float4*>(pre_s + r * PRE_LD + c);
+            const float4 b = *reinterpret_cast<const float4*>(pre_s + r * PRE_LD + c + 4);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        };
+        auto ld_tot8 = [&](int J, int c, float* x) {
+            const float4 a = *reinterpret_cast<const float4*>(tot_s + J * 128 + c);
+            const float4 b = *reinterpret_cast<const float4*>(tot_s + J * 128 + c + 4);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        };
+
+        // ---- (1) in-block prefix products of e^g, block totals --------------------
+        {
+            const int c = tid & 127, Ja = tid >> 7, Jb = Ja + 2;  // blocks Ja and Ja + 2 of channel c
+            float ga[16], gb[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int ra = 16 * Ja + u, rb = 16 * Jb + u;
+                ga[u] = ra < L ? ld_bf(gs, ra, c) : 0.f;
+                gb[u] = rb < L ? ld_bf(gs, rb, c) : 0.f;
+            }
+            float pa = 1.f, pb = 1.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                pa *= __expf(ga[u]);
+                pb *= __expf(gb[u]);
+                pre_s[(16 * Ja + u) * PRE_LD + c] = pa;
+                pre_s[(16 * Jb + u) * PRE_LD + c] = pb;
+            }
+            tot_s[Ja * 128 + c] = pa;
+            tot_s[Jb * 128 + c] = pb;
         }
-        tc::tmem_st_wait();
+        if (tid < C) beta_s[tid] = tid < L ? __bfloat162float(beta_g[(c0 + tid) * H + h]) : 0.f;
         __syncthreads();
 
-        // ---- A and P: four row blocks, reference at each block start -------------
-        for (int R = 0; R < 4; ++R) {
-            const int r0 = R * 16;
-            if (tid < 128) {
-                const int c = tid;
-                // block rows: left factors e^{sum g[r0..r]} and right factors e^{-sum g[r0..j]}
-                float pre = 1.f;
-                for (int j = r0; j < r0 + 16; ++j) {
-                    pre *= E[j * D + c];
-                    const bool in = j < L;
-                    const float kv = in ? __bfloat162float(ks[j * D + c]) : 0.f;
-                    const float qv = in ? __bfloat162float(qs[j * D + c]) : 0.f;
-                    __nv_bfloat16 hi, lo;
-                    tc::split_bf16(kv * pre, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_LQ + tc::kmaj(j - r0, c, D)) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_LQ + 8192 + tc::kmaj(j - r0, c, D)) = lo;
-                    tc::split_bf16(qv * pre, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_LQ + tc::kmaj(16 + j - r0, c, D)) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_LQ + 8192 + tc::kmaj(16 + j - r0, c, D)) = lo;
-                    tc::split_bf16(kv / pre, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_RT + tc::kmaj(j, c, D)) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_RT + 16384 + tc::kmaj(j, c, D)) = lo;
+        // Every build loop below gives a thread the same 8 channels [8 cg, 8 cg + 8).
+        const int cg = (tid >> 3) & 15;
+
+        // ---- (2) (k e^G)^T and v^T into TMEM (lane = channel / value column) ----
+        {
+            const int c = (warp & 3) * 32 + lane;
+            const int jb = (warp >> 2) * 32;
+            const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
+            const float pfx[4] = {1.f, t0v, t0v * t1v, t0v * t1v * t2v};
+            uint32_t kh[16], kl[16], vv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int j = jb + 2 * i;
+                const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
+                const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
+                __nv_bfloat16 h0, l0, h1, l1;
+                tc::split_bf16(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], h0, l0);
+                tc::split_bf16(k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], h1, l1);
+                kh[i] = tc::pack_bf16(h0, h1);
+                kl[i] = tc::pack_bf16(l0, l1);
+                const __nv_bfloat16 z = __float2bfloat16(0.f);
+                const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
+                const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
+                vv[i] = tc::pack_bf16(v0, v1);
+            }
+            tc::tmem_st16(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
+            tc::tmem_st16(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
+            tc::tmem_st16(tm + lane_base(warp) + TM_VT + jb / 2, vv);
+            if (tid < 128) egc_s[c] = t0v * t1v * t2v * tot_s[384 + c];
+        }
+        tc::tmem_st_wait();
+
+        // ---- (3) A and P: two 32-token row blocks, reference at the block centre --
+#pragma unroll
+        for (int R = 0; R < 2; ++R) {
+            const int nrows = 32 * (R + 1);  // columns j of this block's products
+            // L_R (A operand [64 i][128 c]): i < 32 k-rows, i >= 32 q-rows of block R;
+            // e^{G_r - G_mid} = pre_r / tot_{2R} before the centre, pre_r after it
+            float itc[8];
+            ld_tot8(2 * R, 8 * cg, itc);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) itc[u] = __frcp_rn(itc[u]);
+#pragma unroll 2
+            for (int kk = 0; kk < 4; ++kk) {
+                const int item = tid + NT * kk;
+                const int i = ((item >> 7) << 3) | (item & 7);
+                const int r = 32 * R + (i & 31);  // rows i in [16 kk, 16 kk + 16)
+                float x[8], pr[8], f[8];
+                ld8(kk < 2 ? ks : qs, r, 8 * cg, x);
+                ld_pre8(r, 8 * cg, pr);
+                const bool first = (kk & 1) == 0;  // r in the first 16-token block of R
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = x[u] * (first ? pr[u] * itc[u] : pr[u]);
+                uint4 hi, lo;
+                tc::split8(f, hi, lo);
+                *reinterpret_cast<uint4*>(smem + SM_LA + tc::kmaj(i, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_LA + 16384 + tc::kmaj(i, 8 * cg, D)) = lo;
+            }
+            // Rt_R (B operand [nrows j][128 c]): e^{G_mid - G_j} k_j =
+            //   1 / pre_j after the centre, tot_J / pre_j * prod_{J < J2 <= 2R} tot_J2 before it
+#pragma unroll 2
+            for (int kk = 0; kk < 4; ++kk) {
+                if (kk >= nrows / 16) break;
+                const int item = tid + NT * kk;
+                const int j = ((item >> 7) << 3) | (item & 7);
+                const int J = kk;  // j in [16 kk, 16 kk + 16)
+                float x[8], pr[8], m[8], t[8];
+                ld8(ks, j, 8 * cg, x);
+                ld_pre8(j, 8 * cg, pr);
+                // in-block ratio first (in (0, 1], or 1/pre_j <= e^80 after the centre),
+                // then the totals of the later blocks: every intermediate lies between 1
+                // and the true factor, so nothing underflows that the result needs
+                if (J == 2 * R + 1) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) m[u] = __frcp_rn(pr[u]);
+                } else {
+                    ld_tot8(J, 8 * cg, t);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) m[u] = __fdividef(t[u], pr[u]);
                 }
-                // earlier rows: right factor e^{sum g[j+1 .. r0-1]} <= 1
-                float sfx = 1.f;
-                for (int j = r0 - 1; j >= 0; --j) {
-                    const float kv = j < L ? __bfloat162float(ks[j * D + c]) : 0.f;
-                    __nv_bfloat16 hi, lo;
-                    tc::split_bf16(kv * sfx, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_RT + tc::kmaj(j, c, D)) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(smem + SM_RT + 16384 + tc::kmaj(j, c, D)) = lo;
-                    sfx *= E[j * D + c];
+                for (int J2 = J + 1; J2 <= 2 * R; ++J2) {
+                    ld_tot8(J2, 8 * cg, t);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) m[u] *= t[u];
                 }
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = x[u] * m[u];
+                uint4 hi, lo;
+                tc::split8(f, hi, lo);
+                *reinterpret_cast<uint4*>(smem + SM_RB + tc::kmaj(j, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_RB + 16384 + tc::kmaj(j, 8 * cg, D)) = lo;
             }
             publish();
             if (tid == 0) {
-                const uint32_t rt = tc::smem_u32(smem + SM_RT), lq = tc::smem_u32(smem + SM_LQ);
+                const uint32_t la = tc::smem_u32(smem + SM_LA), rb = tc::smem_u32(smem + SM_RB);
                 const uint32_t d = tm + TM_AP + 32 * R;
-                int acc = 0;
+                const uint32_t id = R == 0 ? tc::idesc_bf16(64, 32) : tc::idesc_bf16(64, 64);
                 for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                    const uint64_t ah = tc::sdesc(rt + ks_ * 256, 128, D * 16);
-                    const uint64_t al = tc::sdesc(rt + 16384 + ks_ * 256, 128, D * 16);
-                    const uint64_t bh = tc::sdesc(lq + ks_ * 256, 128, D * 16);
-                    const uint64_t bl = tc::sdesc(lq + 8192 + ks_ * 256, 128, D * 16);
-                    tc::mma_ss(d, ah, bh, id_ap, acc);
-                    acc = 1;
-                    tc::mma_ss(d, ah, bl, id_ap, 1);
-                    tc::mma_ss(d, al, bh, id_ap, 1);
+                    const uint64_t ah = tc::sdesc(la + ks_ * 256, 128, D * 16);
+                    const uint64_t al = tc::sdesc(la + 16384 + ks_ * 256, 128, D * 16);
+                    const uint64_t bh = tc::sdesc(rb + ks_ * 256, 128, D * 16);
+                    const uint64_t bl = tc::sdesc(rb + 16384 + ks_ * 256, 128, D * 16);
+                    tc::mma_ss(d, ah, bh, id, ks_ > 0);
+                    tc::mma_ss(d, ah, bl, id, 1);
+                    tc::mma_ss(d, al, bh, id, 1);
                 }
                 tc::commit(bar_mma);
             }
             mma_sync();
+            if (failed) break;
         }
         if (failed) break;
+
+        // ---- (4) (q e^G) (K-major) and (k e^{G_C - G})^T (MN-major) operands -------
+        {
+#pragma unroll 2
+            for (int kk = 0; kk < 4; ++kk) {
+                const int item = tid + NT * kk;
+                const int r = ((item >> 7) << 3) | (item & 7);
+                const int J = kk;  // r in [16 kk, 16 kk + 16)
+                // products of the block totals before (pf) and after (sf) block J
+                float pf[8], sf[8], tj[8], t[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { pf[u] = 1.f; sf[u] = 1.f; }
+                for (int J2 = 0; J2 < 4; ++J2) {
+                    ld_tot8(J2, 8 * cg, t);
+                    if (J2 == J) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) tj[u] = t[u];
+                    } else if (J2 < J) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) pf[u] *= t[u];
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) sf[u] *= t[u];
+                    }
+                }
+                float q[8], k[8], pr[8], fq[8], fk[8];
+                ld8(qs, r, 8 * cg, q);
+                ld8(ks, r, 8 * cg, k);
+                ld_pre8(r, 8 * cg, pr);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    fq[u] = q[u] * (pf[u] * pr[u]);
+                    fk[u] = k[u] * (sf[u] * __fdividef(tj[u], pr[u]));
+                }
+                uint4 hi, lo;
+                tc::split8(fq, hi, lo);
+                *reinterpret_cast<uint4*>(smem + SM_QT + tc::kmaj(r, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_QT + 16384 + tc::kmaj(r, 8 * cg, D)) = lo;
+                tc::split8(fk, hi, lo);
+                *reinterpret_cast<uint4*>(smem + SM_KB + tc::mnmaj(8 * cg, r, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_KB + 16384 + tc::mnmaj(8 * cg, r, D)) = lo;
+            }
+        }
 
         // staging is consumed: prefetch the next chunk into it
         tc::fence_async_smem();
@@ -359,84 +452,134 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             tma_pending = true;
         }
 
-        // ---- A/P out of TMEM: Diag(beta) A -> fp32, P -> hi/lo operand ----------
+        // ---- (5) A/P out of TMEM: Diag(beta) A -> fp32, P -> hi/lo operand ---------
         {
-            float* Af = reinterpret_cast<float*>(smem + SM_AF);  // [64 r][64 j]
-            const int quad = warp & 3;
-            const int j = quad * 16 + (lane & 15);
-            for (int R = (warp >> 2) * 2; R < (warp >> 2) * 2 + 2; ++R) {
-                uint32_t a[16], b[16];
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R, a);
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 16, b);
-                tc::tmem_ld_wait();
-                if (lane < 16) {
+            float* Af = reinterpret_cast<float*>(smem + SM_AF);  // [64 r][MAT_LD]
+            const int R = warp >> 2;                          // warpgroup R reads block R
+            const int i = (warp & 3) * 16 + (lane & 15);      // M = 64 row held by this lane
+            const bool is_q = i >= 32;
+            const int r = 32 * R + (i & 31);
+            uint32_t a[64];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int r = 16 * R + i;
-                        const float av = __uint_as_float(a[i]);
-                        const float pv = __uint_as_float(b[i]);
-                        Af[r * C + j] = (j < r) ? beta_s[r] * av : 0.f;
-                        __nv_bfloat16 hi, lo;
-                        tc::split_bf16(j <= r ? pv : 0.f, hi, lo);
-                        *reinterpret_cast<__nv_bfloat16*>(smem + SM_PB + tc::kmaj(r, j, C)) = hi;
-                        *reinterpret_cast<__nv_bfloat16*>(smem + SM_PB + 8192 + tc::kmaj(r, j, C)) = lo;
+            for (int u = 0; u < 64; ++u) a[u] = 0u;
+            tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 16, a + 16);
+            if (R == 1) {
+                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 32, a + 32);
+                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 48, a + 48);
+            }
+            tc::tmem_ld_wait();
+            if (lane < 16) {
+                const float br = beta_s[r];
+#pragma unroll
+                for (int j0 = 0; j0 < 64; j0 += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 + u;
+                        const float x = __uint_as_float(a[j]);
+                        v[u] = is_q ? (j <= r ? x : 0.f) : (j < r ? br * x : 0.f);
+                    }
+                    if (is_q) {
+                        uint4 hi, lo;
+                        tc::split8(v, hi, lo);
+                        *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, j0, C)) = hi;
+                        *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, j0, C)) = lo;
+                    } else {
+                        *reinterpret_cast<float4*>(Af + r * MAT_LD + j0) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
                     }
                 }
             }
         }
         __syncthreads();
 
-        // ---- T = (I + Diag(beta) A)^{-1} ----------------------------------------
+        // ---- (6) T = (I + Diag(beta) A)^{-1} ----------------------------------------
         {
             const float* N = reinterpret_cast<const float*>(smem + SM_AF);
             float* T = reinterpret_cast<float*>(smem + SM_TF);
-            float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch [4][16][16]
-            for (int i = tid; i < C * C; i += NT) T[i] = (i / C == i % C) ? 1.f : 0.f;
-            __syncthreads();
-            // diagonal blocks: forward substitution, four lanes per column
+            float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch [3][16][16]
+            // zero the strictly upper blocks (the others are all written below)
+            for (int e = tid; e < 6 * 64; e += NT) {
+                const int blk = e >> 6, rr = (e >> 2) & 15, q4 = e & 3;
+                const int R = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                *reinterpret_cast<float4*>(T + (16 * R + rr) * MAT_LD + 16 * J + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            // diagonal blocks: forward substitution with the column in registers;
+            // warp w: block w/2, columns 8 (w%2) .. + 8; lane: column lane/4, rows = lane%4 (mod 4)
             {
-                const int blk = tid >> 6, col = (tid & 63) >> 2, part = tid & 3;
+                const int blk = warp >> 1, col = 8 * (warp & 1) + (lane >> 2), part = lane & 3;
                 const int i = 16 * blk + col;
+                float x[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) x[m] = (part + 4 * m == col) ? 1.f : 0.f;
+                const float* nb = N + 16 * blk * MAT_LD + 16 * blk;
+#pragma unroll
                 for (int rr = 1; rr < 16; ++rr) {
-                    const int r = 16 * blk + rr;
                     float acc = 0.f;
-                    if (rr > col)
-                        for (int jj = col + part; jj < rr; jj += 4) acc += N[r * C + 16 * blk + jj] * T[(16 * blk + jj) * C + i];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (part + 4 * m < rr) acc += nb[rr * MAT_LD + part + 4 * m] * x[m];
                     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                    if (part == 0 && rr > col) T[r * C + i] = -acc;
-                    __syncwarp();
+                    if (part == (rr & 3) && rr > col) x[rr >> 2] = -acc;
                 }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) T[(16 * blk + part + 4 * m) * MAT_LD + i] = x[m];
             }
             __syncthreads();
             // off-diagonal blocks by distance d = R - J:
             //   Y = sum_{M=J}^{R-1} N_{R,M} T_{M,J};   T_{R,J} = -T_{R,R} Y
+            // one thread per (J, row a, 4 columns)
             for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                for (int e = tid; e < nb * 256; e += NT) {
-                    const int J = e >> 8, a = (e >> 4) & 15, b = e & 15;
-                    const int R = J + d;
-                    float acc = 0.f;
-                    for (int m = 16 * J + b; m < 16 * R; ++m) acc += N[(16 * R + a) * C + m] * T[m * C + 16 * J + b];
-                    Y[e] = acc;
+                const int nitem = (4 - d) * 64;
+                const int J = tid >> 6, a = (tid >> 2) & 15, b4 = tid & 3;
+                const int R = J + d;
+                if (tid < nitem) {
+                    const float* nrow = N + (16 * R + a) * MAT_LD;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int m4 = 4 * J; m4 < 4 * R; ++m4) {
+                        const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
+                        const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float4 t = *reinterpret_cast<const float4*>(T + (4 * m4 + u) * MAT_LD + 16 * J + 4 * b4);
+                            acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
+                        }
+                    }
+                    *reinterpret_cast<float4*>(Y + (J << 8) + (a << 4) + 4 * b4) = acc;
                 }
                 __syncthreads();
-                for (int e = tid; e < nb * 256; e += NT) {
-                    const int J = e >> 8, a = (e >> 4) & 15, b = e & 15;
-                    const int R = J + d;
-                    float acc = 0.f;
-                    for (int m = 0; m <= a; ++m) acc += T[(16 * R + a) * C + 16 * R + m] * Y[(J << 8) + (m << 4) + b];
-                    T[(16 * R + a) * C + 16 * J + b] = -acc;
+                if (tid < nitem) {
+                    const float* trow = T + (16 * R + a) * MAT_LD + 16 * R;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float tv = trow[m];
+                        const float4 y = *reinterpret_cast<const float4*>(Y + (J << 8) + (m << 4) + 4 * b4);
+                        acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
+                    }
+                    *reinterpret_cast<float4*>(T + (16 * R + a) * MAT_LD + 16 * J + 4 * b4) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
                 __syncthreads();
             }
-            // T Diag(beta) -> hi/lo B operand [64 r][64 j]
-            for (int e = tid; e < C * C; e += NT) {
-                const int r = e >> 6, j = e & 63;
-                __nv_bfloat16 hi, lo;
-                tc::split_bf16(T[e] * beta_s[j], hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_TB + tc::kmaj(r, j, C)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_TB + 8192 + tc::kmaj(r, j, C)) = lo;
+            // T Diag(beta) -> hi/lo B operand [64 r][64 j], K-major
+            for (int item = tid; item < 64 * 8; item += NT) {
+                const int r = ((item >> 6) << 3) | (item & 7);
+                const int jg = (item >> 3) & 7;
+                float t[8];
+                // (jg is the same for both items of a thread)
+                const float4 a = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg);
+                const float4 b = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg + 4);
+                t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t[u] *= beta_s[8 * jg + u];
+                uint4 hi, lo;
+                tc::split8(t, hi, lo);
+                *reinterpret_cast<uint4*>(smem + SM_TB + tc::kmaj(r, 8 * jg, C)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_TB + 8192 + tc::kmaj(r, 8 * jg, C)) = lo;
             }
         }
         publish();
@@ -457,7 +600,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         }
         mma_sync();
 
-        // ---- W out of TMEM into the B operand [64 r][128 c] --------------------
+        // ---- W out of TMEM into the B operand (MN-major: n = r, k = c) ----------
         {
             const int c = (warp & 3) * 32 + lane;
             const int rb = (warp >> 2) * 32;
@@ -466,9 +609,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb + 16, b);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float w = __uint_as_float(i < 16 ? a[i] : b[i - 16]);
-                *reinterpret_cast<__nv_bfloat16*>(smem + SM_WB + tc::kmaj(rb + i, c, D)) = __float2bfloat16_rn(w);
+            for (int g8 = 0; g8 < 4; ++g8) {
+                float w[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = 8 * g8 + u;
+                    w[u] = __uint_as_float(i < 16 ? a[i] : b[i - 16]);
+                }
+                *reinterpret_cast<uint4*>(smem + SM_WB + tc::mnmaj(rb + 8 * g8, c, C)) = tc::pack8(w);
             }
         }
         publish();
@@ -478,7 +626,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             const uint32_t wb = tc::smem_u32(smem + SM_WB), qt = tc::smem_u32(smem + SM_QT);
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
                 const uint32_t sh = tm + TM_SH + ks_ * 8, sl = tm + TM_SL + ks_ * 8;
-                tc::mma_ts(tm + TM_AU, sh, tc::sdesc(wb + ks_ * 256, 128, D * 16), id_n64_neg, 1);
+                tc::mma_ts(tm + TM_AU, sh, tc::sdesc(wb + ks_ * 2 * C * 16, C * 16, 128), id_n64_neg_bmn, 1);
                 const uint64_t qh = tc::sdesc(qt + ks_ * 256, 128, D * 16);
                 const uint64_t ql = tc::sdesc(qt + 16384 + ks_ * 256, 128, D * 16);
                 tc::mma_ts(tm + TM_AO, sh, qh, id_n64, ks_ > 0);
@@ -532,11 +680,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 tc::mma_ts(tm + TM_AO, uh, ph, id_n64, 1);
                 tc::mma_ts(tm + TM_AO, uh, pl, id_n64, 1);
                 tc::mma_ts(tm + TM_AO, ul, ph, id_n64, 1);
-                const uint64_t kh = tc::sdesc(kb + ks_ * 256, 128, C * 16);
-                const uint64_t kl = tc::sdesc(kb + 16384 + ks_ * 256, 128, C * 16);
-                tc::mma_ts(tm + TM_S, uh, kh, id_n128, 1);
-                tc::mma_ts(tm + TM_S, uh, kl, id_n128, 1);
-                tc::mma_ts(tm + TM_S, ul, kh, id_n128, 1);
+                const uint64_t kh = tc::sdesc(kb + ks_ * 2 * D * 16, D * 16, 128);
+                const uint64_t kl = tc::sdesc(kb + 16384 + ks_ * 2 * D * 16, D * 16, 128);
+                tc::mma_ts(tm + TM_S, uh, kh, id_n128_bmn, 1);
+                tc::mma_ts(tm + TM_S, uh, kl, id_n128_bmn, 1);
+                tc::mma_ts(tm + TM_S, ul, kh, id_n128_bmn, 1);
             }
             tc::commit(bar_mma);
         }
@@ -604,16 +752,16 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows][H][128] bf16 tensor, box = 64 rows of one head.
+// [rows][H][128] bf16 tensor; box = 64 rows x 64 channels of one head, 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -628,9 +776,10 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
         !make_map(&mv, p.v, map_rows, p.H) || !make_map(&mg, p.g, map_rows, p.H))
         return cudaErrorInvalidValue;
     auto kern = chunk_tc_kernel<TOut>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_TOTAL);
+    const int smem_bytes = (int)SM_TOTAL + 1024;  // + alignment slack
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)blocks, NT, SM_TOTAL, st>>>(mq, mk, mv, mg, p);
+    kern<<<(unsigned)blocks, NT, smem_bytes, st>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
 }
 

@@ -26,10 +26,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 
 // Instruction descriptor, kind::f16 with bf16 operands and fp32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool neg_a = false) {
+// b_mn: B operand stored MN-major (N contiguous) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool neg_a = false, bool b_mn = false) {
     return (1u << 4)                      // D = f32
            | (1u << 7) | (1u << 10)       // A, B = bf16
            | ((neg_a ? 1u : 0u) << 13)    // negate A
+           | ((b_mn ? 1u : 0u) << 16)     // B major-ness
            | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -140,6 +142,43 @@ __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 even, __nv_bfloat16 
 // columns of 16-bit elements: core matrices 128 B, LBO = 128, SBO = Kd * 16.
 __device__ __forceinline__ uint32_t kmaj(int row, int k, int Kd) {
     return (uint32_t)((row >> 3) * (Kd * 16) + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+// Byte offset of element (n, k) in an MN-major, no-swizzle operand with Nd
+// rows along N: a core matrix is 8 k-rows of 8 consecutive n (16 B);
+// SBO = 128 (next 8 n), LBO = Nd * 16 (next 8 k).
+__device__ __forceinline__ uint32_t mnmaj(int n, int k, int Nd) {
+    return (uint32_t)((k >> 3) * (Nd * 16) + (n >> 3) * 128 + (k & 7) * 16 + (n & 7) * 2);
+}
+
+// Element (r, c) of a [rows][128] bf16 tile loaded by TMA as two 64-column
+// boxes with the 128-byte swizzle: 16-byte chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+    return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c >> 3) & 7) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+    uint4 u;
+    u.x = pack_bf16(__float2bfloat16_rn(x[0]), __float2bfloat16_rn(x[1]));
+    u.y = pack_bf16(__float2bfloat16_rn(x[2]), __float2bfloat16_rn(x[3]));
+    u.z = pack_bf16(__float2bfloat16_rn(x[4]), __float2bfloat16_rn(x[5]));
+    u.w = pack_bf16(__float2bfloat16_rn(x[6]), __float2bfloat16_rn(x[7]));
+    return u;
+}
+// 8 values -> 16 bytes of bf16 hi and 16 bytes of bf16 lo (x = hi + lo)
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+    float l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l[i] = x[i] - __bfloat162float(__float2bfloat16_rn(x[i]));
+    hi = pack8(x);
+    lo = pack8(l);
+}
+__device__ __forceinline__ void unpack8(uint4 u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
 }
 
 }  // namespace tc
