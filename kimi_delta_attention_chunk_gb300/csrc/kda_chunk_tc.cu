@@ -38,16 +38,17 @@ namespace {
 
 constexpr int C = 64;
 constexpr int D = 128;  // K = V
-constexpr int NT = 256;
+constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TMEM lanes
 
 // ---- shared memory map (bytes) ----------------------------------------------
 constexpr uint32_t SM_STG = 0;            // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
-constexpr uint32_t SM_OPA = 65536;        // 64 KB, A/P phase: L_R hi|lo (A op [64 i][128 c]), Rt_R hi|lo (B op)
-constexpr uint32_t SM_LA = SM_OPA;        //   then (q e^G) hi|lo (B op [64 r][128 c], K-major)
-constexpr uint32_t SM_RB = SM_OPA + 32768;//   and (k e^{G_C-G}) hi|lo (B op, MN-major: n = c, k = j)
+constexpr uint32_t SM_OPA = 65536;        // 64 KB, A/P phase: row block 1's L hi|lo (A op [64 i][128 c])
+                                          //   and Rt hi|lo (B op [64 j][128 c]); then
+                                          //   (q e^G) hi|lo (B op [64 r][128 c], K-major) and
+                                          //   (k e^{G_C-G}) hi|lo (B op, MN-major: n = c, k = j)
 constexpr uint32_t SM_QT = SM_OPA;
 constexpr uint32_t SM_KB = SM_OPA + 32768;
-constexpr uint32_t SM_OPB = 131072;       // 48 KB:
+constexpr uint32_t SM_OPB = 131072;       // 48 KB, A/P phase: row block 0's L hi|lo and Rt hi|lo (32 rows); then
 constexpr uint32_t SM_TB = SM_OPB;        //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
 constexpr uint32_t SM_PB = SM_OPB + 16384;//   P hi|lo, B op [64 r][64 j] K-major
 constexpr uint32_t SM_WB = SM_OPB + 32768;//   W hi, B op MN-major (n = r, k = c)
@@ -57,10 +58,14 @@ constexpr int MAT_LD = 68;
 constexpr uint32_t SM_AF = SM_PRE;
 constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
 constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
+// A/P operands of row block R: L (A, [64 i][128 c]) and Rt (B, [32 (R+1) j][128 c]), hi then lo
+__host__ __device__ constexpr uint32_t sm_l(int R) { return R == 0 ? SM_OPB : SM_OPA; }
+__host__ __device__ constexpr uint32_t sm_rt(int R) { return R == 0 ? SM_OPB + 32768 : SM_OPA + 32768; }
+__host__ __device__ constexpr uint32_t rt_lo(int R) { return R == 0 ? 8192 : 16384; }
 constexpr uint32_t SM_TOT = SM_SMALL;     // fp32 [4][128] block totals of e^g
 constexpr uint32_t SM_BETA = SM_SMALL + 2048;   // fp32 [64]
 constexpr uint32_t SM_EGC = SM_BETA + 256;      // fp32 [128] e^{G_C}
-constexpr uint32_t SM_BAR = SM_EGC + 512;       // barriers, tmem base
+constexpr uint32_t SM_BAR = SM_EGC + 512;       // barriers (tma, mma, w), tmem base, flag
 constexpr uint32_t SM_TOTAL = SM_BAR + 64;
 static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
 static_assert(SM_TOTAL + 1024 <= 232448, "shared memory");
@@ -98,8 +103,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
-    int* flag_s = reinterpret_cast<int*>(bar_tma + 3);
+    uint64_t* bar_w = bar_tma + 2;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    int* flag_s = reinterpret_cast<int*>(bar_tma + 4);
 
     const int H = p.H;
     const int h = blockIdx.x % H;
@@ -137,6 +143,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     if (tid == 0) {
         tc::bar_init(bar_tma, 1);
         tc::bar_init(bar_mma, 1);
+        tc::bar_init(bar_w, 1);
         tc::bar_init_fence();
         *flag_s = 0;
     }
@@ -146,7 +153,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     tc::fence_after();
     const uint32_t tm = *tmem_base_s;
 
-    uint32_t tma_phase = 0, mma_phase = 0;
+    uint32_t tma_phase = 0, mma_phase = 0, w_phase = 0;
     bool failed = false;
     bool tma_pending = false;  // a tile load was issued and not yet waited for
 
@@ -160,12 +167,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, h, (int)t0, bar_tma);
     };
     // Wait for the MMAs committed so far; all threads.
-    auto mma_sync = [&]() {
-        const bool ok = tc::bar_wait(bar_mma, mma_phase, kWaitIter);
-        mma_phase ^= 1;
+    // One warp polls the barrier; the others park at the CTA barrier, so 16
+    // spinning warps do not compete with the tensor core for shared memory.
+    auto wait_one = [&](uint64_t* bar, uint32_t& phase) {
+        bool ok = true;
+        if (warp == 0) ok = tc::bar_wait(bar, phase, kWaitIter);
+        phase ^= 1;
         failed = __syncthreads_or(failed || !ok);
         tc::fence_after();
     };
+    auto mma_sync = [&]() { wait_one(bar_mma, mma_phase); };
     // Make generic-proxy smem writes and TMEM stores visible to the MMA issuer.
     auto publish = [&]() {
         tc::fence_async_smem();
@@ -183,8 +194,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
     {
         const int x = (warp & 3) * 32 + lane;
-        const int cbeg = (warp >> 2) * 64;  // warpgroup 0: c in [0,64), warpgroup 1: [64,128)
-        for (int cc = cbeg; cc < cbeg + 64; cc += 16) {
+        const int cbeg = (warp >> 2) * 32;  // warpgroup w covers c in [32 w, 32 w + 32)
+        for (int cc = cbeg; cc < cbeg + 32; cc += 16) {
             uint32_t r[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -203,26 +214,22 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 
     // S hi/lo from the fp32 state in TMEM (lane x; warpgroup splits columns).
     auto s_epilogue = [&]() {
-        const int cbeg = (warp >> 2) * 64;
+        const int cc = (warp >> 2) * 32;
+        uint32_t a[32];
+        tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, a);
+        tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, a + 16);
+        tc::tmem_ld_wait();
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int cc = cbeg + 32 * half;
-            uint32_t a[32];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, a + 16);
-            tc::tmem_ld_wait();
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
-                tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
-                hi[i] = tc::pack_bf16(h0, h1);
-                lo[i] = tc::pack_bf16(l0, l1);
-            }
-            tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
-            tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
+        for (int i = 0; i < 16; ++i) {
+            __nv_bfloat16 h0, l0, h1, l1;
+            tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
+            tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
+            hi[i] = tc::pack_bf16(h0, h1);
+            lo[i] = tc::pack_bf16(l0, l1);
         }
+        tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
+        tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
         tc::tmem_st_wait();
     };
     s_epilogue();
@@ -230,10 +237,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     for (int64_t c0 = bos; c0 < eos && !failed; c0 += C) {
         const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
         // ---- wait for this chunk's tiles ------------------------------------
-        const bool ok = tc::bar_wait(bar_tma, tma_phase, kWaitIter);
-        tma_phase ^= 1;
+        wait_one(bar_tma, tma_phase);
         tma_pending = false;
-        failed = __syncthreads_or(!ok);
         if (failed) break;
 
         const uint8_t* qs = smem + SM_STG;
@@ -265,24 +270,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 
         // ---- (1) in-block prefix products of e^g, block totals --------------------
         {
-            const int c = tid & 127, Ja = tid >> 7, Jb = Ja + 2;  // blocks Ja and Ja + 2 of channel c
-            float ga[16], gb[16];
+            const int c = tid & 127, J = tid >> 7;  // block J of channel c
+            float gv[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) gv[u] = 16 * J + u < L ? ld_bf(gs, 16 * J + u, c) : 0.f;
+            float run = 1.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int ra = 16 * Ja + u, rb = 16 * Jb + u;
-                ga[u] = ra < L ? ld_bf(gs, ra, c) : 0.f;
-                gb[u] = rb < L ? ld_bf(gs, rb, c) : 0.f;
+                run *= __expf(gv[u]);
+                pre_s[(16 * J + u) * PRE_LD + c] = run;
             }
-            float pa = 1.f, pb = 1.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                pa *= __expf(ga[u]);
-                pb *= __expf(gb[u]);
-                pre_s[(16 * Ja + u) * PRE_LD + c] = pa;
-                pre_s[(16 * Jb + u) * PRE_LD + c] = pb;
-            }
-            tot_s[Ja * 128 + c] = pa;
-            tot_s[Jb * 128 + c] = pb;
+            tot_s[J * 128 + c] = run;
         }
         if (tid < C) beta_s[tid] = tid < L ? __bfloat162float(beta_g[(c0 + tid) * H + h]) : 0.f;
         __syncthreads();
@@ -293,12 +291,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         // ---- (2) (k e^G)^T and v^T into TMEM (lane = channel / value column) ----
         {
             const int c = (warp & 3) * 32 + lane;
-            const int jb = (warp >> 2) * 32;
+            const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
             const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
             const float pfx[4] = {1.f, t0v, t0v * t1v, t0v * t1v * t2v};
-            uint32_t kh[16], kl[16], vv[16];
+            uint32_t kh[8], kl[8], vv[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const int j = jb + 2 * i;
                 const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
                 const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
@@ -312,14 +310,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
                 vv[i] = tc::pack_bf16(v0, v1);
             }
-            tc::tmem_st16(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
-            tc::tmem_st16(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
-            tc::tmem_st16(tm + lane_base(warp) + TM_VT + jb / 2, vv);
+            tc::tmem_st8(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
+            tc::tmem_st8(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
+            tc::tmem_st8(tm + lane_base(warp) + TM_VT + jb / 2, vv);
             if (tid < 128) egc_s[c] = t0v * t1v * t2v * tot_s[384 + c];
         }
         tc::tmem_st_wait();
 
         // ---- (3) A and P: two 32-token row blocks, reference at the block centre --
+        // Both blocks' operands are built first (block 0 in OPB, block 1 in OPA),
+        // then all their MMAs go out in one round.
 #pragma unroll
         for (int R = 0; R < 2; ++R) {
             const int nrows = 32 * (R + 1);  // columns j of this block's products
@@ -329,30 +329,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             ld_tot8(2 * R, 8 * cg, itc);
 #pragma unroll
             for (int u = 0; u < 8; ++u) itc[u] = __frcp_rn(itc[u]);
-#pragma unroll 2
-            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
                 const int item = tid + NT * kk;
                 const int i = ((item >> 7) << 3) | (item & 7);
-                const int r = 32 * R + (i & 31);  // rows i in [16 kk, 16 kk + 16)
+                const int r = 32 * R + (i & 31);
                 float x[8], pr[8], f[8];
-                ld8(kk < 2 ? ks : qs, r, 8 * cg, x);
+                ld8(i < 32 ? ks : qs, r, 8 * cg, x);
                 ld_pre8(r, 8 * cg, pr);
-                const bool first = (kk & 1) == 0;  // r in the first 16-token block of R
+                const bool first = (i & 16) == 0;  // r in the first 16-token block of R
 #pragma unroll
                 for (int u = 0; u < 8; ++u) f[u] = x[u] * (first ? pr[u] * itc[u] : pr[u]);
                 uint4 hi, lo;
                 tc::split8(f, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_LA + tc::kmaj(i, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_LA + 16384 + tc::kmaj(i, 8 * cg, D)) = lo;
+                *reinterpret_cast<uint4*>(smem + sm_l(R) + tc::kmaj(i, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + sm_l(R) + 16384 + tc::kmaj(i, 8 * cg, D)) = lo;
             }
             // Rt_R (B operand [nrows j][128 c]): e^{G_mid - G_j} k_j =
             //   1 / pre_j after the centre, tot_J / pre_j * prod_{J < J2 <= 2R} tot_J2 before it
-#pragma unroll 2
-            for (int kk = 0; kk < 4; ++kk) {
-                if (kk >= nrows / 16) break;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
                 const int item = tid + NT * kk;
+                if (item >= nrows * 16) break;
                 const int j = ((item >> 7) << 3) | (item & 7);
-                const int J = kk;  // j in [16 kk, 16 kk + 16)
+                const int J = j >> 4;
                 float x[8], pr[8], m[8], t[8];
                 ld8(ks, j, 8 * cg, x);
                 ld_pre8(j, 8 * cg, pr);
@@ -377,37 +377,45 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 for (int u = 0; u < 8; ++u) f[u] = x[u] * m[u];
                 uint4 hi, lo;
                 tc::split8(f, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_RB + tc::kmaj(j, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_RB + 16384 + tc::kmaj(j, 8 * cg, D)) = lo;
+                *reinterpret_cast<uint4*>(smem + sm_rt(R) + tc::kmaj(j, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + sm_rt(R) + rt_lo(R) + tc::kmaj(j, 8 * cg, D)) = lo;
             }
-            publish();
-            if (tid == 0) {
-                const uint32_t la = tc::smem_u32(smem + SM_LA), rb = tc::smem_u32(smem + SM_RB);
-                const uint32_t d = tm + TM_AP + 32 * R;
-                const uint32_t id = R == 0 ? tc::idesc_bf16(64, 32) : tc::idesc_bf16(64, 64);
-                for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                    const uint64_t ah = tc::sdesc(la + ks_ * 256, 128, D * 16);
-                    const uint64_t al = tc::sdesc(la + 16384 + ks_ * 256, 128, D * 16);
-                    const uint64_t bh = tc::sdesc(rb + ks_ * 256, 128, D * 16);
-                    const uint64_t bl = tc::sdesc(rb + 16384 + ks_ * 256, 128, D * 16);
-                    tc::mma_ss(d, ah, bh, id, ks_ > 0);
-                    tc::mma_ss(d, ah, bl, id, 1);
-                    tc::mma_ss(d, al, bh, id, 1);
-                }
-                tc::commit(bar_mma);
-            }
-            mma_sync();
-            if (failed) break;
         }
+        publish();
+        if (warp == 0) {
+            uint64_t ah[2], al[2], bh[2], bl[2];
+#pragma unroll
+            for (int R = 0; R < 2; ++R) {
+                const uint32_t la = tc::smem_u32(smem + sm_l(R)), rb = tc::smem_u32(smem + sm_rt(R));
+                ah[R] = tc::sdesc(la, 128, D * 16);
+                al[R] = tc::sdesc(la + 16384, 128, D * 16);
+                bh[R] = tc::sdesc(rb, 128, D * 16);
+                bl[R] = tc::sdesc(rb + rt_lo(R), 128, D * 16);
+            }
+#pragma unroll
+            for (int ks_ = 0; ks_ < D / 16; ++ks_) {
+#pragma unroll
+                for (int R = 0; R < 2; ++R) {  // two independent accumulators, interleaved
+                    const uint32_t d = tm + TM_AP + 32 * R;
+                    const uint32_t id = R == 0 ? tc::idesc_bf16(64, 32) : tc::idesc_bf16(64, 64);
+                    const uint32_t o = ks_ * 256;
+                    tc::mma_ss_w(d, tc::dadv(ah[R], o), tc::dadv(bh[R], o), id, ks_ > 0);
+                    tc::mma_ss_w(d, tc::dadv(ah[R], o), tc::dadv(bl[R], o), id, 1);
+                    tc::mma_ss_w(d, tc::dadv(al[R], o), tc::dadv(bh[R], o), id, 1);
+                }
+            }
+            tc::commit_w(bar_mma);
+        }
+        mma_sync();
         if (failed) break;
 
         // ---- (4) (q e^G) (K-major) and (k e^{G_C - G})^T (MN-major) operands -------
         {
-#pragma unroll 2
-            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
                 const int item = tid + NT * kk;
                 const int r = ((item >> 7) << 3) | (item & 7);
-                const int J = kk;  // r in [16 kk, 16 kk + 16)
+                const int J = r >> 4;
                 // products of the block totals before (pf) and after (sf) block J
                 float pf[8], sf[8], tj[8], t[8];
 #pragma unroll
@@ -455,39 +463,39 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         // ---- (5) A/P out of TMEM: Diag(beta) A -> fp32, P -> hi/lo operand ---------
         {
             float* Af = reinterpret_cast<float*>(smem + SM_AF);  // [64 r][MAT_LD]
-            const int R = warp >> 2;                          // warpgroup R reads block R
+            const int R = (warp >> 2) & 1;                    // warpgroup w: block w % 2,
+            const int jb = 32 * (warp >> 3);                  //   columns [32 (w / 2), +32)
+            const int ncol = 32 * (R + 1);
             const int i = (warp & 3) * 16 + (lane & 15);      // M = 64 row held by this lane
             const bool is_q = i >= 32;
             const int r = 32 * R + (i & 31);
-            uint32_t a[64];
+            uint32_t a[32];
 #pragma unroll
-            for (int u = 0; u < 64; ++u) a[u] = 0u;
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 16, a + 16);
-            if (R == 1) {
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 32, a + 32);
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + 48, a + 48);
+            for (int u = 0; u < 32; ++u) a[u] = 0u;
+            if (jb < ncol) {
+                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + jb, a);
+                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + jb + 16, a + 16);
+                tc::tmem_ld_wait();
             }
-            tc::tmem_ld_wait();
             if (lane < 16) {
                 const float br = beta_s[r];
 #pragma unroll
-                for (int j0 = 0; j0 < 64; j0 += 8) {
+                for (int j0 = 0; j0 < 32; j0 += 8) {
                     float v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        const int j = j0 + u;
-                        const float x = __uint_as_float(a[j]);
+                        const int j = jb + j0 + u;
+                        const float x = __uint_as_float(a[j0 + u]);
                         v[u] = is_q ? (j <= r ? x : 0.f) : (j < r ? br * x : 0.f);
                     }
                     if (is_q) {
                         uint4 hi, lo;
                         tc::split8(v, hi, lo);
-                        *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, j0, C)) = hi;
-                        *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, j0, C)) = lo;
+                        *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, jb + j0, C)) = hi;
+                        *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, jb + j0, C)) = lo;
                     } else {
-                        *reinterpret_cast<float4*>(Af + r * MAT_LD + j0) = make_float4(v[0], v[1], v[2], v[3]);
-                        *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                        *reinterpret_cast<float4*>(Af + r * MAT_LD + jb + j0) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4*>(Af + r * MAT_LD + jb + j0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
                     }
                 }
             }
@@ -508,7 +516,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             // diagonal blocks: forward substitution with the column in registers;
             // warp w: block w/2, columns 8 (w%2) .. + 8; lane: column lane/4, rows = lane%4 (mod 4)
-            {
+            if (warp < 8) {
                 const int blk = warp >> 1, col = 8 * (warp & 1) + (lane >> 2), part = lane & 3;
                 const int i = 16 * blk + col;
                 float x[4];
@@ -584,128 +592,130 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         }
         publish();
 
-        // ---- W^T = (k e^G)^T (T Diag beta)^T ;  U~^T = v^T (T Diag beta)^T ------
-        if (tid == 0) {
-            const uint32_t tb = tc::smem_u32(smem + SM_TB);
+        // ---- W^T = (k e^G)^T (T Diag beta)^T into the U accumulator's columns (then
+        //      read out); O^T = S^T (q e^G)^T behind it on a second commit -------------
+        if (warp == 0) {
+            const uint32_t tb = tc::smem_u32(smem + SM_TB), qt = tc::smem_u32(smem + SM_QT);
+            const uint64_t tbh = tc::sdesc(tb, 128, C * 16), tbl = tc::sdesc(tb + 8192, 128, C * 16);
+            const uint64_t qth = tc::sdesc(qt, 128, D * 16), qtl = tc::sdesc(qt + 16384, 128, D * 16);
+#pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
-                const uint64_t bh = tc::sdesc(tb + ks_ * 256, 128, C * 16);
-                const uint64_t bl = tc::sdesc(tb + 8192 + ks_ * 256, 128, C * 16);
-                tc::mma_ts(tm + TM_AO, tm + TM_KTH + ks_ * 8, bh, id_n64, ks_ > 0);
-                tc::mma_ts(tm + TM_AO, tm + TM_KTH + ks_ * 8, bl, id_n64, 1);
-                tc::mma_ts(tm + TM_AO, tm + TM_KTL + ks_ * 8, bh, id_n64, 1);
-                tc::mma_ts(tm + TM_AU, tm + TM_VT + ks_ * 8, bh, id_n64, ks_ > 0);
-                tc::mma_ts(tm + TM_AU, tm + TM_VT + ks_ * 8, bl, id_n64, 1);
+                const uint64_t bh = tc::dadv(tbh, ks_ * 256), bl = tc::dadv(tbl, ks_ * 256);
+                tc::mma_ts_w(tm + TM_AU, tm + TM_KTH + ks_ * 8, bh, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TM_AU, tm + TM_KTH + ks_ * 8, bl, id_n64, 1);
+                tc::mma_ts_w(tm + TM_AU, tm + TM_KTL + ks_ * 8, bh, id_n64, 1);
             }
-            tc::commit(bar_mma);
+            tc::commit_w(bar_w);
+#pragma unroll
+            for (int ks_ = 0; ks_ < D / 16; ++ks_) {
+                const uint32_t sh = tm + TM_SH + ks_ * 8, sl = tm + TM_SL + ks_ * 8;
+                const uint64_t qh = tc::dadv(qth, ks_ * 256), ql = tc::dadv(qtl, ks_ * 256);
+                tc::mma_ts_w(tm + TM_AO, sh, qh, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TM_AO, sh, ql, id_n64, 1);
+                tc::mma_ts_w(tm + TM_AO, sl, qh, id_n64, 1);
+            }
+            tc::commit_w(bar_mma);
         }
-        mma_sync();
+        wait_one(bar_w, w_phase);
 
         // ---- W out of TMEM into the B operand (MN-major: n = r, k = c) ----------
         {
             const int c = (warp & 3) * 32 + lane;
-            const int rb = (warp >> 2) * 32;
-            uint32_t a[16], b[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb + 16, b);
+            const int rb = (warp >> 2) * 16;
+            uint32_t a[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb, a);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
+            for (int g8 = 0; g8 < 2; ++g8) {
                 float w[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = 8 * g8 + u;
-                    w[u] = __uint_as_float(i < 16 ? a[i] : b[i - 16]);
-                }
+                for (int u = 0; u < 8; ++u) w[u] = __uint_as_float(a[8 * g8 + u]);
                 *reinterpret_cast<uint4*>(smem + SM_WB + tc::mnmaj(rb + 8 * g8, c, C)) = tc::pack8(w);
             }
         }
         publish();
+        mma_sync();  // S^T (q e^G)^T done as well
 
-        // ---- U^T = U~^T - S^T W^T ;  O^T = S^T (q e^G)^T -------------------------
-        if (tid == 0) {
-            const uint32_t wb = tc::smem_u32(smem + SM_WB), qt = tc::smem_u32(smem + SM_QT);
-            for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                const uint32_t sh = tm + TM_SH + ks_ * 8, sl = tm + TM_SL + ks_ * 8;
-                tc::mma_ts(tm + TM_AU, sh, tc::sdesc(wb + ks_ * 2 * C * 16, C * 16, 128), id_n64_neg_bmn, 1);
-                const uint64_t qh = tc::sdesc(qt + ks_ * 256, 128, D * 16);
-                const uint64_t ql = tc::sdesc(qt + 16384 + ks_ * 256, 128, D * 16);
-                tc::mma_ts(tm + TM_AO, sh, qh, id_n64, ks_ > 0);
-                tc::mma_ts(tm + TM_AO, sh, ql, id_n64, 1);
-                tc::mma_ts(tm + TM_AO, sl, qh, id_n64, 1);
+        // ---- U^T = v^T (T Diag beta)^T - S^T W^T ---------------------------------
+        if (warp == 0) {
+            const uint32_t tb = tc::smem_u32(smem + SM_TB), wb = tc::smem_u32(smem + SM_WB);
+            const uint64_t tbh = tc::sdesc(tb, 128, C * 16), tbl = tc::sdesc(tb + 8192, 128, C * 16);
+            const uint64_t wbd = tc::sdesc(wb, C * 16, 128);
+#pragma unroll
+            for (int ks_ = 0; ks_ < C / 16; ++ks_) {
+                tc::mma_ts_w(tm + TM_AU, tm + TM_VT + ks_ * 8, tc::dadv(tbh, ks_ * 256), id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TM_AU, tm + TM_VT + ks_ * 8, tc::dadv(tbl, ks_ * 256), id_n64, 1);
             }
-            tc::commit(bar_mma);
+#pragma unroll
+            for (int ks_ = 0; ks_ < D / 16; ++ks_)
+                tc::mma_ts_w(tm + TM_AU, tm + TM_SH + ks_ * 8, tc::dadv(wbd, ks_ * 2 * C * 16), id_n64_neg_bmn, 1);
+            tc::commit_w(bar_mma);
         }
         mma_sync();
 
         // ---- U hi/lo into TMEM; decay the fp32 state by e^{G_C} -----------------
         {
-            const int rb = (warp >> 2) * 32;
-            uint32_t a[16], b[16];
+            const int rb = (warp >> 2) * 16;
+            const int cc = (warp >> 2) * 32;
+            uint32_t a[16], s0[16], s1[16];
             tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb + 16, b);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
             tc::tmem_ld_wait();
-            uint32_t hi[16], lo[16];
+            uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float x0 = __uint_as_float(i < 8 ? a[2 * i] : b[2 * i - 16]);
-                const float x1 = __uint_as_float(i < 8 ? a[2 * i + 1] : b[2 * i - 15]);
+            for (int i = 0; i < 8; ++i) {
                 __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(x0, h0, l0);
-                tc::split_bf16(x1, h1, l1);
+                tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
+                tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
                 hi[i] = tc::pack_bf16(h0, h1);
                 lo[i] = tc::pack_bf16(l0, l1);
             }
-            tc::tmem_st16(tm + lane_base(warp) + TM_UH + rb / 2, hi);
-            tc::tmem_st16(tm + lane_base(warp) + TM_UL + rb / 2, lo);
-            const int cbeg = (warp >> 2) * 64;
-            for (int cc = cbeg; cc < cbeg + 64; cc += 16) {
-                uint32_t s[16];
-                tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s);
-                tc::tmem_ld_wait();
+            tc::tmem_st8(tm + lane_base(warp) + TM_UH + rb / 2, hi);
+            tc::tmem_st8(tm + lane_base(warp) + TM_UL + rb / 2, lo);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) s[i] = __float_as_uint(__uint_as_float(s[i]) * egc_s[cc + i]);
-                tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, s);
+            for (int i = 0; i < 16; ++i) {
+                s0[i] = __float_as_uint(__uint_as_float(s0[i]) * egc_s[cc + i]);
+                s1[i] = __float_as_uint(__uint_as_float(s1[i]) * egc_s[cc + 16 + i]);
             }
+            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, s0);
+            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc + 16, s1);
             tc::tmem_st_wait();
         }
         publish();
 
         // ---- O^T += U^T P^T ;  S^T += U^T (k e^{G_C-G}) --------------------------
-        if (tid == 0) {
+        if (warp == 0) {
             const uint32_t pb = tc::smem_u32(smem + SM_PB), kb = tc::smem_u32(smem + SM_KB);
+            const uint64_t pbh = tc::sdesc(pb, 128, C * 16), pbl = tc::sdesc(pb + 8192, 128, C * 16);
+            const uint64_t kbh = tc::sdesc(kb, D * 16, 128), kbl = tc::sdesc(kb + 16384, D * 16, 128);
+#pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
                 const uint32_t uh = tm + TM_UH + ks_ * 8, ul = tm + TM_UL + ks_ * 8;
-                const uint64_t ph = tc::sdesc(pb + ks_ * 256, 128, C * 16);
-                const uint64_t pl = tc::sdesc(pb + 8192 + ks_ * 256, 128, C * 16);
-                tc::mma_ts(tm + TM_AO, uh, ph, id_n64, 1);
-                tc::mma_ts(tm + TM_AO, uh, pl, id_n64, 1);
-                tc::mma_ts(tm + TM_AO, ul, ph, id_n64, 1);
-                const uint64_t kh = tc::sdesc(kb + ks_ * 2 * D * 16, D * 16, 128);
-                const uint64_t kl = tc::sdesc(kb + 16384 + ks_ * 2 * D * 16, D * 16, 128);
-                tc::mma_ts(tm + TM_S, uh, kh, id_n128_bmn, 1);
-                tc::mma_ts(tm + TM_S, uh, kl, id_n128_bmn, 1);
-                tc::mma_ts(tm + TM_S, ul, kh, id_n128_bmn, 1);
+                const uint64_t ph = tc::dadv(pbh, ks_ * 256), pl = tc::dadv(pbl, ks_ * 256);
+                const uint64_t kh = tc::dadv(kbh, ks_ * 2 * D * 16), kl = tc::dadv(kbl, ks_ * 2 * D * 16);
+                tc::mma_ts_w(tm + TM_S, uh, kh, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TM_AO, uh, ph, id_n64, 1);
+                tc::mma_ts_w(tm + TM_S, uh, kl, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TM_AO, uh, pl, id_n64, 1);
+                tc::mma_ts_w(tm + TM_S, ul, kh, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TM_AO, ul, ph, id_n64, 1);
             }
-            tc::commit(bar_mma);
+            tc::commit_w(bar_mma);
         }
         mma_sync();
 
         // ---- o out; S hi/lo for the next chunk ------------------------------------
         {
             const int x = (warp & 3) * 32 + lane;
-            const int rb = (warp >> 2) * 32;
-            uint32_t a[16], b[16];
+            const int rb = (warp >> 2) * 16;
+            uint32_t a[16];
             tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb + 16, b);
             tc::tmem_ld_wait();
             const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (rb + i < L) {
-                    const float v = scale * __uint_as_float(i < 16 ? a[i] : b[i - 16]);
-                    o[ob + (int64_t)i * H * D] = from_f32<TOut>(v);
-                }
-            }
+            for (int i = 0; i < 16; ++i)
+                if (rb + i < L) o[ob + (int64_t)i * H * D] = from_f32<TOut>(scale * __uint_as_float(a[i]));
         }
         s_epilogue();
         tc::fence_before();
@@ -720,8 +730,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     }
     if (p.final_state) {
         const int x = (warp & 3) * 32 + lane;
-        const int cbeg = (warp >> 2) * 64;
-        for (int cc = cbeg; cc < cbeg + 64; cc += 16) {
+        const int cbeg = (warp >> 2) * 32;
+        for (int cc = cbeg; cc < cbeg + 32; cc += 16) {
             uint32_t s[16];
             tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s);
             tc::tmem_ld_wait();
