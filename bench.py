@@ -354,14 +354,43 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """A few launches of one kernel on a chosen size, for ncu captures (prints 'ok')."""
+    import kimi_delta_attention_chunk_gb300 as kda
+    from kimi_delta_attention_chunk_gb300 import synth
+    dev = torch.device("cuda", 0)
+    if args.profile_case == "prefill":
+        inp = synth.direct_inputs(args.profile_T, args.profile_H, 128, 128, torch.bfloat16, seed=1)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        for _ in range(args.profile_reps):
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"])
+    else:
+        w = synth.WORKLOADS["decode"]
+        dec = synth.decode_inputs(w.B, w.H, w.K, w.V, args.profile_reps, w.dtype, w.seed)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dec.items()}
+        state = d["state"].clone()
+        for i in range(args.profile_reps):
+            kda.recurrent_step(d["q"][i], d["k"][i], d["v"][i], d["g"][i], d["beta"][i], state, scale=d["scale"])
+    torch.cuda.synchronize()
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+                    help="run a few launches of one kernel for an ncu capture instead of the benchmark")
+    ap.add_argument("--profile-T", type=int, default=2048)
+    ap.add_argument("--profile-H", type=int, default=16)
+    ap.add_argument("--profile-reps", type=int, default=2)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args)
+        return
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
