@@ -184,14 +184,18 @@ def oracle_prefill_rate(H: int, T: int, heads: int, seed: int = 1):
 
 
 def cpu_baseline(H: int, T: int, budget_s: float = 12.0):
-    # calibrate on 2 heads, then size the sample to about budget_s seconds
-    rate1, dt1, threads = oracle_prefill_rate(H, T, 2)
-    per_head = dt1 / 2
-    heads = int(max(2, min(H, budget_s / max(per_head, 1e-6))))
-    rate, dt, threads = oracle_prefill_rate(H, T, heads)
-    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{T} tokens x {heads} of {H} heads (K=V=128, bf16 inputs upcast to fp64), "
-                      f"{dt:.1f} s; rate scaled to all {H} heads"}
+    """The oracle on the host cores: the whole T-token, H-head prefill, repeated
+    until about budget_s seconds of work (at least once); mean tokens/s."""
+    rates, total, reps, threads = [], 0.0, 0, 1
+    while reps == 0 or total < budget_s:
+        r, dt, threads = oracle_prefill_rate(H, T, H)
+        rates.append(r)
+        total += dt
+        reps += 1
+        if reps >= 50:
+            break
+    return {"value": sum(rates) / len(rates), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} x ({T} tokens x {H} heads, K=V=128, bf16 inputs upcast to fp64), {total:.1f} s"}
 
 
 def run_reference(args, world, rank):

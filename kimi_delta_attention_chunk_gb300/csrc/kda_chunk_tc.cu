@@ -506,14 +506,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         {
             const float* N = reinterpret_cast<const float*>(smem + SM_AF);
             float* T = reinterpret_cast<float*>(smem + SM_TF);
-            float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch [3][16][16]
-            // zero the strictly upper blocks (the others are all written below)
-            for (int e = tid; e < 6 * 64; e += NT) {
-                const int blk = e >> 6, rr = (e >> 2) & 15, q4 = e & 3;
-                const int R = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                *reinterpret_cast<float4*>(T + (16 * R + rr) * MAT_LD + 16 * J + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch: [2][16][16] then [32][32]
+            // (blocks above the diagonal are never written; the operand build masks them)
             // diagonal blocks: forward substitution with the column in registers;
             // warp w: block w/2, columns 8 (w%2) .. + 8; lane: column lane/4, rows = lane%4 (mod 4)
             if (warp < 8) {
@@ -537,39 +531,75 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 for (int m = 0; m < 4; ++m) T[(16 * blk + part + 4 * m) * MAT_LD + i] = x[m];
             }
             __syncthreads();
-            // off-diagonal blocks by distance d = R - J:
-            //   Y = sum_{M=J}^{R-1} N_{R,M} T_{M,J};   T_{R,J} = -T_{R,R} Y
-            // one thread per (J, row a, 4 columns)
-            for (int d = 1; d < 4; ++d) {
-                const int nitem = (4 - d) * 64;
-                const int J = tid >> 6, a = (tid >> 2) & 15, b4 = tid & 3;
-                const int R = J + d;
-                if (tid < nitem) {
-                    const float* nrow = N + (16 * R + a) * MAT_LD;
+            // off-diagonal blocks, as two 32 x 32 halves T11 (tokens 0..31) and T22
+            // (32..63): first the lower 16 x 16 block inside each half,
+            //   T_{2p+1,2p} = -T_{2p+1,2p+1} (N_{2p+1,2p} T_{2p,2p}),   p = 0, 1,
+            // then the lower half  T21 = -T22 (N21 T11).
+            {
+                // one thread per (p, row a, 4 columns): 128 items
+                const int pp = tid >> 6, a = (tid >> 2) & 15, b4 = tid & 3;
+                const int R = 2 * pp + 1, J = 2 * pp;
+                if (tid < 128) {
+                    const float* nrow = N + (16 * R + a) * MAT_LD + 16 * J;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int m4 = 4 * J; m4 < 4 * R; ++m4) {
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
                         const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
                         const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const float4 t = *reinterpret_cast<const float4*>(T + (4 * m4 + u) * MAT_LD + 16 * J + 4 * b4);
+                            const float4 t = *reinterpret_cast<const float4*>(T + (16 * J + 4 * m4 + u) * MAT_LD + 16 * J + 4 * b4);
                             acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
                         }
                     }
-                    *reinterpret_cast<float4*>(Y + (J << 8) + (a << 4) + 4 * b4) = acc;
+                    *reinterpret_cast<float4*>(Y + (pp << 8) + (a << 4) + 4 * b4) = acc;
                 }
                 __syncthreads();
-                if (tid < nitem) {
+                if (tid < 128) {
                     const float* trow = T + (16 * R + a) * MAT_LD + 16 * R;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
                         const float tv = trow[m];
-                        const float4 y = *reinterpret_cast<const float4*>(Y + (J << 8) + (m << 4) + 4 * b4);
+                        const float4 y = *reinterpret_cast<const float4*>(Y + (pp << 8) + (m << 4) + 4 * b4);
                         acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
                     }
                     *reinterpret_cast<float4*>(T + (16 * R + a) * MAT_LD + 16 * J + 4 * b4) =
                         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                }
+                __syncthreads();
+            }
+            {
+                // one thread per (row a, 4 columns) of a 32 x 32 block: 256 items
+                float* X = Y + 512;
+                const int a = tid >> 3, b4 = tid & 7;
+                if (tid < 256) {
+                    const float* nrow = N + (32 + a) * MAT_LD;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    // T11 is zero above its diagonal blocks: columns >= 16 start at row 16
+                    for (int m4 = (b4 >= 4 ? 4 : 0); m4 < 8; ++m4) {
+                        const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
+                        const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float4 t = *reinterpret_cast<const float4*>(T + (4 * m4 + u) * MAT_LD + 4 * b4);
+                            acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
+                        }
+                    }
+                    *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
+                }
+                __syncthreads();
+                if (tid < 256) {
+                    const float* trow = T + (32 + a) * MAT_LD + 32;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int mmax = a < 16 ? 16 : 32;  // T22 is zero above its diagonal blocks
+#pragma unroll 4
+                    for (int m = 0; m < mmax; ++m) {
+                        const float tv = trow[m];
+                        const float4 y = *reinterpret_cast<const float4*>(X + m * 32 + 4 * b4);
+                        acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
+                    }
+                    *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
                 __syncthreads();
             }
@@ -583,7 +613,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 const float4 b = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg + 4);
                 t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) t[u] *= beta_s[8 * jg + u];
+                for (int u = 0; u < 8; ++u) t[u] = (8 * jg + u > r) ? 0.f : t[u] * beta_s[8 * jg + u];
                 uint4 hi, lo;
                 tc::split8(t, hi, lo);
                 *reinterpret_cast<uint4*>(smem + SM_TB + tc::kmaj(r, 8 * jg, C)) = hi;
@@ -709,15 +739,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         {
             const int x = (warp & 3) * 32 + lane;
             const int rb = (warp >> 2) * 16;
-            uint32_t a[16];
+            const int cc = (warp >> 2) * 32;
+            uint32_t a[16], s0[16], s1[16];
             tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
             tc::tmem_ld_wait();
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat16 h0, l0, h1, l1;
+                tc::split_bf16(__uint_as_float(i < 8 ? s0[2 * i] : s1[2 * i - 16]), h0, l0);
+                tc::split_bf16(__uint_as_float(i < 8 ? s0[2 * i + 1] : s1[2 * i - 15]), h1, l1);
+                hi[i] = tc::pack_bf16(h0, h1);
+                lo[i] = tc::pack_bf16(l0, l1);
+            }
+            tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
+            tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
             const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (rb + i < L) o[ob + (int64_t)i * H * D] = from_f32<TOut>(scale * __uint_as_float(a[i]));
+            tc::tmem_st_wait();
         }
-        s_epilogue();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
