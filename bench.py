@@ -338,6 +338,43 @@ def run_ours(args, world, rank, local):
                            "peak_kind": peak_kind}}
     del dd, state, qs, ks, vs, gs, bs
 
+    # ---- the other prefill workloads, each with its own roofline
+    extra = {}
+    for name in (["varlen"] if not args.skip_varlen else []) + (["long"] if not args.skip_long else []):
+        wl = synth.WORKLOADS[name]
+        inp = synth.device_inputs(name, dev, seed_offset=rank)
+        Ttot = inp["beta"].shape[1]
+        N = wl.n_seqs if wl.n_seqs else wl.B
+        ox = torch.empty((1, Ttot, wl.H, wl.V), dtype=torch.float32, device=dev)
+        sx = torch.empty((N, wl.H, wl.K, wl.V), dtype=torch.float32, device=dev)
+        if wl.prologue:
+            def run_x():
+                kda.chunk_fwd_fused(inp["q_raw"], inp["k_raw"], inp["v_raw"], inp["gate_x"], inp["beta"],
+                                    inp["conv_w"], inp["A_log"], inp["dt_bias"], scale=inp["scale"],
+                                    initial_state=inp["initial_state"], o=ox, final_state=sx)
+        else:
+            def run_x():
+                kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
+                              initial_state=inp["initial_state"], cu_seqlens=inp["cu_seqlens"], o=ox, final_state=sx)
+        run_x()
+        torch.cuda.synchronize()
+        barrier(world)
+        reps = 3 if name == "varlen" else 1
+        xt, xper = time_launches(run_x, reps, stream)
+        xt = max_over_ranks(xt, world) / reps
+        xbytes = prefill_bytes(Ttot, wl.H, wl.K, wl.V, N, 2, reads_state=wl.init_state)
+        xk = sum(xper) / len(xper)
+        xach = xbytes / (xk * 1e-3) / 1e9
+        extra[name] = {
+            "value": world * Ttot / (xt * 1e-3), "unit": "tokens/s", "ms_per_launch": xt,
+            "workload": ("varlen prefill: 16 sequences of 512..8192 tokens (%d total) packed by cu_seqlens, "
+                         "H=96 K=V=128 bf16, fp32 initial states" % Ttot) if name == "varlen" else
+                        ("long prefill with fused prologue (conv4, L2-norm, gate): T=65536 H=96 K=V=128 bf16, "
+                         "nonzero initial state; runs the CUDA-core fused kernel"),
+            "roofline": {"bound": "hbm", "achieved": xach, "peak": hbm, "unit": "GB/s", "frac": xach / hbm,
+                         "traffic": None, "algorithmic_bytes": xbytes, "peak_kind": peak_kind}}
+        del inp, ox, sx
+
     if rank != 0:
         return
     line = {
@@ -353,6 +390,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk, "e2e": e2e, "gpu_launches": args.steps,
         "decode": decode,
     }
+    line.update(extra)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(H, T)
     print(json.dumps(line), flush=True)
@@ -391,6 +429,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-varlen", action="store_true", help="skip the 16-sequence varlen prefill line")
+    ap.add_argument("--skip-long", action="store_true", help="skip the 65536-token fused-prologue line")
     args = ap.parse_args()
     if args.profile_case:
         profile_case(args)

@@ -190,6 +190,36 @@ def decode_inputs(N: int, H: int, K: int, V: int, steps: int, dtype: torch.dtype
     return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "state": s0, "scale": float(K) ** -0.5}
 
 
+def device_inputs(name: str, device, seed_offset: int = 0) -> dict:
+    """Inputs of a named workload drawn directly on a CUDA device (torch's seeded
+    Philox generator), with the same shapes and value distributions as the host
+    generators above.  For timing only: the host generators are the ones the
+    parity tests share with the oracle."""
+    w = WORKLOADS[name]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1000003 * (w.seed + 1) + seed_offset)
+    lengths = varlen_lengths(w.seed, w.n_seqs) if w.n_seqs else None
+    B, T = (1, int(np.sum(lengths))) if lengths is not None else (w.B, w.T)
+    H, K, V, dt = w.H, w.K, w.V, w.dtype
+    rn = lambda *shape: torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)  # noqa: E731
+    unit = lambda x: x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)  # noqa: E731
+    out = {"scale": float(K) ** -0.5,
+           "cu_seqlens": cu_from_lengths(lengths).to(device) if lengths is not None else None}
+    N = len(lengths) if lengths is not None else B
+    if w.prologue:
+        out.update(q_raw=rn(B, T, H, K).to(dt), k_raw=rn(B, T, H, K).to(dt), v_raw=rn(B, T, H, V).to(dt),
+                   gate_x=rn(B, T, H, K).to(dt), beta=torch.sigmoid(rn(B, T, H)).to(dt),
+                   conv_w=(0.5 * rn(3, H * max(K, V), 4)),
+                   A_log=torch.rand(K, generator=gen, device=device) * 2 - 1,
+                   dt_bias=torch.rand(H * K, generator=gen, device=device) * 2 - 1)
+    else:
+        out.update(q=unit(rn(B, T, H, K)).to(dt), k=unit(rn(B, T, H, K)).to(dt), v=rn(B, T, H, V).to(dt),
+                   g=torch.clamp(-torch.nn.functional.softplus(rn(B, T, H, K)), min=GATE_LOWER_BOUND).to(dt),
+                   beta=torch.sigmoid(rn(B, T, H)).to(dt))
+    out["initial_state"] = STATE_STD * rn(N, H, K, V) if w.init_state else None
+    return out
+
+
 def workload_inputs(name: str) -> dict:
     """Full-size inputs of a named workload."""
     w = WORKLOADS[name]
