@@ -288,35 +288,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         // Every build loop below gives a thread the same 8 channels [8 cg, 8 cg + 8).
         const int cg = (tid >> 3) & 15;
 
-        // ---- (2) (k e^G)^T and v^T into TMEM (lane = channel / value column) ----
-        {
-            const int c = (warp & 3) * 32 + lane;
-            const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
-            const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
-            const float pfx[4] = {1.f, t0v, t0v * t1v, t0v * t1v * t2v};
-            uint32_t kh[8], kl[8], vv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = jb + 2 * i;
-                const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
-                const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], h0, l0);
-                tc::split_bf16(k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], h1, l1);
-                kh[i] = tc::pack_bf16(h0, h1);
-                kl[i] = tc::pack_bf16(l0, l1);
-                const __nv_bfloat16 z = __float2bfloat16(0.f);
-                const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
-                const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
-                vv[i] = tc::pack_bf16(v0, v1);
-            }
-            tc::tmem_st8(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
-            tc::tmem_st8(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
-            tc::tmem_st8(tm + lane_base(warp) + TM_VT + jb / 2, vv);
-            if (tid < 128) egc_s[c] = t0v * t1v * t2v * tot_s[384 + c];
-        }
-        tc::tmem_st_wait();
-
         // ---- (3) A and P: two 32-token row blocks, reference at the block centre --
         // Both blocks' operands are built first (block 0 in OPB, block 1 in OPA),
         // then all their MMAs go out in one round.
@@ -328,7 +299,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             float itc[8];
             ld_tot8(2 * R, 8 * cg, itc);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) itc[u] = __frcp_rn(itc[u]);
+            for (int u = 0; u < 8; ++u) itc[u] = __fdividef(1.f, itc[u]);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int item = tid + NT * kk;
@@ -361,7 +332,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 // and the true factor, so nothing underflows that the result needs
                 if (J == 2 * R + 1) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) m[u] = __frcp_rn(pr[u]);
+                    for (int u = 0; u < 8; ++u) m[u] = __fdividef(1.f, pr[u]);
                 } else {
                     ld_tot8(J, 8 * cg, t);
 #pragma unroll
@@ -406,6 +377,36 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             tc::commit_w(bar_mma);
         }
+        // ---- (2) (k e^G)^T and v^T into TMEM (lane = channel / value column), while
+        //      the A/P MMAs run (disjoint TMEM columns, no shared memory they read) --
+        {
+            const int c = (warp & 3) * 32 + lane;
+            const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
+            const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
+            const float pfx[4] = {1.f, t0v, t0v * t1v, t0v * t1v * t2v};
+            uint32_t kh[8], kl[8], vv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = jb + 2 * i;
+                const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
+                const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
+                __nv_bfloat16 h0, l0, h1, l1;
+                tc::split_bf16(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], h0, l0);
+                tc::split_bf16(k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], h1, l1);
+                kh[i] = tc::pack_bf16(h0, h1);
+                kl[i] = tc::pack_bf16(l0, l1);
+                const __nv_bfloat16 z = __float2bfloat16(0.f);
+                const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
+                const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
+                vv[i] = tc::pack_bf16(v0, v1);
+            }
+            tc::tmem_st8(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
+            tc::tmem_st8(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
+            tc::tmem_st8(tm + lane_base(warp) + TM_VT + jb / 2, vv);
+            if (tid < 128) egc_s[c] = t0v * t1v * t2v * tot_s[384 + c];
+        }
+        tc::tmem_st_wait();
+
         mma_sync();
         if (failed) break;
 
@@ -570,14 +571,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 __syncthreads();
             }
             {
-                // one thread per (row a, 4 columns) of a 32 x 32 block: 256 items
+                // two lanes per (row a, 4 columns) of a 32 x 32 block, each summing half of
+                // the inner range; 256 items over 512 threads
                 float* X = Y + 512;
-                const int a = tid >> 3, b4 = tid & 7;
-                if (tid < 256) {
+                const int item = tid >> 1, half = tid & 1;
+                const int a = item >> 3, b4 = item & 7;
+                {
                     const float* nrow = N + (32 + a) * MAT_LD;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     // T11 is zero above its diagonal blocks: columns >= 16 start at row 16
-                    for (int m4 = (b4 >= 4 ? 4 : 0); m4 < 8; ++m4) {
+                    const int m0 = (b4 >= 4 ? 4 : 0) + half * (b4 >= 4 ? 2 : 4);
+                    const int m1 = b4 >= 4 ? m0 + 2 : m0 + 4;
+                    for (int m4 = m0; m4 < m1; ++m4) {
                         const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
                         const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
 #pragma unroll
@@ -586,20 +591,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                             acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
                         }
                     }
-                    *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
+                    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
+                    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
+                    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
+                    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
+                    if (half == 0) *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
                 }
                 __syncthreads();
-                if (tid < 256) {
+                {
                     const float* trow = T + (32 + a) * MAT_LD + 32;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int mmax = a < 16 ? 16 : 32;  // T22 is zero above its diagonal blocks
+                    // T22 is zero above its diagonal blocks: rows < 16 stop at 16
+                    const int mlen = a < 16 ? 8 : 16;
+                    const int mb = half * mlen;
 #pragma unroll 4
-                    for (int m = 0; m < mmax; ++m) {
+                    for (int m = mb; m < mb + mlen; ++m) {
                         const float tv = trow[m];
                         const float4 y = *reinterpret_cast<const float4*>(X + m * 32 + 4 * b4);
                         acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
                     }
-                    *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
+                    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
+                    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
+                    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
+                    if (half == 0)
+                        *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
                 __syncthreads();
             }
@@ -646,6 +662,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             tc::commit_w(bar_mma);
         }
+        // decay the fp32 state by e^{G_C} while those MMAs run (they read S hi/lo,
+        // not the fp32 state; the K-bar^T U MMA accumulates into it later)
+        {
+            const int cc = (warp >> 2) * 32;
+            uint32_t s0[16], s1[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
+            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                s0[i] = __float_as_uint(__uint_as_float(s0[i]) * egc_s[cc + i]);
+                s1[i] = __float_as_uint(__uint_as_float(s1[i]) * egc_s[cc + 16 + i]);
+            }
+            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, s0);
+            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc + 16, s1);
+            tc::tmem_st_wait();
+        }
         wait_one(bar_w, w_phase);
 
         // ---- W out of TMEM into the B operand (MN-major: n = r, k = c) ----------
@@ -683,14 +716,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         }
         mma_sync();
 
-        // ---- U hi/lo into TMEM; decay the fp32 state by e^{G_C} -----------------
+        // ---- U hi/lo into TMEM -------------------------------------------------------
         {
             const int rb = (warp >> 2) * 16;
-            const int cc = (warp >> 2) * 32;
-            uint32_t a[16], s0[16], s1[16];
+            uint32_t a[16];
             tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
             tc::tmem_ld_wait();
             uint32_t hi[8], lo[8];
 #pragma unroll
@@ -703,13 +733,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             tc::tmem_st8(tm + lane_base(warp) + TM_UH + rb / 2, hi);
             tc::tmem_st8(tm + lane_base(warp) + TM_UL + rb / 2, lo);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s0[i] = __float_as_uint(__uint_as_float(s0[i]) * egc_s[cc + i]);
-                s1[i] = __float_as_uint(__uint_as_float(s1[i]) * egc_s[cc + 16 + i]);
-            }
-            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, s0);
-            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc + 16, s1);
             tc::tmem_st_wait();
         }
         publish();

@@ -199,12 +199,17 @@ __device__ __forceinline__ uint4 pack8(const float* x) {
     u.w = pack_bf16(__float2bfloat16_rn(x[6]), __float2bfloat16_rn(x[7]));
     return u;
 }
-// 8 values -> 16 bytes of bf16 hi and 16 bytes of bf16 lo (x = hi + lo)
+// 8 values -> 16 bytes of bf16 hi and 16 bytes of bf16 lo (x = hi + lo); the
+// residual is taken against the packed hi (bf16 -> fp32 is a 16-bit shift).
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+    hi = pack8(x);
+    const uint32_t w[4] = {hi.x, hi.y, hi.z, hi.w};
     float l[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) l[i] = x[i] - __bfloat162float(__float2bfloat16_rn(x[i]));
-    hi = pack8(x);
+    for (int i = 0; i < 4; ++i) {
+        l[2 * i] = x[2 * i] - __uint_as_float(w[i] << 16);
+        l[2 * i + 1] = x[2 * i + 1] - __uint_as_float(w[i] & 0xffff0000u);
+    }
     lo = pack8(l);
 }
 __device__ __forceinline__ void unpack8(uint4 u, float* x) {
