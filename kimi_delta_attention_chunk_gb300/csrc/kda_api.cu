@@ -24,7 +24,10 @@ kda_status check_sizes(int B, int T, int H, int K, int V, int N) {
 
 float resolve_scale(float scale, int K) { return scale > 0.f ? scale : 1.0f / sqrtf((float)K); }
 
-kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+kda_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    return e == cudaErrorMemoryAllocation ? KDA_ERR_WORKSPACE : KDA_ERR_CUDA;
+}
 
 kda_status check_common(const void* q, const void* k, const void* v, const void* g,
                         const void* beta, kda_dtype in_dtype, const float* initial_state,
@@ -65,7 +68,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head size or dtype not supported";
-        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: device workspace could not be allocated";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
         case KDA_ERR_RANGE: return "KDA_ERR_RANGE: input out of range";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: device-side wait gave up";

@@ -1,33 +1,50 @@
 // Chunked KDA prefill on the sm_103a tensor cores (bf16 inputs, K = V = 128).
 //
-// One CTA owns one (sequence, head) chain and walks it in chunks of C = 64
-// tokens.  The fp32 state lives in tensor memory for the whole sequence as
-// S^T (lane = value column x, column = key channel c).  Per chunk (G = in-chunk
-// cumulative log-decay per key channel; all products below are the chunk
-// algebra of the recurrence, see kda_chunk_simt.cu):
+// Per chunk of C = 64 tokens (G = in-chunk cumulative log-decay per key
+// channel; the chunk algebra of the recurrence, see kda_chunk_simt.cu):
 //
-//   A, P   gated in-chunk products, per 32-token row block R with the decay
-//          reference at the block centre (so every factor is within e^{+-80}):
-//          D_R[i, j] = L_R[i] . Rt_R[j]   (tcgen05, M = 64: 32 rows of k and 32
-//          rows of q, N = 32 (R+1))
-//   T      = (I + Diag(beta) A)^{-1}, 16x16 block forward substitution (CUDA cores)
-//   W^T    = (k e^G)^T (T Diag(beta))^T,   U~^T = v^T (T Diag(beta))^T     (tcgen05)
-//   U^T    = U~^T - S^T W^T                                              (tcgen05, negated A)
-//   O^T    = S^T (q e^G)^T + U^T P^T                                     (tcgen05)
-//   S^T   <- S^T Diag(e^{G_C}) + U^T (k e^{G_C - G})                     (tcgen05, in TMEM)
+//   A, P   gated in-chunk products (A strictly lower, P lower incl. diagonal)
+//   T      = (I + Diag(beta) A)^{-1}
+//   W      = T Diag(beta) (k e^G),      U~ = T Diag(beta) v
+//   U      = U~ - W S
+//   O      = scale (q e^G) S + scale P U
+//   S     <- Diag(e^{G_C}) S + (k e^{G_C - G})^T U
+//
+// Only the last three lines touch the state.  Substituting U into O gives
+//
+//   O = O_loc + Qh S,   O_loc = scale P U~,   Qh = scale ((q e^G) - P W),
+//
+// so everything except U = U~ - W S, O = O_loc + Qh S and the state update is
+// independent of S and is computed for all chunks at once.  The prefill is
+// therefore two kernels:
+//
+//   chunk_local_kernel   persistent, one (chunk, head) task at a time per CTA:
+//                        A, P, T, W, U~, O_loc, Qh, Kbar = k e^{G_C - G} and
+//                        e^{G_C}, written to a per-(chunk, head) workspace slot
+//                        (the MMA operands already in their shared-memory
+//                        layout, so the next kernel fetches them with bulk
+//                        copies)
+//   chunk_state_kernel   one CTA per (sequence, head): the fp32 state lives in
+//                        tensor memory as S^T for the whole sequence; per chunk
+//                        three MMA rounds (U^T = U~^T - S^T W^T, O^T = O_loc^T +
+//                        S^T Qh^T, S^T <- S^T Diag(e^{G_C}) + U^T Kbar).
 //
 // Operand precision: every operand that feeds o or the state directly is
 // split x = hi + lo into two bf16 values and multiplied as hi*hi + hi*lo +
 // lo*hi (about 16 significant bits); W and the correction W S use one bf16
-// term; v is exact in bf16.  Decay factors are running products of e^{g}
-// over exactly the tokens they span, built from per-16-token-block prefix
-// products (each >= e^-80 since g >= -5, so ratios inside a block are safe)
-// and block totals; nothing overflows and nothing cancels.
+// term (the same bf16 W in U and in Qh, so the substitution above holds for
+// the rounded W as well); v is exact in bf16.  Decay factors are running
+// products of e^{g} over exactly the tokens they span, built from
+// per-16-token-block prefix products (each >= e^-80 since g >= -5, so ratios
+// inside a block are safe) and block totals; nothing overflows and nothing
+// cancels.
 //
 // Sources: "ISEEKYAN/k3" README (chunked KDA forward as the compute path);
 // "kimi-k3-mlx" review, "The A_log shape mismatch ..." (per-channel decay) and
 // "Attention is 93 layers ..." (gate lower bound -5, 96 heads of 128).
 #include <cuda.h>
+
+#include <mutex>
 
 #include "kda_chunk.h"
 #include "kda_common.cuh"
@@ -37,23 +54,81 @@ namespace kda {
 namespace {
 
 constexpr int C = 64;
-constexpr int D = 128;  // K = V
+constexpr int D = 128;   // K = V
 constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TMEM lanes
+constexpr uint32_t kWaitIter = 1u << 26;
+
+// ---- workspace slot of one (chunk, head), written by the local kernel --------
+constexpr uint32_t SLOT_WT = 0;         // W (bf16) as B operand, MN-major (n = r, k = c)
+constexpr uint32_t SLOT_QH = 16384;     // Qh hi, same layout
+constexpr uint32_t SLOT_QL = 32768;     // Qh lo
+constexpr uint32_t SLOT_KH = 49152;     // Kbar hi as B operand, MN-major (n = c, k = r)
+constexpr uint32_t SLOT_KL = 65536;     // Kbar lo
+constexpr uint32_t SLOT_IMG = 81920;    // bytes of the five operand images above
+constexpr uint32_t SLOT_UT = 81920;     // U~ fp32 [64 r][128 v]
+constexpr uint32_t SLOT_OL = 114688;    // O_loc fp32 [64 r][128 v]
+constexpr uint32_t SLOT_EGC = 147456;   // e^{G_C} fp32 [128]
+constexpr uint32_t SLOT_BYTES = 147968;
+
+__device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
+
+// Work description shared by the kernels.  Sequences are either B dense rows
+// of T tokens (cu_seqlens == nullptr) or packed by cu_seqlens; chunks are
+// numbered sequence by sequence (global chunk index gc), slots by gc * H + h.
+struct Plan {
+    const int32_t* cu_seqlens;
+    const int32_t* chunk_off;  // [N + 1] first global chunk of each sequence (packed only)
+    const int32_t* order;      // [N] sequences longest first (packed only; nullptr = identity)
+    const int32_t* chunk_seq;  // [max_chunks] sequence of each global chunk, -1 past the end
+    int T, H, N;
+    int cps;                   // chunks per sequence (dense only)
+    int64_t max_chunks;        // number of workspace chunk slots (an upper bound when packed)
+    uint8_t* slots;
+};
+
+struct Chunk {
+    int64_t c0, eos;  // first token of the chunk, end of its sequence
+    int64_t gc;       // global chunk index
+    int h;
+    bool valid;
+};
+
+__device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
+    Chunk ch{};
+    ch.valid = false;
+    if (task >= pl.max_chunks * pl.H) return ch;
+    ch.gc = task / pl.H;
+    ch.h = (int)(task % pl.H);
+    if (pl.cu_seqlens == nullptr) {
+        const int64_t n = ch.gc / pl.cps, j = ch.gc % pl.cps;
+        ch.c0 = n * pl.T + j * C;
+        ch.eos = n * pl.T + pl.T;
+    } else {
+        const int n = pl.chunk_seq[ch.gc];
+        if (n < 0) return ch;
+        const int64_t bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
+        ch.c0 = bos + (ch.gc - pl.chunk_off[n]) * C;
+        ch.eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
+    }
+    ch.valid = true;
+    return ch;
+}
+
+// ============================================================================
+// Chunk-local kernel
+// ============================================================================
 
 // ---- shared memory map (bytes) ----------------------------------------------
-constexpr uint32_t SM_STG = 0;            // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
-constexpr uint32_t SM_OPA = 65536;        // 64 KB, A/P phase: row block 1's L hi|lo (A op [64 i][128 c])
-                                          //   and Rt hi|lo (B op [64 j][128 c]); then
-                                          //   (q e^G) hi|lo (B op [64 r][128 c], K-major) and
-                                          //   (k e^{G_C-G}) hi|lo (B op, MN-major: n = c, k = j)
+constexpr uint32_t SM_STG = 0;             // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
+constexpr uint32_t SM_OPA = 65536;         // 64 KB, A/P phase: row block 1's L hi|lo (A op [64 i][128 c])
+                                           //   and Rt hi|lo (B op [64 j][128 c]); then (q e^G) fp32 [64][QT_LD]
 constexpr uint32_t SM_QT = SM_OPA;
-constexpr uint32_t SM_KB = SM_OPA + 32768;
-constexpr uint32_t SM_OPB = 131072;       // 48 KB, A/P phase: row block 0's L hi|lo and Rt hi|lo (32 rows); then
-constexpr uint32_t SM_TB = SM_OPB;        //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
-constexpr uint32_t SM_PB = SM_OPB + 16384;//   P hi|lo, B op [64 r][64 j] K-major
-constexpr uint32_t SM_WB = SM_OPB + 32768;//   W hi, B op MN-major (n = r, k = c)
-constexpr uint32_t SM_PRE = 180224;       // fp32 [64][PRE_LD] in-block prefix products of e^g,
-constexpr int PRE_LD = 132;               //   later Diag(beta) A and T as fp32 [64][MAT_LD] each
+constexpr int QT_LD = 132;
+constexpr uint32_t SM_OPB = 131072;        // 48 KB, A/P phase: row block 0's L hi|lo and Rt hi|lo (32 rows); then
+constexpr uint32_t SM_TB = SM_OPB;         //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
+constexpr uint32_t SM_PB = SM_OPB + 16384; //   P hi|lo, B op [64 r][64 j] K-major
+constexpr uint32_t SM_PRE = 180224;        // fp32 [64][PRE_LD] in-block prefix products of e^g,
+constexpr int PRE_LD = 132;                //   later Diag(beta) A and T as fp32 [64][MAT_LD] each
 constexpr int MAT_LD = 68;
 constexpr uint32_t SM_AF = SM_PRE;
 constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
@@ -62,90 +137,49 @@ constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
 __host__ __device__ constexpr uint32_t sm_l(int R) { return R == 0 ? SM_OPB : SM_OPA; }
 __host__ __device__ constexpr uint32_t sm_rt(int R) { return R == 0 ? SM_OPB + 32768 : SM_OPA + 32768; }
 __host__ __device__ constexpr uint32_t rt_lo(int R) { return R == 0 ? 8192 : 16384; }
-constexpr uint32_t SM_TOT = SM_SMALL;     // fp32 [4][128] block totals of e^g
-constexpr uint32_t SM_BETA = SM_SMALL + 2048;   // fp32 [64]
-constexpr uint32_t SM_EGC = SM_BETA + 256;      // fp32 [128] e^{G_C}
-constexpr uint32_t SM_BAR = SM_EGC + 512;       // barriers (tma, mma, w), tmem base, flag
-constexpr uint32_t SM_TOTAL = SM_BAR + 64;
+constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals of e^g
+constexpr uint32_t SM_BETA = SM_SMALL + 2048;    // fp32 [64]
+constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base
+constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
 static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
-static_assert(SM_TOTAL + 1024 <= 232448, "shared memory");
+static_assert(64 * QT_LD * 4 <= 65536, "(q e^G) fits its region");
+static_assert(SM_LOCAL_TOTAL + 1024 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
-constexpr uint32_t TM_S = 0;      // S^T fp32 [128 x][128 c]
-constexpr uint32_t TM_SH = 128;   // S^T hi (bf16 pairs) [128 x][64]
-constexpr uint32_t TM_SL = 192;   // S^T lo
-constexpr uint32_t TM_VT = 256;   // v^T (bf16 pairs) [128 x][32]
-constexpr uint32_t TM_UH = 288;   // U^T hi [128 x][32]   (alias: (k e^G)^T hi [128 c][32])
-constexpr uint32_t TM_UL = 320;   // U^T lo               (alias: (k e^G)^T lo)
-constexpr uint32_t TM_KTH = TM_UH;
-constexpr uint32_t TM_KTL = TM_UL;
-constexpr uint32_t TM_AU = 352;   // U^T accumulator fp32 [128 x][64 r]
-constexpr uint32_t TM_AO = 416;   // O^T accumulator fp32 [128 x][64 r]   (alias: W^T [128 c][64 r])
-constexpr uint32_t TM_AP = 352;   // A/P accumulators (M = 64 layout): R=0 32 cols, R=1 64 cols
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TL_AP = 0;      // A/P accumulators (M = 64 layout): R=0 32 cols, R=1 64 cols
+constexpr uint32_t TL_KTH = 96;    // (k e^G)^T hi (bf16 pairs) [128 c][32]
+constexpr uint32_t TL_KTL = 128;   // (k e^G)^T lo
+constexpr uint32_t TL_VT = 160;    // v^T (bf16 pairs) [128 v][32]
+constexpr uint32_t TL_AW = 192;    // W^T accumulator fp32 [128 c][64 r], then (P W)^T
+constexpr uint32_t TL_AU = 256;    // U~^T accumulator fp32 [128 v][64 r], then (P U~)^T
+constexpr uint32_t TL_WT = 320;    // W^T (bf16 pairs) [128 c][32], A operand
+constexpr uint32_t TL_UH = 352;    // U~^T hi (bf16 pairs) [128 v][32], A operand
+constexpr uint32_t TL_UL = 384;    // U~^T lo
+constexpr uint32_t TL_COLS = 512;
 
-constexpr uint32_t kWaitIter = 1u << 26;
-
-__device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
-
-template <typename TOut>
 __global__ void __launch_bounds__(NT, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
-                const ChunkParams p) {
+chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
+                   const void* __restrict__ beta_ptr, const float scale, const Plan pl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte-swizzled TMA tiles need a 1024-byte aligned base
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float* beta_s = reinterpret_cast<float*>(smem + SM_BETA);   // [64]
-    float* egc_s = reinterpret_cast<float*>(smem + SM_EGC);     // [128]
     float* tot_s = reinterpret_cast<float*>(smem + SM_TOT);     // [4][128]
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
+    float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][QT_LD]
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
-    uint64_t* bar_w = bar_tma + 2;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 3);
-    int* flag_s = reinterpret_cast<int*>(bar_tma + 4);
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
+    const int H = pl.H;
+    const __nv_bfloat16* __restrict__ beta_g = reinterpret_cast<const __nv_bfloat16*>(beta_ptr);
 
-    const int H = p.H;
-    const int h = blockIdx.x % H;
-    const int rank = blockIdx.x / H;
-
-    // ---- sequence of this CTA: longest first when packed -------------------
-    __shared__ int s_seq;
-    int n = rank;
-    if (p.cu_seqlens != nullptr && p.N <= 1024) {
-        if (tid == 0) s_seq = rank;
-        __syncthreads();
-        for (int m = tid; m < p.N; m += NT) {
-            const int lm = seq_len_clamped(p.cu_seqlens, m, p.T);
-            int r = 0;
-            for (int x = 0; x < p.N; ++x) {
-                const int lx = seq_len_clamped(p.cu_seqlens, x, p.T);
-                r += (lx > lm) || (lx == lm && x < m);
-            }
-            if (r == rank) s_seq = m;
-        }
-        __syncthreads();
-        n = s_seq;
-    }
-    int64_t bos, eos;
-    if (p.cu_seqlens != nullptr) {
-        bos = min(max((int)p.cu_seqlens[n], 0), p.T);
-        eos = min(max((int)p.cu_seqlens[n + 1], 0), p.T);
-        if (eos < bos) eos = bos;
-    } else {
-        bos = (int64_t)n * p.T;
-        eos = bos + p.T;
-    }
-
-    if (warp == 0) tc::tmem_alloc(tmem_base_s, TM_COLS);
+    if (warp == 0) tc::tmem_alloc(tmem_base_s, TL_COLS);
     if (tid == 0) {
         tc::bar_init(bar_tma, 1);
         tc::bar_init(bar_mma, 1);
-        tc::bar_init(bar_w, 1);
         tc::bar_init_fence();
-        *flag_s = 0;
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -153,22 +187,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     tc::fence_after();
     const uint32_t tm = *tmem_base_s;
 
-    uint32_t tma_phase = 0, mma_phase = 0, w_phase = 0;
+    uint32_t tma_phase = 0, mma_phase = 0;
     bool failed = false;
-    bool tma_pending = false;  // a tile load was issued and not yet waited for
+    bool tma_pending = false;
 
-    auto issue_tma = [&](int64_t t0) {
+    auto issue_tma = [&](const Chunk& ch) {
         tc::bar_expect_tx(bar_tma, 4u * 16384u);
         const CUtensorMap* maps[4] = {&mq, &mk, &mv, &mg};
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int half = 0; half < 2; ++half)
-                tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, h, (int)t0, bar_tma);
+                tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, ch.h, (int)ch.c0, bar_tma);
     };
-    // Wait for the MMAs committed so far; all threads.
-    // One warp polls the barrier; the others park at the CTA barrier, so 16
-    // spinning warps do not compete with the tensor core for shared memory.
+    // One warp polls the barrier; the others park at the CTA barrier.
     auto wait_one = [&](uint64_t* bar, uint32_t& phase) {
         bool ok = true;
         if (warp == 0) ok = tc::bar_wait(bar, phase, kWaitIter);
@@ -185,58 +217,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         tc::fence_after();
     };
 
-    if (eos > bos) {
-        if (tid == 0) issue_tma(bos);
+    const uint32_t id_n64 = tc::idesc_bf16(128, 64);
+
+    int64_t task = blockIdx.x;
+    Chunk cur = decode_task(pl, task);
+    if (cur.valid) {
+        if (tid == 0) issue_tma(cur);
         tma_pending = true;
     }
 
-    // ---- initial state: S^T in TMEM (lane x holds row x of S^T = column x of S)
-    const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    {
-        const int x = (warp & 3) * 32 + lane;
-        const int cbeg = (warp >> 2) * 32;  // warpgroup w covers c in [32 w, 32 w + 32)
-        for (int cc = cbeg; cc < cbeg + 32; cc += 16) {
-            uint32_t r[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                r[i] = __float_as_uint(p.initial_state ? p.initial_state[sbase + (int64_t)(cc + i) * D + x] : 0.f);
-            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, r);
-        }
-        tc::tmem_st_wait();
-    }
+    while (cur.valid) {
+        const int h = cur.h;
+        const int64_t c0 = cur.c0;
+        const int L = (cur.eos - c0 < (int64_t)C) ? (int)(cur.eos - c0) : C;
+        uint8_t* slot = pl.slots + ((int64_t)cur.gc * H + h) * (int64_t)SLOT_BYTES;
+        const int64_t next_task = task + gridDim.x;
+        const Chunk nxt = decode_task(pl, next_task);
 
-    const uint32_t id_n64 = tc::idesc_bf16(128, 64);
-    const uint32_t id_n64_neg_bmn = tc::idesc_bf16(128, 64, true, true);
-    const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
-    const float scale = p.scale;
-    TOut* __restrict__ o = reinterpret_cast<TOut*>(p.o);
-    const __nv_bfloat16* __restrict__ beta_g = reinterpret_cast<const __nv_bfloat16*>(p.beta);
-
-    // S hi/lo from the fp32 state in TMEM (lane x; warpgroup splits columns).
-    auto s_epilogue = [&]() {
-        const int cc = (warp >> 2) * 32;
-        uint32_t a[32];
-        tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, a);
-        tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, a + 16);
-        tc::tmem_ld_wait();
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            __nv_bfloat16 h0, l0, h1, l1;
-            tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
-            tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
-            hi[i] = tc::pack_bf16(h0, h1);
-            lo[i] = tc::pack_bf16(l0, l1);
-        }
-        tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
-        tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
-        tc::tmem_st_wait();
-    };
-    s_epilogue();
-
-    for (int64_t c0 = bos; c0 < eos && !failed; c0 += C) {
-        const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
-        // ---- wait for this chunk's tiles ------------------------------------
         wait_one(bar_tma, tma_phase);
         tma_pending = false;
         if (failed) break;
@@ -288,7 +285,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         // Every build loop below gives a thread the same 8 channels [8 cg, 8 cg + 8).
         const int cg = (tid >> 3) & 15;
 
-        // ---- (3) A and P: two 32-token row blocks, reference at the block centre --
+        // ---- (2) A and P: two 32-token row blocks, reference at the block centre --
         // Both blocks' operands are built first (block 0 in OPB, block 1 in OPA),
         // then all their MMAs go out in one round.
 #pragma unroll
@@ -367,7 +364,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
 #pragma unroll
                 for (int R = 0; R < 2; ++R) {  // two independent accumulators, interleaved
-                    const uint32_t d = tm + TM_AP + 32 * R;
+                    const uint32_t d = tm + TL_AP + 32 * R;
                     const uint32_t id = R == 0 ? tc::idesc_bf16(64, 32) : tc::idesc_bf16(64, 64);
                     const uint32_t o = ks_ * 256;
                     tc::mma_ss_w(d, tc::dadv(ah[R], o), tc::dadv(bh[R], o), id, ks_ > 0);
@@ -377,8 +374,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             tc::commit_w(bar_mma);
         }
-        // ---- (2) (k e^G)^T and v^T into TMEM (lane = channel / value column), while
-        //      the A/P MMAs run (disjoint TMEM columns, no shared memory they read) --
+        // ---- (3) (k e^G)^T and v^T into TMEM (lane = channel / value column) and
+        //      e^{G_C} out, while the A/P MMAs run ---------------------------------
         {
             const int c = (warp & 3) * 32 + lane;
             const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
@@ -400,17 +397,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
                 vv[i] = tc::pack_bf16(v0, v1);
             }
-            tc::tmem_st8(tm + lane_base(warp) + TM_KTH + jb / 2, kh);
-            tc::tmem_st8(tm + lane_base(warp) + TM_KTL + jb / 2, kl);
-            tc::tmem_st8(tm + lane_base(warp) + TM_VT + jb / 2, vv);
-            if (tid < 128) egc_s[c] = t0v * t1v * t2v * tot_s[384 + c];
+            tc::tmem_st8(tm + lane_base(warp) + TL_KTH + jb / 2, kh);
+            tc::tmem_st8(tm + lane_base(warp) + TL_KTL + jb / 2, kl);
+            tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vv);
+            if (tid < 128)
+                reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * tot_s[384 + c];
         }
         tc::tmem_st_wait();
 
         mma_sync();
         if (failed) break;
 
-        // ---- (4) (q e^G) (K-major) and (k e^{G_C - G})^T (MN-major) operands -------
+        // ---- (4) (q e^G) fp32 into shared memory, Kbar = k e^{G_C - G} hi|lo out ----
         {
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
@@ -443,21 +441,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                     fq[u] = q[u] * (pf[u] * pr[u]);
                     fk[u] = k[u] * (sf[u] * __fdividef(tj[u], pr[u]));
                 }
+                *reinterpret_cast<float4*>(qt_s + r * QT_LD + 8 * cg) = make_float4(fq[0], fq[1], fq[2], fq[3]);
+                *reinterpret_cast<float4*>(qt_s + r * QT_LD + 8 * cg + 4) = make_float4(fq[4], fq[5], fq[6], fq[7]);
                 uint4 hi, lo;
-                tc::split8(fq, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_QT + tc::kmaj(r, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_QT + 16384 + tc::kmaj(r, 8 * cg, D)) = lo;
                 tc::split8(fk, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_KB + tc::mnmaj(8 * cg, r, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_KB + 16384 + tc::mnmaj(8 * cg, r, D)) = lo;
+                *reinterpret_cast<uint4*>(slot + SLOT_KH + tc::mnmaj(8 * cg, r, D)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_KL + tc::mnmaj(8 * cg, r, D)) = lo;
             }
         }
 
-        // staging is consumed: prefetch the next chunk into it
+        // staging is consumed: prefetch the next task into it
         tc::fence_async_smem();
         __syncthreads();
-        if (c0 + C < eos) {
-            if (tid == 0) issue_tma(c0 + C);
+        if (nxt.valid) {
+            if (tid == 0) issue_tma(nxt);
             tma_pending = true;
         }
 
@@ -474,8 +471,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < 32; ++u) a[u] = 0u;
             if (jb < ncol) {
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + jb, a);
-                tc::tmem_ld16(tm + lane_base(warp) + TM_AP + 32 * R + jb + 16, a + 16);
+                tc::tmem_ld16(tm + lane_base(warp) + TL_AP + 32 * R + jb, a);
+                tc::tmem_ld16(tm + lane_base(warp) + TL_AP + 32 * R + jb + 16, a + 16);
                 tc::tmem_ld_wait();
             }
             if (lane < 16) {
@@ -571,18 +568,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 __syncthreads();
             }
             {
-                // two lanes per (row a, 4 columns) of a 32 x 32 block, each summing half of
-                // the inner range; 256 items over 512 threads
+                // one thread per (row a, 4 columns) of a 32 x 32 block: 256 items
                 float* X = Y + 512;
-                const int item = tid >> 1, half = tid & 1;
-                const int a = item >> 3, b4 = item & 7;
-                {
+                const int a = tid >> 3, b4 = tid & 7;
+                if (tid < 256) {
                     const float* nrow = N + (32 + a) * MAT_LD;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                     // T11 is zero above its diagonal blocks: columns >= 16 start at row 16
-                    const int m0 = (b4 >= 4 ? 4 : 0) + half * (b4 >= 4 ? 2 : 4);
-                    const int m1 = b4 >= 4 ? m0 + 2 : m0 + 4;
-                    for (int m4 = m0; m4 < m1; ++m4) {
+                    for (int m4 = (b4 >= 4 ? 4 : 0); m4 < 8; ++m4) {
                         const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
                         const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
 #pragma unroll
@@ -591,31 +584,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                             acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
                         }
                     }
-                    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-                    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-                    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
-                    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
-                    if (half == 0) *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
+                    *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
                 }
                 __syncthreads();
-                {
+                if (tid < 256) {
                     const float* trow = T + (32 + a) * MAT_LD + 32;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    // T22 is zero above its diagonal blocks: rows < 16 stop at 16
-                    const int mlen = a < 16 ? 8 : 16;
-                    const int mb = half * mlen;
+                    const int mmax = a < 16 ? 16 : 32;  // T22 is zero above its diagonal blocks
 #pragma unroll 4
-                    for (int m = mb; m < mb + mlen; ++m) {
+                    for (int m = 0; m < mmax; ++m) {
                         const float tv = trow[m];
                         const float4 y = *reinterpret_cast<const float4*>(X + m * 32 + 4 * b4);
                         acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
                     }
-                    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 1);
-                    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 1);
-                    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 1);
-                    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 1);
-                    if (half == 0)
-                        *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                    *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
                 __syncthreads();
             }
@@ -624,7 +606,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 const int r = ((item >> 6) << 3) | (item & 7);
                 const int jg = (item >> 3) & 7;
                 float t[8];
-                // (jg is the same for both items of a thread)
                 const float4 a = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg);
                 const float4 b = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg + 4);
                 t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
@@ -638,179 +619,485 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         }
         publish();
 
-        // ---- W^T = (k e^G)^T (T Diag beta)^T into the U accumulator's columns (then
-        //      read out); O^T = S^T (q e^G)^T behind it on a second commit -------------
+        // ---- (7) W^T = (k e^G)^T (T Diag beta)^T,  U~^T = v^T (T Diag beta)^T -------
         if (warp == 0) {
-            const uint32_t tb = tc::smem_u32(smem + SM_TB), qt = tc::smem_u32(smem + SM_QT);
+            const uint32_t tb = tc::smem_u32(smem + SM_TB);
             const uint64_t tbh = tc::sdesc(tb, 128, C * 16), tbl = tc::sdesc(tb + 8192, 128, C * 16);
-            const uint64_t qth = tc::sdesc(qt, 128, D * 16), qtl = tc::sdesc(qt + 16384, 128, D * 16);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
                 const uint64_t bh = tc::dadv(tbh, ks_ * 256), bl = tc::dadv(tbl, ks_ * 256);
-                tc::mma_ts_w(tm + TM_AU, tm + TM_KTH + ks_ * 8, bh, id_n64, ks_ > 0);
-                tc::mma_ts_w(tm + TM_AU, tm + TM_KTH + ks_ * 8, bl, id_n64, 1);
-                tc::mma_ts_w(tm + TM_AU, tm + TM_KTL + ks_ * 8, bh, id_n64, 1);
-            }
-            tc::commit_w(bar_w);
-#pragma unroll
-            for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                const uint32_t sh = tm + TM_SH + ks_ * 8, sl = tm + TM_SL + ks_ * 8;
-                const uint64_t qh = tc::dadv(qth, ks_ * 256), ql = tc::dadv(qtl, ks_ * 256);
-                tc::mma_ts_w(tm + TM_AO, sh, qh, id_n64, ks_ > 0);
-                tc::mma_ts_w(tm + TM_AO, sh, ql, id_n64, 1);
-                tc::mma_ts_w(tm + TM_AO, sl, qh, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_KTH + ks_ * 8, bh, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TL_AU, tm + TL_VT + ks_ * 8, bh, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_KTH + ks_ * 8, bl, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AU, tm + TL_VT + ks_ * 8, bl, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_KTL + ks_ * 8, bh, id_n64, 1);
             }
             tc::commit_w(bar_mma);
         }
-        // decay the fp32 state by e^{G_C} while those MMAs run (they read S hi/lo,
-        // not the fp32 state; the K-bar^T U MMA accumulates into it later)
-        {
-            const int cc = (warp >> 2) * 32;
-            uint32_t s0[16], s1[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s0[i] = __float_as_uint(__uint_as_float(s0[i]) * egc_s[cc + i]);
-                s1[i] = __float_as_uint(__uint_as_float(s1[i]) * egc_s[cc + 16 + i]);
-            }
-            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc, s0);
-            tc::tmem_st16(tm + lane_base(warp) + TM_S + cc + 16, s1);
-            tc::tmem_st_wait();
-        }
-        wait_one(bar_w, w_phase);
+        mma_sync();
+        if (failed) break;
 
-        // ---- W out of TMEM into the B operand (MN-major: n = r, k = c) ----------
+        // ---- (8) W: bf16 image out and W^T as A operand; U~: fp32 out, hi/lo operand --
         {
-            const int c = (warp & 3) * 32 + lane;
+            const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
-            uint32_t a[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb, a);
+            uint32_t a[16], b[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
             tc::tmem_ld_wait();
+            uint32_t wt[8];
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
                 float w[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) w[u] = __uint_as_float(a[8 * g8 + u]);
-                *reinterpret_cast<uint4*>(smem + SM_WB + tc::mnmaj(rb + 8 * g8, c, C)) = tc::pack8(w);
+                const uint4 pk = tc::pack8(w);
+                *reinterpret_cast<uint4*>(slot + SLOT_WT + tc::mnmaj(rb + 8 * g8, x, C)) = pk;
+                wt[4 * g8 + 0] = pk.x; wt[4 * g8 + 1] = pk.y; wt[4 * g8 + 2] = pk.z; wt[4 * g8 + 3] = pk.w;
             }
-        }
-        publish();
-        mma_sync();  // S^T (q e^G)^T done as well
-
-        // ---- U^T = v^T (T Diag beta)^T - S^T W^T ---------------------------------
-        if (warp == 0) {
-            const uint32_t tb = tc::smem_u32(smem + SM_TB), wb = tc::smem_u32(smem + SM_WB);
-            const uint64_t tbh = tc::sdesc(tb, 128, C * 16), tbl = tc::sdesc(tb + 8192, 128, C * 16);
-            const uint64_t wbd = tc::sdesc(wb, C * 16, 128);
+            tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wt);
+            float* ut = reinterpret_cast<float*>(slot + SLOT_UT);
 #pragma unroll
-            for (int ks_ = 0; ks_ < C / 16; ++ks_) {
-                tc::mma_ts_w(tm + TM_AU, tm + TM_VT + ks_ * 8, tc::dadv(tbh, ks_ * 256), id_n64, ks_ > 0);
-                tc::mma_ts_w(tm + TM_AU, tm + TM_VT + ks_ * 8, tc::dadv(tbl, ks_ * 256), id_n64, 1);
-            }
-#pragma unroll
-            for (int ks_ = 0; ks_ < D / 16; ++ks_)
-                tc::mma_ts_w(tm + TM_AU, tm + TM_SH + ks_ * 8, tc::dadv(wbd, ks_ * 2 * C * 16), id_n64_neg_bmn, 1);
-            tc::commit_w(bar_mma);
-        }
-        mma_sync();
-
-        // ---- U hi/lo into TMEM -------------------------------------------------------
-        {
-            const int rb = (warp >> 2) * 16;
-            uint32_t a[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AU + rb, a);
-            tc::tmem_ld_wait();
+            for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
-                tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
+                tc::split_bf16(__uint_as_float(b[2 * i]), h0, l0);
+                tc::split_bf16(__uint_as_float(b[2 * i + 1]), h1, l1);
                 hi[i] = tc::pack_bf16(h0, h1);
                 lo[i] = tc::pack_bf16(l0, l1);
             }
-            tc::tmem_st8(tm + lane_base(warp) + TM_UH + rb / 2, hi);
-            tc::tmem_st8(tm + lane_base(warp) + TM_UL + rb / 2, lo);
+            tc::tmem_st8(tm + lane_base(warp) + TL_UH + rb / 2, hi);
+            tc::tmem_st8(tm + lane_base(warp) + TL_UL + rb / 2, lo);
             tc::tmem_st_wait();
         }
         publish();
 
-        // ---- O^T += U^T P^T ;  S^T += U^T (k e^{G_C-G}) --------------------------
+        // ---- (9) (P W)^T = W^T P^T,  (P U~)^T = U~^T P^T ---------------------------------
         if (warp == 0) {
-            const uint32_t pb = tc::smem_u32(smem + SM_PB), kb = tc::smem_u32(smem + SM_KB);
+            const uint32_t pb = tc::smem_u32(smem + SM_PB);
             const uint64_t pbh = tc::sdesc(pb, 128, C * 16), pbl = tc::sdesc(pb + 8192, 128, C * 16);
-            const uint64_t kbh = tc::sdesc(kb, D * 16, 128), kbl = tc::sdesc(kb + 16384, D * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
-                const uint32_t uh = tm + TM_UH + ks_ * 8, ul = tm + TM_UL + ks_ * 8;
-                const uint64_t ph = tc::dadv(pbh, ks_ * 256), pl = tc::dadv(pbl, ks_ * 256);
-                const uint64_t kh = tc::dadv(kbh, ks_ * 2 * D * 16), kl = tc::dadv(kbl, ks_ * 2 * D * 16);
-                tc::mma_ts_w(tm + TM_S, uh, kh, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TM_AO, uh, ph, id_n64, 1);
-                tc::mma_ts_w(tm + TM_S, uh, kl, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TM_AO, uh, pl, id_n64, 1);
-                tc::mma_ts_w(tm + TM_S, ul, kh, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TM_AO, ul, ph, id_n64, 1);
+                const uint64_t ph = tc::dadv(pbh, ks_ * 256), pl_ = tc::dadv(pbl, ks_ * 256);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_WT + ks_ * 8, ph, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, ph, id_n64, ks_ > 0);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_WT + ks_ * 8, pl_, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, pl_, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AU, tm + TL_UL + ks_ * 8, ph, id_n64, 1);
             }
             tc::commit_w(bar_mma);
         }
         mma_sync();
+        if (failed) break;
 
-        // ---- o out; S hi/lo for the next chunk ------------------------------------
+        // ---- (10) Qh = scale ((q e^G) - P W) hi|lo out, O_loc = scale P U~ out ------------
         {
             const int x = (warp & 3) * 32 + lane;
             const int rb = (warp >> 2) * 16;
-            const int cc = (warp >> 2) * 32;
-            uint32_t a[16], s0[16], s1[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_AO + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s0);
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc + 16, s1);
+            uint32_t a[16], b[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
             tc::tmem_ld_wait();
-            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(__uint_as_float(i < 8 ? s0[2 * i] : s1[2 * i - 16]), h0, l0);
-                tc::split_bf16(__uint_as_float(i < 8 ? s0[2 * i + 1] : s1[2 * i - 15]), h1, l1);
-                hi[i] = tc::pack_bf16(h0, h1);
-                lo[i] = tc::pack_bf16(l0, l1);
+            for (int g8 = 0; g8 < 2; ++g8) {
+                float qh[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int r = rb + 8 * g8 + u;
+                    qh[u] = scale * (qt_s[r * QT_LD + x] - __uint_as_float(a[8 * g8 + u]));
+                }
+                uint4 hi, lo;
+                tc::split8(qh, hi, lo);
+                *reinterpret_cast<uint4*>(slot + SLOT_QH + tc::mnmaj(rb + 8 * g8, x, C)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_QL + tc::mnmaj(rb + 8 * g8, x, C)) = lo;
             }
-            tc::tmem_st16(tm + lane_base(warp) + TM_SH + cc / 2, hi);
-            tc::tmem_st16(tm + lane_base(warp) + TM_SL + cc / 2, lo);
-            const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
+            float* ol = reinterpret_cast<float*>(slot + SLOT_OL);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (rb + i < L) o[ob + (int64_t)i * H * D] = from_f32<TOut>(scale * __uint_as_float(a[i]));
-            tc::tmem_st_wait();
+            for (int i = 0; i < 16; ++i) ol[(rb + i) * D + x] = scale * __uint_as_float(b[i]);
         }
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
+
+        task = next_task;
+        cur = nxt;
+    }
+
+    if (failed) {
+        // mark the slot of the task that could not finish (its e^{G_C} becomes NaN,
+        // which poisons the state of that sequence), then drain a tile load in flight
+        if (cur.valid && tid < 128)
+            reinterpret_cast<float*>(pl.slots + ((int64_t)cur.gc * H + cur.h) * (int64_t)SLOT_BYTES + SLOT_EGC)[tid] =
+                __int_as_float(0x7fc00000);
+        if (tma_pending && tid == 0) tc::bar_wait(bar_tma, tma_phase, kWaitIter);
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, TL_COLS);
+}
+
+// ============================================================================
+// Chunk bookkeeping for packed sequences
+// ============================================================================
+
+// chunk_off[n] = first global chunk of sequence n (exclusive prefix of
+// ceil(len / C)); order = sequences longest first (ties by index) when given;
+// chunk_seq[gc] = sequence of global chunk gc, -1 past the last chunk.
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024)
+chunk_plan_kernel(const int32_t* __restrict__ cu, int N, int T, int64_t max_chunks,
+                  int32_t* __restrict__ chunk_off, int32_t* __restrict__ order, int32_t* __restrict__ chunk_seq) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        const int cnt = n < N ? (seq_len_clamped(cu, n, T) + C - 1) / C : 0;
+        int v = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, d);
+            if (lane >= d) v += y;
+        }
+        if (lane == 31) warp_sums[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, d);
+                if (lane >= d) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int incl = v + (warp > 0 ? warp_sums[warp - 1] : 0);
+        const int carry = carry_s;
+        if (n < N) chunk_off[n] = carry + incl - cnt;
+        __syncthreads();
+        if (tid == 1023) carry_s = carry + incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_off[N] = carry_s;
+    if (order != nullptr) {
+        for (int m = tid; m < N; m += 1024) {
+            const int lm = seq_len_clamped(cu, m, T);
+            int r = 0;
+            for (int x = 0; x < N; ++x) {
+                const int lx = seq_len_clamped(cu, x, T);
+                r += (lx > lm) || (lx == lm && x < m);
+            }
+            order[r] = m;
+        }
+    }
+    __syncthreads();
+    const int total = chunk_off[N];
+    for (int64_t gc = tid; gc < max_chunks; gc += 1024) {
+        int s = -1;
+        if (gc < total) {
+            // the last sequence starting at or before gc holds it (empty ones are skipped)
+            int lo = 0, hi = N - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (chunk_off[mid] <= gc) lo = mid; else hi = mid - 1;
+            }
+            s = lo;
+        }
+        chunk_seq[gc] = s;
+    }
+}
+
+// ============================================================================
+// State kernel
+// ============================================================================
+
+// ---- shared memory map (bytes): the operand images of two chunks ---------------
+constexpr uint32_t SS_BAR = 2 * SLOT_IMG;   // barriers (img 0, img 1, u, o, s), tmem base
+constexpr uint32_t SS_TOTAL = SS_BAR + 64;
+static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
+
+// ---- tensor memory map (columns) ----------------------------------------------
+constexpr uint32_t TS_S = 0;      // S^T fp32 [128 v][128 c]
+constexpr uint32_t TS_SH = 128;   // S^T hi (bf16 pairs) [128 v][64]
+constexpr uint32_t TS_SL = 192;   // S^T lo
+constexpr uint32_t TS_AU = 256;   // U^T accumulator fp32 [128 v][64 r]
+constexpr uint32_t TS_AO = 320;   // O^T accumulator fp32 [128 v][64 r]
+constexpr uint32_t TS_UH = 384;   // U^T hi (bf16 pairs) [128 v][32]
+constexpr uint32_t TS_UL = 416;   // U^T lo
+constexpr uint32_t TS_COLS = 512;
+
+template <typename TOut>
+__global__ void __launch_bounds__(NT, 1)
+chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ final_state,
+                   TOut* __restrict__ o, const Plan pl) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t* bar_img = reinterpret_cast<uint64_t*>(smem + SS_BAR);  // [2]
+    uint64_t* bar_u = bar_img + 2;
+    uint64_t* bar_o = bar_img + 3;
+    uint64_t* bar_s = bar_img + 4;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 5);
+
+    const int H = pl.H;
+    const int h = blockIdx.x % H;
+    const int rank = blockIdx.x / H;
+    int n;
+    int64_t bos, eos, g0, nchunks;
+    if (pl.cu_seqlens == nullptr) {
+        n = rank;
+        bos = (int64_t)n * pl.T;
+        eos = bos + pl.T;
+        g0 = (int64_t)n * pl.cps;
+        nchunks = pl.cps;
+    } else {
+        n = pl.order != nullptr ? pl.order[rank] : rank;
+        bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
+        eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
+        if (eos < bos) eos = bos;
+        // (offsets that overlap can need more chunks than the workspace holds:
+        //  those are left out, never read past the end)
+        g0 = min((int64_t)pl.chunk_off[n], pl.max_chunks);
+        nchunks = min((int64_t)pl.chunk_off[n + 1], pl.max_chunks) - g0;
+        if (nchunks < 0) nchunks = 0;
+    }
+
+    if (warp == 0) tc::tmem_alloc(tmem_base_s, TS_COLS);
+    if (tid == 0) {
+#pragma unroll
+        for (int b = 0; b < 5; ++b) tc::bar_init(bar_img + b, 1);
+        tc::bar_init_fence();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tmem_base_s;
+
+    auto slot_of = [&](int64_t i) { return pl.slots + ((g0 + i) * H + h) * (int64_t)SLOT_BYTES; };
+    auto issue_img = [&](int64_t i) {
+        uint64_t* b = bar_img + (i & 1);
+        tc::bar_expect_tx(b, SLOT_IMG);
+        uint8_t* dst = smem + (i & 1) * SLOT_IMG;
+        const uint8_t* src = slot_of(i);
+#pragma unroll
+        for (int part = 0; part < 5; ++part) tc::bulk_load(dst + part * 16384, src + part * 16384, 16384, b);
+    };
+    if (tid == 0) {
+        if (nchunks > 0) issue_img(0);
+        if (nchunks > 1) issue_img(1);
+    }
+    int64_t issued = nchunks < 2 ? nchunks : 2, waited = 0;
+
+    bool failed = false;
+    uint32_t u_phase = 0, o_phase = 0, s_phase = 0;
+    auto wait_one = [&](uint64_t* bar, uint32_t parity) {
+        bool ok = true;
+        if (warp == 0) ok = tc::bar_wait(bar, parity, kWaitIter);
+        failed = __syncthreads_or(failed || !ok);
+        tc::fence_after();
+    };
+    auto publish = [&]() {
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+    };
+
+    // ---- initial state: S^T in TMEM (lane x holds row x of S^T = column x of S)
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    const int x = (warp & 3) * 32 + lane;   // TMEM lane: value column v
+    const int rb = (warp >> 2) * 16;        // accumulator columns (tokens) of this warp
+    const int cc = (warp >> 2) * 32;        // state columns (key channels) of this warp
+    {
+        for (int c = cc; c < cc + 32; c += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                r[i] = __float_as_uint(initial_state ? initial_state[sbase + (int64_t)(c + i) * D + x] : 0.f);
+            tc::tmem_st16(tm + lane_base(warp) + TS_S + c, r);
+        }
+        tc::tmem_st_wait();
+    }
+    // S hi/lo from the fp32 state in TMEM
+    auto s_epilogue = [&]() {
+        uint32_t a[32];
+        tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, a);
+        tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, a + 16);
+        tc::tmem_ld_wait();
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            __nv_bfloat16 h0, l0, h1, l1;
+            tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
+            tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
+            hi[i] = tc::pack_bf16(h0, h1);
+            lo[i] = tc::pack_bf16(l0, l1);
+        }
+        tc::tmem_st16(tm + lane_base(warp) + TS_SH + cc / 2, hi);
+        tc::tmem_st16(tm + lane_base(warp) + TS_SL + cc / 2, lo);
+        tc::tmem_st_wait();
+    };
+    s_epilogue();
+    publish();
+
+    const uint32_t id_n64_bmn = tc::idesc_bf16(128, 64, false, true);
+    const uint32_t id_n64_neg_bmn = tc::idesc_bf16(128, 64, true, true);
+    const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
+
+    for (int64_t i = 0; i < nchunks && !failed; ++i) {
+        const int64_t c0 = bos + i * C;
+        const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
+        const uint8_t* slot = slot_of(i);
+        // this thread's U~ and O_loc entries and e^{G_C} factors, fetched early
+        float ut[16], ol[16];
+        {
+            const float* utg = reinterpret_cast<const float*>(slot + SLOT_UT);
+            const float* olg = reinterpret_cast<const float*>(slot + SLOT_OL);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                ut[j] = utg[(rb + j) * D + x];
+                ol[j] = olg[(rb + j) * D + x];
+            }
+        }
+        float eg[32];
+        {
+            const float4* e4 = reinterpret_cast<const float4*>(slot + SLOT_EGC) + cc / 4;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 e = e4[j];
+                eg[4 * j] = e.x; eg[4 * j + 1] = e.y; eg[4 * j + 2] = e.z; eg[4 * j + 3] = e.w;
+            }
+        }
+
+        wait_one(bar_img + (i & 1), (uint32_t)((i >> 1) & 1));
+        ++waited;
+        if (failed) break;
+        const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
+
+        // ---- U^T = -S^T W^T (S hi only: the correction is single bf16), then
+        //      O^T = S^T Qh^T on a second commit ----------------------------------
+        if (warp == 0) {
+            const uint64_t wd = tc::sdesc(img + SLOT_WT, C * 16, 128);
+            const uint64_t qhd = tc::sdesc(img + SLOT_QH, C * 16, 128), qld = tc::sdesc(img + SLOT_QL, C * 16, 128);
+#pragma unroll
+            for (int ks_ = 0; ks_ < D / 16; ++ks_)
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(wd, ks_ * 2 * C * 16), id_n64_neg_bmn, ks_ > 0);
+            tc::commit_w(bar_u);
+#pragma unroll
+            for (int ks_ = 0; ks_ < D / 16; ++ks_) {
+                const uint32_t sh = tm + TS_SH + ks_ * 8, sl = tm + TS_SL + ks_ * 8;
+                const uint64_t bh = tc::dadv(qhd, ks_ * 2 * C * 16), bl = tc::dadv(qld, ks_ * 2 * C * 16);
+                tc::mma_ts_w(tm + TS_AO, sh, bh, id_n64_bmn, ks_ > 0);
+                tc::mma_ts_w(tm + TS_AO, sh, bl, id_n64_bmn, 1);
+                tc::mma_ts_w(tm + TS_AO, sl, bh, id_n64_bmn, 1);
+            }
+            tc::commit_w(bar_o);
+        }
+        // decay the fp32 state by e^{G_C} while those MMAs run (they read S hi/lo)
+        {
+            uint32_t s0[16], s1[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, s0);
+            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, s1);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[j]);
+                s1[j] = __float_as_uint(__uint_as_float(s1[j]) * eg[16 + j]);
+            }
+            tc::tmem_st16(tm + lane_base(warp) + TS_S + cc, s0);
+            tc::tmem_st16(tm + lane_base(warp) + TS_S + cc + 16, s1);
+            tc::tmem_st_wait();
+        }
+        wait_one(bar_u, u_phase);
+        u_phase ^= 1;
+        if (failed) break;
+
+        // ---- U = U~ - W S, hi/lo into TMEM ------------------------------------------
+        {
+            uint32_t a[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TS_AU + rb, a);
+            tc::tmem_ld_wait();
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                __nv_bfloat16 h0, l0, h1, l1;
+                tc::split_bf16(ut[2 * j] + __uint_as_float(a[2 * j]), h0, l0);
+                tc::split_bf16(ut[2 * j + 1] + __uint_as_float(a[2 * j + 1]), h1, l1);
+                hi[j] = tc::pack_bf16(h0, h1);
+                lo[j] = tc::pack_bf16(l0, l1);
+            }
+            tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
+            tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
+            tc::tmem_st_wait();
+        }
+        publish();
+
+        // ---- S^T += U^T Kbar ---------------------------------------------------------
+        if (warp == 0) {
+            const uint64_t khd = tc::sdesc(img + SLOT_KH, D * 16, 128), kld = tc::sdesc(img + SLOT_KL, D * 16, 128);
+#pragma unroll
+            for (int ks_ = 0; ks_ < C / 16; ++ks_) {
+                const uint32_t uh = tm + TS_UH + ks_ * 8, ul = tm + TS_UL + ks_ * 8;
+                const uint64_t bh = tc::dadv(khd, ks_ * 2 * D * 16), bl = tc::dadv(kld, ks_ * 2 * D * 16);
+                tc::mma_ts_w(tm + TS_S, uh, bh, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_S, uh, bl, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_S, ul, bh, id_n128_bmn, 1);
+            }
+            tc::commit_w(bar_s);
+        }
+
+        // ---- o = O_loc + S Qh ------------------------------------------------------------
+        wait_one(bar_o, o_phase);
+        o_phase ^= 1;
+        if (failed) break;
+        {
+            uint32_t a[16];
+            tc::tmem_ld16(tm + lane_base(warp) + TS_AO + rb, a);
+            tc::tmem_ld_wait();
+            const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol[j] + __uint_as_float(a[j]));
+        }
+
+        // ---- S hi/lo for the next chunk; refill this image buffer ---------------------
+        wait_one(bar_s, s_phase);
+        s_phase ^= 1;
+        if (failed) break;
+        s_epilogue();
+        if (i + 2 < nchunks) {
+            if (tid == 0) issue_img(i + 2);
+            issued = i + 3;
+        }
+        publish();
     }
 
     // ---- final state -----------------------------------------------------------
-    if (failed && tma_pending) {
-        // drain a tile load that may still be in flight before the CTA exits
-        tc::bar_wait(bar_tma, tma_phase, kWaitIter);
+    if (failed && tid == 0) {
+        // drain image loads that may still be in flight before the CTA exits
+        for (int64_t j = waited; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
     }
-    if (p.final_state) {
-        const int x = (warp & 3) * 32 + lane;
-        const int cbeg = (warp >> 2) * 32;
-        for (int cc = cbeg; cc < cbeg + 32; cc += 16) {
+    if (final_state) {
+        for (int c = cc; c < cc + 32; c += 16) {
             uint32_t s[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TM_S + cc, s);
+            tc::tmem_ld16(tm + lane_base(warp) + TS_S + c, s);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                p.final_state[sbase + (int64_t)(cc + i) * D + x] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(s[i]);
+            for (int j = 0; j < 16; ++j)
+                final_state[sbase + (int64_t)(c + j) * D + x] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(s[j]);
         }
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tm, TS_COLS);
 }
+
+// ============================================================================
+// Host side
+// ============================================================================
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -842,22 +1129,107 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Library-owned stream-ordered memory pool, one per device, that keeps what it
+// has reserved (release threshold = unlimited), so repeated calls reuse it.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pool[kMaxDevices];
+bool g_pool_ready[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+cudaError_t device_pool(cudaMemPool_t* pool, int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (!g_pool_ready[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        e = cudaMemPoolCreate(&g_pool[dev], &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_pool_ready[dev] = true;
+    }
+    *pool = g_pool[dev];
+    *sms = g_sm_count[dev];
+    return cudaSuccess;
+}
+
 template <typename TOut>
 cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
-    const int64_t blocks = (int64_t)p.N * p.H;
-    if (blocks == 0) return cudaSuccess;
-    const int64_t rows = (int64_t)p.B * p.T;
-    CUtensorMap mq, mk, mv, mg;
-    const int64_t map_rows = rows > 0 ? rows : 1;
-    if (!make_map(&mq, p.q, map_rows, p.H) || !make_map(&mk, p.k, map_rows, p.H) ||
-        !make_map(&mv, p.v, map_rows, p.H) || !make_map(&mg, p.g, map_rows, p.H))
-        return cudaErrorInvalidValue;
-    auto kern = chunk_tc_kernel<TOut>;
-    const int smem_bytes = (int)SM_TOTAL + 1024;  // + alignment slack
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    const int64_t NH = (int64_t)p.N * p.H;
+    if (NH == 0) return cudaSuccess;
+    const bool packed = p.cu_seqlens != nullptr;
+    Plan pl{};
+    pl.cu_seqlens = p.cu_seqlens;
+    pl.T = p.T;
+    pl.H = p.H;
+    pl.N = p.N;
+    pl.cps = packed ? 0 : (p.T + C - 1) / C;
+    pl.max_chunks = packed ? ((int64_t)p.T + C - 1) / C + p.N : (int64_t)p.B * pl.cps;
+    const size_t hdr_ints = packed ? (size_t)(2 * (int64_t)p.N + 1) + (size_t)pl.max_chunks : 0;
+    const size_t hdr_bytes = (hdr_ints * 4 + 1023) & ~size_t(1023);
+    const size_t bytes = hdr_bytes + (size_t)pl.max_chunks * (size_t)p.H * SLOT_BYTES;
+
+    cudaMemPool_t pool;
+    int sms = 0;
+    cudaError_t e = device_pool(&pool, &sms);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)blocks, NT, smem_bytes, st>>>(mq, mk, mv, mg, p);
-    return cudaGetLastError();
+    void* ws = nullptr;
+    if (bytes > 0) {
+        e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+        if (e != cudaSuccess) return cudaErrorMemoryAllocation;
+    }
+    int32_t* hdr = reinterpret_cast<int32_t*>(ws);
+    pl.slots = reinterpret_cast<uint8_t*>(ws) + hdr_bytes;
+    if (packed) {
+        pl.chunk_off = hdr;
+        pl.order = p.N <= 1024 ? hdr + (p.N + 1) : nullptr;
+        pl.chunk_seq = hdr + (2 * (int64_t)p.N + 1);
+        chunk_plan_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.N, p.T, pl.max_chunks,
+                                              const_cast<int32_t*>(pl.chunk_off), const_cast<int32_t*>(pl.order),
+                                              const_cast<int32_t*>(pl.chunk_seq));
+        e = cudaGetLastError();
+    }
+    const int64_t tasks = pl.max_chunks * p.H;
+    if (e == cudaSuccess && tasks > 0) {
+        const int64_t rows = (int64_t)p.B * p.T;
+        CUtensorMap mq, mk, mv, mg;
+        if (!make_map(&mq, p.q, rows, p.H) || !make_map(&mk, p.k, rows, p.H) ||
+            !make_map(&mv, p.v, rows, p.H) || !make_map(&mg, p.g, rows, p.H)) {
+            e = cudaErrorInvalidValue;
+        } else {
+            const int smem_bytes = (int)SM_LOCAL_TOTAL + 1024;  // + alignment slack
+            e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            if (e == cudaSuccess) {
+                const int64_t grid = tasks < sms ? tasks : sms;
+                chunk_local_kernel<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, p.beta, p.scale, pl);
+                e = cudaGetLastError();
+            }
+        }
+    }
+    if (e == cudaSuccess) {
+        auto kern = chunk_state_kernel<TOut>;
+        const int smem_bytes = (int)SS_TOTAL + 128;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e == cudaSuccess) {
+            kern<<<(unsigned)NH, NT, smem_bytes, st>>>(p.initial_state, p.final_state, reinterpret_cast<TOut*>(p.o), pl);
+            e = cudaGetLastError();
+        }
+    }
+    if (ws != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(ws, st);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e;
 }
 
 }  // namespace
