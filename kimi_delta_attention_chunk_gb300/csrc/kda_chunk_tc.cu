@@ -59,15 +59,15 @@ constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TME
 constexpr uint32_t kWaitIter = 1u << 26;
 
 // ---- workspace slot of one (chunk, head), written by the local kernel --------
-constexpr uint32_t SLOT_WT = 0;         // W (bf16) as B operand, MN-major (n = r, k = c)
-constexpr uint32_t SLOT_QH = 16384;     // Qh hi, same layout
-constexpr uint32_t SLOT_QL = 32768;     // Qh lo
+constexpr uint32_t SLOT_WQ = 0;         // [-W | Qh hi] (bf16) as one B operand, MN-major
+                                        //   (n = r for -W, n = 64 + r for Qh; k = c)
+constexpr uint32_t SLOT_QL = 32768;     // Qh lo as B operand, MN-major (n = r, k = c)
 constexpr uint32_t SLOT_KH = 49152;     // Kbar hi as B operand, MN-major (n = c, k = r)
 constexpr uint32_t SLOT_KL = 65536;     // Kbar lo
-constexpr uint32_t SLOT_IMG = 81920;    // bytes of the five operand images above
-constexpr uint32_t SLOT_UT = 81920;     // U~ fp32 [64 r][128 v]
-constexpr uint32_t SLOT_OL = 114688;    // O_loc fp32 [64 r][128 v]
-constexpr uint32_t SLOT_EGC = 147456;   // e^{G_C} fp32 [128]
+constexpr uint32_t SLOT_EGC = 81920;    // e^{G_C} fp32 [128]
+constexpr uint32_t SLOT_IMG = 82432;    // bytes of the images above (one shared-memory copy)
+constexpr uint32_t SLOT_UT = 82432;     // U~ fp32 [64 r][128 v]
+constexpr uint32_t SLOT_OL = 115200;    // O_loc fp32 [64 r][128 v]
 constexpr uint32_t SLOT_BYTES = 147968;
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
@@ -652,7 +652,9 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int u = 0; u < 8; ++u) w[u] = __uint_as_float(a[8 * g8 + u]);
                 const uint4 pk = tc::pack8(w);
-                *reinterpret_cast<uint4*>(slot + SLOT_WT + tc::mnmaj(rb + 8 * g8, x, C)) = pk;
+                // the state kernel needs -W (bf16 negation is exact)
+                *reinterpret_cast<uint4*>(slot + SLOT_WQ + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
+                    make_uint4(pk.x ^ 0x80008000u, pk.y ^ 0x80008000u, pk.z ^ 0x80008000u, pk.w ^ 0x80008000u);
                 wt[4 * g8 + 0] = pk.x; wt[4 * g8 + 1] = pk.y; wt[4 * g8 + 2] = pk.z; wt[4 * g8 + 3] = pk.w;
             }
             tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wt);
@@ -710,7 +712,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 }
                 uint4 hi, lo;
                 tc::split8(qh, hi, lo);
-                *reinterpret_cast<uint4*>(slot + SLOT_QH + tc::mnmaj(rb + 8 * g8, x, C)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_WQ + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
                 *reinterpret_cast<uint4*>(slot + SLOT_QL + tc::mnmaj(rb + 8 * g8, x, C)) = lo;
             }
             float* ol = reinterpret_cast<float*>(slot + SLOT_OL);
@@ -815,23 +817,30 @@ chunk_plan_kernel(const int32_t* __restrict__ cu, int N, int T, int64_t max_chun
 // State kernel
 // ============================================================================
 
-// ---- shared memory map (bytes): the operand images of two chunks ---------------
-constexpr uint32_t SS_BAR = 2 * SLOT_IMG;   // barriers (img 0, img 1, u, o, s), tmem base
-constexpr uint32_t SS_TOTAL = SS_BAR + 64;
+// Warps 0..15 do the TMEM epilogues (warp w: TMEM lanes 32 (w % 4).., column
+// group w / 4); warp 16 only issues MMAs and bulk copies.  The two sides meet
+// at mbarriers: MMA commits (u, o, s) and the epilogue warps' arrivals
+// (uready: U hi/lo written, sready: S hi/lo written), each once per chunk.
+constexpr int NT2 = 544;
+constexpr int ISSUER = 16;
+
+// ---- shared memory map (bytes): the images of two chunks, then barriers --------
+constexpr uint32_t SS_BAR = 2 * SLOT_IMG;   // img 0, img 1, u, o, s, uready, sready; tmem base; abort flag
+constexpr uint32_t SS_TOTAL = SS_BAR + 128;
 static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
 constexpr uint32_t TS_S = 0;      // S^T fp32 [128 v][128 c]
 constexpr uint32_t TS_SH = 128;   // S^T hi (bf16 pairs) [128 v][64]
 constexpr uint32_t TS_SL = 192;   // S^T lo
-constexpr uint32_t TS_AU = 256;   // U^T accumulator fp32 [128 v][64 r]
-constexpr uint32_t TS_AO = 320;   // O^T accumulator fp32 [128 v][64 r]
+constexpr uint32_t TS_AU = 256;   // U^T accumulator fp32 [128 v][64 r]   } one N = 128
+constexpr uint32_t TS_AO = 320;   // O^T accumulator fp32 [128 v][64 r]   } accumulator
 constexpr uint32_t TS_UH = 384;   // U^T hi (bf16 pairs) [128 v][32]
 constexpr uint32_t TS_UL = 416;   // U^T lo
 constexpr uint32_t TS_COLS = 512;
 
 template <typename TOut>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT2, 1)
 chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ final_state,
                    TOut* __restrict__ o, const Plan pl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -841,7 +850,10 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
     uint64_t* bar_u = bar_img + 2;
     uint64_t* bar_o = bar_img + 3;
     uint64_t* bar_s = bar_img + 4;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 5);
+    uint64_t* bar_uready = bar_img + 5;
+    uint64_t* bar_sready = bar_img + 6;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 7);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 8);
 
     const int H = pl.H;
     const int h = blockIdx.x % H;
@@ -870,6 +882,9 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
     if (tid == 0) {
 #pragma unroll
         for (int b = 0; b < 5; ++b) tc::bar_init(bar_img + b, 1);
+        tc::bar_init(bar_uready, 16);
+        tc::bar_init(bar_sready, 16);
+        *abort_s = 0;
         tc::bar_init_fence();
     }
     tc::fence_before();
@@ -878,165 +893,54 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
     const uint32_t tm = *tmem_base_s;
 
     auto slot_of = [&](int64_t i) { return pl.slots + ((g0 + i) * H + h) * (int64_t)SLOT_BYTES; };
-    auto issue_img = [&](int64_t i) {
-        uint64_t* b = bar_img + (i & 1);
-        tc::bar_expect_tx(b, SLOT_IMG);
-        uint8_t* dst = smem + (i & 1) * SLOT_IMG;
-        const uint8_t* src = slot_of(i);
-#pragma unroll
-        for (int part = 0; part < 5; ++part) tc::bulk_load(dst + part * 16384, src + part * 16384, 16384, b);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return tc::bar_wait_or_abort(bar, parity, kWaitIter, abort_s);
     };
-    if (tid == 0) {
-        if (nchunks > 0) issue_img(0);
-        if (nchunks > 1) issue_img(1);
-    }
-    int64_t issued = nchunks < 2 ? nchunks : 2, waited = 0;
-
-    bool failed = false;
-    uint32_t u_phase = 0, o_phase = 0, s_phase = 0;
-    auto wait_one = [&](uint64_t* bar, uint32_t parity) {
-        bool ok = true;
-        if (warp == 0) ok = tc::bar_wait(bar, parity, kWaitIter);
-        failed = __syncthreads_or(failed || !ok);
-        tc::fence_after();
-    };
-    auto publish = [&]() {
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-    };
-
-    // ---- initial state: S^T in TMEM (lane x holds row x of S^T = column x of S)
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    const int x = (warp & 3) * 32 + lane;   // TMEM lane: value column v
-    const int rb = (warp >> 2) * 16;        // accumulator columns (tokens) of this warp
-    const int cc = (warp >> 2) * 32;        // state columns (key channels) of this warp
-    {
-        for (int c = cc; c < cc + 32; c += 16) {
-            uint32_t r[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                r[i] = __float_as_uint(initial_state ? initial_state[sbase + (int64_t)(c + i) * D + x] : 0.f);
-            tc::tmem_st16(tm + lane_base(warp) + TS_S + c, r);
-        }
-        tc::tmem_st_wait();
-    }
-    // S hi/lo from the fp32 state in TMEM
-    auto s_epilogue = [&]() {
-        uint32_t a[32];
-        tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, a);
-        tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, a + 16);
-        tc::tmem_ld_wait();
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            __nv_bfloat16 h0, l0, h1, l1;
-            tc::split_bf16(__uint_as_float(a[2 * i]), h0, l0);
-            tc::split_bf16(__uint_as_float(a[2 * i + 1]), h1, l1);
-            hi[i] = tc::pack_bf16(h0, h1);
-            lo[i] = tc::pack_bf16(l0, l1);
-        }
-        tc::tmem_st16(tm + lane_base(warp) + TS_SH + cc / 2, hi);
-        tc::tmem_st16(tm + lane_base(warp) + TS_SL + cc / 2, lo);
-        tc::tmem_st_wait();
-    };
-    s_epilogue();
-    publish();
 
-    const uint32_t id_n64_bmn = tc::idesc_bf16(128, 64, false, true);
-    const uint32_t id_n64_neg_bmn = tc::idesc_bf16(128, 64, true, true);
-    const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
-
-    for (int64_t i = 0; i < nchunks && !failed; ++i) {
-        const int64_t c0 = bos + i * C;
-        const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
-        const uint8_t* slot = slot_of(i);
-        // this thread's U~ and O_loc entries and e^{G_C} factors, fetched early
-        float ut[16], ol[16];
-        {
-            const float* utg = reinterpret_cast<const float*>(slot + SLOT_UT);
-            const float* olg = reinterpret_cast<const float*>(slot + SLOT_OL);
+    if (warp == ISSUER) {
+        // ================= MMA and copy issue =================
+        auto issue_img = [&](int64_t i) {
+            if (lane == 0) {
+                uint64_t* b = bar_img + (i & 1);
+                tc::bar_expect_tx(b, SLOT_IMG);
+                uint8_t* dst = smem + (i & 1) * SLOT_IMG;
+                const uint8_t* src = slot_of(i);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                ut[j] = utg[(rb + j) * D + x];
-                ol[j] = olg[(rb + j) * D + x];
+                for (int part = 0; part < 5; ++part) tc::bulk_load(dst + part * 16384, src + part * 16384, 16384, b);
+                tc::bulk_load(dst + SLOT_EGC, src + SLOT_EGC, SLOT_IMG - SLOT_EGC, b);
             }
-        }
-        float eg[32];
-        {
-            const float4* e4 = reinterpret_cast<const float4*>(slot + SLOT_EGC) + cc / 4;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 e = e4[j];
-                eg[4 * j] = e.x; eg[4 * j + 1] = e.y; eg[4 * j + 2] = e.z; eg[4 * j + 3] = e.w;
-            }
-        }
-
-        wait_one(bar_img + (i & 1), (uint32_t)((i >> 1) & 1));
-        ++waited;
-        if (failed) break;
-        const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
-
-        // ---- U^T = -S^T W^T (S hi only: the correction is single bf16), then
-        //      O^T = S^T Qh^T on a second commit ----------------------------------
-        if (warp == 0) {
-            const uint64_t wd = tc::sdesc(img + SLOT_WT, C * 16, 128);
-            const uint64_t qhd = tc::sdesc(img + SLOT_QH, C * 16, 128), qld = tc::sdesc(img + SLOT_QL, C * 16, 128);
+            __syncwarp();
+        };
+        int64_t issued = 0, done = 0;  // image loads issued / known complete
+        if (nchunks > 0) { issue_img(0); issued = 1; }
+        if (nchunks > 1) { issue_img(1); issued = 2; }
+        const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
+        const uint32_t id_n64_bmn = tc::idesc_bf16(128, 64, false, true);
+        for (int64_t i = 0; i < nchunks; ++i) {
+            const uint32_t par = (uint32_t)(i & 1);
+            if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+            done = i + 1;
+            if (!wait(bar_sready, par)) break;
+            tc::fence_after();
+            const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
+            // [U^T | O^T] = S_hi^T [-W | Qh_hi]^T, then O^T += S_hi^T Qh_lo^T + S_lo^T Qh_hi^T
+            const uint64_t wq = tc::sdesc(img + SLOT_WQ, 2 * C * 16, 128);
+            const uint64_t qh = tc::sdesc(img + SLOT_WQ + 8 * 128, 2 * C * 16, 128);
+            const uint64_t ql = tc::sdesc(img + SLOT_QL, C * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_)
-                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(wd, ks_ * 2 * C * 16), id_n64_neg_bmn, ks_ > 0);
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(wq, ks_ * 2 * 2 * C * 16), id_n128_bmn, ks_ > 0);
             tc::commit_w(bar_u);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                const uint32_t sh = tm + TS_SH + ks_ * 8, sl = tm + TS_SL + ks_ * 8;
-                const uint64_t bh = tc::dadv(qhd, ks_ * 2 * C * 16), bl = tc::dadv(qld, ks_ * 2 * C * 16);
-                tc::mma_ts_w(tm + TS_AO, sh, bh, id_n64_bmn, ks_ > 0);
-                tc::mma_ts_w(tm + TS_AO, sh, bl, id_n64_bmn, 1);
-                tc::mma_ts_w(tm + TS_AO, sl, bh, id_n64_bmn, 1);
+                tc::mma_ts_w(tm + TS_AO, tm + TS_SH + ks_ * 8, tc::dadv(ql, ks_ * 2 * C * 16), id_n64_bmn, 1);
+                tc::mma_ts_w(tm + TS_AO, tm + TS_SL + ks_ * 8, tc::dadv(qh, ks_ * 2 * 2 * C * 16), id_n64_bmn, 1);
             }
             tc::commit_w(bar_o);
-        }
-        // decay the fp32 state by e^{G_C} while those MMAs run (they read S hi/lo)
-        {
-            uint32_t s0[16], s1[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, s0);
-            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, s1);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[j]);
-                s1[j] = __float_as_uint(__uint_as_float(s1[j]) * eg[16 + j]);
-            }
-            tc::tmem_st16(tm + lane_base(warp) + TS_S + cc, s0);
-            tc::tmem_st16(tm + lane_base(warp) + TS_S + cc + 16, s1);
-            tc::tmem_st_wait();
-        }
-        wait_one(bar_u, u_phase);
-        u_phase ^= 1;
-        if (failed) break;
-
-        // ---- U = U~ - W S, hi/lo into TMEM ------------------------------------------
-        {
-            uint32_t a[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TS_AU + rb, a);
-            tc::tmem_ld_wait();
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(ut[2 * j] + __uint_as_float(a[2 * j]), h0, l0);
-                tc::split_bf16(ut[2 * j + 1] + __uint_as_float(a[2 * j + 1]), h1, l1);
-                hi[j] = tc::pack_bf16(h0, h1);
-                lo[j] = tc::pack_bf16(l0, l1);
-            }
-            tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
-            tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
-            tc::tmem_st_wait();
-        }
-        publish();
-
-        // ---- S^T += U^T Kbar ---------------------------------------------------------
-        if (warp == 0) {
+            // S^T += U^T Kbar once U hi/lo are in TMEM (the decay came before them)
+            if (!wait(bar_uready, par)) break;
+            tc::fence_after();
             const uint64_t khd = tc::sdesc(img + SLOT_KH, D * 16, 128), kld = tc::sdesc(img + SLOT_KL, D * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
@@ -1047,47 +951,152 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
                 tc::mma_ts_w(tm + TS_S, ul, bh, id_n128_bmn, 1);
             }
             tc::commit_w(bar_s);
+            // this image buffer is free once every MMA of the chunk has completed
+            if (i + 2 < nchunks) {
+                if (!wait(bar_s, par)) break;
+                issue_img(i + 2);
+                issued = i + 3;
+            }
         }
-
-        // ---- o = O_loc + S Qh ------------------------------------------------------------
-        wait_one(bar_o, o_phase);
-        o_phase ^= 1;
-        if (failed) break;
-        {
-            uint32_t a[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TS_AO + rb, a);
-            tc::tmem_ld_wait();
-            const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol[j] + __uint_as_float(a[j]));
-        }
-
-        // ---- S hi/lo for the next chunk; refill this image buffer ---------------------
-        wait_one(bar_s, s_phase);
-        s_phase ^= 1;
-        if (failed) break;
-        s_epilogue();
-        if (i + 2 < nchunks) {
-            if (tid == 0) issue_img(i + 2);
-            issued = i + 3;
-        }
-        publish();
-    }
-
-    // ---- final state -----------------------------------------------------------
-    if (failed && tid == 0) {
         // drain image loads that may still be in flight before the CTA exits
-        for (int64_t j = waited; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
-    }
-    if (final_state) {
+        if (*abort_s && lane == 0)
+            for (int64_t j = done; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
+    } else {
+        // ================= TMEM epilogues =================
+        const int x = (warp & 3) * 32 + lane;   // TMEM lane: value column v
+        const int rb = (warp >> 2) * 16;        // accumulator columns (tokens) of this warp
+        const int cc = (warp >> 2) * 32;        // state columns (key channels) of this warp
+        auto arrive = [&](uint64_t* bar) {
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::bar_arrive(bar);
+        };
+        // S hi/lo from the fp32 state in TMEM, 16 columns at a time
+        auto s_epilogue = [&]() {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t a[16];
+                tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16 * half, a);
+                tc::tmem_ld_wait();
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    __nv_bfloat16 h0, l0, h1, l1;
+                    tc::split_bf16(__uint_as_float(a[2 * j]), h0, l0);
+                    tc::split_bf16(__uint_as_float(a[2 * j + 1]), h1, l1);
+                    hi[j] = tc::pack_bf16(h0, h1);
+                    lo[j] = tc::pack_bf16(l0, l1);
+                }
+                tc::tmem_st8(tm + lane_base(warp) + TS_SH + cc / 2 + 8 * half, hi);
+                tc::tmem_st8(tm + lane_base(warp) + TS_SL + cc / 2 + 8 * half, lo);
+            }
+            tc::tmem_st_wait();
+        };
+        // initial state: S^T in TMEM (lane x holds row x of S^T = column x of S)
         for (int c = cc; c < cc + 32; c += 16) {
-            uint32_t s[16];
-            tc::tmem_ld16(tm + lane_base(warp) + TS_S + c, s);
-            tc::tmem_ld_wait();
+            uint32_t r[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                final_state[sbase + (int64_t)(c + j) * D + x] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(s[j]);
+                r[j] = __float_as_uint(initial_state ? initial_state[sbase + (int64_t)(c + j) * D + x] : 0.f);
+            tc::tmem_st16(tm + lane_base(warp) + TS_S + c, r);
+        }
+        tc::tmem_st_wait();
+        s_epilogue();
+        arrive(bar_sready);
+
+        // this thread's U~ and O_loc entries of a chunk, fetched a chunk ahead so
+        // that their global-memory latency hides behind a whole chunk
+        float ut[16], ol[16];
+        auto fetch_ut = [&](int64_t i) {
+            const float* g = reinterpret_cast<const float*>(slot_of(i) + SLOT_UT);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ut[j] = g[(rb + j) * D + x];
+        };
+        auto fetch_ol = [&](int64_t i) {
+            const float* g = reinterpret_cast<const float*>(slot_of(i) + SLOT_OL);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ol[j] = g[(rb + j) * D + x];
+        };
+        if (nchunks > 0) {
+            fetch_ut(0);
+            fetch_ol(0);
+        }
+        for (int64_t i = 0; i < nchunks; ++i) {
+            const uint32_t par = (uint32_t)(i & 1);
+            const int64_t c0 = bos + i * C;
+            const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
+            const bool more = i + 1 < nchunks;
+
+            // decay the fp32 state by e^{G_C} (the MMAs under way read S hi/lo)
+            if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+            {
+                const float* eg = reinterpret_cast<const float*>(smem + (i & 1) * SLOT_IMG + SLOT_EGC) + cc;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t s0[16];
+                    tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16 * half, s0);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[16 * half + j]);
+                    tc::tmem_st16(tm + lane_base(warp) + TS_S + cc + 16 * half, s0);
+                }
+                tc::tmem_st_wait();
+            }
+
+            // U = U~ - W S, hi/lo into TMEM
+            if (!wait(bar_u, par)) break;
+            tc::fence_after();
+            {
+                uint32_t a[16];
+                tc::tmem_ld16(tm + lane_base(warp) + TS_AU + rb, a);
+                tc::tmem_ld_wait();
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    __nv_bfloat16 h0, l0, h1, l1;
+                    tc::split_bf16(ut[2 * j] + __uint_as_float(a[2 * j]), h0, l0);
+                    tc::split_bf16(ut[2 * j + 1] + __uint_as_float(a[2 * j + 1]), h1, l1);
+                    hi[j] = tc::pack_bf16(h0, h1);
+                    lo[j] = tc::pack_bf16(l0, l1);
+                }
+                tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
+                tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
+                tc::tmem_st_wait();
+            }
+            arrive(bar_uready);
+            if (more) fetch_ut(i + 1);
+
+            // o = O_loc + S Qh
+            if (!wait(bar_o, par)) break;
+            tc::fence_after();
+            {
+                uint32_t a[16];
+                tc::tmem_ld16(tm + lane_base(warp) + TS_AO + rb, a);
+                tc::tmem_ld_wait();
+                const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol[j] + __uint_as_float(a[j]));
+            }
+            if (more) fetch_ol(i + 1);
+
+            // S hi/lo for the next chunk
+            if (!wait(bar_s, par)) break;
+            tc::fence_after();
+            s_epilogue();
+            arrive(bar_sready);
+        }
+        // ---- final state ---------------------------------------------------------
+        if (final_state) {
+            const bool failed = *abort_s != 0;
+            for (int c = cc; c < cc + 32; c += 16) {
+                uint32_t sv[16];
+                tc::tmem_ld16(tm + lane_base(warp) + TS_S + c, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    final_state[sbase + (int64_t)(c + j) * D + x] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(sv[j]);
+            }
         }
     }
     tc::fence_before();
@@ -1221,7 +1230,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
         const int smem_bytes = (int)SS_TOTAL + 128;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e == cudaSuccess) {
-            kern<<<(unsigned)NH, NT, smem_bytes, st>>>(p.initial_state, p.final_state, reinterpret_cast<TOut*>(p.o), pl);
+            kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(p.initial_state, p.final_state, reinterpret_cast<TOut*>(p.o), pl);
             e = cudaGetLastError();
         }
     }

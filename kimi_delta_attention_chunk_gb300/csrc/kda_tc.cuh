@@ -153,6 +153,28 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_
     return false;
 }
 
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bounded wait that also gives up as soon as *abort is set by another thread;
+// on running out of iterations it sets *abort itself.  false if it gave up.
+__device__ __forceinline__ bool bar_wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t max_iter,
+                                                  volatile int* abort) {
+    for (uint32_t it = 0; it < max_iter; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+            "p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 63) == 63 && *abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
 // ---- TMA -------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
