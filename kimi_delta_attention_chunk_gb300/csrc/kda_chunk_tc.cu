@@ -387,11 +387,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const int j = jb + 2 * i;
                 const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
                 const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], h0, l0);
-                tc::split_bf16(k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], h1, l1);
-                kh[i] = tc::pack_bf16(h0, h1);
-                kl[i] = tc::pack_bf16(l0, l1);
+                tc::split2(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], kh[i], kl[i]);
                 const __nv_bfloat16 z = __float2bfloat16(0.f);
                 const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
                 const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
@@ -664,11 +660,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                tc::split_bf16(__uint_as_float(b[2 * i]), h0, l0);
-                tc::split_bf16(__uint_as_float(b[2 * i + 1]), h1, l1);
-                hi[i] = tc::pack_bf16(h0, h1);
-                lo[i] = tc::pack_bf16(l0, l1);
+                tc::split2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]), hi[i], lo[i]);
             }
             tc::tmem_st8(tm + lane_base(warp) + TL_UH + rb / 2, hi);
             tc::tmem_st8(tm + lane_base(warp) + TL_UL + rb / 2, lo);
@@ -824,9 +816,11 @@ chunk_plan_kernel(const int32_t* __restrict__ cu, int N, int T, int64_t max_chun
 constexpr int NT2 = 544;
 constexpr int ISSUER = 16;
 
-// ---- shared memory map (bytes): the images of two chunks, then barriers --------
-constexpr uint32_t SS_BAR = 2 * SLOT_IMG;   // img 0, img 1, u, o, s, uready, sready; tmem base; abort flag
-constexpr uint32_t SS_TOTAL = SS_BAR + 128;
+// ---- shared memory map (bytes) -------------------------------------------------
+constexpr uint32_t SS_UT = 2 * SLOT_IMG;    // images of two chunks, then U~ and O_loc of one chunk
+constexpr uint32_t SS_OL = SS_UT + 32768;
+constexpr uint32_t SS_BAR = SS_OL + 32768;  // img 0, img 1, u, o, s, ut, ol, uready, oready, sready;
+constexpr uint32_t SS_TOTAL = SS_BAR + 128; //   tmem base; abort flag
 static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
@@ -841,8 +835,8 @@ constexpr uint32_t TS_COLS = 512;
 
 template <typename TOut>
 __global__ void __launch_bounds__(NT2, 1)
-chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ final_state,
-                   TOut* __restrict__ o, const Plan pl) {
+chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restrict__ initial_state,
+                   float* __restrict__ final_state, TOut* __restrict__ o, const Plan pl) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -850,10 +844,15 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
     uint64_t* bar_u = bar_img + 2;
     uint64_t* bar_o = bar_img + 3;
     uint64_t* bar_s = bar_img + 4;
-    uint64_t* bar_uready = bar_img + 5;
-    uint64_t* bar_sready = bar_img + 6;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 7);
-    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 8);
+    uint64_t* bar_ut = bar_img + 5;
+    uint64_t* bar_ol = bar_img + 6;
+    uint64_t* bar_uready = bar_img + 7;
+    uint64_t* bar_oready = bar_img + 8;
+    uint64_t* bar_sready = bar_img + 9;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 10);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 11);
+    const float* ut_s = reinterpret_cast<const float*>(smem + SS_UT);   // U~ [64 r][128 v]
+    const float* ol_s = reinterpret_cast<const float*>(smem + SS_OL);   // O_loc [64 r][128 v]
 
     const int H = pl.H;
     const int h = blockIdx.x % H;
@@ -881,8 +880,9 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
     if (warp == 0) tc::tmem_alloc(tmem_base_s, TS_COLS);
     if (tid == 0) {
 #pragma unroll
-        for (int b = 0; b < 5; ++b) tc::bar_init(bar_img + b, 1);
+        for (int b = 0; b < 7; ++b) tc::bar_init(bar_img + b, 1);
         tc::bar_init(bar_uready, 16);
+        tc::bar_init(bar_oready, 16);
         tc::bar_init(bar_sready, 16);
         *abort_s = 0;
         tc::bar_init_fence();
@@ -912,8 +912,23 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
             }
             __syncwarp();
         };
+        // U~ and O_loc of one chunk (single buffers, refilled once consumed)
+        auto issue_vec = [&](int64_t i, uint64_t* bar, uint32_t sm_off, uint32_t slot_off) {
+            if (lane == 0) {
+                tc::bar_expect_tx(bar, 32768);
+                tc::bulk_load(smem + sm_off, slot_of(i) + slot_off, 32768, bar);
+            }
+            __syncwarp();
+        };
         int64_t issued = 0, done = 0;  // image loads issued / known complete
-        if (nchunks > 0) { issue_img(0); issued = 1; }
+        int64_t ut_issued = 0, ol_issued = 0;
+        if (nchunks > 0) {
+            issue_img(0);
+            issue_vec(0, bar_ut, SS_UT, SLOT_UT);
+            issue_vec(0, bar_ol, SS_OL, SLOT_OL);
+            issued = 1;
+            ut_issued = ol_issued = 1;
+        }
         if (nchunks > 1) { issue_img(1); issued = 2; }
         const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
         const uint32_t id_n64_bmn = tc::idesc_bf16(128, 64, false, true);
@@ -951,16 +966,43 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
                 tc::mma_ts_w(tm + TS_S, ul, bh, id_n128_bmn, 1);
             }
             tc::commit_w(bar_s);
+            // U~ of this chunk is consumed (U hi/lo are written): fetch the next one
+            if (i + 1 < nchunks) {
+                issue_vec(i + 1, bar_ut, SS_UT, SLOT_UT);
+                ut_issued = i + 2;
+            }
+            // the o epilogue is through: write the chunk's o rows (staged in this
+            // image buffer's [-W | Qh] region) and fetch the next O_loc
+            if (!wait(bar_oready, par)) break;
+            {
+                // (a sequence's ragged last chunk is stored by the epilogue warps)
+                const int64_t c0 = bos + i * C;
+                if (eos - c0 >= C && lane == 0) {
+                    tc::tma_store_3d(&mo, smem + (i & 1) * SLOT_IMG + SLOT_WQ, 0, h, (int)c0);
+                    tc::bulk_commit();
+                }
+            }
+            if (i + 1 < nchunks) {
+                issue_vec(i + 1, bar_ol, SS_OL, SLOT_OL);
+                ol_issued = i + 2;
+            }
             // this image buffer is free once every MMA of the chunk has completed
+            // and the o rows have left it
             if (i + 2 < nchunks) {
                 if (!wait(bar_s, par)) break;
+                tc::bulk_wait_read();
+                __syncwarp();
                 issue_img(i + 2);
                 issued = i + 3;
             }
         }
-        // drain image loads that may still be in flight before the CTA exits
-        if (*abort_s && lane == 0)
+        tc::bulk_wait();
+        // drain loads that may still be in flight before the CTA exits
+        if (*abort_s && lane == 0) {
             for (int64_t j = done; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
+            if (ut_issued > 0) tc::bar_wait(bar_ut, (uint32_t)((ut_issued - 1) & 1), kWaitIter);
+            if (ol_issued > 0) tc::bar_wait(bar_ol, (uint32_t)((ol_issued - 1) & 1), kWaitIter);
+        }
     } else {
         // ================= TMEM epilogues =================
         const int x = (warp & 3) * 32 + lane;   // TMEM lane: value column v
@@ -971,21 +1013,18 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
             __syncwarp();
             if (lane == 0) tc::bar_arrive(bar);
         };
-        // S hi/lo from the fp32 state in TMEM, 16 columns at a time
+        // S hi/lo from the fp32 state in TMEM
         auto s_epilogue = [&]() {
+            uint32_t a[32];
+            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, a);
+            tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, a + 16);
+            tc::tmem_ld_wait();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                uint32_t a[16];
-                tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16 * half, a);
-                tc::tmem_ld_wait();
                 uint32_t hi[8], lo[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    __nv_bfloat16 h0, l0, h1, l1;
-                    tc::split_bf16(__uint_as_float(a[2 * j]), h0, l0);
-                    tc::split_bf16(__uint_as_float(a[2 * j + 1]), h1, l1);
-                    hi[j] = tc::pack_bf16(h0, h1);
-                    lo[j] = tc::pack_bf16(l0, l1);
+                    tc::split2(__uint_as_float(a[16 * half + 2 * j]), __uint_as_float(a[16 * half + 2 * j + 1]), hi[j], lo[j]);
                 }
                 tc::tmem_st8(tm + lane_base(warp) + TS_SH + cc / 2 + 8 * half, hi);
                 tc::tmem_st8(tm + lane_base(warp) + TS_SL + cc / 2 + 8 * half, lo);
@@ -1004,47 +1043,31 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
         s_epilogue();
         arrive(bar_sready);
 
-        // this thread's U~ and O_loc entries of a chunk, fetched a chunk ahead so
-        // that their global-memory latency hides behind a whole chunk
-        float ut[16], ol[16];
-        auto fetch_ut = [&](int64_t i) {
-            const float* g = reinterpret_cast<const float*>(slot_of(i) + SLOT_UT);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ut[j] = g[(rb + j) * D + x];
-        };
-        auto fetch_ol = [&](int64_t i) {
-            const float* g = reinterpret_cast<const float*>(slot_of(i) + SLOT_OL);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ol[j] = g[(rb + j) * D + x];
-        };
-        if (nchunks > 0) {
-            fetch_ut(0);
-            fetch_ol(0);
-        }
         for (int64_t i = 0; i < nchunks; ++i) {
             const uint32_t par = (uint32_t)(i & 1);
             const int64_t c0 = bos + i * C;
             const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
-            const bool more = i + 1 < nchunks;
 
             // decay the fp32 state by e^{G_C} (the MMAs under way read S hi/lo)
             if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
             {
                 const float* eg = reinterpret_cast<const float*>(smem + (i & 1) * SLOT_IMG + SLOT_EGC) + cc;
+                uint32_t s0[16], s1[16];
+                tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, s0);
+                tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, s1);
+                tc::tmem_ld_wait();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t s0[16];
-                    tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16 * half, s0);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[16 * half + j]);
-                    tc::tmem_st16(tm + lane_base(warp) + TS_S + cc + 16 * half, s0);
+                for (int j = 0; j < 16; ++j) {
+                    s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[j]);
+                    s1[j] = __float_as_uint(__uint_as_float(s1[j]) * eg[16 + j]);
                 }
+                tc::tmem_st16(tm + lane_base(warp) + TS_S + cc, s0);
+                tc::tmem_st16(tm + lane_base(warp) + TS_S + cc + 16, s1);
                 tc::tmem_st_wait();
             }
 
             // U = U~ - W S, hi/lo into TMEM
-            if (!wait(bar_u, par)) break;
+            if (!wait(bar_ut, par) || !wait(bar_u, par)) break;
             tc::fence_after();
             {
                 uint32_t a[16];
@@ -1053,32 +1076,37 @@ chunk_state_kernel(const float* __restrict__ initial_state, float* __restrict__ 
                 uint32_t hi[8], lo[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    __nv_bfloat16 h0, l0, h1, l1;
-                    tc::split_bf16(ut[2 * j] + __uint_as_float(a[2 * j]), h0, l0);
-                    tc::split_bf16(ut[2 * j + 1] + __uint_as_float(a[2 * j + 1]), h1, l1);
-                    hi[j] = tc::pack_bf16(h0, h1);
-                    lo[j] = tc::pack_bf16(l0, l1);
+                    tc::split2(ut_s[(rb + 2 * j) * D + x] + __uint_as_float(a[2 * j]), ut_s[(rb + 2 * j + 1) * D + x] + __uint_as_float(a[2 * j + 1]), hi[j], lo[j]);
                 }
                 tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
                 tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
                 tc::tmem_st_wait();
             }
             arrive(bar_uready);
-            if (more) fetch_ut(i + 1);
 
-            // o = O_loc + S Qh
-            if (!wait(bar_o, par)) break;
+            // o = O_loc + S Qh (while the state-update MMAs run); a full chunk is staged
+            // as [64 r][128 v] in the [-W | Qh] image region, which the MMAs of this
+            // chunk are done with, for one tiled store by the issuer
+            if (!wait(bar_ol, par) || !wait(bar_o, par)) break;
             tc::fence_after();
             {
                 uint32_t a[16];
                 tc::tmem_ld16(tm + lane_base(warp) + TS_AO + rb, a);
                 tc::tmem_ld_wait();
-                const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
+                if (L == C) {
+                    TOut* ost = reinterpret_cast<TOut*>(smem + (i & 1) * SLOT_IMG + SLOT_WQ);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol[j] + __uint_as_float(a[j]));
+                    for (int j = 0; j < 16; ++j)
+                        ost[(rb + j) * D + x] = from_f32<TOut>(ol_s[(rb + j) * D + x] + __uint_as_float(a[j]));
+                } else {
+                    const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol_s[(rb + j) * D + x] + __uint_as_float(a[j]));
+                }
             }
-            if (more) fetch_ol(i + 1);
+            tc::fence_async_smem();
+            arrive(bar_oready);
 
             // S hi/lo for the next chunk
             if (!wait(bar_s, par)) break;
@@ -1123,6 +1151,21 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     }
     return fn;
+}
+
+// [rows][H][128] output tensor; box = 64 rows x 128 values of one head, no swizzle.
+template <typename TOut>
+bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * sizeof(TOut), (cuuint64_t)H * D * sizeof(TOut)};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    cuuint32_t es[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        sizeof(TOut) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return fn(m, dt, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // [rows][H][128] bf16 tensor; box = 64 rows x 64 channels of one head, 128B swizzle.
@@ -1228,10 +1271,17 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
     if (e == cudaSuccess) {
         auto kern = chunk_state_kernel<TOut>;
         const int smem_bytes = (int)SS_TOTAL + 128;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (e == cudaSuccess) {
-            kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(p.initial_state, p.final_state, reinterpret_cast<TOut*>(p.o), pl);
-            e = cudaGetLastError();
+        CUtensorMap mo;
+        const int64_t rows = (int64_t)p.B * p.T;
+        if (!make_out_map<TOut>(&mo, p.o, rows > 0 ? rows : 1, p.H)) {
+            e = cudaErrorInvalidValue;
+        } else {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            if (e == cudaSuccess) {
+                kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(mo, p.initial_state, p.final_state,
+                                                           reinterpret_cast<TOut*>(p.o), pl);
+                e = cudaGetLastError();
+            }
         }
     }
     if (ws != nullptr) {

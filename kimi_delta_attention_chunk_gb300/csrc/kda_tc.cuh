@@ -195,12 +195,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-// ---- bf16 helpers ------------------------------------------------------------
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): a 16-bit-significand split.
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+// Tiled TMA store shared -> global in the calling thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- bf16 helpers ------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 even, __nv_bfloat16 odd) {
     return (uint32_t)__bfloat16_as_ushort(even) | ((uint32_t)__bfloat16_as_ushort(odd) << 16);
 }
@@ -223,26 +231,26 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c >> 3) & 7) ^ (r & 7)) << 4) + (c & 7) * 2);
 }
 
-__device__ __forceinline__ uint4 pack8(const float* x) {
-    uint4 u;
-    u.x = pack_bf16(__float2bfloat16_rn(x[0]), __float2bfloat16_rn(x[1]));
-    u.y = pack_bf16(__float2bfloat16_rn(x[2]), __float2bfloat16_rn(x[3]));
-    u.z = pack_bf16(__float2bfloat16_rn(x[4]), __float2bfloat16_rn(x[5]));
-    u.w = pack_bf16(__float2bfloat16_rn(x[6]), __float2bfloat16_rn(x[7]));
-    return u;
+// Two floats rounded to bf16 in one conversion: a in the low half, b in the high half.
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
-// 8 values -> 16 bytes of bf16 hi and 16 bytes of bf16 lo (x = hi + lo); the
-// residual is taken against the packed hi (bf16 -> fp32 is a 16-bit shift).
+// a = hi.lo16 + lo.lo16, b = hi.hi16 + lo.hi16 (x = hi + lo split of two values);
+// the residual is taken against the packed hi (bf16 -> fp32 is a 16-bit shift).
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack2(a, b);
+    lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
+__device__ __forceinline__ uint4 pack8(const float* x) {
+    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+}
+// 8 values -> 16 bytes of bf16 hi and 16 bytes of bf16 lo (x = hi + lo).
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-    hi = pack8(x);
-    const uint32_t w[4] = {hi.x, hi.y, hi.z, hi.w};
-    float l[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        l[2 * i] = x[2 * i] - __uint_as_float(w[i] << 16);
-        l[2 * i + 1] = x[2 * i + 1] - __uint_as_float(w[i] & 0xffff0000u);
-    }
-    lo = pack8(l);
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
 }
 __device__ __forceinline__ void unpack8(uint4 u, float* x) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
