@@ -71,6 +71,9 @@ constexpr uint32_t SLOT_OL = 115200;    // O_loc fp32 [64 r][128 v]
 constexpr uint32_t SLOT_BYTES = 147968;
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
+// (q e^G) fp32 [64 r][128 c] in shared memory: float4 column f of row r stored at
+// f ^ (r % 8), so both the row-blocked writes and the column reads are conflict-free
+__device__ __forceinline__ int qt_idx(int r, int c) { return r * 128 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
 
 // Work description shared by the kernels.  Sequences are either B dense rows
 // of T tokens (cu_seqlens == nullptr) or packed by cu_seqlens; chunks are
@@ -93,21 +96,25 @@ struct Chunk {
     bool valid;
 };
 
+// (the host keeps the number of tasks below 2^31, so the divisions are 32-bit)
 __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
     Chunk ch{};
     ch.valid = false;
     if (task >= pl.max_chunks * pl.H) return ch;
-    ch.gc = task / pl.H;
-    ch.h = (int)(task % pl.H);
+    const uint32_t t = (uint32_t)task, H = (uint32_t)pl.H;
+    const uint32_t gc = t / H;
+    ch.gc = gc;
+    ch.h = (int)(t - gc * H);
     if (pl.cu_seqlens == nullptr) {
-        const int64_t n = ch.gc / pl.cps, j = ch.gc % pl.cps;
-        ch.c0 = n * pl.T + j * C;
-        ch.eos = n * pl.T + pl.T;
+        const uint32_t cps = (uint32_t)pl.cps;
+        const uint32_t n = gc / cps, j = gc - n * cps;
+        ch.c0 = (int64_t)n * pl.T + (int64_t)j * C;
+        ch.eos = (int64_t)n * pl.T + pl.T;
     } else {
-        const int n = pl.chunk_seq[ch.gc];
+        const int n = pl.chunk_seq[gc];
         if (n < 0) return ch;
         const int64_t bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
-        ch.c0 = bos + (ch.gc - pl.chunk_off[n]) * C;
+        ch.c0 = bos + (int64_t)(gc - (uint32_t)pl.chunk_off[n]) * C;
         ch.eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
     }
     ch.valid = true;
@@ -120,11 +127,11 @@ __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
 
 // ---- shared memory map (bytes) ----------------------------------------------
 constexpr uint32_t SM_STG = 0;             // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
-constexpr uint32_t SM_OPA = 65536;         // 64 KB, A/P phase: row block 1's L hi|lo (A op [64 i][128 c])
-                                           //   and Rt hi|lo (B op [64 j][128 c]); then (q e^G) fp32 [64][QT_LD]
-constexpr uint32_t SM_QT = SM_OPA;
-constexpr int QT_LD = 132;
-constexpr uint32_t SM_OPB = 131072;        // 48 KB, A/P phase: row block 0's L hi|lo and Rt hi|lo (32 rows); then
+constexpr uint32_t SM_OPA = 65536;         // 64 KB, A/P phase: L hi|lo (A op [128 i][128 c]); then
+                                           //   (q e^G) fp32 [64][128]
+constexpr uint32_t SM_QT = SM_OPA;         //   (float4 columns XOR-swizzled by row) and the staged Kbar
+constexpr uint32_t SM_KST = SM_OPA + 32768;//   images, later the staged [-W | Qh hi] image
+constexpr uint32_t SM_OPB = 131072;        // 48 KB, A/P phase: Rt hi|lo (B op [96 j][128 c]); then
 constexpr uint32_t SM_TB = SM_OPB;         //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
 constexpr uint32_t SM_PB = SM_OPB + 16384; //   P hi|lo, B op [64 r][64 j] K-major
 constexpr uint32_t SM_PRE = 180224;        // fp32 [64][PRE_LD] in-block prefix products of e^g,
@@ -133,20 +140,18 @@ constexpr int MAT_LD = 68;
 constexpr uint32_t SM_AF = SM_PRE;
 constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
 constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
-// A/P operands of row block R: L (A, [64 i][128 c]) and Rt (B, [32 (R+1) j][128 c]), hi then lo
-__host__ __device__ constexpr uint32_t sm_l(int R) { return R == 0 ? SM_OPB : SM_OPA; }
-__host__ __device__ constexpr uint32_t sm_rt(int R) { return R == 0 ? SM_OPB + 32768 : SM_OPA + 32768; }
-__host__ __device__ constexpr uint32_t rt_lo(int R) { return R == 0 ? 8192 : 16384; }
+// A/P operands of both row blocks R: L rows 64 R + i (i < 32: k rows, else q rows of
+// block R), Rt rows j (block 0, j < 32) and 32 + j (block 1, j < 64)
+constexpr uint32_t RT_LO = 96 * D * 2;
 constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals of e^g
 constexpr uint32_t SM_BETA = SM_SMALL + 2048;    // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base
 constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
 static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
-static_assert(64 * QT_LD * 4 <= 65536, "(q e^G) fits its region");
 static_assert(SM_LOCAL_TOTAL + 1024 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
-constexpr uint32_t TL_AP = 0;      // A/P accumulators (M = 64 layout): R=0 32 cols, R=1 64 cols
+constexpr uint32_t TL_AP = 0;      // [L_0; L_1] [Rt_0 | Rt_1]^T accumulator, M = 128, N = 96
 constexpr uint32_t TL_KTH = 96;    // (k e^G)^T hi (bf16 pairs) [128 c][32]
 constexpr uint32_t TL_KTL = 128;   // (k e^G)^T lo
 constexpr uint32_t TL_VT = 160;    // v^T (bf16 pairs) [128 v][32]
@@ -156,6 +161,9 @@ constexpr uint32_t TL_WT = 320;    // W^T (bf16 pairs) [128 c][32], A operand
 constexpr uint32_t TL_UH = 352;    // U~^T hi (bf16 pairs) [128 v][32], A operand
 constexpr uint32_t TL_UL = 384;    // U~^T lo
 constexpr uint32_t TL_COLS = 512;
+// Thread that issues the tile loads and bulk stores: warps 8..15 are idle while
+// warps 0..7 invert the diagonal blocks of T, so the issue costs no barrier time.
+constexpr int kIssueTid = 256;
 
 __global__ void __launch_bounds__(NT, 1)
 chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -168,7 +176,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     float* beta_s = reinterpret_cast<float*>(smem + SM_BETA);   // [64]
     float* tot_s = reinterpret_cast<float*>(smem + SM_TOT);     // [4][128]
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
-    float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][QT_LD]
+    float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][128], swizzled
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -219,11 +227,22 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
     const uint32_t id_n64 = tc::idesc_bf16(128, 64);
 
+    // beta of a task, fetched into registers of threads kIssueTid .. + 63 when its
+    // tiles are requested
+    const int bt = tid - kIssueTid;
+    auto fetch_beta = [&](const Chunk& ch) {
+        float b = 0.f;
+        if (bt >= 0 && bt < C && ch.c0 + bt < ch.eos) b = __bfloat162float(beta_g[(ch.c0 + bt) * H + ch.h]);
+        return b;
+    };
+
     int64_t task = blockIdx.x;
     Chunk cur = decode_task(pl, task);
+    float beta_r = 0.f;
     if (cur.valid) {
-        if (tid == 0) issue_tma(cur);
+        if (tid == kIssueTid) issue_tma(cur);
         tma_pending = true;
+        beta_r = fetch_beta(cur);
     }
 
     while (cur.valid) {
@@ -234,6 +253,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const int64_t next_task = task + gridDim.x;
         const Chunk nxt = decode_task(pl, next_task);
 
+        // shared memory written by bulk stores of the previous task is reused only
+        // once they have read it: U~ (A/T region) before pass 1, the last group
+        // (O_loc, [-W | Qh], Qh lo in the operand regions) before the A/P operands
+        if (tid == kIssueTid) tc::bulk_wait_read_but1();
         wait_one(bar_tma, tma_phase);
         tma_pending = false;
         if (failed) break;
@@ -279,19 +302,21 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tot_s[J * 128 + c] = run;
         }
-        if (tid < C) beta_s[tid] = tid < L ? __bfloat162float(beta_g[(c0 + tid) * H + h]) : 0.f;
+        if (bt >= 0 && bt < C) beta_s[bt] = beta_r;
+        if (tid == kIssueTid) tc::bulk_wait_read();
         __syncthreads();
 
         // Every build loop below gives a thread the same 8 channels [8 cg, 8 cg + 8).
         const int cg = (tid >> 3) & 15;
 
         // ---- (2) A and P: two 32-token row blocks, reference at the block centre --
-        // Both blocks' operands are built first (block 0 in OPB, block 1 in OPA),
-        // then all their MMAs go out in one round.
+        // Both blocks' operands are stacked (L rows 64 R + i, Rt rows of block 1 after
+        // those of block 0) and multiplied in one M = 128, N = 96 round; the two
+        // off-diagonal products of the stack are not used.
 #pragma unroll
         for (int R = 0; R < 2; ++R) {
             const int nrows = 32 * (R + 1);  // columns j of this block's products
-            // L_R (A operand [64 i][128 c]): i < 32 k-rows, i >= 32 q-rows of block R;
+            // L_R (A operand rows 64 R + i): i < 32 k-rows, i >= 32 q-rows of block R;
             // e^{G_r - G_mid} = pre_r / tot_{2R} before the centre, pre_r after it
             float itc[8];
             ld_tot8(2 * R, 8 * cg, itc);
@@ -310,10 +335,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int u = 0; u < 8; ++u) f[u] = x[u] * (first ? pr[u] * itc[u] : pr[u]);
                 uint4 hi, lo;
                 tc::split8(f, hi, lo);
-                *reinterpret_cast<uint4*>(smem + sm_l(R) + tc::kmaj(i, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + sm_l(R) + 16384 + tc::kmaj(i, 8 * cg, D)) = lo;
+                *reinterpret_cast<uint4*>(smem + SM_OPA + tc::kmaj(64 * R + i, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_OPA + 32768 + tc::kmaj(64 * R + i, 8 * cg, D)) = lo;
             }
-            // Rt_R (B operand [nrows j][128 c]): e^{G_mid - G_j} k_j =
+            // Rt_R (B operand rows 32 R + j): e^{G_mid - G_j} k_j =
             //   1 / pre_j after the centre, tot_J / pre_j * prod_{J < J2 <= 2R} tot_J2 before it
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
@@ -345,32 +370,22 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int u = 0; u < 8; ++u) f[u] = x[u] * m[u];
                 uint4 hi, lo;
                 tc::split8(f, hi, lo);
-                *reinterpret_cast<uint4*>(smem + sm_rt(R) + tc::kmaj(j, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + sm_rt(R) + rt_lo(R) + tc::kmaj(j, 8 * cg, D)) = lo;
+                *reinterpret_cast<uint4*>(smem + SM_OPB + tc::kmaj(32 * R + j, 8 * cg, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_OPB + RT_LO + tc::kmaj(32 * R + j, 8 * cg, D)) = lo;
             }
         }
         publish();
         if (warp == 0) {
-            uint64_t ah[2], al[2], bh[2], bl[2];
-#pragma unroll
-            for (int R = 0; R < 2; ++R) {
-                const uint32_t la = tc::smem_u32(smem + sm_l(R)), rb = tc::smem_u32(smem + sm_rt(R));
-                ah[R] = tc::sdesc(la, 128, D * 16);
-                al[R] = tc::sdesc(la + 16384, 128, D * 16);
-                bh[R] = tc::sdesc(rb, 128, D * 16);
-                bl[R] = tc::sdesc(rb + rt_lo(R), 128, D * 16);
-            }
+            const uint32_t la = tc::smem_u32(smem + SM_OPA), rb = tc::smem_u32(smem + SM_OPB);
+            const uint64_t ah = tc::sdesc(la, 128, D * 16), al = tc::sdesc(la + 32768, 128, D * 16);
+            const uint64_t bh = tc::sdesc(rb, 128, D * 16), bl = tc::sdesc(rb + RT_LO, 128, D * 16);
+            const uint32_t id = tc::idesc_bf16(128, 96);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-#pragma unroll
-                for (int R = 0; R < 2; ++R) {  // two independent accumulators, interleaved
-                    const uint32_t d = tm + TL_AP + 32 * R;
-                    const uint32_t id = R == 0 ? tc::idesc_bf16(64, 32) : tc::idesc_bf16(64, 64);
-                    const uint32_t o = ks_ * 256;
-                    tc::mma_ss_w(d, tc::dadv(ah[R], o), tc::dadv(bh[R], o), id, ks_ > 0);
-                    tc::mma_ss_w(d, tc::dadv(ah[R], o), tc::dadv(bl[R], o), id, 1);
-                    tc::mma_ss_w(d, tc::dadv(al[R], o), tc::dadv(bh[R], o), id, 1);
-                }
+                const uint32_t o = ks_ * 256;
+                tc::mma_ss_w(tm + TL_AP, tc::dadv(ah, o), tc::dadv(bh, o), id, ks_ > 0);
+                tc::mma_ss_w(tm + TL_AP, tc::dadv(ah, o), tc::dadv(bl, o), id, 1);
+                tc::mma_ss_w(tm + TL_AP, tc::dadv(al, o), tc::dadv(bh, o), id, 1);
             }
             tc::commit_w(bar_mma);
         }
@@ -437,63 +452,61 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     fq[u] = q[u] * (pf[u] * pr[u]);
                     fk[u] = k[u] * (sf[u] * __fdividef(tj[u], pr[u]));
                 }
-                *reinterpret_cast<float4*>(qt_s + r * QT_LD + 8 * cg) = make_float4(fq[0], fq[1], fq[2], fq[3]);
-                *reinterpret_cast<float4*>(qt_s + r * QT_LD + 8 * cg + 4) = make_float4(fq[4], fq[5], fq[6], fq[7]);
+                *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg)) = make_float4(fq[0], fq[1], fq[2], fq[3]);
+                *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg + 4)) = make_float4(fq[4], fq[5], fq[6], fq[7]);
                 uint4 hi, lo;
                 tc::split8(fk, hi, lo);
-                *reinterpret_cast<uint4*>(slot + SLOT_KH + tc::mnmaj(8 * cg, r, D)) = hi;
-                *reinterpret_cast<uint4*>(slot + SLOT_KL + tc::mnmaj(8 * cg, r, D)) = lo;
+                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(8 * cg, r, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_KST + 16384 + tc::mnmaj(8 * cg, r, D)) = lo;
             }
-        }
-
-        // staging is consumed: prefetch the next task into it
-        tc::fence_async_smem();
-        __syncthreads();
-        if (nxt.valid) {
-            if (tid == 0) issue_tma(nxt);
-            tma_pending = true;
         }
 
         // ---- (5) A/P out of TMEM: Diag(beta) A -> fp32, P -> hi/lo operand ---------
+        // lane quadrant q4 holds stack rows 32 q4 + lane: block R = q4 / 2, k rows for
+        // even q4, q rows for odd; block 0 uses columns 0..31, block 1 columns 32..95
         {
             float* Af = reinterpret_cast<float*>(smem + SM_AF);  // [64 r][MAT_LD]
-            const int R = (warp >> 2) & 1;                    // warpgroup w: block w % 2,
-            const int jb = 32 * (warp >> 3);                  //   columns [32 (w / 2), +32)
-            const int ncol = 32 * (R + 1);
-            const int i = (warp & 3) * 16 + (lane & 15);      // M = 64 row held by this lane
-            const bool is_q = i >= 32;
-            const int r = 32 * R + (i & 31);
-            uint32_t a[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) a[u] = 0u;
-            if (jb < ncol) {
-                tc::tmem_ld16(tm + lane_base(warp) + TL_AP + 32 * R + jb, a);
-                tc::tmem_ld16(tm + lane_base(warp) + TL_AP + 32 * R + jb + 16, a + 16);
-                tc::tmem_ld_wait();
+            const int q4 = warp & 3, wg = warp >> 2;
+            const int R = q4 >> 1;
+            const bool is_q = (q4 & 1) != 0;
+            const int r = 32 * R + lane;
+            const int j0 = R == 0 ? 8 * wg : 16 * wg;
+            uint32_t a[16];
+            if (R == 0) {
+                tc::tmem_ld8(tm + lane_base(warp) + TL_AP + j0, a);
+            } else {
+                tc::tmem_ld16(tm + lane_base(warp) + TL_AP + 32 + j0, a);
             }
-            if (lane < 16) {
-                const float br = beta_s[r];
+            tc::tmem_ld_wait();
+            const float br = beta_s[r];
 #pragma unroll
-                for (int j0 = 0; j0 < 32; j0 += 8) {
-                    float v[8];
+            for (int g8 = 0; g8 < 2; ++g8) {
+                if (R == 0 && g8 == 1) break;
+                float v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int j = jb + j0 + u;
-                        const float x = __uint_as_float(a[j0 + u]);
-                        v[u] = is_q ? (j <= r ? x : 0.f) : (j < r ? br * x : 0.f);
-                    }
-                    if (is_q) {
-                        uint4 hi, lo;
-                        tc::split8(v, hi, lo);
-                        *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, jb + j0, C)) = hi;
-                        *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, jb + j0, C)) = lo;
-                    } else {
-                        *reinterpret_cast<float4*>(Af + r * MAT_LD + jb + j0) = make_float4(v[0], v[1], v[2], v[3]);
-                        *reinterpret_cast<float4*>(Af + r * MAT_LD + jb + j0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
-                    }
+                for (int u = 0; u < 8; ++u) {
+                    const int j = j0 + 8 * g8 + u;
+                    const float xv = __uint_as_float(a[8 * g8 + u]);
+                    v[u] = is_q ? (j <= r ? xv : 0.f) : (j < r ? br * xv : 0.f);
+                }
+                if (is_q) {
+                    uint4 hi, lo;
+                    tc::split8(v, hi, lo);
+                    *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, j0 + 8 * g8, C)) = hi;
+                    *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, j0 + 8 * g8, C)) = lo;
+                } else {
+                    *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 8 * g8) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 8 * g8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
                 }
             }
+            // P rows of block 0 are zero in columns 32..63 (the P operand spans all 64)
+            if (R == 0 && is_q) {
+                *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+        // (the staged Kbar images go to the async proxy; the staging tiles are consumed)
+        tc::fence_async_smem();
         __syncthreads();
 
         // ---- (6) T = (I + Diag(beta) A)^{-1} ----------------------------------------
@@ -523,7 +536,16 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 }
 #pragma unroll
                 for (int m = 0; m < 4; ++m) T[(16 * blk + part + 4 * m) * MAT_LD + i] = x[m];
+            } else {
+                // Kbar hi|lo out; prefetch the next task into the consumed staging
+                if (tid == kIssueTid) {
+                    tc::bulk_store(slot + SLOT_KH, smem + SM_KST, 32768);
+                    tc::bulk_commit();
+                    if (nxt.valid) issue_tma(nxt);
+                }
+                if (nxt.valid) beta_r = fetch_beta(nxt);
             }
+            if (nxt.valid) tma_pending = true;
             __syncthreads();
             // off-diagonal blocks, as two 32 x 32 halves T11 (tokens 0..31) and T22
             // (32..63): first the lower 16 x 16 block inside each half,
@@ -634,6 +656,9 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (failed) break;
 
         // ---- (8) W: bf16 image out and W^T as A operand; U~: fp32 out, hi/lo operand --
+        // (the [-W | Qh hi] image is staged where the Kbar images were)
+        if (tid == kIssueTid) tc::bulk_wait_read();
+        __syncthreads();
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
@@ -649,12 +674,13 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int u = 0; u < 8; ++u) w[u] = __uint_as_float(a[8 * g8 + u]);
                 const uint4 pk = tc::pack8(w);
                 // the state kernel needs -W (bf16 negation is exact)
-                *reinterpret_cast<uint4*>(slot + SLOT_WQ + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
+                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
                     make_uint4(pk.x ^ 0x80008000u, pk.y ^ 0x80008000u, pk.z ^ 0x80008000u, pk.w ^ 0x80008000u);
                 wt[4 * g8 + 0] = pk.x; wt[4 * g8 + 1] = pk.y; wt[4 * g8 + 2] = pk.z; wt[4 * g8 + 3] = pk.w;
             }
             tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wt);
-            float* ut = reinterpret_cast<float*>(slot + SLOT_UT);
+            // U~ staged as [64 r][128 v] in the (now dead) A/T region for one bulk store
+            float* ut = reinterpret_cast<float*>(smem + SM_PRE);
 #pragma unroll
             for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
             uint32_t hi[8], lo[8];
@@ -669,6 +695,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         publish();
 
         // ---- (9) (P W)^T = W^T P^T,  (P U~)^T = U~^T P^T ---------------------------------
+        if (tid == kIssueTid) {
+            tc::bulk_store(slot + SLOT_UT, smem + SM_PRE, 32768);
+            tc::bulk_commit();
+        }
         if (warp == 0) {
             const uint32_t pb = tc::smem_u32(smem + SM_PB);
             const uint64_t pbh = tc::sdesc(pb, 128, C * 16), pbl = tc::sdesc(pb + 8192, 128, C * 16);
@@ -700,20 +730,28 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int r = rb + 8 * g8 + u;
-                    qh[u] = scale * (qt_s[r * QT_LD + x] - __uint_as_float(a[8 * g8 + u]));
+                    qh[u] = scale * (qt_s[qt_idx(r, x)] - __uint_as_float(a[8 * g8 + u]));
                 }
                 uint4 hi, lo;
                 tc::split8(qh, hi, lo);
-                *reinterpret_cast<uint4*>(slot + SLOT_WQ + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
-                *reinterpret_cast<uint4*>(slot + SLOT_QL + tc::mnmaj(rb + 8 * g8, x, C)) = lo;
+                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_OPB + 32768 + tc::mnmaj(rb + 8 * g8, x, C)) = lo;
             }
-            float* ol = reinterpret_cast<float*>(slot + SLOT_OL);
+            // O_loc (and Qh lo above) staged in the (now dead) T / P operand region
+            float* ol = reinterpret_cast<float*>(smem + SM_OPB);
 #pragma unroll
             for (int i = 0; i < 16; ++i) ol[(rb + i) * D + x] = scale * __uint_as_float(b[i]);
         }
+        tc::fence_async_smem();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
+        if (tid == kIssueTid) {
+            tc::bulk_store(slot + SLOT_OL, smem + SM_OPB, 32768);
+            tc::bulk_store(slot + SLOT_WQ, smem + SM_KST, 32768);
+            tc::bulk_store(slot + SLOT_QL, smem + SM_OPB + 32768, 16384);
+            tc::bulk_commit();
+        }
 
         task = next_task;
         cur = nxt;
@@ -727,6 +765,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 __int_as_float(0x7fc00000);
         if (tma_pending && tid == 0) tc::bar_wait(bar_tma, tma_phase, kWaitIter);
     }
+    if (tid == kIssueTid) tc::bulk_wait();
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, TL_COLS);
@@ -1252,6 +1291,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
         e = cudaGetLastError();
     }
     const int64_t tasks = pl.max_chunks * p.H;
+    if (tasks >= ((int64_t)1 << 31)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess && tasks > 0) {
         const int64_t rows = (int64_t)p.B * p.T;
         CUtensorMap mq, mk, mv, mg;
