@@ -456,8 +456,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg + 4)) = make_float4(fq[4], fq[5], fq[6], fq[7]);
                 uint4 hi, lo;
                 tc::split8(fk, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(8 * cg, r, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_KST + 16384 + tc::mnmaj(8 * cg, r, D)) = lo;
+                *reinterpret_cast<uint4*>(slot + SLOT_KH + tc::mnmaj(8 * cg, r, D)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_KL + tc::mnmaj(8 * cg, r, D)) = lo;
             }
         }
 
@@ -505,7 +505,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        // (the staged Kbar images go to the async proxy; the staging tiles are consumed)
+        // (the staging tiles are consumed)
         tc::fence_async_smem();
         __syncthreads();
 
@@ -537,12 +537,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int m = 0; m < 4; ++m) T[(16 * blk + part + 4 * m) * MAT_LD + i] = x[m];
             } else {
-                // Kbar hi|lo out; prefetch the next task into the consumed staging
-                if (tid == kIssueTid) {
-                    tc::bulk_store(slot + SLOT_KH, smem + SM_KST, 32768);
-                    tc::bulk_commit();
-                    if (nxt.valid) issue_tma(nxt);
-                }
+                // prefetch the next task into the consumed staging
+                if (tid == kIssueTid && nxt.valid) issue_tma(nxt);
                 if (nxt.valid) beta_r = fetch_beta(nxt);
             }
             if (nxt.valid) tma_pending = true;
@@ -656,9 +652,6 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (failed) break;
 
         // ---- (8) W: bf16 image out and W^T as A operand; U~: fp32 out, hi/lo operand --
-        // (the [-W | Qh hi] image is staged where the Kbar images were)
-        if (tid == kIssueTid) tc::bulk_wait_read();
-        __syncthreads();
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
