@@ -16,9 +16,13 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
- *    allocates no memory and keeps no state between calls, so calls from
- *    different host threads are safe.
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    tensor-core prefill (kda_chunk_fwd with bf16 inputs and K = V = 128)
+ *    takes a device workspace for the duration of the call from a
+ *    stream-ordered memory pool that the library owns (one per device, kept
+ *    across calls for reuse); kda_chunk_fwd_noalloc uses a fixed array
+ *    instead; nothing else allocates.  Calls from different host threads are
+ *    safe.
  *  - Layouts are row-major and token-major, as the K3 gate tensor (B, T, 96, 128):
  *        q, k, g [B, T, H, K]    v [B, T, H, V]    beta [B, T, H]
  *        o [B, T, H, V]          states [N, H, K, V] (V contiguous, fp32)
@@ -57,7 +61,7 @@ typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, inconsistent B/N */
     KDA_ERR_UNSUPPORTED = 2, /* head size or dtype outside the supported set */
-    KDA_ERR_WORKSPACE = 3,   /* reserved */
+    KDA_ERR_WORKSPACE = 3,   /* device workspace unavailable (see kda_chunk_fwd, kda_chunk_fwd_noalloc) */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     KDA_ERR_RANGE = 5,       /* reserved for input-range checks */
     KDA_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
@@ -98,12 +102,52 @@ KDA_API int kda_abi_version(void);
  *                     or NULL to skip.  May alias initial_state exactly (the
  *                     state is then updated in place); no other overlap is
  *                     allowed.
+ *
+ *  Workspace (bf16, K = V = 128): 147968 bytes per (chunk, head) slot for
+ *  every 64-token chunk of every sequence (an upper bound of ceil(T / 64) + N
+ *  chunks per head when cu_seqlens is given), returned to the pool when the
+ *  call's work completes.  KDA_ERR_WORKSPACE if the pool cannot provide it.
  */
 KDA_API kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                          const void *beta, kda_dtype in_dtype, float scale,
                          const float *initial_state, const int32_t *cu_seqlens,
                          int B, int T, int H, int K, int V, int N,
                          void *o, kda_dtype o_dtype, float *final_state, void *stream);
+
+/*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd without any memory allocation.
+ *
+ * (The paper has no counterpart: this is a deployment variant of the entry
+ * point above.)  Some callers cannot let a library allocate device memory in
+ * the middle of their work: a serving process that reserved all free HBM for
+ * its own state pool at start-up, or a runtime whose memory is managed by a
+ * custom allocator that the library does not know about.  kda_chunk_fwd takes
+ * its workspace from a pool and would fail or compete for memory there.  This
+ * entry point computes exactly what kda_chunk_fwd computes, with the same
+ * arguments, but keeps its workspace in one fixed 64 MiB device array that
+ * every GPU loading libkda.so holds until the process exits; it calls no
+ * allocation routine.  The caller still passes all inputs and outputs.
+ *
+ *  - Supported: in_dtype KDA_BF16 with K = V = 128 (the tensor-core path);
+ *    anything else returns KDA_ERR_UNSUPPORTED.
+ *  - The workspace needed is 147968 bytes per (chunk, head) slot, with
+ *    ceil(T / 64) * B slots per head without cu_seqlens and ceil(T / 64) + N
+ *    with it (plus 4 * (2 N + 1 + slots per head) bytes, rounded up to 1 KiB,
+ *    of chunk bookkeeping).  A call needing more than 64 MiB returns
+ *    KDA_ERR_WORKSPACE before anything is enqueued (e.g. H = 96: T <= 256 for
+ *    one sequence; H = 8: T <= 3584).
+ *  - The first call made on a device looks up the array's device address (a
+ *    CUDA runtime call); make that first call before any stream capture.
+ *  - Every call shares the one array and leaves its last contents there;
+ *    nothing in it needs to start at zero (each call writes every byte it
+ *    reads).  Calls whose GPU work overlaps (different streams without
+ *    ordering between them) race on the array and give wrong results.
+ */
+KDA_API kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                 const void *beta, kda_dtype in_dtype, float scale,
+                                 const float *initial_state, const int32_t *cu_seqlens,
+                                 int B, int T, int H, int K, int V, int N,
+                                 void *o, kda_dtype o_dtype, float *final_state, void *stream);
 
 /*
  * kda_chunk_fwd_fused -- chunked prefill with the input prologue fused into

@@ -11,6 +11,7 @@ from .kda import (  # noqa: F401
     SIGNATURES,
     chunk_fwd,
     chunk_fwd_fused,
+    chunk_fwd_noalloc,
     library_path,
     load_library,
     recurrent_step,

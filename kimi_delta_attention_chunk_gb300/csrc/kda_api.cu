@@ -68,7 +68,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head size or dtype not supported";
-        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: device workspace could not be allocated";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: device workspace could not be allocated, or the call needs more than kda_chunk_fwd_noalloc's fixed scratch holds";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
         case KDA_ERR_RANGE: return "KDA_ERR_RANGE: input out of range";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: device-side wait gave up";
@@ -97,6 +97,26 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
     cudaStream_t st = (cudaStream_t)stream;
     if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc(o_dtype, p, st));
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, false, p, st));
+}
+
+kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                 const void* beta, kda_dtype in_dtype, float scale,
+                                 const float* initial_state, const int32_t* cu_seqlens, int B,
+                                 int T, int H, int K, int V, int N, void* o, kda_dtype o_dtype,
+                                 float* final_state, void* stream) {
+    kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H,
+                                K, V, N, o, o_dtype, final_state);
+    if (s != KDA_OK) return s;
+    if (!kda::chunk_tc_supported(in_dtype, K, V)) return KDA_ERR_UNSUPPORTED;
+    kda::ChunkParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.scale = resolve_scale(scale, K);
+    p.initial_state = initial_state;
+    p.cu_seqlens = cu_seqlens;
+    p.B = B; p.T = T; p.H = H; p.N = N;
+    p.o = o;
+    p.final_state = final_state;
+    return from_cuda(kda::chunk_tc_fixed_scratch(o_dtype, p, (cudaStream_t)stream));
 }
 
 kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v_raw,

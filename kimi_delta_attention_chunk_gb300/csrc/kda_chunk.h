@@ -37,9 +37,16 @@ struct ChunkParams {
 cudaError_t chunk_simt(kda_dtype in_dt, kda_dtype out_dt, int K, int V, bool prologue,
                        const ChunkParams& p, cudaStream_t st);
 
-// Tensor-core chunk kernel (bf16 inputs, K = V = 128).
+// Tensor-core chunk kernels (bf16 inputs, K = V = 128), workspace from the
+// library's stream-ordered pool.
 bool chunk_tc_supported(kda_dtype in_dt, int K, int V);
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+
+// The same with the workspace in a fixed device array of kFixedScratchBytes
+// (no allocation); cudaErrorMemoryAllocation, before anything is enqueued,
+// when the call needs more.
+constexpr size_t kFixedScratchBytes = (size_t)64 << 20;
+cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
 
 // Single-token decode.
 cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const void* q,

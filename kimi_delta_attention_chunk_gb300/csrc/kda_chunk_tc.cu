@@ -1247,8 +1247,11 @@ cudaError_t device_pool(cudaMemPool_t* pool, int* sms) {
     return cudaSuccess;
 }
 
+// The prefill's kernels, with the workspace taken from the library's pool
+// (fixed_ws == nullptr) or from a caller-side buffer of fixed_bytes.
 template <typename TOut>
-cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
+cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nullptr, size_t fixed_bytes = 0,
+                      int fixed_sms = 0) {
     const int64_t NH = (int64_t)p.N * p.H;
     if (NH == 0) return cudaSuccess;
     const bool packed = p.cu_seqlens != nullptr;
@@ -1263,14 +1266,20 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
     const size_t hdr_bytes = (hdr_ints * 4 + 1023) & ~size_t(1023);
     const size_t bytes = hdr_bytes + (size_t)pl.max_chunks * (size_t)p.H * SLOT_BYTES;
 
-    cudaMemPool_t pool;
-    int sms = 0;
-    cudaError_t e = device_pool(&pool, &sms);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    int sms = fixed_sms;
     void* ws = nullptr;
-    if (bytes > 0) {
-        e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
-        if (e != cudaSuccess) return cudaErrorMemoryAllocation;
+    if (fixed_ws != nullptr) {
+        if (bytes > fixed_bytes) return cudaErrorMemoryAllocation;
+        ws = fixed_ws;
+    } else {
+        cudaMemPool_t pool;
+        e = device_pool(&pool, &sms);
+        if (e != cudaSuccess) return e;
+        if (bytes > 0) {
+            e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
+            if (e != cudaSuccess) return cudaErrorMemoryAllocation;
+        }
     }
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
     pl.slots = reinterpret_cast<uint8_t*>(ws) + hdr_bytes;
@@ -1317,11 +1326,39 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st) {
             }
         }
     }
-    if (ws != nullptr) {
+    if (ws != nullptr && fixed_ws == nullptr) {
         const cudaError_t ef = cudaFreeAsync(ws, st);
         if (e == cudaSuccess) e = ef;
     }
     return e;
+}
+
+// ---- prefill without any allocation ---------------------------------------------
+// Workspace in a fixed device array that every GPU loading the library holds
+// until exit.  Its device address is looked up once per device, on the first
+// call made with that device current.
+static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
+std::mutex g_fixed_mutex;
+void* g_fixed_ptr[kMaxDevices];
+int g_fixed_sms[kMaxDevices];
+
+cudaError_t fixed_scratch(void** ptr, int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_fixed_mutex);
+    if (g_fixed_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&g_fixed_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_fixed_ptr[dev] = p;
+    }
+    *ptr = g_fixed_ptr[dev];
+    *sms = g_fixed_sms[dev];
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -1331,6 +1368,15 @@ bool chunk_tc_supported(kda_dtype in_dt, int K, int V) { return in_dt == KDA_BF1
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
     if (out_dt == KDA_F32) return launch_tc<float>(p, st);
     return launch_tc<__nv_bfloat16>(p, st);
+}
+
+cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
+    void* ws = nullptr;
+    int sms = 0;
+    const cudaError_t e = fixed_scratch(&ws, &sms);
+    if (e != cudaSuccess) return e;
+    if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, kFixedScratchBytes, sms);
+    return launch_tc<__nv_bfloat16>(p, st, ws, kFixedScratchBytes, sms);
 }
 
 }  // namespace kda

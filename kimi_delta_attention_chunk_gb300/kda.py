@@ -30,6 +30,8 @@ SIGNATURES = {
     "kda_abi_version": (_i, []),
     "kda_chunk_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
                            _vp, _i, _fp, _vp]),
+    "kda_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i,
+                                   _i, _vp, _i, _fp, _vp]),
     "kda_chunk_fwd_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _fp, _fp, _f, _f,
                                  _f, _fp, _i32p, _i, _i, _i, _i, _i, _i, _vp, _i, _fp, _vp]),
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
@@ -114,6 +116,28 @@ def chunk_fwd(q, k, v, g, beta, scale: float | None = None, initial_state=None, 
                            float(scale or 0.0), _ptr(initial_state), _ptr(cu_seqlens),
                            B, T, H, K, V, N, _ptr(o), _dt(o), _ptr(final_state), _stream(q.device))
     _check("kda_chunk_fwd", st)
+    return o, final_state
+
+
+def chunk_fwd_noalloc(q, k, v, g, beta, scale: float | None = None, initial_state=None, cu_seqlens=None,
+                      output_final_state: bool = True, o_dtype=torch.float32, o=None, final_state=None):
+    """``chunk_fwd`` through ``kda_chunk_fwd_noalloc``: the library allocates no
+    device memory for the call (its workspace is a fixed 64 MiB array, so only
+    small calls fit; bf16 inputs with K = V = 128 only).  For callers whose
+    device memory is all reserved by their own allocator.  ``o`` and
+    ``final_state`` can be passed in so that nothing at all is allocated."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty((B, T, H, V), dtype=o_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    st = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q),
+                                   float(scale or 0.0), _ptr(initial_state), _ptr(cu_seqlens),
+                                   B, T, H, K, V, N, _ptr(o), _dt(o), _ptr(final_state), _stream(q.device))
+    _check("kda_chunk_fwd_noalloc", st)
     return o, final_state
 
 
