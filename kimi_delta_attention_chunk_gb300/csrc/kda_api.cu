@@ -151,6 +151,7 @@ kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void*
     p.lower_bound = lower_bound;
     p.l2_eps = l2_eps;
     cudaStream_t st = (cudaStream_t)stream;
+    if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc_fused(o_dtype, p, st));
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, true, p, st));
 }
 

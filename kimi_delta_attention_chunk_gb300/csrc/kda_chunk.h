@@ -41,6 +41,8 @@ cudaError_t chunk_simt(kda_dtype in_dt, kda_dtype out_dt, int K, int V, bool pro
 // library's stream-ordered pool.
 bool chunk_tc_supported(kda_dtype in_dt, int K, int V);
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+// With the input prologue (p.q, p.k, p.v, p.g are the raw inputs).
+cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
 
 // The same with the workspace in a fixed device array of kFixedScratchBytes
 // (no allocation); cudaErrorMemoryAllocation, before anything is enqueued,

@@ -59,16 +59,16 @@ constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TME
 constexpr uint32_t kWaitIter = 1u << 26;
 
 // ---- workspace slot of one (chunk, head), written by the local kernel --------
-constexpr uint32_t SLOT_WQ = 0;         // [-W | Qh hi] (bf16) as one B operand, MN-major
+constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qh hi] (bf16) as one B operand, MN-major
                                         //   (n = r for -W, n = 64 + r for Qh; k = c)
-constexpr uint32_t SLOT_QL = 32768;     // Qh lo as B operand, MN-major (n = r, k = c)
-constexpr uint32_t SLOT_KH = 49152;     // Kbar hi as B operand, MN-major (n = c, k = r)
-constexpr uint32_t SLOT_KL = 65536;     // Kbar lo
-constexpr uint32_t SLOT_EGC = 81920;    // e^{G_C} fp32 [128]
-constexpr uint32_t SLOT_IMG = 82432;    // bytes of the images above (one shared-memory copy)
-constexpr uint32_t SLOT_UT = 82432;     // U~ fp32 [64 r][128 v]
-constexpr uint32_t SLOT_OL = 115200;    // O_loc fp32 [64 r][128 v]
-constexpr uint32_t SLOT_BYTES = 147968;
+constexpr uint32_t SLOT_WQL = 32768;    // [-W lo | Qh lo], same layout
+constexpr uint32_t SLOT_EGC = 65536;    // e^{G_C} fp32 [128]
+constexpr uint32_t SLOT_IMG = 66048;    // bytes of the images above (one shared-memory copy)
+constexpr uint32_t SLOT_KH = 66048;     // Kbar hi as B operand, MN-major (n = c, k = r)
+constexpr uint32_t SLOT_KL = 82432;     // Kbar lo
+constexpr uint32_t SLOT_UT = 98816;     // U~ fp32 [64 r][128 v]
+constexpr uint32_t SLOT_OL = 131584;    // O_loc fp32 [64 r][128 v]
+constexpr uint32_t SLOT_BYTES = 164352;
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
 // (q e^G) fp32 [64 r][128 c] in shared memory: float4 column f of row r stored at
@@ -91,6 +91,7 @@ struct Plan {
 
 struct Chunk {
     int64_t c0, eos;  // first token of the chunk, end of its sequence
+    int64_t bos;      // first token of its sequence
     int64_t gc;       // global chunk index
     int h;
     bool valid;
@@ -108,13 +109,14 @@ __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
     if (pl.cu_seqlens == nullptr) {
         const uint32_t cps = (uint32_t)pl.cps;
         const uint32_t n = gc / cps, j = gc - n * cps;
-        ch.c0 = (int64_t)n * pl.T + (int64_t)j * C;
-        ch.eos = (int64_t)n * pl.T + pl.T;
+        ch.bos = (int64_t)n * pl.T;
+        ch.c0 = ch.bos + (int64_t)j * C;
+        ch.eos = ch.bos + pl.T;
     } else {
         const int n = pl.chunk_seq[gc];
         if (n < 0) return ch;
-        const int64_t bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
-        ch.c0 = bos + (int64_t)(gc - (uint32_t)pl.chunk_off[n]) * C;
+        ch.bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
+        ch.c0 = ch.bos + (int64_t)(gc - (uint32_t)pl.chunk_off[n]) * C;
         ch.eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
     }
     ch.valid = true;
@@ -147,8 +149,18 @@ constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals o
 constexpr uint32_t SM_BETA = SM_SMALL + 2048;    // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base
 constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
+// with the input prologue (raw q, k, v and gate input in the staging tiles):
+constexpr uint32_t SM_RED = SM_SMALL + 2432;     // fp32 [2][64][4] partial sums of squares of q, k rows
+constexpr uint32_t SM_HALO = SM_RED + 2048;      // bf16 [3][2][3][64] the 3 raw rows before the chunk (q, k, v)
+constexpr uint32_t SM_CONV = SM_HALO + 2304;     // fp32 [3][128][4] this head's conv weights (q, k, v)
+constexpr uint32_t SM_DTB = SM_CONV + 6144;      // fp32 [128] this head's dt_bias
+constexpr uint32_t SM_ALOG = SM_DTB + 512;       // fp32 [128] A_log
+constexpr uint32_t SM_LOCAL_TOTAL_FUSED = SM_ALOG + 512;
+constexpr uint32_t PRO_TX = 6 * 384 + 6144 + 512 + 512;   // prologue bytes per task load
 static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
 static_assert(SM_LOCAL_TOTAL + 1024 <= 232448, "shared memory");
+static_assert(SM_RED >= SM_LOCAL_TOTAL && SM_HALO % 128 == 0, "prologue regions");
+static_assert(SM_LOCAL_TOTAL_FUSED + 1024 <= 232448, "shared memory with the prologue");
 
 // ---- tensor memory map (columns) ----------------------------------------------
 constexpr uint32_t TL_AP = 0;      // [L_0; L_1] [Rt_0 | Rt_1]^T accumulator, M = 128, N = 96
@@ -157,18 +169,45 @@ constexpr uint32_t TL_KTL = 128;   // (k e^G)^T lo
 constexpr uint32_t TL_VT = 160;    // v^T (bf16 pairs) [128 v][32]
 constexpr uint32_t TL_AW = 192;    // W^T accumulator fp32 [128 c][64 r], then (P W)^T
 constexpr uint32_t TL_AU = 256;    // U~^T accumulator fp32 [128 v][64 r], then (P U~)^T
-constexpr uint32_t TL_WT = 320;    // W^T (bf16 pairs) [128 c][32], A operand
+constexpr uint32_t TL_WT = 320;    // W^T hi (bf16 pairs) [128 c][32], A operand
 constexpr uint32_t TL_UH = 352;    // U~^T hi (bf16 pairs) [128 v][32], A operand
 constexpr uint32_t TL_UL = 384;    // U~^T lo
+constexpr uint32_t TL_VTL = 416;   // v^T lo (bf16 pairs), with the prologue (v is then not bf16-exact)
+constexpr uint32_t TL_WTL = 448;   // W^T lo (bf16 pairs) [128 c][32], A operand
 constexpr uint32_t TL_COLS = 512;
 // Thread that issues the tile loads and bulk stores: warps 8..15 are idle while
 // warps 0..7 invert the diagonal blocks of T, so the issue costs no barrier time.
 constexpr int kIssueTid = 256;
 
+// Input prologue ("kimi-k3-mlx" review: short convolution of kernel size 4 on
+// q, k, v; per-channel forget gate with gate_lower_bound; A_log of K entries
+// shared by all heads): q, k = l2norm(act(conv4(raw))), v = act(conv4(raw)),
+// g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias)).
+struct Prologue {
+    const float* conv_q;   // [H * 128][4]
+    const float* conv_k;
+    const float* conv_v;
+    const float* A_log;    // [128]
+    const float* dt_bias;  // [H * 128]
+    int act;               // 0: none, 1: SiLU after the convolution
+    float lower_bound;
+    float l2_eps;
+};
+
+__device__ __forceinline__ float softplus_f(float z) {
+    return z > 0.f ? z + log1pf(__expf(-z)) : log1pf(__expf(z));
+}
+
+// FUSED: the staging tiles hold the raw inputs (q_raw, k_raw, v_raw, gate_x);
+// the prologue runs on them first and leaves q, k as bf16 hi (in the q, k tiles)
+// plus lo (in the v, g tiles), v as hi/lo in TMEM and g folded into pass 1.
+template <bool FUSED>
 __global__ void __launch_bounds__(NT, 1)
 chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
-                   const void* __restrict__ beta_ptr, const float scale, const Plan pl) {
+                   const __grid_constant__ CUtensorMap hq, const __grid_constant__ CUtensorMap hk,
+                   const __grid_constant__ CUtensorMap hv, const void* __restrict__ beta_ptr, const float scale,
+                   const Plan pl, const Prologue pro) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte-swizzled TMA tiles need a 1024-byte aligned base
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,13 +239,29 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     bool tma_pending = false;
 
     auto issue_tma = [&](const Chunk& ch) {
-        tc::bar_expect_tx(bar_tma, 4u * 16384u);
+        tc::bar_expect_tx(bar_tma, 4u * 16384u + (FUSED ? PRO_TX : 0u));
         const CUtensorMap* maps[4] = {&mq, &mk, &mv, &mg};
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int half = 0; half < 2; ++half)
                 tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, ch.h, (int)ch.c0, bar_tma);
+        if constexpr (FUSED) {
+            // the 3 raw rows before the chunk (row -3 and up; rows before the tensor
+            // arrive as zeros, rows of another sequence are masked when used)
+            const CUtensorMap* hmaps[3] = {&hq, &hk, &hv};
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    tc::tma_load_3d(smem + SM_HALO + t * 768 + half * 384, hmaps[t], half * 64, ch.h, (int)ch.c0 - 3,
+                                    bar_tma);
+            tc::bulk_load(smem + SM_CONV, pro.conv_q + (int64_t)ch.h * D * 4, 2048, bar_tma);
+            tc::bulk_load(smem + SM_CONV + 2048, pro.conv_k + (int64_t)ch.h * D * 4, 2048, bar_tma);
+            tc::bulk_load(smem + SM_CONV + 4096, pro.conv_v + (int64_t)ch.h * D * 4, 2048, bar_tma);
+            tc::bulk_load(smem + SM_DTB, pro.dt_bias + (int64_t)ch.h * D, 512, bar_tma);
+            tc::bulk_load(smem + SM_ALOG, pro.A_log, 512, bar_tma);
+        }
     };
     // One warp polls the barrier; the others park at the CTA barrier.
     auto wait_one = [&](uint64_t* bar, uint32_t& phase) {
@@ -261,21 +316,34 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         tma_pending = false;
         if (failed) break;
 
-        const uint8_t* qs = smem + SM_STG;
-        const uint8_t* ks = smem + SM_STG + 16384;
-        const uint8_t* vs = smem + SM_STG + 32768;
-        const uint8_t* gs = smem + SM_STG + 49152;
+        uint8_t* qs = smem + SM_STG;
+        uint8_t* ks = smem + SM_STG + 16384;
+        uint8_t* vs = smem + SM_STG + 32768;
+        uint8_t* gs = smem + SM_STG + 49152;
         auto ld_bf = [&](const uint8_t* t, int r, int c) {
             return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(t + tc::swz128(r, c)));
         };
-        // 8 consecutive channels [c, c+8) of row r as floats (0 for rows >= L)
-        auto ld8 = [&](const uint8_t* t, int r, int c, float* x) {
+        // q (is_q) or k: 8 consecutive channels [c, c+8) of row r as floats (0 for
+        // rows >= L); after the prologue the value is its hi + lo
+        auto ld8 = [&](bool is_q, int r, int c, float* x) {
             if (r < L) {
-                tc::unpack8(*reinterpret_cast<const uint4*>(t + tc::swz128(r, c)), x);
+                tc::unpack8(*reinterpret_cast<const uint4*>((is_q ? qs : ks) + tc::swz128(r, c)), x);
+                if constexpr (FUSED) {
+                    float y[8];
+                    tc::unpack8(*reinterpret_cast<const uint4*>((is_q ? vs : gs) + tc::swz128(r, c)), y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] += y[i];
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[i] = 0.f;
             }
+        };
+        // one channel of k
+        auto ld_k = [&](int r, int c) {
+            float x = ld_bf(ks, r, c);
+            if constexpr (FUSED) x += ld_bf(gs, r, c);
+            return x;
         };
         auto ld_pre8 = [&](int r, int c, float* x) {
             const float4 a = *reinterpret_cast<const float4*>(pre_s + r * PRE_LD + c);
@@ -288,12 +356,43 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
         };
 
+        // raw input of tensor t (0 q, 1 k, 2 v) at chunk row sr >= -3, channel c;
+        // zero before the start of the sequence
+        auto raw1 = [&](int t, int sr, int c) -> float {
+            if (c0 + sr < cur.bos) return 0.f;
+            if (sr < 0)
+                return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    smem + SM_HALO + t * 768 + (c >> 6) * 384 + (sr + 3) * 128 + (c & 63) * 2));
+            return ld_bf(t == 0 ? qs : (t == 1 ? ks : vs), sr, c);
+        };
+        auto raw8 = [&](int t, int sr, int c, float* x) {
+            if (c0 + sr < cur.bos) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = 0.f;
+            } else if (sr < 0) {
+                tc::unpack8(*reinterpret_cast<const uint4*>(smem + SM_HALO + t * 768 + (c >> 6) * 384 +
+                                                            (sr + 3) * 128 + (c & 63) * 2), x);
+            } else {
+                tc::unpack8(*reinterpret_cast<const uint4*>((t == 0 ? qs : ks) + tc::swz128(sr, c)), x);
+            }
+        };
+        auto act = [&](float y) { return pro.act == 1 ? __fdividef(y, 1.f + __expf(-y)) : y; };
+
         // ---- (1) in-block prefix products of e^g, block totals --------------------
         {
             const int c = tid & 127, J = tid >> 7;  // block J of channel c
             float gv[16];
+            if constexpr (FUSED) {
+                // g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias))
+                const float ea = __expf(reinterpret_cast<const float*>(smem + SM_ALOG)[c]);
+                const float db = reinterpret_cast<const float*>(smem + SM_DTB)[c];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) gv[u] = 16 * J + u < L ? ld_bf(gs, 16 * J + u, c) : 0.f;
+                for (int u = 0; u < 16; ++u)
+                    gv[u] = 16 * J + u < L ? fmaxf(pro.lower_bound, -ea * softplus_f(ld_bf(gs, 16 * J + u, c) + db)) : 0.f;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) gv[u] = 16 * J + u < L ? ld_bf(gs, 16 * J + u, c) : 0.f;
+            }
             float run = 1.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
@@ -302,9 +401,96 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tot_s[J * 128 + c] = run;
         }
+        if constexpr (FUSED) {
+            // v = act(conv4(v_raw)): this thread's value column, 16 tokens, as hi|lo
+            // pairs into TMEM (lane = value column)
+            const int c = (warp & 3) * 32 + lane;
+            const int jb = (warp >> 2) * 16;
+            const float4 w = *reinterpret_cast<const float4*>(smem + SM_CONV + 4096 + c * 16);
+            float xr[19];
+#pragma unroll
+            for (int m = 0; m < 19; ++m) xr[m] = raw1(2, jb - 3 + m, c);
+            uint32_t vh[8], vl[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float y[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int m = 2 * i + e;
+                    const float acc = act(w.x * xr[m] + w.y * xr[m + 1] + w.z * xr[m + 2] + w.w * xr[m + 3]);
+                    y[e] = jb + m < L ? acc : 0.f;
+                }
+                tc::split2(y[0], y[1], vh[i], vl[i]);
+            }
+            tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vh);
+            tc::tmem_st8(tm + lane_base(warp) + TL_VTL + jb / 2, vl);
+            tc::tmem_st_wait();
+        }
         if (bt >= 0 && bt < C) beta_s[bt] = beta_r;
         if (tid == kIssueTid) tc::bulk_wait_read();
         __syncthreads();
+
+        if constexpr (FUSED) {
+            // q, k = l2norm(act(conv4(raw))) over the 128 channels of each row, written
+            // back as bf16 hi (q, k tiles) + lo (v, g tiles, consumed above)
+            const int cgp = (tid >> 3) & 15;
+            float* red = reinterpret_cast<float*>(smem + SM_RED);  // [2][64][4]
+            float y[2][2][8];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const float* wt = reinterpret_cast<const float*>(smem + SM_CONV + t * 2048) + 8 * cgp * 4;
+                float4 w[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const float4*>(wt + 4 * u);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int item = tid + NT * kk;
+                    const int r = ((item >> 7) << 3) | (item & 7);
+                    float acc[8], xv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+                    raw8(t, r - 3, 8 * cgp, xv);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] += w[u].x * xv[u];
+                    raw8(t, r - 2, 8 * cgp, xv);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] += w[u].y * xv[u];
+                    raw8(t, r - 1, 8 * cgp, xv);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] += w[u].z * xv[u];
+                    raw8(t, r, 8 * cgp, xv);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[u] += w[u].w * xv[u];
+                    float ss = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        acc[u] = r < L ? act(acc[u]) : 0.f;
+                        ss += acc[u] * acc[u];
+                        y[t][kk][u] = acc[u];
+                    }
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                    if (lane < 8) red[(t * 64 + r) * 4 + (warp & 3)] = ss;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int item = tid + NT * kk;
+                    const int r = ((item >> 7) << 3) | (item & 7);
+                    const float4 pss = *reinterpret_cast<const float4*>(red + (t * 64 + r) * 4);
+                    const float inv = rsqrtf(pss.x + pss.y + pss.z + pss.w + pro.l2_eps);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) y[t][kk][u] *= inv;
+                    uint4 hi, lo;
+                    tc::split8(y[t][kk], hi, lo);
+                    *reinterpret_cast<uint4*>((t == 0 ? qs : ks) + tc::swz128(r, 8 * cgp)) = hi;
+                    *reinterpret_cast<uint4*>((t == 0 ? vs : gs) + tc::swz128(r, 8 * cgp)) = lo;
+                }
+            __syncthreads();
+        }
 
         // Every build loop below gives a thread the same 8 channels [8 cg, 8 cg + 8).
         const int cg = (tid >> 3) & 15;
@@ -328,7 +514,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const int i = ((item >> 7) << 3) | (item & 7);
                 const int r = 32 * R + (i & 31);
                 float x[8], pr[8], f[8];
-                ld8(i < 32 ? ks : qs, r, 8 * cg, x);
+                ld8(i >= 32, r, 8 * cg, x);
                 ld_pre8(r, 8 * cg, pr);
                 const bool first = (i & 16) == 0;  // r in the first 16-token block of R
 #pragma unroll
@@ -347,7 +533,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const int j = ((item >> 7) << 3) | (item & 7);
                 const int J = j >> 4;
                 float x[8], pr[8], m[8], t[8];
-                ld8(ks, j, 8 * cg, x);
+                ld8(false, j, 8 * cg, x);
                 ld_pre8(j, 8 * cg, pr);
                 // in-block ratio first (in (0, 1], or 1/pre_j <= e^80 after the centre),
                 // then the totals of the later blocks: every intermediate lies between 1
@@ -400,17 +586,19 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int j = jb + 2 * i;
-                const float k0 = j < L ? ld_bf(ks, j, c) : 0.f;
-                const float k1 = j + 1 < L ? ld_bf(ks, j + 1, c) : 0.f;
+                const float k0 = j < L ? ld_k(j, c) : 0.f;
+                const float k1 = j + 1 < L ? ld_k(j + 1, c) : 0.f;
                 tc::split2(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], kh[i], kl[i]);
-                const __nv_bfloat16 z = __float2bfloat16(0.f);
-                const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
-                const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
-                vv[i] = tc::pack_bf16(v0, v1);
+                if constexpr (!FUSED) {
+                    const __nv_bfloat16 z = __float2bfloat16(0.f);
+                    const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
+                    const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
+                    vv[i] = tc::pack_bf16(v0, v1);
+                }
             }
             tc::tmem_st8(tm + lane_base(warp) + TL_KTH + jb / 2, kh);
             tc::tmem_st8(tm + lane_base(warp) + TL_KTL + jb / 2, kl);
-            tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vv);
+            if constexpr (!FUSED) tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vv);
             if (tid < 128)
                 reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * tot_s[384 + c];
         }
@@ -444,8 +632,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     }
                 }
                 float q[8], k[8], pr[8], fq[8], fk[8];
-                ld8(qs, r, 8 * cg, q);
-                ld8(ks, r, 8 * cg, k);
+                ld8(true, r, 8 * cg, q);
+                ld8(false, r, 8 * cg, k);
                 ld_pre8(r, 8 * cg, pr);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -645,13 +833,14 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tc::mma_ts_w(tm + TL_AW, tm + TL_KTH + ks_ * 8, bl, id_n64, 1);
                 tc::mma_ts_w(tm + TL_AU, tm + TL_VT + ks_ * 8, bl, id_n64, 1);
                 tc::mma_ts_w(tm + TL_AW, tm + TL_KTL + ks_ * 8, bh, id_n64, 1);
+                if constexpr (FUSED) tc::mma_ts_w(tm + TL_AU, tm + TL_VTL + ks_ * 8, bh, id_n64, 1);
             }
             tc::commit_w(bar_mma);
         }
         mma_sync();
         if (failed) break;
 
-        // ---- (8) W: bf16 image out and W^T as A operand; U~: fp32 out, hi/lo operand --
+        // ---- (8) W^T hi/lo and U~^T hi/lo as A operands; U~ fp32 staged for the slot --
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
@@ -659,19 +848,11 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
             tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
             tc::tmem_ld_wait();
-            uint32_t wt[8];
+            uint32_t wh[8], wl[8];
 #pragma unroll
-            for (int g8 = 0; g8 < 2; ++g8) {
-                float w[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) w[u] = __uint_as_float(a[8 * g8 + u]);
-                const uint4 pk = tc::pack8(w);
-                // the state kernel needs -W (bf16 negation is exact)
-                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
-                    make_uint4(pk.x ^ 0x80008000u, pk.y ^ 0x80008000u, pk.z ^ 0x80008000u, pk.w ^ 0x80008000u);
-                wt[4 * g8 + 0] = pk.x; wt[4 * g8 + 1] = pk.y; wt[4 * g8 + 2] = pk.z; wt[4 * g8 + 3] = pk.w;
-            }
-            tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wt);
+            for (int i = 0; i < 8; ++i) tc::split2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]), wh[i], wl[i]);
+            tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wh);
+            tc::tmem_st8(tm + lane_base(warp) + TL_WTL + rb / 2, wl);
             // U~ staged as [64 r][128 v] in the (now dead) A/T region for one bulk store
             float* ut = reinterpret_cast<float*>(smem + SM_PRE);
 #pragma unroll
@@ -702,6 +883,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, ph, id_n64, ks_ > 0);
                 tc::mma_ts_w(tm + TL_AW, tm + TL_WT + ks_ * 8, pl_, id_n64, 1);
                 tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, pl_, id_n64, 1);
+                tc::mma_ts_w(tm + TL_AW, tm + TL_WTL + ks_ * 8, ph, id_n64, 1);
                 tc::mma_ts_w(tm + TL_AU, tm + TL_UL + ks_ * 8, ph, id_n64, 1);
             }
             tc::commit_w(bar_mma);
@@ -709,16 +891,29 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         mma_sync();
         if (failed) break;
 
-        // ---- (10) Qh = scale ((q e^G) - P W) hi|lo out, O_loc = scale P U~ out ------------
+        // ---- (10) Qh = scale ((q e^G) - P W) and -W, hi|lo, staged as the two merged
+        //      B images (hi: where the Kbar-free OPA half is, lo: in the dead T / P
+        //      operand region); O_loc = scale P U~ out -----------------------------------
         {
             const int x = (warp & 3) * 32 + lane;
             const int rb = (warp >> 2) * 16;
-            uint32_t a[16], b[16];
+            uint32_t a[16], b[16], wh[8], wl[8];
             tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
             tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
+            tc::tmem_ld8(tm + lane_base(warp) + TL_WT + rb / 2, wh);
+            tc::tmem_ld8(tm + lane_base(warp) + TL_WTL + rb / 2, wl);
             tc::tmem_ld_wait();
+            uint8_t* bh_s = smem + SM_KST;
+            uint8_t* bl_s = smem + SM_OPB;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
+                // -W (bf16 negation is exact): the packed pairs are 8 consecutive r
+                const uint32_t* h4 = wh + 4 * g8;
+                const uint32_t* l4 = wl + 4 * g8;
+                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
+                    make_uint4(h4[0] ^ 0x80008000u, h4[1] ^ 0x80008000u, h4[2] ^ 0x80008000u, h4[3] ^ 0x80008000u);
+                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
+                    make_uint4(l4[0] ^ 0x80008000u, l4[1] ^ 0x80008000u, l4[2] ^ 0x80008000u, l4[3] ^ 0x80008000u);
                 float qh[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -727,11 +922,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 }
                 uint4 hi, lo;
                 tc::split8(qh, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_KST + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_OPB + 32768 + tc::mnmaj(rb + 8 * g8, x, C)) = lo;
+                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
+                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = lo;
             }
-            // O_loc (and Qh lo above) staged in the (now dead) T / P operand region
-            float* ol = reinterpret_cast<float*>(smem + SM_OPB);
+            float* ol = reinterpret_cast<float*>(slot + SLOT_OL);
 #pragma unroll
             for (int i = 0; i < 16; ++i) ol[(rb + i) * D + x] = scale * __uint_as_float(b[i]);
         }
@@ -740,9 +934,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         __syncthreads();
         tc::fence_after();
         if (tid == kIssueTid) {
-            tc::bulk_store(slot + SLOT_OL, smem + SM_OPB, 32768);
-            tc::bulk_store(slot + SLOT_WQ, smem + SM_KST, 32768);
-            tc::bulk_store(slot + SLOT_QL, smem + SM_OPB + 32768, 16384);
+            tc::bulk_store(slot + SLOT_WQH, smem + SM_KST, 32768);
+            tc::bulk_store(slot + SLOT_WQL, smem + SM_OPB, 32768);
             tc::bulk_commit();
         }
 
@@ -849,9 +1042,10 @@ constexpr int NT2 = 544;
 constexpr int ISSUER = 16;
 
 // ---- shared memory map (bytes) -------------------------------------------------
-constexpr uint32_t SS_UT = 2 * SLOT_IMG;    // images of two chunks, then U~ and O_loc of one chunk
+constexpr uint32_t SS_KB = 2 * SLOT_IMG;    // [-W | Qh] images + e^{G_C} of two chunks, then Kbar,
+constexpr uint32_t SS_UT = SS_KB + 32768;   //   U~ and O_loc of one chunk
 constexpr uint32_t SS_OL = SS_UT + 32768;
-constexpr uint32_t SS_BAR = SS_OL + 32768;  // img 0, img 1, u, o, s, ut, ol, uready, oready, sready;
+constexpr uint32_t SS_BAR = SS_OL + 32768;  // img 0, img 1, u, o, s, ut, ol, kb, uready, oready, sready;
 constexpr uint32_t SS_TOTAL = SS_BAR + 128; //   tmem base; abort flag
 static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
 
@@ -878,11 +1072,12 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     uint64_t* bar_s = bar_img + 4;
     uint64_t* bar_ut = bar_img + 5;
     uint64_t* bar_ol = bar_img + 6;
-    uint64_t* bar_uready = bar_img + 7;
-    uint64_t* bar_oready = bar_img + 8;
-    uint64_t* bar_sready = bar_img + 9;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 10);
-    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 11);
+    uint64_t* bar_kb = bar_img + 7;
+    uint64_t* bar_uready = bar_img + 8;
+    uint64_t* bar_oready = bar_img + 9;
+    uint64_t* bar_sready = bar_img + 10;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 11);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 12);
     const float* ut_s = reinterpret_cast<const float*>(smem + SS_UT);   // U~ [64 r][128 v]
     const float* ol_s = reinterpret_cast<const float*>(smem + SS_OL);   // O_loc [64 r][128 v]
 
@@ -912,7 +1107,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     if (warp == 0) tc::tmem_alloc(tmem_base_s, TS_COLS);
     if (tid == 0) {
 #pragma unroll
-        for (int b = 0; b < 7; ++b) tc::bar_init(bar_img + b, 1);
+        for (int b = 0; b < 8; ++b) tc::bar_init(bar_img + b, 1);
         tc::bar_init(bar_uready, 16);
         tc::bar_init(bar_oready, 16);
         tc::bar_init(bar_sready, 16);
@@ -938,13 +1133,13 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::bar_expect_tx(b, SLOT_IMG);
                 uint8_t* dst = smem + (i & 1) * SLOT_IMG;
                 const uint8_t* src = slot_of(i);
-#pragma unroll
-                for (int part = 0; part < 5; ++part) tc::bulk_load(dst + part * 16384, src + part * 16384, 16384, b);
+                tc::bulk_load(dst, src, 32768, b);
+                tc::bulk_load(dst + 32768, src + 32768, 32768, b);
                 tc::bulk_load(dst + SLOT_EGC, src + SLOT_EGC, SLOT_IMG - SLOT_EGC, b);
             }
             __syncwarp();
         };
-        // U~ and O_loc of one chunk (single buffers, refilled once consumed)
+        // Kbar, U~ and O_loc of one chunk (single buffers, refilled once consumed)
         auto issue_vec = [&](int64_t i, uint64_t* bar, uint32_t sm_off, uint32_t slot_off) {
             if (lane == 0) {
                 tc::bar_expect_tx(bar, 32768);
@@ -953,17 +1148,17 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             __syncwarp();
         };
         int64_t issued = 0, done = 0;  // image loads issued / known complete
-        int64_t ut_issued = 0, ol_issued = 0;
+        int64_t ut_issued = 0, ol_issued = 0, kb_issued = 0;
         if (nchunks > 0) {
             issue_img(0);
+            issue_vec(0, bar_kb, SS_KB, SLOT_KH);
             issue_vec(0, bar_ut, SS_UT, SLOT_UT);
             issue_vec(0, bar_ol, SS_OL, SLOT_OL);
             issued = 1;
-            ut_issued = ol_issued = 1;
+            ut_issued = ol_issued = kb_issued = 1;
         }
         if (nchunks > 1) { issue_img(1); issued = 2; }
         const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
-        const uint32_t id_n64_bmn = tc::idesc_bf16(128, 64, false, true);
         for (int64_t i = 0; i < nchunks; ++i) {
             const uint32_t par = (uint32_t)(i & 1);
             if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
@@ -971,31 +1166,31 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             if (!wait(bar_sready, par)) break;
             tc::fence_after();
             const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
-            // [U^T | O^T] = S_hi^T [-W | Qh_hi]^T, then O^T += S_hi^T Qh_lo^T + S_lo^T Qh_hi^T
-            const uint64_t wq = tc::sdesc(img + SLOT_WQ, 2 * C * 16, 128);
-            const uint64_t qh = tc::sdesc(img + SLOT_WQ + 8 * 128, 2 * C * 16, 128);
-            const uint64_t ql = tc::sdesc(img + SLOT_QL, C * 16, 128);
-#pragma unroll
-            for (int ks_ = 0; ks_ < D / 16; ++ks_)
-                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(wq, ks_ * 2 * 2 * C * 16), id_n128_bmn, ks_ > 0);
-            tc::commit_w(bar_u);
+            // [U^T | O^T] = S^T [-W | Qh]^T with both operands split hi|lo:
+            //   S_hi [-W hi | Qh hi] + S_lo [-W hi | Qh hi] + S_hi [-W lo | Qh lo]
+            const uint64_t bh = tc::sdesc(img + SLOT_WQH, 2 * C * 16, 128);
+            const uint64_t bl = tc::sdesc(img + SLOT_WQL, 2 * C * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                tc::mma_ts_w(tm + TS_AO, tm + TS_SH + ks_ * 8, tc::dadv(ql, ks_ * 2 * C * 16), id_n64_bmn, 1);
-                tc::mma_ts_w(tm + TS_AO, tm + TS_SL + ks_ * 8, tc::dadv(qh, ks_ * 2 * 2 * C * 16), id_n64_bmn, 1);
+                const uint32_t o = ks_ * 2 * 2 * C * 16;
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bh, o), id_n128_bmn, ks_ > 0);
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SL + ks_ * 8, tc::dadv(bh, o), id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bl, o), id_n128_bmn, 1);
             }
+            tc::commit_w(bar_u);
             tc::commit_w(bar_o);
             // S^T += U^T Kbar once U hi/lo are in TMEM (the decay came before them)
-            if (!wait(bar_uready, par)) break;
+            if (!wait(bar_uready, par) || !wait(bar_kb, par)) break;
             tc::fence_after();
-            const uint64_t khd = tc::sdesc(img + SLOT_KH, D * 16, 128), kld = tc::sdesc(img + SLOT_KL, D * 16, 128);
+            const uint32_t kb = tc::smem_u32(smem + SS_KB);
+            const uint64_t khd = tc::sdesc(kb, D * 16, 128), kld = tc::sdesc(kb + 16384, D * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
                 const uint32_t uh = tm + TS_UH + ks_ * 8, ul = tm + TS_UL + ks_ * 8;
-                const uint64_t bh = tc::dadv(khd, ks_ * 2 * D * 16), bl = tc::dadv(kld, ks_ * 2 * D * 16);
-                tc::mma_ts_w(tm + TS_S, uh, bh, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TS_S, uh, bl, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TS_S, ul, bh, id_n128_bmn, 1);
+                const uint64_t bh2 = tc::dadv(khd, ks_ * 2 * D * 16), bl2 = tc::dadv(kld, ks_ * 2 * D * 16);
+                tc::mma_ts_w(tm + TS_S, uh, bh2, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_S, uh, bl2, id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_S, ul, bh2, id_n128_bmn, 1);
             }
             tc::commit_w(bar_s);
             // U~ of this chunk is consumed (U hi/lo are written): fetch the next one
@@ -1010,7 +1205,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 // (a sequence's ragged last chunk is stored by the epilogue warps)
                 const int64_t c0 = bos + i * C;
                 if (eos - c0 >= C && lane == 0) {
-                    tc::tma_store_3d(&mo, smem + (i & 1) * SLOT_IMG + SLOT_WQ, 0, h, (int)c0);
+                    tc::tma_store_3d(&mo, smem + (i & 1) * SLOT_IMG + SLOT_WQH, 0, h, (int)c0);
                     tc::bulk_commit();
                 }
             }
@@ -1018,10 +1213,14 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 issue_vec(i + 1, bar_ol, SS_OL, SLOT_OL);
                 ol_issued = i + 2;
             }
-            // this image buffer is free once every MMA of the chunk has completed
-            // and the o rows have left it
-            if (i + 2 < nchunks) {
+            // Kbar's buffer is free once the state-update MMAs have completed, this
+            // image buffer once the o rows have left it as well
+            if (i + 1 < nchunks) {
                 if (!wait(bar_s, par)) break;
+                issue_vec(i + 1, bar_kb, SS_KB, SLOT_KH);
+                kb_issued = i + 2;
+            }
+            if (i + 2 < nchunks) {
                 tc::bulk_wait_read();
                 __syncwarp();
                 issue_img(i + 2);
@@ -1033,6 +1232,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
         if (*abort_s && lane == 0) {
             for (int64_t j = done; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
             if (ut_issued > 0) tc::bar_wait(bar_ut, (uint32_t)((ut_issued - 1) & 1), kWaitIter);
+            if (kb_issued > 0) tc::bar_wait(bar_kb, (uint32_t)((kb_issued - 1) & 1), kWaitIter);
             if (ol_issued > 0) tc::bar_wait(bar_ol, (uint32_t)((ol_issued - 1) & 1), kWaitIter);
         }
     } else {
@@ -1126,7 +1326,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::tmem_ld16(tm + lane_base(warp) + TS_AO + rb, a);
                 tc::tmem_ld_wait();
                 if (L == C) {
-                    TOut* ost = reinterpret_cast<TOut*>(smem + (i & 1) * SLOT_IMG + SLOT_WQ);
+                    TOut* ost = reinterpret_cast<TOut*>(smem + (i & 1) * SLOT_IMG + SLOT_WQH);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         ost[(rb + j) * D + x] = from_f32<TOut>(ol_s[(rb + j) * D + x] + __uint_as_float(a[j]));
@@ -1200,17 +1400,18 @@ bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int H) {
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][H][128] bf16 tensor; box = 64 rows x 64 channels of one head, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
+// [rows][H][128] bf16 tensor; box = 64 rows x 64 channels of one head, 128B
+// swizzle (halo = false), or 3 rows x 64 channels without swizzle (halo = true).
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, bool halo = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {64, 1, halo ? 3u : (cuuint32_t)C};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, halo ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Library-owned stream-ordered memory pool, one per device, that keeps what it
@@ -1251,7 +1452,7 @@ cudaError_t device_pool(cudaMemPool_t* pool, int* sms) {
 // (fixed_ws == nullptr) or from a caller-side buffer of fixed_bytes.
 template <typename TOut>
 cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nullptr, size_t fixed_bytes = 0,
-                      int fixed_sms = 0) {
+                      int fixed_sms = 0, bool fused = false) {
     const int64_t NH = (int64_t)p.N * p.H;
     if (NH == 0) return cudaSuccess;
     const bool packed = p.cu_seqlens != nullptr;
@@ -1296,16 +1497,28 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
     if (tasks >= ((int64_t)1 << 31)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess && tasks > 0) {
         const int64_t rows = (int64_t)p.B * p.T;
-        CUtensorMap mq, mk, mv, mg;
-        if (!make_map(&mq, p.q, rows, p.H) || !make_map(&mk, p.k, rows, p.H) ||
-            !make_map(&mv, p.v, rows, p.H) || !make_map(&mg, p.g, rows, p.H)) {
+        CUtensorMap mq, mk, mv, mg, hq, hk, hv;
+        bool ok = make_map(&mq, p.q, rows, p.H) && make_map(&mk, p.k, rows, p.H) && make_map(&mv, p.v, rows, p.H) &&
+                  make_map(&mg, p.g, rows, p.H);
+        if (fused) {
+            ok = ok && make_map(&hq, p.q, rows, p.H, true) && make_map(&hk, p.k, rows, p.H, true) &&
+                 make_map(&hv, p.v, rows, p.H, true);
+        } else {
+            hq = mq; hk = mk; hv = mv;  // unused
+        }
+        if (!ok) {
             e = cudaErrorInvalidValue;
         } else {
-            const int smem_bytes = (int)SM_LOCAL_TOTAL + 1024;  // + alignment slack
-            e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            Prologue pro{};
+            pro.conv_q = p.conv_q; pro.conv_k = p.conv_k; pro.conv_v = p.conv_v;
+            pro.A_log = p.A_log; pro.dt_bias = p.dt_bias;
+            pro.act = p.conv_act; pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
+            auto kern = fused ? chunk_local_kernel<true> : chunk_local_kernel<false>;
+            const int smem_bytes = (int)(fused ? SM_LOCAL_TOTAL_FUSED : SM_LOCAL_TOTAL) + 1024;  // + alignment slack
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
             if (e == cudaSuccess) {
                 const int64_t grid = tasks < sms ? tasks : sms;
-                chunk_local_kernel<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, p.beta, p.scale, pl);
+                kern<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, hq, hk, hv, p.beta, p.scale, pl, pro);
                 e = cudaGetLastError();
             }
         }
@@ -1368,6 +1581,11 @@ bool chunk_tc_supported(kda_dtype in_dt, int K, int V) { return in_dt == KDA_BF1
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
     if (out_dt == KDA_F32) return launch_tc<float>(p, st);
     return launch_tc<__nv_bfloat16>(p, st);
+}
+
+cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
+    if (out_dt == KDA_F32) return launch_tc<float>(p, st, nullptr, 0, 0, true);
+    return launch_tc<__nv_bfloat16>(p, st, nullptr, 0, 0, true);
 }
 
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {

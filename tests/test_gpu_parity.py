@@ -136,23 +136,27 @@ def test_gate_at_lower_bound():
 
 
 # ------------------------------------------------------------------ fused prologue
+# bf16 with K = V = 128 runs the prologue inside the tensor-core chunk-local
+# kernel; the other combinations run the CUDA-core kernel's prologue.
+@pytest.mark.parametrize("dtype,K,V", [(torch.bfloat16, 128, 128), (torch.float32, 128, 128),
+                                       (torch.bfloat16, 64, 64)])
 @pytest.mark.parametrize("act", [0, 1])
-def test_fused_prologue_small(act):
-    lengths = [5, 64, 131, 1]
-    inp = synth.prologue_inputs(0, 3, 128, 128, torch.bfloat16, seed=13, lengths=lengths)
+def test_fused_prologue_small(act, dtype, K, V):
+    lengths = [5, 64, 131, 1, 70]
+    H = 3
+    inp = synth.prologue_inputs(0, H, K, V, dtype, seed=13 + K + act, lengths=lengths)
     d = to_dev(inp)
     o, sT = kda.chunk_fwd_fused(d["q_raw"], d["k_raw"], d["v_raw"], d["gate_x"], d["beta"], d["conv_w"],
                                 d["A_log"], d["dt_bias"], scale=d["scale"], initial_state=d["initial_state"],
                                 cu_seqlens=d["cu_seqlens"], conv_act=act)
     torch.cuda.synchronize()
-    H, K, V = 3, 128, 128
     cw = inp["conv_w"]
     q, k, v, g = oracle.prologue(inp["q_raw"][0], inp["k_raw"][0], inp["v_raw"][0], inp["gate_x"][0],
                                  (cw[0, :H * K], cw[1, :H * K], cw[2, :H * V]), inp["A_log"], inp["dt_bias"],
                                  cu_seqlens=inp["cu_seqlens"], act=act)
     o_ref, s_ref = oracle.kda_forward(q, k, v, g, inp["beta"][0], scale=inp["scale"],
                                       initial_state=inp["initial_state"], cu_seqlens=inp["cu_seqlens"])
-    check(o.cpu()[0], sT.cpu(), o_ref, s_ref, torch.bfloat16)
+    check(o.cpu()[0], sT.cpu(), o_ref, s_ref, dtype)
 
 
 # ------------------------------------------------------------------ decode
