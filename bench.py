@@ -50,6 +50,24 @@ def prefill_bytes(T_tokens: int, H: int, K: int, V: int, N: int, in_bytes: int, 
     return T_tokens * per_token + states
 
 
+# Bytes of one (64-token chunk, head) workspace slot of the tensor-core prefill
+# (include/kda.h): what the chunk-local kernel writes and the state kernel reads.
+SLOT_BYTES = 164352
+
+
+def kernel_bytes(T_tokens: int, n_chunks: int, H: int, K: int, V: int, N: int, reads_state: bool, prologue: bool):
+    """HBM bytes each kernel of the two-kernel prefill has to move by design:
+    the chunk-local kernel reads q, k, v, g (bf16) and beta and writes one
+    workspace slot per (chunk, head) (plus the prologue weights); the state
+    kernel reads the slots and the initial state and writes o (fp32) and the
+    final state."""
+    local = T_tokens * H * ((3 * K + V) * 2 + 2) + n_chunks * H * SLOT_BYTES
+    if prologue:  # conv weights, dt_bias and A_log, read once from HBM
+        local += H * (2 * K + V) * 16 + H * K * 4 + K * 4
+    state = n_chunks * H * SLOT_BYTES + T_tokens * H * V * 4 + N * H * K * V * 4 * (2 if reads_state else 1)
+    return local, state
+
+
 def decode_bytes(N: int, H: int, K: int, V: int, in_bytes: int) -> int:
     """One decode step: the fp32 state read and written once, plus q, k, g, v, beta and o."""
     return 2 * N * H * K * V * 4 + N * H * ((3 * K + V) * in_bytes + in_bytes + V * 4)
@@ -238,6 +256,46 @@ def time_launches(fn, steps: int, stream):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in ev]
 
 
+def time_traced(kda, fn, steps: int, stream):
+    """Like time_launches, with the prefill's own timing hook: per call the
+    events before its first kernel, after the chunk-local kernel and after its
+    last kernel.  Returns (total ms, per-call ms, chunk-local ms, state ms)."""
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    for trio in ev:
+        for e in trio:
+            e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for b, sp, e in ev:
+        kda.trace_events(b, sp, e)
+        fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [b.elapsed_time(e) for b, _, e in ev]
+    k1 = [b.elapsed_time(sp) for b, sp, _ in ev]
+    k2 = [sp.elapsed_time(e) for _, sp, e in ev]
+    return t0.elapsed_time(t1), per, k1, k2
+
+
+def sum_traffic(kernels):
+    """DRAM bytes of one call (both kernels) from the committed ncu summary, or None."""
+    t = [k["traffic"] for k in kernels]
+    return None if any(x is None for x in t) else sum(t)
+
+
+def kernel_split(k1, k2, local_bytes, state_bytes, hbm, traffic_keys):
+    """Per-kernel live durations and design-traffic bandwidth of one call."""
+    m1, m2 = sum(k1) / len(k1), sum(k2) / len(k2)
+    out = []
+    for name, ms, nbytes, key in (("chunk_local_kernel", m1, local_bytes, traffic_keys[0]),
+                                   ("chunk_state_kernel", m2, state_bytes, traffic_keys[1])):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out.append({"kernel": name, "ms": ms, "share": ms / (m1 + m2), "design_bytes": nbytes,
+                    "design_gbs": gbs, "frac_of_hbm": gbs / hbm, "traffic": recorded_traffic(key)})
+    return out
+
+
 def run_ours(args, world, rank, local):
     import kimi_delta_attention_chunk_gb300 as kda
     from kimi_delta_attention_chunk_gb300 import synth
@@ -266,7 +324,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     clocks.mark("t0")
-    total_ms, per = time_launches(prefill, args.steps, stream)
+    total_ms, per, k1, k2 = time_traced(kda, prefill, args.steps, stream)
     clocks.mark("t1")
     barrier(world)
     clk = clocks.stop()
@@ -277,6 +335,8 @@ def run_ours(args, world, rank, local):
     kernel_ms = sum(per) / len(per)
     pbytes = prefill_bytes(T, H, K, V, 1, 2, reads_state=False)
     achieved = pbytes / (kernel_ms * 1e-3) / 1e9
+    lb, sb = kernel_bytes(T, (T + 63) // 64, H, K, V, 1, reads_state=False, prologue=False)
+    kernels = kernel_split(k1, k2, lb, sb, hbm, ("chunk_local_kernel/prefill", "chunk_state_kernel/prefill"))
 
     # ---- end to end through the public call: pinned host in, host out
     pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
@@ -359,20 +419,30 @@ def run_ours(args, world, rank, local):
         run_x()
         torch.cuda.synchronize()
         barrier(world)
-        reps = 3 if name == "varlen" else 1
-        xt, xper = time_launches(run_x, reps, stream)
+        reps = 3
+        xt, xper, xk1, xk2 = time_traced(kda, run_x, reps, stream)
         xt = max_over_ranks(xt, world) / reps
         xbytes = prefill_bytes(Ttot, wl.H, wl.K, wl.V, N, 2, reads_state=wl.init_state)
         xk = sum(xper) / len(xper)
         xach = xbytes / (xk * 1e-3) / 1e9
+        if inp.get("cu_seqlens") is not None:
+            cu = inp["cu_seqlens"].cpu().tolist()
+            nch = sum((cu[i + 1] - cu[i] + 63) // 64 for i in range(len(cu) - 1))
+        else:
+            nch = (Ttot + 63) // 64
+        xlb, xsb = kernel_bytes(Ttot, nch, wl.H, wl.K, wl.V, N, reads_state=wl.init_state, prologue=wl.prologue)
+        xkernels = kernel_split(xk1, xk2, xlb, xsb, hbm,
+                                (f"chunk_local_kernel/{name}", f"chunk_state_kernel/{name}"))
         extra[name] = {
             "value": world * Ttot / (xt * 1e-3), "unit": "tokens/s", "ms_per_launch": xt,
             "workload": ("varlen prefill: 16 sequences of 512..8192 tokens (%d total) packed by cu_seqlens, "
                          "H=96 K=V=128 bf16, fp32 initial states" % Ttot) if name == "varlen" else
                         ("long prefill with fused prologue (conv4, L2-norm, gate): T=65536 H=96 K=V=128 bf16, "
-                         "nonzero initial state; runs the CUDA-core fused kernel"),
+                         "nonzero initial state; prologue inside the chunk-local kernel"),
+            "gpu_launches": reps * (3 if name == "varlen" else 2),
             "roofline": {"bound": "hbm", "achieved": xach, "peak": hbm, "unit": "GB/s", "frac": xach / hbm,
-                         "traffic": None, "algorithmic_bytes": xbytes, "peak_kind": peak_kind}}
+                         "traffic": sum_traffic(xkernels), "algorithmic_bytes": xbytes, "peak_kind": peak_kind,
+                         "kernels": xkernels}}
         del inp, ox, sx
 
     if rank != 0:
@@ -385,9 +455,9 @@ def run_ours(args, world, rank, local):
                                "zero initial state", "parallelism": f"replicas x{world}",
                    "l2": "inputs (611 MB per step) larger than L2; no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": recorded_traffic("chunk_prefill"), "algorithmic_bytes": pbytes,
-                     "kernel_ms": kernel_ms, "peak_kind": peak_kind},
-        "clocks": clk, "e2e": e2e, "gpu_launches": args.steps,
+                     "traffic": sum_traffic(kernels), "algorithmic_bytes": pbytes,
+                     "kernel_ms": kernel_ms, "peak_kind": peak_kind, "kernels": kernels},
+        "clocks": clk, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "decode": decode,
     }
     line.update(extra)
@@ -406,6 +476,12 @@ def profile_case(args):
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         for _ in range(args.profile_reps):
             kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"])
+    elif args.profile_case == "fused":
+        inp = synth.prologue_inputs(args.profile_T, args.profile_H, 128, 128, torch.bfloat16, seed=4)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        for _ in range(args.profile_reps):
+            kda.chunk_fwd_fused(d["q_raw"], d["k_raw"], d["v_raw"], d["gate_x"], d["beta"], d["conv_w"],
+                                d["A_log"], d["dt_bias"], scale=d["scale"], initial_state=d["initial_state"])
     else:
         w = synth.WORKLOADS["decode"]
         dec = synth.decode_inputs(w.B, w.H, w.K, w.V, args.profile_reps, w.dtype, w.seed)
@@ -419,7 +495,7 @@ def profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode"], default=None,
                     help="run a few launches of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-T", type=int, default=2048)
     ap.add_argument("--profile-H", type=int, default=16)

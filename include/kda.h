@@ -181,6 +181,20 @@ KDA_API kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, con
                                void *o, kda_dtype o_dtype, float *final_state, void *stream);
 
 /*
+ * kda_trace_events -- timing hook for the tensor-core prefill.
+ *
+ * (The pages have no counterpart: instrumentation.)  The tensor-core prefill
+ * runs as two kernels, the chunk-local one and the state chain.  The next
+ * kda_chunk_fwd, kda_chunk_fwd_fused or kda_chunk_fwd_noalloc call made by the
+ * calling host thread records these CUDA events (cudaEvent_t passed as void*;
+ * any may be NULL) on its stream: begin before its first kernel, split after
+ * the chunk-local kernel, end after its last kernel.  That call consumes the
+ * setting; a call that takes the CUDA-core path records nothing and clears it
+ * too.  The events belong to the caller.
+ */
+KDA_API void kda_trace_events(void *begin, void *split, void *end);
+
+/*
  * kda_recurrent_step -- one decode token for each of N sequences.
  *
  * Applies one step of the recurrence to the fp32 state in place, streaming it

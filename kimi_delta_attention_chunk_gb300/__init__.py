@@ -15,4 +15,5 @@ from .kda import (  # noqa: F401
     library_path,
     load_library,
     recurrent_step,
+    trace_events,
 )

@@ -96,6 +96,7 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
     p.final_state = final_state;
     cudaStream_t st = (cudaStream_t)stream;
     if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc(o_dtype, p, st));
+    kda::trace_set(nullptr, nullptr, nullptr);
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, false, p, st));
 }
 
@@ -152,8 +153,11 @@ kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void*
     p.l2_eps = l2_eps;
     cudaStream_t st = (cudaStream_t)stream;
     if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc_fused(o_dtype, p, st));
+    kda::trace_set(nullptr, nullptr, nullptr);
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, true, p, st));
 }
+
+void kda_trace_events(void* begin, void* split, void* end) { kda::trace_set(begin, split, end); }
 
 kda_status kda_recurrent_step(const void* q, const void* k, const void* v, const void* g,
                               const void* beta, kda_dtype in_dtype, float scale, float* state,

@@ -50,6 +50,11 @@ cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, cudaStream_t 
 constexpr size_t kFixedScratchBytes = (size_t)64 << 20;
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
 
+// Events that the next tensor-core prefill call made on this host thread
+// records: before its first kernel, after the chunk-local kernel, after its
+// last kernel (any may be null); the call consumes them.
+void trace_set(void* begin, void* split, void* end);
+
 // Single-token decode.
 cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const void* q,
                         const void* k, const void* v, const void* g, const void* beta,

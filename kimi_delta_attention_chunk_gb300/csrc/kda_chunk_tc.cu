@@ -1448,6 +1448,13 @@ cudaError_t device_pool(cudaMemPool_t* pool, int* sms) {
     return cudaSuccess;
 }
 
+// Events that the next prefill call on this host thread records (timing hook).
+thread_local cudaEvent_t g_trace[3] = {nullptr, nullptr, nullptr};
+
+void trace_record(cudaEvent_t ev, cudaStream_t st) {
+    if (ev != nullptr) cudaEventRecord(ev, st);
+}
+
 // The prefill's kernels, with the workspace taken from the library's pool
 // (fixed_ws == nullptr) or from a caller-side buffer of fixed_bytes.
 template <typename TOut>
@@ -1456,6 +1463,8 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
     const int64_t NH = (int64_t)p.N * p.H;
     if (NH == 0) return cudaSuccess;
     const bool packed = p.cu_seqlens != nullptr;
+    cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
+    g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
     Plan pl{};
     pl.cu_seqlens = p.cu_seqlens;
     pl.T = p.T;
@@ -1484,6 +1493,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
     }
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
     pl.slots = reinterpret_cast<uint8_t*>(ws) + hdr_bytes;
+    trace_record(trace[0], st);
     if (packed) {
         pl.chunk_off = hdr;
         pl.order = p.N <= 1024 ? hdr + (p.N + 1) : nullptr;
@@ -1520,6 +1530,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
                 const int64_t grid = tasks < sms ? tasks : sms;
                 kern<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, hq, hk, hv, p.beta, p.scale, pl, pro);
                 e = cudaGetLastError();
+                trace_record(trace[1], st);
             }
         }
     }
@@ -1536,6 +1547,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
                 kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(mo, p.initial_state, p.final_state,
                                                            reinterpret_cast<TOut*>(p.o), pl);
                 e = cudaGetLastError();
+                trace_record(trace[2], st);
             }
         }
     }
@@ -1577,6 +1589,12 @@ cudaError_t fixed_scratch(void** ptr, int* sms) {
 }  // namespace
 
 bool chunk_tc_supported(kda_dtype in_dt, int K, int V) { return in_dt == KDA_BF16 && K == D && V == D; }
+
+void trace_set(void* begin, void* split, void* end) {
+    g_trace[0] = static_cast<cudaEvent_t>(begin);
+    g_trace[1] = static_cast<cudaEvent_t>(split);
+    g_trace[2] = static_cast<cudaEvent_t>(end);
+}
 
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
     if (out_dt == KDA_F32) return launch_tc<float>(p, st);

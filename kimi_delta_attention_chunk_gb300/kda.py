@@ -34,6 +34,7 @@ SIGNATURES = {
                                    _i, _vp, _i, _fp, _vp]),
     "kda_chunk_fwd_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _fp, _fp, _f, _f,
                                  _f, _fp, _i32p, _i, _i, _i, _i, _i, _i, _vp, _i, _fp, _vp]),
+    "kda_trace_events": (None, [_vp, _vp, _vp]),
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
 }
@@ -172,6 +173,22 @@ def chunk_fwd_fused(q_raw, k_raw, v_raw, gate_x, beta, conv_w, A_log, dt_bias,
                                  _dt(o), _ptr(final_state), _stream(q_raw.device))
     _check("kda_chunk_fwd_fused", st)
     return o, final_state
+
+
+def trace_events(begin=None, split=None, end=None):
+    """Have the next prefill call on this thread record these torch.cuda.Event
+    objects on its stream: before its first kernel, after the chunk-local
+    kernel, after its last kernel (tensor-core path only)."""
+    lib = load_library()
+    h = []
+    for e in (begin, split, end):
+        if e is None:
+            h.append(None)
+        else:
+            if not e.cuda_event:  # torch creates the CUDA event on first record
+                e.record()
+            h.append(e.cuda_event)
+    lib.kda_trace_events(*h)
 
 
 def recurrent_step(q, k, v, g, beta, state, scale: float | None = None, o_dtype=torch.float32, o=None):
