@@ -73,25 +73,26 @@ def decode_bytes(N: int, H: int, K: int, V: int, in_bytes: int) -> int:
     return 2 * N * H * K * V * 4 + N * H * ((3 * K + V) * in_bytes + in_bytes + V * 4)
 
 
-def source_sha() -> str:
+def source_sha(files) -> str:
+    """Hash of the CUDA sources a kernel is built from (names relative to csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kimi_delta_attention_chunk_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; otherwise None."""
+def recorded_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
+    if it was taken on the kernel's current sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    rec = d.get(kernel)
-    if not rec or rec.get("source_sha") != source_sha():
+    rec = d.get(key)
+    if not rec or rec.get("source_sha") != source_sha(rec.get("sources", [])):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -394,7 +395,7 @@ def run_ours(args, world, rank, local):
     decode = {"value": world / (dec_ms * 1e-3), "unit": "steps/s", "tokens_per_s": world * dw.B / (dec_ms * 1e-3),
               "ms_per_step": dec_ms, "workload": "decode N=256 H=96 K=V=128 bf16, fp32 state in place, 64 steps",
               "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s", "frac": dach / hbm,
-                           "traffic": recorded_traffic("decode_step_kernel"), "algorithmic_bytes": dbytes,
+                           "traffic": recorded_traffic("decode_step_kernel/decode"), "algorithmic_bytes": dbytes,
                            "peak_kind": peak_kind}}
     del dd, state, qs, ks, vs, gs, bs
 

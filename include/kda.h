@@ -81,7 +81,9 @@ KDA_API int kda_abi_version(void);
  * Computes the recurrence above for N independent sequences with a chunked
  * (64-token) algorithm: in-chunk gated products A = K K^T and P = Q K^T with
  * cumulative per-channel decay, a UT transform of the decayed keys, and the
- * state carried from chunk to chunk on chip.  Results equal the token-by-token
+ * state carried from chunk to chunk (tensor-core path: a chunk-local kernel
+ * over all chunks at once, then one state chain per sequence and head with
+ * the state in tensor memory).  Results equal the token-by-token
  * recurrence up to rounding.
  *
  *  q, k, g, v, beta   inputs as laid out above, element type in_dtype.
