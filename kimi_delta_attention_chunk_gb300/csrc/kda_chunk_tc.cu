@@ -585,14 +585,16 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             const int c = (warp & 3) * 32 + lane;
             const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
             const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
-            const float pfx[4] = {1.f, t0v, t0v * t1v, t0v * t1v * t2v};
+            // product of the block totals before this warpgroup's 16-token block
+            const int jblk = warp >> 2;
+            const float pf = jblk == 0 ? 1.f : (jblk == 1 ? t0v : (jblk == 2 ? t0v * t1v : t0v * t1v * t2v));
             uint32_t kh[8], kl[8], vv[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int j = jb + 2 * i;
                 const float k0 = j < L ? ld_k(j, c) : 0.f;
                 const float k1 = j + 1 < L ? ld_k(j + 1, c) : 0.f;
-                tc::split2(k0 * pfx[j >> 4] * pre_s[j * PRE_LD + c], k1 * pfx[(j + 1) >> 4] * pre_s[(j + 1) * PRE_LD + c], kh[i], kl[i]);
+                tc::split2(k0 * pf * pre_s[j * PRE_LD + c], k1 * pf * pre_s[(j + 1) * PRE_LD + c], kh[i], kl[i]);
                 if constexpr (!FUSED) {
                     const __nv_bfloat16 z = __float2bfloat16(0.f);
                     const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
@@ -707,28 +709,24 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             float* T = reinterpret_cast<float*>(smem + SM_TF);
             float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch: [2][16][16] then [32][32]
             // (blocks above the diagonal are never written; the operand build masks them)
-            // diagonal blocks: forward substitution with the column in registers;
-            // warp w: block w/2, columns 8 (w%2) .. + 8; lane: column lane/4, rows = lane%4 (mod 4)
-            if (warp < 8) {
-                const int blk = warp >> 1, col = 8 * (warp & 1) + (lane >> 2), part = lane & 3;
-                const int i = 16 * blk + col;
-                float x[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) x[m] = (part + 4 * m == col) ? 1.f : 0.f;
+            // diagonal blocks: one thread per column of each 16 x 16 block (warps 0, 1),
+            // right-looking: once x[m] is known every later row's sum takes its term,
+            // so each step waits for one FMA
+            if (warp < 2) {
+                const int blk = tid >> 4, col = tid & 15;
                 const float* nb = N + 16 * blk * MAT_LD + 16 * blk;
+                float x[16], acc[16];
 #pragma unroll
-                for (int rr = 1; rr < 16; ++rr) {
-                    float acc = 0.f;
+                for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        if (part + 4 * m < rr) acc += nb[rr * MAT_LD + part + 4 * m] * x[m];
-                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                    if (part == (rr & 3) && rr > col) x[rr >> 2] = -acc;
+                for (int m = 0; m < 16; ++m) {
+                    x[m] = m == col ? 1.f : (m > col ? -acc[m] : 0.f);
+#pragma unroll
+                    for (int r = m + 1; r < 16; ++r) acc[r] += nb[r * MAT_LD + m] * x[m];
                 }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) T[(16 * blk + part + 4 * m) * MAT_LD + i] = x[m];
-            } else {
+                for (int r = 0; r < 16; ++r) T[(16 * blk + r) * MAT_LD + 16 * blk + col] = x[r];
+            } else if (warp >= 8) {
                 // prefetch the next task into the consumed staging
                 if (tid == kIssueTid && nxt.valid) issue_tma(nxt);
                 if (nxt.valid) beta_r = fetch_beta(nxt);
