@@ -195,3 +195,20 @@ def test_decode_equals_prefill():
     torch.cuda.synchronize()
     assert rel_err(o_d.cpu(), o_p.cpu().double().numpy()) <= 1e-3
     assert rel_err(state.cpu(), s_p.cpu().double().numpy()) <= 1e-3
+
+
+# ------------------------------------------------------------------ timing hook
+def test_trace_events_bracket_the_two_kernels():
+    inp = synth.direct_inputs(300, 4, 128, 128, torch.bfloat16, seed=21)
+    d = to_dev(inp)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    kda.trace_events(*ev)
+    kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"])
+    torch.cuda.synchronize()
+    t_local, t_state = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+    assert t_local > 0 and t_state > 0
+    # the setting is consumed by that call: the next call records nothing new
+    before = ev[2].query()
+    kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"])
+    torch.cuda.synchronize()
+    assert before and ev[0].elapsed_time(ev[2]) == pytest.approx(t_local + t_state, rel=1e-3, abs=1e-3)
