@@ -52,7 +52,7 @@ def prefill_bytes(T_tokens: int, H: int, K: int, V: int, N: int, in_bytes: int, 
 
 # Bytes of one (64-token chunk, head) workspace slot of the tensor-core prefill
 # (include/kda.h): what the chunk-local kernel writes and the state kernel reads.
-SLOT_BYTES = 164352
+SLOT_BYTES = 147968
 
 
 def kernel_bytes(T_tokens: int, n_chunks: int, H: int, K: int, V: int, N: int, reads_state: bool, prologue: bool):

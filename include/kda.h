@@ -105,7 +105,7 @@ KDA_API int kda_abi_version(void);
  *                     state is then updated in place); no other overlap is
  *                     allowed.
  *
- *  Workspace (bf16, K = V = 128): 164352 bytes per (chunk, head) slot for
+ *  Workspace (bf16, K = V = 128): 147968 bytes per (chunk, head) slot for
  *  every 64-token chunk of every sequence (an upper bound of ceil(T / 64) + N
  *  chunks per head when cu_seqlens is given), returned to the pool when the
  *  call's work completes.  KDA_ERR_WORKSPACE if the pool cannot provide it.
@@ -132,12 +132,12 @@ KDA_API kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, co
  *
  *  - Supported: in_dtype KDA_BF16 with K = V = 128 (the tensor-core path);
  *    anything else returns KDA_ERR_UNSUPPORTED.
- *  - The workspace needed is 164352 bytes per (chunk, head) slot, with
+ *  - The workspace needed is 147968 bytes per (chunk, head) slot, with
  *    ceil(T / 64) * B slots per head without cu_seqlens and ceil(T / 64) + N
  *    with it (plus 4 * (2 N + 1 + slots per head) bytes, rounded up to 1 KiB,
  *    of chunk bookkeeping).  A call needing more than 64 MiB returns
  *    KDA_ERR_WORKSPACE before anything is enqueued (e.g. H = 96: T <= 256 for
- *    one sequence; H = 8: T <= 3264).
+ *    one sequence; H = 8: T <= 3584).
  *  - The first call made on a device looks up the array's device address (a
  *    CUDA runtime call); make that first call before any stream capture.
  *  - Every call shares the one array and leaves its last contents there;

@@ -10,30 +10,26 @@
 //   O      = scale (q e^G) S + scale P U
 //   S     <- Diag(e^{G_C}) S + (k e^{G_C - G})^T U
 //
-// Only the last three lines touch the state.  Substituting U into O gives
-//
-//   O = O_loc + Qh S,   O_loc = scale P U~,   Qh = scale ((q e^G) - P W),
-//
-// so everything except U = U~ - W S, O = O_loc + Qh S and the state update is
-// independent of S and is computed for all chunks at once.  The prefill is
-// therefore two kernels:
+// Only the last three lines touch the state; everything else is independent of
+// S and is computed for all chunks at once.  The prefill is therefore two
+// kernels:
 //
 //   chunk_local_kernel   persistent, one (chunk, head) task at a time per CTA:
-//                        A, P, T, W, U~, O_loc, Qh, Kbar = k e^{G_C - G} and
+//                        A, P, T, W, U~, Kbar = k e^{G_C - G}, scale (q e^G) and
 //                        e^{G_C}, written to a per-(chunk, head) workspace slot
 //                        (the MMA operands already in their shared-memory
 //                        layout, so the next kernel fetches them with bulk
 //                        copies)
 //   chunk_state_kernel   one CTA per (sequence, head): the fp32 state lives in
 //                        tensor memory as S^T for the whole sequence; per chunk
-//                        three MMA rounds (U^T = U~^T - S^T W^T, O^T = O_loc^T +
-//                        S^T Qh^T, S^T <- S^T Diag(e^{G_C}) + U^T Kbar).
+//                        [U^T | O^T] = [U~^T | 0] + S^T [-W | scale q e^G]^T,
+//                        then S^T <- S^T Diag(e^{G_C}) + U^T Kbar and
+//                        O^T += U^T (scale P)^T.
 //
 // Operand precision: every operand that feeds o or the state directly is
 // split x = hi + lo into two bf16 values and multiplied as hi*hi + hi*lo +
 // lo*hi (about 16 significant bits); W and the correction W S use one bf16
-// term (the same bf16 W in U and in Qh, so the substitution above holds for
-// the rounded W as well); v is exact in bf16.  Decay factors are running
+// term; v is exact in bf16.  Decay factors are running
 // products of e^{g} over exactly the tokens they span, built from
 // per-16-token-block prefix products (each >= e^-80 since g >= -5, so ratios
 // inside a block are safe) and block totals; nothing overflows and nothing
@@ -59,16 +55,17 @@ constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TME
 constexpr uint32_t kWaitIter = 1u << 26;
 
 // ---- workspace slot of one (chunk, head), written by the local kernel --------
-constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qh hi] (bf16) as one B operand, MN-major
-                                        //   (n = r for -W, n = 64 + r for Qh; k = c)
-constexpr uint32_t SLOT_WQL = 32768;    // [-W lo | Qh lo], same layout
+constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qs hi] (bf16) as one B operand, MN-major
+                                        //   (n = r for -W, n = 64 + r for Qs = scale q e^G; k = c)
+constexpr uint32_t SLOT_WQL = 32768;    // [-W lo | Qs lo], same layout
 constexpr uint32_t SLOT_EGC = 65536;    // e^{G_C} fp32 [128]
 constexpr uint32_t SLOT_IMG = 66048;    // bytes of the images above (one shared-memory copy)
 constexpr uint32_t SLOT_KH = 66048;     // Kbar hi as B operand, MN-major (n = c, k = r)
 constexpr uint32_t SLOT_KL = 82432;     // Kbar lo
-constexpr uint32_t SLOT_UT = 98816;     // U~ fp32 [64 r][128 v]
-constexpr uint32_t SLOT_OL = 131584;    // O_loc fp32 [64 r][128 v]
-constexpr uint32_t SLOT_BYTES = 164352;
+constexpr uint32_t SLOT_P = 98816;      // scale P hi | lo, B operand [64 r][64 j] K-major
+constexpr uint32_t SLOT_KBP = 49152;    // bytes of Kbar and P (one shared-memory copy)
+constexpr uint32_t SLOT_UT = 115200;    // U~ fp32 [64 r][128 v]
+constexpr uint32_t SLOT_BYTES = 147968;
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
 // (q e^G) fp32 [64 r][128 c] in shared memory: float4 column f of row r stored at
@@ -167,13 +164,9 @@ constexpr uint32_t TL_AP = 0;      // [L_0; L_1] [Rt_0 | Rt_1]^T accumulator, M 
 constexpr uint32_t TL_KTH = 96;    // (k e^G)^T hi (bf16 pairs) [128 c][32]
 constexpr uint32_t TL_KTL = 128;   // (k e^G)^T lo
 constexpr uint32_t TL_VT = 160;    // v^T (bf16 pairs) [128 v][32]
-constexpr uint32_t TL_AW = 192;    // W^T accumulator fp32 [128 c][64 r], then (P W)^T
-constexpr uint32_t TL_AU = 256;    // U~^T accumulator fp32 [128 v][64 r], then (P U~)^T
-constexpr uint32_t TL_WT = 320;    // W^T hi (bf16 pairs) [128 c][32], A operand
-constexpr uint32_t TL_UH = 352;    // U~^T hi (bf16 pairs) [128 v][32], A operand
-constexpr uint32_t TL_UL = 384;    // U~^T lo
-constexpr uint32_t TL_VTL = 416;   // v^T lo (bf16 pairs), with the prologue (v is then not bf16-exact)
-constexpr uint32_t TL_WTL = 448;   // W^T lo (bf16 pairs) [128 c][32], A operand
+constexpr uint32_t TL_AW = 192;    // W^T accumulator fp32 [128 c][64 r]
+constexpr uint32_t TL_AU = 256;    // U~^T accumulator fp32 [128 v][64 r]
+constexpr uint32_t TL_VTL = 320;   // v^T lo (bf16 pairs), with the prologue (v is then not bf16-exact)
 constexpr uint32_t TL_COLS = 512;
 // Thread that issues the tile loads and bulk stores: warps 8..15 are idle while
 // warps 0..7 invert the diagonal blocks of T, so the issue costs no barrier time.
@@ -681,7 +674,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int u = 0; u < 8; ++u) {
                     const int j = j0 + 8 * g8 + u;
                     const float xv = __uint_as_float(a[8 * g8 + u]);
-                    v[u] = is_q ? (j <= r ? xv : 0.f) : (j < r ? br * xv : 0.f);
+                    v[u] = is_q ? (j <= r ? scale * xv : 0.f) : (j < r ? br * xv : 0.f);
                 }
                 if (is_q) {
                     uint4 hi, lo;
@@ -727,7 +720,11 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int r = 0; r < 16; ++r) T[(16 * blk + r) * MAT_LD + 16 * blk + col] = x[r];
             } else if (warp >= 8) {
-                // prefetch the next task into the consumed staging
+                // scale P out; prefetch the next task into the consumed staging
+                if (tid == kIssueTid) {
+                    tc::bulk_store(slot + SLOT_P, smem + SM_PB, 16384);
+                    tc::bulk_commit();
+                }
                 if (tid == kIssueTid && nxt.valid) issue_tma(nxt);
                 if (nxt.valid) beta_r = fetch_beta(nxt);
             }
@@ -839,10 +836,13 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tc::commit_w(bar_mma);
         }
+        if (tid == kIssueTid) tc::bulk_wait_read();  // P has left its staging
         mma_sync();
         if (failed) break;
 
-        // ---- (8) W^T hi/lo and U~^T hi/lo as A operands; U~ fp32 staged for the slot --
+        // ---- (8) -W and Qs = scale q e^G, hi|lo, staged as the two merged B images
+        //      (hi where L lo was, lo in the dead T Diag(beta) / P region once P has
+        //      left it); U~ fp32 staged in the dead prefix-product region -------------
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
@@ -850,92 +850,35 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
             tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
             tc::tmem_ld_wait();
-            uint32_t wh[8], wl[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) tc::split2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]), wh[i], wl[i]);
-            tc::tmem_st8(tm + lane_base(warp) + TL_WT + rb / 2, wh);
-            tc::tmem_st8(tm + lane_base(warp) + TL_WTL + rb / 2, wl);
-            // U~ staged as [64 r][128 v] in the (now dead) A/T region for one bulk store
-            float* ut = reinterpret_cast<float*>(smem + SM_PRE);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                tc::split2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]), hi[i], lo[i]);
-            }
-            tc::tmem_st8(tm + lane_base(warp) + TL_UH + rb / 2, hi);
-            tc::tmem_st8(tm + lane_base(warp) + TL_UL + rb / 2, lo);
-            tc::tmem_st_wait();
-        }
-        publish();
-
-        // ---- (9) (P W)^T = W^T P^T,  (P U~)^T = U~^T P^T ---------------------------------
-        if (tid == kIssueTid) {
-            tc::bulk_store(slot + SLOT_UT, smem + SM_PRE, 32768);
-            tc::bulk_commit();
-        }
-        if (warp == 0) {
-            const uint32_t pb = tc::smem_u32(smem + SM_PB);
-            const uint64_t pbh = tc::sdesc(pb, 128, C * 16), pbl = tc::sdesc(pb + 8192, 128, C * 16);
-#pragma unroll
-            for (int ks_ = 0; ks_ < C / 16; ++ks_) {
-                const uint64_t ph = tc::dadv(pbh, ks_ * 256), pl_ = tc::dadv(pbl, ks_ * 256);
-                tc::mma_ts_w(tm + TL_AW, tm + TL_WT + ks_ * 8, ph, id_n64, ks_ > 0);
-                tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, ph, id_n64, ks_ > 0);
-                tc::mma_ts_w(tm + TL_AW, tm + TL_WT + ks_ * 8, pl_, id_n64, 1);
-                tc::mma_ts_w(tm + TL_AU, tm + TL_UH + ks_ * 8, pl_, id_n64, 1);
-                tc::mma_ts_w(tm + TL_AW, tm + TL_WTL + ks_ * 8, ph, id_n64, 1);
-                tc::mma_ts_w(tm + TL_AU, tm + TL_UL + ks_ * 8, ph, id_n64, 1);
-            }
-            tc::commit_w(bar_mma);
-        }
-        mma_sync();
-        if (failed) break;
-
-        // ---- (10) Qh = scale ((q e^G) - P W) and -W, hi|lo, staged as the two merged
-        //      B images (hi: where the Kbar-free OPA half is, lo: in the dead T / P
-        //      operand region); O_loc = scale P U~ out -----------------------------------
-        {
-            const int x = (warp & 3) * 32 + lane;
-            const int rb = (warp >> 2) * 16;
-            uint32_t a[16], b[16], wh[8], wl[8];
-            tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
-            tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
-            tc::tmem_ld8(tm + lane_base(warp) + TL_WT + rb / 2, wh);
-            tc::tmem_ld8(tm + lane_base(warp) + TL_WTL + rb / 2, wl);
-            tc::tmem_ld_wait();
             uint8_t* bh_s = smem + SM_KST;
             uint8_t* bl_s = smem + SM_OPB;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
-                // -W (bf16 negation is exact): the packed pairs are 8 consecutive r
-                const uint32_t* h4 = wh + 4 * g8;
-                const uint32_t* l4 = wl + 4 * g8;
-                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
-                    make_uint4(h4[0] ^ 0x80008000u, h4[1] ^ 0x80008000u, h4[2] ^ 0x80008000u, h4[3] ^ 0x80008000u);
-                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) =
-                    make_uint4(l4[0] ^ 0x80008000u, l4[1] ^ 0x80008000u, l4[2] ^ 0x80008000u, l4[3] ^ 0x80008000u);
-                float qh[8];
+                // -W (the 8 consecutive r of a core-matrix row)
+                float w[8], qs[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int r = rb + 8 * g8 + u;
-                    qh[u] = scale * (qt_s[qt_idx(r, x)] - __uint_as_float(a[8 * g8 + u]));
-                }
+                for (int u = 0; u < 8; ++u) w[u] = -__uint_as_float(a[8 * g8 + u]);
                 uint4 hi, lo;
-                tc::split8(qh, hi, lo);
+                tc::split8(w, hi, lo);
+                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) = hi;
+                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) = lo;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) qs[u] = scale * qt_s[qt_idx(rb + 8 * g8 + u, x)];
+                tc::split8(qs, hi, lo);
                 *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
                 *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = lo;
             }
-            float* ol = reinterpret_cast<float*>(slot + SLOT_OL);
+            float* ut = reinterpret_cast<float*>(smem + SM_PRE);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ol[(rb + i) * D + x] = scale * __uint_as_float(b[i]);
+            for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
         }
         tc::fence_async_smem();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
         if (tid == kIssueTid) {
+            tc::bulk_store(slot + SLOT_UT, smem + SM_PRE, 32768);
+            tc::bulk_commit();
             tc::bulk_store(slot + SLOT_WQH, smem + SM_KST, 32768);
             tc::bulk_store(slot + SLOT_WQL, smem + SM_OPB, 32768);
             tc::bulk_commit();
@@ -1038,16 +981,16 @@ chunk_plan_kernel(const int32_t* __restrict__ cu, int N, int T, int64_t max_chun
 
 // Warps 0..15 do the TMEM epilogues (warp w: TMEM lanes 32 (w % 4).., column
 // group w / 4); warp 16 only issues MMAs and bulk copies.  The two sides meet
-// at mbarriers: MMA commits (u, o, s) and the epilogue warps' arrivals
-// (uready: U hi/lo written, sready: S hi/lo written), each once per chunk.
+// at mbarriers: MMA commits (u: the first round, s: the state update, o: the
+// P U term) and the epilogue warps' arrivals (uready: U hi/lo written; sready:
+// S hi/lo written, O read out and the chunk's o staged), once per chunk.
 constexpr int NT2 = 544;
 constexpr int ISSUER = 16;
 
 // ---- shared memory map (bytes) -------------------------------------------------
-constexpr uint32_t SS_KB = 2 * SLOT_IMG;    // [-W | Qh] images + e^{G_C} of two chunks, then Kbar,
-constexpr uint32_t SS_UT = SS_KB + 32768;   //   U~ and O_loc of one chunk
-constexpr uint32_t SS_OL = SS_UT + 32768;
-constexpr uint32_t SS_BAR = SS_OL + 32768;  // img 0, img 1, u, o, s, ut, ol, kb, uready, oready, sready;
+constexpr uint32_t SS_KB = 2 * SLOT_IMG;    // [-W | Qs] images + e^{G_C} of two chunks, then Kbar
+constexpr uint32_t SS_UT = SS_KB + SLOT_KBP;//   and P, and U~, of one chunk
+constexpr uint32_t SS_BAR = SS_UT + 32768;  // img 0, img 1, u, o, s, ut, kb, uready, sready;
 constexpr uint32_t SS_TOTAL = SS_BAR + 128; //   tmem base; abort flag
 static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
 
@@ -1073,15 +1016,12 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     uint64_t* bar_o = bar_img + 3;
     uint64_t* bar_s = bar_img + 4;
     uint64_t* bar_ut = bar_img + 5;
-    uint64_t* bar_ol = bar_img + 6;
-    uint64_t* bar_kb = bar_img + 7;
-    uint64_t* bar_uready = bar_img + 8;
-    uint64_t* bar_oready = bar_img + 9;
-    uint64_t* bar_sready = bar_img + 10;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 11);
-    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 12);
+    uint64_t* bar_kb = bar_img + 6;
+    uint64_t* bar_uready = bar_img + 7;
+    uint64_t* bar_sready = bar_img + 8;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 9);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 10);
     const float* ut_s = reinterpret_cast<const float*>(smem + SS_UT);   // U~ [64 r][128 v]
-    const float* ol_s = reinterpret_cast<const float*>(smem + SS_OL);   // O_loc [64 r][128 v]
 
     const int H = pl.H;
     const int h = blockIdx.x % H;
@@ -1109,9 +1049,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     if (warp == 0) tc::tmem_alloc(tmem_base_s, TS_COLS);
     if (tid == 0) {
 #pragma unroll
-        for (int b = 0; b < 8; ++b) tc::bar_init(bar_img + b, 1);
+        for (int b = 0; b < 7; ++b) tc::bar_init(bar_img + b, 1);
         tc::bar_init(bar_uready, 16);
-        tc::bar_init(bar_oready, 16);
         tc::bar_init(bar_sready, 16);
         *abort_s = 0;
         tc::bar_init_fence();
@@ -1124,6 +1063,10 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     auto slot_of = [&](int64_t i) { return pl.slots + ((g0 + i) * H + h) * (int64_t)SLOT_BYTES; };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         return tc::bar_wait_or_abort(bar, parity, kWaitIter, abort_s);
+    };
+    auto chunk_rows = [&](int64_t i) {
+        const int64_t c0 = bos + i * C;
+        return (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
     };
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
@@ -1141,51 +1084,71 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             }
             __syncwarp();
         };
-        // Kbar, U~ and O_loc of one chunk (single buffers, refilled once consumed)
-        auto issue_vec = [&](int64_t i, uint64_t* bar, uint32_t sm_off, uint32_t slot_off) {
+        // Kbar + P and U~ of one chunk (single buffers, refilled once consumed)
+        auto issue_vec = [&](int64_t i, uint64_t* bar, uint32_t sm_off, uint32_t slot_off, uint32_t bytes) {
             if (lane == 0) {
-                tc::bar_expect_tx(bar, 32768);
-                tc::bulk_load(smem + sm_off, slot_of(i) + slot_off, 32768, bar);
+                tc::bar_expect_tx(bar, bytes);
+                tc::bulk_load(smem + sm_off, slot_of(i) + slot_off, bytes, bar);
             }
             __syncwarp();
         };
+        // o of a full chunk, staged in its image buffer by the epilogue warps
+        // (a sequence's ragged last chunk is stored by the epilogue warps)
+        auto store_o = [&](int64_t i) {
+            if (chunk_rows(i) == C && lane == 0) {
+                tc::tma_store_3d(&mo, smem + (i & 1) * SLOT_IMG + SLOT_WQH, 0, h, (int)(bos + i * C));
+                tc::bulk_commit();
+            }
+        };
         int64_t issued = 0, done = 0;  // image loads issued / known complete
-        int64_t ut_issued = 0, ol_issued = 0, kb_issued = 0;
+        int64_t ut_issued = 0, kb_issued = 0;
         if (nchunks > 0) {
             issue_img(0);
-            issue_vec(0, bar_kb, SS_KB, SLOT_KH);
-            issue_vec(0, bar_ut, SS_UT, SLOT_UT);
-            issue_vec(0, bar_ol, SS_OL, SLOT_OL);
+            issue_vec(0, bar_kb, SS_KB, SLOT_KH, SLOT_KBP);
+            issue_vec(0, bar_ut, SS_UT, SLOT_UT, 32768);
             issued = 1;
-            ut_issued = ol_issued = kb_issued = 1;
+            ut_issued = kb_issued = 1;
         }
         if (nchunks > 1) { issue_img(1); issued = 2; }
         const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
+        const uint32_t id_n64 = tc::idesc_bf16(128, 64);
+        bool ok = true;
         for (int64_t i = 0; i < nchunks; ++i) {
             const uint32_t par = (uint32_t)(i & 1);
-            if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+            if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) { ok = false; break; }
             done = i + 1;
-            if (!wait(bar_sready, par)) break;
+            // S_i hi/lo are written, and chunk i-1's o is staged
+            if (!wait(bar_sready, par)) { ok = false; break; }
             tc::fence_after();
+            if (i >= 1) store_o(i - 1);
             const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
-            // [U^T | O^T] = S^T [-W | Qh]^T with both operands split hi|lo:
-            //   S_hi [-W hi | Qh hi] + S_lo [-W hi | Qh hi] + S_hi [-W lo | Qh lo]
+            // [U^T | O^T] = S^T [-W | Qs]^T with both operands split hi|lo:
+            //   S_hi [-W hi | Qs hi] + S_lo [-W hi | Qs hi] + S_hi [-W lo | Qs lo]
             const uint64_t bh = tc::sdesc(img + SLOT_WQH, 2 * C * 16, 128);
             const uint64_t bl = tc::sdesc(img + SLOT_WQL, 2 * C * 16, 128);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                const uint32_t o = ks_ * 2 * 2 * C * 16;
-                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bh, o), id_n128_bmn, ks_ > 0);
-                tc::mma_ts_w(tm + TS_AU, tm + TS_SL + ks_ * 8, tc::dadv(bh, o), id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bl, o), id_n128_bmn, 1);
+                const uint32_t off = ks_ * 2 * 2 * C * 16;
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bh, off), id_n128_bmn, ks_ > 0);
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SL + ks_ * 8, tc::dadv(bh, off), id_n128_bmn, 1);
+                tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bl, off), id_n128_bmn, 1);
             }
             tc::commit_w(bar_u);
-            tc::commit_w(bar_o);
-            // S^T += U^T Kbar once U hi/lo are in TMEM (the decay came before them)
-            if (!wait(bar_uready, par) || !wait(bar_kb, par)) break;
+            // chunk i+1's images go where chunk i-1's were, once its o has left
+            if (i >= 1 && i + 1 < nchunks) {
+                tc::bulk_wait_read();
+                __syncwarp();
+                issue_img(i + 1);
+                issued = i + 2;
+            }
+            // once U hi/lo are in TMEM (the decay came before them):
+            // S^T += U^T Kbar, then O^T += U^T (scale P)^T
+            if (!wait(bar_uready, par) || !wait(bar_kb, par)) { ok = false; break; }
             tc::fence_after();
             const uint32_t kb = tc::smem_u32(smem + SS_KB);
             const uint64_t khd = tc::sdesc(kb, D * 16, 128), kld = tc::sdesc(kb + 16384, D * 16, 128);
+            const uint64_t phd = tc::sdesc(kb + (SLOT_P - SLOT_KH), 128, C * 16);
+            const uint64_t pld = tc::sdesc(kb + (SLOT_P - SLOT_KH) + 8192, 128, C * 16);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
                 const uint32_t uh = tm + TS_UH + ks_ * 8, ul = tm + TS_UL + ks_ * 8;
@@ -1195,48 +1158,34 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::mma_ts_w(tm + TS_S, ul, bh2, id_n128_bmn, 1);
             }
             tc::commit_w(bar_s);
+#pragma unroll
+            for (int ks_ = 0; ks_ < C / 16; ++ks_) {
+                const uint32_t uh = tm + TS_UH + ks_ * 8, ul = tm + TS_UL + ks_ * 8;
+                const uint64_t ph = tc::dadv(phd, ks_ * 256), pl_ = tc::dadv(pld, ks_ * 256);
+                tc::mma_ts_w(tm + TS_AO, uh, ph, id_n64, 1);
+                tc::mma_ts_w(tm + TS_AO, uh, pl_, id_n64, 1);
+                tc::mma_ts_w(tm + TS_AO, ul, ph, id_n64, 1);
+            }
+            tc::commit_w(bar_o);
             // U~ of this chunk is consumed (U hi/lo are written): fetch the next one
             if (i + 1 < nchunks) {
-                issue_vec(i + 1, bar_ut, SS_UT, SLOT_UT);
+                issue_vec(i + 1, bar_ut, SS_UT, SLOT_UT, 32768);
                 ut_issued = i + 2;
-            }
-            // the o epilogue is through: write the chunk's o rows (staged in this
-            // image buffer's [-W | Qh] region) and fetch the next O_loc
-            if (!wait(bar_oready, par)) break;
-            {
-                // (a sequence's ragged last chunk is stored by the epilogue warps)
-                const int64_t c0 = bos + i * C;
-                if (eos - c0 >= C && lane == 0) {
-                    tc::tma_store_3d(&mo, smem + (i & 1) * SLOT_IMG + SLOT_WQH, 0, h, (int)c0);
-                    tc::bulk_commit();
-                }
-            }
-            if (i + 1 < nchunks) {
-                issue_vec(i + 1, bar_ol, SS_OL, SLOT_OL);
-                ol_issued = i + 2;
-            }
-            // Kbar's buffer is free once the state-update MMAs have completed, this
-            // image buffer once the o rows have left it as well
-            if (i + 1 < nchunks) {
-                if (!wait(bar_s, par)) break;
-                issue_vec(i + 1, bar_kb, SS_KB, SLOT_KH);
+                // Kbar and P are free once this chunk's last MMAs have completed
+                if (!wait(bar_o, par)) { ok = false; break; }
+                issue_vec(i + 1, bar_kb, SS_KB, SLOT_KH, SLOT_KBP);
                 kb_issued = i + 2;
             }
-            if (i + 2 < nchunks) {
-                tc::bulk_wait_read();
-                __syncwarp();
-                issue_img(i + 2);
-                issued = i + 3;
-            }
         }
-        tc::bulk_wait();
+        // the last chunk's o
+        if (ok && nchunks > 0 && wait(bar_sready, (uint32_t)(nchunks & 1))) store_o(nchunks - 1);
         // drain loads that may still be in flight before the CTA exits
         if (*abort_s && lane == 0) {
             for (int64_t j = done; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
             if (ut_issued > 0) tc::bar_wait(bar_ut, (uint32_t)((ut_issued - 1) & 1), kWaitIter);
             if (kb_issued > 0) tc::bar_wait(bar_kb, (uint32_t)((kb_issued - 1) & 1), kWaitIter);
-            if (ol_issued > 0) tc::bar_wait(bar_ol, (uint32_t)((ol_issued - 1) & 1), kWaitIter);
         }
+        tc::bulk_wait();
     } else {
         // ================= TMEM epilogues =================
         const int x = (warp & 3) * 32 + lane;   // TMEM lane: value column v
@@ -1257,9 +1206,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             for (int half = 0; half < 2; ++half) {
                 uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 8; ++j)
                     tc::split2(__uint_as_float(a[16 * half + 2 * j]), __uint_as_float(a[16 * half + 2 * j + 1]), hi[j], lo[j]);
-                }
                 tc::tmem_st8(tm + lane_base(warp) + TS_SH + cc / 2 + 8 * half, hi);
                 tc::tmem_st8(tm + lane_base(warp) + TS_SL + cc / 2 + 8 * half, lo);
             }
@@ -1280,7 +1228,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
         for (int64_t i = 0; i < nchunks; ++i) {
             const uint32_t par = (uint32_t)(i & 1);
             const int64_t c0 = bos + i * C;
-            const int L = (eos - c0 < (int64_t)C) ? (int)(eos - c0) : C;
+            const int L = chunk_rows(i);
 
             // decay the fp32 state by e^{G_C} (the MMAs under way read S hi/lo)
             if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) break;
@@ -1309,19 +1257,24 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::tmem_ld_wait();
                 uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    tc::split2(ut_s[(rb + 2 * j) * D + x] + __uint_as_float(a[2 * j]), ut_s[(rb + 2 * j + 1) * D + x] + __uint_as_float(a[2 * j + 1]), hi[j], lo[j]);
-                }
+                for (int j = 0; j < 8; ++j)
+                    tc::split2(ut_s[(rb + 2 * j) * D + x] + __uint_as_float(a[2 * j]),
+                               ut_s[(rb + 2 * j + 1) * D + x] + __uint_as_float(a[2 * j + 1]), hi[j], lo[j]);
                 tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
                 tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
                 tc::tmem_st_wait();
             }
             arrive(bar_uready);
 
-            // o = O_loc + S Qh (while the state-update MMAs run); a full chunk is staged
-            // as [64 r][128 v] in the [-W | Qh] image region, which the MMAs of this
-            // chunk are done with, for one tiled store by the issuer
-            if (!wait(bar_ol, par) || !wait(bar_o, par)) break;
+            // S hi/lo for the next chunk
+            if (!wait(bar_s, par)) break;
+            tc::fence_after();
+            s_epilogue();
+
+            // o = O: a full chunk is staged as [64 r][128 v] in the [-W | Qs] image
+            // region, which this chunk's MMAs are done with, for one tiled store by
+            // the issuer
+            if (!wait(bar_o, par)) break;
             tc::fence_after();
             {
                 uint32_t a[16];
@@ -1330,22 +1283,15 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 if (L == C) {
                     TOut* ost = reinterpret_cast<TOut*>(smem + (i & 1) * SLOT_IMG + SLOT_WQH);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        ost[(rb + j) * D + x] = from_f32<TOut>(ol_s[(rb + j) * D + x] + __uint_as_float(a[j]));
+                    for (int j = 0; j < 16; ++j) ost[(rb + j) * D + x] = from_f32<TOut>(__uint_as_float(a[j]));
                 } else {
                     const int64_t ob = ((c0 + rb) * H + h) * (int64_t)D + x;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(ol_s[(rb + j) * D + x] + __uint_as_float(a[j]));
+                        if (rb + j < L) o[ob + (int64_t)j * H * D] = from_f32<TOut>(__uint_as_float(a[j]));
                 }
             }
             tc::fence_async_smem();
-            arrive(bar_oready);
-
-            // S hi/lo for the next chunk
-            if (!wait(bar_s, par)) break;
-            tc::fence_after();
-            s_epilogue();
             arrive(bar_sready);
         }
         // ---- final state ---------------------------------------------------------

@@ -47,7 +47,7 @@ def test_noalloc_matches_chunk_fwd_on_two_calls_in_a_row():
 
 
 def test_noalloc_at_capacity_and_rejects_beyond():
-    # H = 96: 4 chunks per head fit in 64 MiB (4 * 96 * 164352 bytes), 5 do not
+    # H = 96: 4 chunks per head fit in 64 MiB (4 * 96 * 147968 bytes), 5 do not
     d = to_dev(synth.direct_inputs(256, 96, 128, 128, torch.bfloat16, seed=903))
     assert_close(*both(d))
     d = to_dev(synth.direct_inputs(320, 96, 128, 128, torch.bfloat16, seed=904))
