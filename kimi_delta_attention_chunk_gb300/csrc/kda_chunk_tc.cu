@@ -769,36 +769,50 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 __syncthreads();
             }
             {
-                // one thread per (row a, 4 columns) of a 32 x 32 block: 256 items
+                // one thread per (rows a and a + 16, 4 columns) of a 32 x 32 block:
+                // 128 items, each loaded row serving two outputs
                 float* X = Y + 512;
                 const int a = tid >> 3, b4 = tid & 7;
-                if (tid < 256) {
-                    const float* nrow = N + (32 + a) * MAT_LD;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < 128) {
+                    const float* n0 = N + (32 + a) * MAT_LD;
+                    const float* n1 = N + (48 + a) * MAT_LD;
+                    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
                     // T11 is zero above its diagonal blocks: columns >= 16 start at row 16
                     for (int m4 = (b4 >= 4 ? 4 : 0); m4 < 8; ++m4) {
-                        const float4 nv = *reinterpret_cast<const float4*>(nrow + 4 * m4);
-                        const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
+                        const float4 v0 = *reinterpret_cast<const float4*>(n0 + 4 * m4);
+                        const float4 v1 = *reinterpret_cast<const float4*>(n1 + 4 * m4);
+                        const float nn0[4] = {v0.x, v0.y, v0.z, v0.w}, nn1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const float4 t = *reinterpret_cast<const float4*>(T + (4 * m4 + u) * MAT_LD + 4 * b4);
-                            acc.x += nn[u] * t.x; acc.y += nn[u] * t.y; acc.z += nn[u] * t.z; acc.w += nn[u] * t.w;
+                            acc0.x += nn0[u] * t.x; acc0.y += nn0[u] * t.y; acc0.z += nn0[u] * t.z; acc0.w += nn0[u] * t.w;
+                            acc1.x += nn1[u] * t.x; acc1.y += nn1[u] * t.y; acc1.z += nn1[u] * t.z; acc1.w += nn1[u] * t.w;
                         }
                     }
-                    *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc;
+                    *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc0;
+                    *reinterpret_cast<float4*>(X + (a + 16) * 32 + 4 * b4) = acc1;
                 }
                 __syncthreads();
-                if (tid < 256) {
-                    const float* trow = T + (32 + a) * MAT_LD + 32;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int mmax = a < 16 ? 16 : 32;  // T22 is zero above its diagonal blocks
+                if (tid < 128) {
+                    // T22 is zero above its diagonal blocks: row a < 16 stops at column 16
+                    const float* t0 = T + (32 + a) * MAT_LD + 32;
+                    const float* t1 = T + (48 + a) * MAT_LD + 32;
+                    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll 4
-                    for (int m = 0; m < mmax; ++m) {
-                        const float tv = trow[m];
+                    for (int m = 0; m < 16; ++m) {
+                        const float tv0 = t0[m], tv1 = t1[m];
                         const float4 y = *reinterpret_cast<const float4*>(X + m * 32 + 4 * b4);
-                        acc.x += tv * y.x; acc.y += tv * y.y; acc.z += tv * y.z; acc.w += tv * y.w;
+                        acc0.x += tv0 * y.x; acc0.y += tv0 * y.y; acc0.z += tv0 * y.z; acc0.w += tv0 * y.w;
+                        acc1.x += tv1 * y.x; acc1.y += tv1 * y.y; acc1.z += tv1 * y.z; acc1.w += tv1 * y.w;
                     }
-                    *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+#pragma unroll 4
+                    for (int m = 16; m < 32; ++m) {
+                        const float tv1 = t1[m];
+                        const float4 y = *reinterpret_cast<const float4*>(X + m * 32 + 4 * b4);
+                        acc1.x += tv1 * y.x; acc1.y += tv1 * y.y; acc1.z += tv1 * y.z; acc1.w += tv1 * y.w;
+                    }
+                    *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w);
+                    *reinterpret_cast<float4*>(T + (48 + a) * MAT_LD + 4 * b4) = make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w);
                 }
                 __syncthreads();
             }
