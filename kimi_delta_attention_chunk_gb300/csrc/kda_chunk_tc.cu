@@ -279,18 +279,22 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
     const uint32_t id_n64 = tc::idesc_bf16(128, 64);
 
-    // beta of a task, fetched into registers of threads kIssueTid .. + 63 when its
-    // tiles are requested
+    // beta of a task, fetched as raw bf16 bits into registers of threads
+    // kIssueTid .. + 63 when its tiles are requested (a predicated load into the
+    // zeroed register: nothing waits for it until the next task stores it)
     const int bt = tid - kIssueTid;
     auto fetch_beta = [&](const Chunk& ch) {
-        float b = 0.f;
-        if (bt >= 0 && bt < C && ch.c0 + bt < ch.eos) b = __bfloat162float(beta_g[(ch.c0 + bt) * H + ch.h]);
+        unsigned short b = 0;
+        const bool have = bt >= 0 && bt < C && ch.c0 + bt < ch.eos;
+        const __nv_bfloat16* src = beta_g + (have ? (ch.c0 + bt) * H + ch.h : 0);
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p ld.global.nc.u16 %0, [%1];\n\t}"
+                     : "+h"(b) : "l"(src), "r"((uint32_t)have));
         return b;
     };
 
     int64_t task = blockIdx.x;
     Chunk cur = decode_task(pl, task);
-    float beta_r = 0.f;
+    unsigned short beta_r = 0;
     if (cur.valid) {
         if (tid == kIssueTid) issue_tma(cur);
         tma_pending = true;
@@ -305,10 +309,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const int64_t next_task = task + gridDim.x;
         const Chunk nxt = decode_task(pl, next_task);
 
-        // shared memory written by bulk stores of the previous task is reused only
-        // once they have read it: U~ (A/T region) before pass 1, the last group
-        // (O_loc, [-W | Qh], Qh lo in the operand regions) before the A/P operands
-        if (tid == kIssueTid) tc::bulk_wait_read_but1();
+        // (the previous task's bulk stores read only the operand regions, which are
+        // rewritten once they are done: see the wait before the A/P operands)
         wait_one(bar_tma, tma_phase);
         tma_pending = false;
         if (failed) break;
@@ -423,8 +425,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_st8(tm + lane_base(warp) + TL_VTL + jb / 2, vl);
             tc::tmem_st_wait();
         }
-        if (bt >= 0 && bt < C) beta_s[bt] = beta_r;
-        if (tid == kIssueTid) tc::bulk_wait_read();
+        if (bt >= 0 && bt < C) beta_s[bt] = __uint_as_float((uint32_t)beta_r << 16);
+        if (tid == kIssueTid) tc::bulk_wait_read();  // last task's stores left the operand regions
         __syncthreads();
 
         if constexpr (FUSED) {
@@ -856,7 +858,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
         // ---- (8) -W and Qs = scale q e^G, hi|lo, staged as the two merged B images
         //      (hi where L lo was, lo in the dead T Diag(beta) / P region once P has
-        //      left it); U~ fp32 staged in the dead prefix-product region -------------
+        //      left it); U~ fp32 staged over (q e^G) once that is read -------------
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
@@ -882,7 +884,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
                 *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = lo;
             }
-            float* ut = reinterpret_cast<float*>(smem + SM_PRE);
+            __syncthreads();
+            float* ut = reinterpret_cast<float*>(smem + SM_QT);
 #pragma unroll
             for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
         }
@@ -891,7 +894,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         __syncthreads();
         tc::fence_after();
         if (tid == kIssueTid) {
-            tc::bulk_store(slot + SLOT_UT, smem + SM_PRE, 32768);
+            tc::bulk_store(slot + SLOT_UT, smem + SM_QT, 32768);
             tc::bulk_commit();
             tc::bulk_store(slot + SLOT_WQH, smem + SM_KST, 32768);
             tc::bulk_store(slot + SLOT_WQL, smem + SM_OPB, 32768);
