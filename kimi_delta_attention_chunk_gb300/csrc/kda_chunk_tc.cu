@@ -126,10 +126,9 @@ __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
 
 // ---- shared memory map (bytes) ----------------------------------------------
 constexpr uint32_t SM_STG = 0;             // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
-constexpr uint32_t SM_OPA = 65536;         // 64 KB, A/P phase: L hi|lo (A op [128 i][128 c]); then
-                                           //   (q e^G) fp32 [64][128]
-constexpr uint32_t SM_QT = SM_OPA;         //   (float4 columns XOR-swizzled by row) and the staged Kbar
-constexpr uint32_t SM_KST = SM_OPA + 32768;//   images, later the staged [-W | Qh hi] image
+constexpr uint32_t SM_OPA = 65536;         // 64 KB: (q e^G) fp32 [64][128] (float4 columns
+constexpr uint32_t SM_QT = SM_OPA;         //   XOR-swizzled by row), later U~ staged for its store;
+constexpr uint32_t SM_KST = SM_OPA + 32768;//   the staged [-W | Qs hi] image
 constexpr uint32_t SM_OPB = 131072;        // 48 KB, A/P phase: Rt hi|lo (B op [96 j][128 c]); then
 constexpr uint32_t SM_TB = SM_OPB;         //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
 constexpr uint32_t SM_PB = SM_OPB + 16384; //   P hi|lo, B op [64 r][64 j] K-major
@@ -140,14 +139,15 @@ constexpr uint32_t SM_AF = SM_PRE;
 constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
 constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
 // A/P operands of both row blocks R: L rows 64 R + i (i < 32: k rows, else q rows of
-// block R), Rt rows j (block 0, j < 32) and 32 + j (block 1, j < 64)
+// block R) in TMEM, Rt rows j (block 0, j < 32) and 32 + j (block 1, j < 64) in SM_OPB
 constexpr uint32_t RT_LO = 96 * D * 2;
 constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals of e^g
-constexpr uint32_t SM_BETA = SM_SMALL + 2048;    // fp32 [64]
+constexpr uint32_t SM_ITOT = SM_SMALL + 2048;    // fp32 [2][128] inverses of the totals of blocks 0, 2
+constexpr uint32_t SM_BETA = SM_SMALL + 3072;    // fp32 [64]
 constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base
 constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
 // with the input prologue (raw q, k, v and gate input in the staging tiles):
-constexpr uint32_t SM_RED = SM_SMALL + 2432;     // fp32 [2][64][4] partial sums of squares of q, k rows
+constexpr uint32_t SM_RED = SM_SMALL + 3456;     // fp32 [2][64][4] partial sums of squares of q, k rows
 constexpr uint32_t SM_HALO = SM_RED + 2048;      // bf16 [3][2][3][64] the 3 raw rows before the chunk (q, k, v)
 constexpr uint32_t SM_CONV = SM_HALO + 2304;     // fp32 [3][128][4] this head's conv weights (q, k, v)
 constexpr uint32_t SM_DTB = SM_CONV + 6144;      // fp32 [128] this head's dt_bias
@@ -167,6 +167,8 @@ constexpr uint32_t TL_VT = 160;    // v^T (bf16 pairs) [128 v][32]
 constexpr uint32_t TL_AW = 192;    // W^T accumulator fp32 [128 c][64 r]
 constexpr uint32_t TL_AU = 256;    // U~^T accumulator fp32 [128 v][64 r]
 constexpr uint32_t TL_VTL = 320;   // v^T lo (bf16 pairs), with the prologue (v is then not bf16-exact)
+constexpr uint32_t TL_LH = 352;    // A/P A operand [L_0; L_1] hi (bf16 pairs) [128 i][64]
+constexpr uint32_t TL_LL = 416;    // its lo
 constexpr uint32_t TL_COLS = 512;
 // Thread that issues the tile loads and bulk stores: warps 8..15 are idle while
 // warps 0..7 invert the diagonal blocks of T, so the issue costs no barrier time.
@@ -211,6 +213,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float* beta_s = reinterpret_cast<float*>(smem + SM_BETA);   // [64]
     float* tot_s = reinterpret_cast<float*>(smem + SM_TOT);     // [4][128]
+    float* itot_s = reinterpret_cast<float*>(smem + SM_ITOT);   // [2][128]
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
     float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][128], swizzled
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
@@ -399,6 +402,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 pre_s[(16 * J + u) * PRE_LD + c] = run;
             }
             tot_s[J * 128 + c] = run;
+            if ((J & 1) == 0) itot_s[(J >> 1) * 128 + c] = __fdividef(1.f, run);
         }
         if constexpr (FUSED) {
             // v = act(conv4(v_raw)): this thread's value column, 16 tokens, as hi|lo
@@ -498,31 +502,39 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // Both blocks' operands are stacked (L rows 64 R + i, Rt rows of block 1 after
         // those of block 0) and multiplied in one M = 128, N = 96 round; the two
         // off-diagonal products of the stack are not used.
+        {
+            // L (A operand, TMEM lane = stack row 64 R + i): lane quadrant q4 holds the
+            // k rows (even q4) or q rows (odd q4) of block R = q4 / 2, warpgroup wg the
+            // channels [32 wg, 32 wg + 32); e^{G_r - G_mid} = pre_r / tot_{2R} before the
+            // centre, pre_r after it
+            const int q4 = warp & 3, wg = warp >> 2, R = q4 >> 1;
+            const int r = 32 * R + lane;
+            const bool first = (lane & 16) == 0;  // r in the first 16-token block of R
+#pragma unroll
+            for (int h16 = 0; h16 < 2; ++h16) {
+                uint32_t lh[8], ll[8];
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    const int c = 32 * wg + 16 * h16 + 8 * g8;
+                    float x[8], pr[8], it[8];
+                    ld8((q4 & 1) != 0, r, c, x);
+                    ld_pre8(r, c, pr);
+                    const float4 a = *reinterpret_cast<const float4*>(itot_s + R * 128 + c);
+                    const float4 b = *reinterpret_cast<const float4*>(itot_s + R * 128 + c + 4);
+                    it[0] = a.x; it[1] = a.y; it[2] = a.z; it[3] = a.w; it[4] = b.x; it[5] = b.y; it[6] = b.z; it[7] = b.w;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        tc::split2(x[2 * u] * (first ? pr[2 * u] * it[2 * u] : pr[2 * u]),
+                                   x[2 * u + 1] * (first ? pr[2 * u + 1] * it[2 * u + 1] : pr[2 * u + 1]),
+                                   lh[4 * g8 + u], ll[4 * g8 + u]);
+                }
+                tc::tmem_st8(tm + lane_base(warp) + TL_LH + 16 * wg + 8 * h16, lh);
+                tc::tmem_st8(tm + lane_base(warp) + TL_LL + 16 * wg + 8 * h16, ll);
+            }
+        }
 #pragma unroll
         for (int R = 0; R < 2; ++R) {
             const int nrows = 32 * (R + 1);  // columns j of this block's products
-            // L_R (A operand rows 64 R + i): i < 32 k-rows, i >= 32 q-rows of block R;
-            // e^{G_r - G_mid} = pre_r / tot_{2R} before the centre, pre_r after it
-            float itc[8];
-            ld_tot8(2 * R, 8 * cg, itc);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) itc[u] = __fdividef(1.f, itc[u]);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int item = tid + NT * kk;
-                const int i = ((item >> 7) << 3) | (item & 7);
-                const int r = 32 * R + (i & 31);
-                float x[8], pr[8], f[8];
-                ld8(i >= 32, r, 8 * cg, x);
-                ld_pre8(r, 8 * cg, pr);
-                const bool first = (i & 16) == 0;  // r in the first 16-token block of R
-#pragma unroll
-                for (int u = 0; u < 8; ++u) f[u] = x[u] * (first ? pr[u] * itc[u] : pr[u]);
-                uint4 hi, lo;
-                tc::split8(f, hi, lo);
-                *reinterpret_cast<uint4*>(smem + SM_OPA + tc::kmaj(64 * R + i, 8 * cg, D)) = hi;
-                *reinterpret_cast<uint4*>(smem + SM_OPA + 32768 + tc::kmaj(64 * R + i, 8 * cg, D)) = lo;
-            }
             // Rt_R (B operand rows 32 R + j): e^{G_mid - G_j} k_j =
             //   1 / pre_j after the centre, tot_J / pre_j * prod_{J < J2 <= 2R} tot_J2 before it
 #pragma unroll
@@ -559,18 +571,18 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 *reinterpret_cast<uint4*>(smem + SM_OPB + RT_LO + tc::kmaj(32 * R + j, 8 * cg, D)) = lo;
             }
         }
+        tc::tmem_st_wait();
         publish();
         if (warp == 0) {
-            const uint32_t la = tc::smem_u32(smem + SM_OPA), rb = tc::smem_u32(smem + SM_OPB);
-            const uint64_t ah = tc::sdesc(la, 128, D * 16), al = tc::sdesc(la + 32768, 128, D * 16);
+            const uint32_t rb = tc::smem_u32(smem + SM_OPB);
             const uint64_t bh = tc::sdesc(rb, 128, D * 16), bl = tc::sdesc(rb + RT_LO, 128, D * 16);
             const uint32_t id = tc::idesc_bf16(128, 96);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
                 const uint32_t o = ks_ * 256;
-                tc::mma_ss_w(tm + TL_AP, tc::dadv(ah, o), tc::dadv(bh, o), id, ks_ > 0);
-                tc::mma_ss_w(tm + TL_AP, tc::dadv(ah, o), tc::dadv(bl, o), id, 1);
-                tc::mma_ss_w(tm + TL_AP, tc::dadv(al, o), tc::dadv(bh, o), id, 1);
+                tc::mma_ts_w(tm + TL_AP, tm + TL_LH + ks_ * 8, tc::dadv(bh, o), id, ks_ > 0);
+                tc::mma_ts_w(tm + TL_AP, tm + TL_LH + ks_ * 8, tc::dadv(bl, o), id, 1);
+                tc::mma_ts_w(tm + TL_AP, tm + TL_LL + ks_ * 8, tc::dadv(bh, o), id, 1);
             }
             tc::commit_w(bar_mma);
         }
