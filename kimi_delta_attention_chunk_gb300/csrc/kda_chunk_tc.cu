@@ -170,9 +170,10 @@ constexpr uint32_t TL_VTL = 320;   // v^T lo (bf16 pairs), with the prologue (v 
 constexpr uint32_t TL_LH = 352;    // A/P A operand [L_0; L_1] hi (bf16 pairs) [128 i][64]
 constexpr uint32_t TL_LL = 416;    // its lo
 constexpr uint32_t TL_COLS = 512;
-// Thread that issues the tile loads and bulk stores: warps 8..15 are idle while
-// warps 0..7 invert the diagonal blocks of T, so the issue costs no barrier time.
-constexpr int kIssueTid = 256;
+// Thread that issues the bulk stores (and the first task's tile loads).  While warps
+// 0 and 1 (scheduler partitions 0 and 1) invert the diagonal blocks of T, the warps of
+// partitions 2 and 3, this one among them, issue the next task's tile loads.
+constexpr int kIssueTid = 320;
 
 // Input prologue ("kimi-k3-mlx" review: short convolution of kernel size 4 on
 // q, k, v; per-channel forget gate with gate_lower_bound; A_log of K entries
@@ -263,6 +264,31 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::bulk_load(smem + SM_ALOG, pro.A_log, 512, bar_tma);
         }
     };
+    // The same, spread over lane 0 of the warps of scheduler partitions 2 and 3 (one
+    // tile each, the prologue's extra loads round-robin), for a task whose byte count
+    // bar_tma already expects.
+    auto issue_tma_spread = [&](const Chunk& ch) {
+        if ((warp & 2) == 0 || lane != 0) return;
+        const int i = ((warp >> 2) << 1) | (warp & 1);
+        const CUtensorMap* mp = i < 2 ? &mq : (i < 4 ? &mk : (i < 6 ? &mv : &mg));
+        tc::tma_load_3d(smem + SM_STG + (i >> 1) * 16384 + (i & 1) * 8192, mp, (i & 1) * 64, ch.h, (int)ch.c0,
+                        bar_tma);
+        if constexpr (FUSED) {
+            if (i < 6) {
+                const int t = i >> 1, half = i & 1;
+                tc::tma_load_3d(smem + SM_HALO + t * 768 + half * 384, t == 0 ? &hq : (t == 1 ? &hk : &hv),
+                                half * 64, ch.h, (int)ch.c0 - 3, bar_tma);
+            }
+            if (i < 3) {
+                const float* w = i == 0 ? pro.conv_q : (i == 1 ? pro.conv_k : pro.conv_v);
+                tc::bulk_load(smem + SM_CONV + i * 2048, w + (int64_t)ch.h * D * 4, 2048, bar_tma);
+            } else if (i == 3) {
+                tc::bulk_load(smem + SM_DTB, pro.dt_bias + (int64_t)ch.h * D, 512, bar_tma);
+            } else if (i == 4) {
+                tc::bulk_load(smem + SM_ALOG, pro.A_log, 512, bar_tma);
+            }
+        }
+    };
     // One warp polls the barrier; the others park at the CTA barrier.
     auto wait_one = [&](uint64_t* bar, uint32_t& phase) {
         bool ok = true;
@@ -317,6 +343,9 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         wait_one(bar_tma, tma_phase);
         tma_pending = false;
         if (failed) break;
+        // the next task's byte count, posted long before its loads are issued (by
+        // several threads, so none of them may complete the phase early)
+        if (tid == kIssueTid && nxt.valid) tc::bar_expect_tx(bar_tma, 4u * 16384u + (FUSED ? PRO_TX : 0u));
 
         uint8_t* qs = smem + SM_STG;
         uint8_t* ks = smem + SM_STG + 16384;
@@ -725,21 +754,32 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 float x[16], acc[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+                // four columns m of N at a time, each row's four as one float4
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    x[m] = m == col ? 1.f : (m > col ? -acc[m] : 0.f);
+                for (int w4 = 0; w4 < 4; ++w4) {
+                    float4 nv[16];
 #pragma unroll
-                    for (int r = m + 1; r < 16; ++r) acc[r] += nb[r * MAT_LD + m] * x[m];
+                    for (int r = 4 * w4 + 1; r < 16; ++r) nv[r] = *reinterpret_cast<const float4*>(nb + r * MAT_LD + 4 * w4);
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        const int m = 4 * w4 + mm;
+                        x[m] = m == col ? 1.f : (m > col ? -acc[m] : 0.f);
+#pragma unroll
+                        for (int r = m + 1; r < 16; ++r) {
+                            const float nrm = mm == 0 ? nv[r].x : (mm == 1 ? nv[r].y : (mm == 2 ? nv[r].z : nv[r].w));
+                            acc[r] += nrm * x[m];
+                        }
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) T[(16 * blk + r) * MAT_LD + 16 * blk + col] = x[r];
-            } else if (warp >= 8) {
+            } else if ((warp & 2) != 0) {
                 // scale P out; prefetch the next task into the consumed staging
                 if (tid == kIssueTid) {
                     tc::bulk_store(slot + SLOT_P, smem + SM_PB, 16384);
                     tc::bulk_commit();
                 }
-                if (tid == kIssueTid && nxt.valid) issue_tma(nxt);
+                if (nxt.valid) issue_tma_spread(nxt);
                 if (nxt.valid) beta_r = fetch_beta(nxt);
             }
             if (nxt.valid) tma_pending = true;
