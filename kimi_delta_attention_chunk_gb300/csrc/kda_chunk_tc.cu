@@ -539,7 +539,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             const int q4 = warp & 3, wg = warp >> 2, R = q4 >> 1;
             const int r = 32 * R + lane;
             const bool first = (lane & 16) == 0;  // r in the first 16-token block of R
-#pragma unroll
+#pragma unroll 1
             for (int h16 = 0; h16 < 2; ++h16) {
                 uint32_t lh[8], ll[8];
 #pragma unroll
@@ -651,7 +651,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
         // ---- (4) (q e^G) fp32 into shared memory, Kbar = k e^{G_C - G} hi|lo out ----
         {
-#pragma unroll
+#pragma unroll 1
             for (int kk = 0; kk < 2; ++kk) {
                 const int item = tid + NT * kk;
                 const int r = ((item >> 7) << 3) | (item & 7);
