@@ -389,23 +389,20 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
         // raw input of tensor t (0 q, 1 k, 2 v) at chunk row sr >= -3, channel c;
         // zero before the start of the sequence
+        // (branch-free: the address is selected, rows of another sequence read as zero)
+        auto raw_addr = [&](int t, int sr, int c) -> const uint8_t* {
+            const uint8_t* halo = smem + SM_HALO + t * 768 + (c >> 6) * 384 + (sr + 3) * 128 + (c & 63) * 2;
+            const uint8_t* stg = smem + SM_STG + t * 16384 + tc::swz128(sr, c);
+            return sr < 0 ? halo : stg;
+        };
         auto raw1 = [&](int t, int sr, int c) -> float {
-            if (c0 + sr < cur.bos) return 0.f;
-            if (sr < 0)
-                return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                    smem + SM_HALO + t * 768 + (c >> 6) * 384 + (sr + 3) * 128 + (c & 63) * 2));
-            return ld_bf(t == 0 ? qs : (t == 1 ? ks : vs), sr, c);
+            const float x = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(raw_addr(t, sr, c)));
+            return c0 + sr < cur.bos ? 0.f : x;
         };
         auto raw8 = [&](int t, int sr, int c, float* x) {
-            if (c0 + sr < cur.bos) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = 0.f;
-            } else if (sr < 0) {
-                tc::unpack8(*reinterpret_cast<const uint4*>(smem + SM_HALO + t * 768 + (c >> 6) * 384 +
-                                                            (sr + 3) * 128 + (c & 63) * 2), x);
-            } else {
-                tc::unpack8(*reinterpret_cast<const uint4*>((t == 0 ? qs : ks) + tc::swz128(sr, c)), x);
-            }
+            uint4 v = *reinterpret_cast<const uint4*>(raw_addr(t, sr, c));
+            if (c0 + sr < cur.bos) v = make_uint4(0u, 0u, 0u, 0u);
+            tc::unpack8(v, x);
         };
         auto act = [&](float y) { return pro.act == 1 ? __fdividef(y, 1.f + __expf(-y)) : y; };
 
