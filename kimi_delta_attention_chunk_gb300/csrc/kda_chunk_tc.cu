@@ -190,12 +190,19 @@ struct Prologue {
     float l2_eps;
 };
 
-// softplus(z) = log(1 + e^z) on the fast exp / log units.  Only the absolute
-// error of the gate matters (it enters as e^g): for z <= 15 log(1 + e^z) is
-// within ~1e-7 absolute of the exact value; above, z + e^-z (the remainder is
-// below 1e-13).
-__device__ __forceinline__ float softplus_f(float z) {
-    return z > 15.f ? z + __expf(-z) : __logf(1.f + __expf(z));
+// Base-2 exponential and logarithm on the special-function unit (PTX ex2.approx,
+// lg2.approx).  The gate uses them: only its absolute error matters (it enters
+// as e^g), and log2(1 + t), t in (0, 1], is within ~1e-7 absolute.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // FUSED: the staging tiles hold the raw inputs (q_raw, k_raw, v_raw, gate_x);
@@ -409,22 +416,29 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // ---- (1) in-block prefix products of e^g, block totals --------------------
         {
             const int c = tid & 127, J = tid >> 7;  // block J of channel c
-            float gv[16];
+            float eg[16];  // e^g (1 past the sequence end)
             if constexpr (FUSED) {
-                // g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias))
+                // g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias)), in base 2:
+                //   g log2(e) = max(lower_bound log2(e), -exp(A_log) sp2(y)),  y = (gate_x + dt_bias) log2(e),
+                //   sp2(y) = log2(1 + 2^y) = max(y, 0) + log2(1 + 2^-|y|)
+                // (three special-function operations per element, no branch)
                 const float ea = __expf(reinterpret_cast<const float*>(smem + SM_ALOG)[c]);
                 const float db = reinterpret_cast<const float*>(smem + SM_DTB)[c];
+                const float lb2 = pro.lower_bound * kLog2e;
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    gv[u] = 16 * J + u < L ? fmaxf(pro.lower_bound, -ea * softplus_f(ld_bf(gs, 16 * J + u, c) + db)) : 0.f;
+                for (int u = 0; u < 16; ++u) {
+                    const float y = (ld_bf(gs, 16 * J + u, c) + db) * kLog2e;
+                    const float sp2 = fmaxf(y, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(y)));
+                    eg[u] = 16 * J + u < L ? ex2_approx(fmaxf(lb2, -ea * sp2)) : 1.f;
+                }
             } else {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) gv[u] = 16 * J + u < L ? ld_bf(gs, 16 * J + u, c) : 0.f;
+                for (int u = 0; u < 16; ++u) eg[u] = 16 * J + u < L ? __expf(ld_bf(gs, 16 * J + u, c)) : 1.f;
             }
             float run = 1.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                run *= __expf(gv[u]);
+                run *= eg[u];
                 pre_s[(16 * J + u) * PRE_LD + c] = run;
             }
             tot_s[J * 128 + c] = run;
