@@ -185,7 +185,6 @@ struct Prologue {
     const float* conv_v;
     const float* A_log;    // [128]
     const float* dt_bias;  // [H * 128]
-    int act;               // 0: none, 1: SiLU after the convolution
     float lower_bound;
     float l2_eps;
 };
@@ -208,7 +207,9 @@ __device__ __forceinline__ float lg2_approx(float x) {
 // FUSED: the staging tiles hold the raw inputs (q_raw, k_raw, v_raw, gate_x);
 // the prologue runs on them first and leaves q, k as bf16 hi (in the q, k tiles)
 // plus lo (in the v, g tiles), v as hi/lo in TMEM and g folded into pass 1.
-template <bool FUSED>
+// SILU: the convolution is followed by SiLU (a separate instance, so that the
+// other never evaluates it).
+template <bool FUSED, bool SILU = false>
 __global__ void __launch_bounds__(NT, 1)
 chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
@@ -411,7 +412,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (c0 + sr < cur.bos) v = make_uint4(0u, 0u, 0u, 0u);
             tc::unpack8(v, x);
         };
-        auto act = [&](float y) { return pro.act == 1 ? __fdividef(y, 1.f + __expf(-y)) : y; };
+        auto act = [&](float y) {
+            if constexpr (SILU) return __fdividef(y, 1.f + __expf(-y));
+            else return y;
+        };
 
         // ---- (1) in-block prefix products of e^g, block totals --------------------
         {
@@ -1550,8 +1554,9 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
             Prologue pro{};
             pro.conv_q = p.conv_q; pro.conv_k = p.conv_k; pro.conv_v = p.conv_v;
             pro.A_log = p.A_log; pro.dt_bias = p.dt_bias;
-            pro.act = p.conv_act; pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
-            auto kern = fused ? chunk_local_kernel<true> : chunk_local_kernel<false>;
+            pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
+            auto kern = !fused ? chunk_local_kernel<false>
+                               : (p.conv_act == 1 ? chunk_local_kernel<true, true> : chunk_local_kernel<true, false>);
             const int smem_bytes = (int)(fused ? SM_LOCAL_TOTAL_FUSED : SM_LOCAL_TOTAL) + 1024;  // + alignment slack
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
             if (e == cudaSuccess) {
