@@ -247,7 +247,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // the residual is taken against the packed hi (bf16 -> fp32 is a 16-bit shift).
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     hi = pack2(a, b);
-    lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+    // both residuals in one packed fp32x2 subtraction
+    float ra, rb;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(ra), "=f"(rb)
+        : "f"(a), "f"(b), "f"(__uint_as_float(hi << 16)), "f"(__uint_as_float(hi & 0xffff0000u)));
+    lo = pack2(ra, rb);
 }
 __device__ __forceinline__ uint4 pack8(const float* x) {
     return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
