@@ -23,13 +23,19 @@ with gcc into ``oracle/_build/libkda_oracle.so`` on first use.  Functions:
   with ``A_log`` broadcast along the 128-wide channel axis and shared by all
   heads ("kimi-k3-mlx" review, "The A_log shape mismatch ...").
 * :func:`prologue` -- short_conv on q, k, v, then l2norm on q and k, then gate.
+* :func:`output_gate` -- the layer's output gate on o: per (token, head)
+  ``o / sqrt(mean_v o^2 + eps) * w * sigmoid(gate)`` ("kimi-k3-mlx" review,
+  "Attention is 93 layers ...": a full-rank output gate; "NeMo AutoModel
+  draft_kimi_k3": RMS norms with fp32 variance, sigmoid output gates).
 
 Pins (tests/test_oracle_pins.py): the T=1 closed form, the delta-rule
 overwrite invariant, the beta=0 pure-decay invariant, brute-force products of
 ``(I - beta k k^T) Diag(e^g)``, the scalar-decay (gated delta rule) special
 case, linearity in (v, S0), the Householder norm invariant, padding tokens,
 a hand-worked golden fixture, and library routines for the prologue
-(``numpy.convolve``, ``numpy.linalg.norm``, ``numpy.logaddexp``).  No function
+(``numpy.convolve``, ``numpy.linalg.norm``, ``numpy.logaddexp``); for the output
+gate, degree-0 homogeneity in o, the sigmoid reflection, unit RMS of the normed
+rows, per-channel equivariance and the constant-row closed form.  No function
 here is "parity unpinned".
 """
 from __future__ import annotations
@@ -83,6 +89,9 @@ def _load():
             lib.kda_oracle_gate.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_double, _dp]
             lib.kda_oracle_gate.restype = ctypes.c_int
+            lib.kda_oracle_output_gate.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                                   ctypes.c_double, _dp]
+            lib.kda_oracle_output_gate.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -222,3 +231,27 @@ def prologue(q_raw, k_raw, v_raw, gate_x, conv_w, A_log, dt_bias, cu_seqlens=Non
     k = l2norm(k, l2_eps)
     g = gate(gate_x, A_log, dt_bias, lower_bound)
     return q, k, v, g
+
+
+def output_gate(o, gate, weight=None, eps: float = 1e-6):
+    """Output gate of the layer on o: per row of the last axis (length V),
+    ``o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)``.
+
+    o, gate: [..., V]; weight: [V] or None (ones).  Returns float64 in o's shape.
+    """
+    o = _f64(o)
+    g = _f64(gate)
+    if g.shape != o.shape:
+        raise ValueError(f"gate has shape {g.shape}, expected {o.shape}")
+    V = o.shape[-1]
+    w = None
+    if weight is not None:
+        w = _f64(weight)
+        if w.shape != (V,):
+            raise ValueError(f"weight must be [{V}]")
+    out = np.zeros_like(o)
+    rc = _load().kda_oracle_output_gate(_ptr(o), _ptr(g), _ptr(w) if w is not None else None,
+                                        o.size // V, V, float(eps), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_output_gate failed with status {rc}")
+    return out

@@ -243,3 +243,29 @@ int kda_oracle_gate(const double *x, const double *A_log, const double *dt_bias,
             }
     return 0;
 }
+
+/*
+ * Output gate of the KDA layer ("kimi-k3-mlx" review, section "Attention is 93
+ * layers ...": KDA has a full-rank output gate; "NeMo AutoModel draft_kimi_k3",
+ * module description: K3's norms are RMS norms with the variance in fp32 and its
+ * output gates are sigmoid gates).  Per row (token, head) of length V:
+ *
+ *     out[v] = o[v] / sqrt(mean_v(o^2) + eps) * w[v] * sigmoid(gate[v])
+ *
+ * w has V entries shared by all heads (NULL: all ones).  o, gate, out: [rows, V].
+ */
+int kda_oracle_output_gate(const double *o, const double *gate, const double *w, int64_t rows,
+                           int64_t V, double eps, double *out)
+{
+    if (!o || !gate || !out || rows < 0 || V <= 0 || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t c = 0; c < V; ++c) ss += o[r * V + c] * o[r * V + c];
+        const double inv = 1.0 / sqrt(ss / (double)V + eps);
+        for (int64_t c = 0; c < V; ++c) {
+            const double sig = 1.0 / (1.0 + exp(-gate[r * V + c]));
+            out[r * V + c] = o[r * V + c] * inv * (w ? w[c] : 1.0) * sig;
+        }
+    }
+    return 0;
+}

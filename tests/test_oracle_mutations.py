@@ -32,6 +32,10 @@ MUTATIONS = {
     "dt_bias transposed": ("dt_bias[h * K + c]", "dt_bias[c * H + h]"),
     "A_log not exponentiated": ("val = -exp(A_log[c]) * softplus", "val = A_log[c] * softplus"),
     "no lower bound": ("g[i] = val > lower_bound ? val : lower_bound;", "g[i] = val;"),
+    "output norm over the sum, not the mean": ("sqrt(ss / (double)V + eps)", "sqrt(ss + eps)"),
+    "output gate sigmoid sign": ("exp(-gate[r * V + c])", "exp(gate[r * V + c])"),
+    "output weight dropped": ("(w ? w[c] : 1.0)", "1.0"),
+    "output eps outside the root": ("sqrt(ss / (double)V + eps)", "(sqrt(ss / (double)V) + eps)"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and n != "test_thread_count_does_not_change_results"]
@@ -54,7 +58,8 @@ def test_pins_catch_mutation(tmp_path, name, monkeypatch):
     so = _build_mutant(tmp_path, name, old, new)
     real = oracle._load()
     mutant = ctypes.CDLL(so)
-    for fn in ("kda_oracle_forward", "kda_oracle_short_conv", "kda_oracle_l2norm", "kda_oracle_gate"):
+    for fn in ("kda_oracle_forward", "kda_oracle_short_conv", "kda_oracle_l2norm", "kda_oracle_gate",
+               "kda_oracle_output_gate"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)

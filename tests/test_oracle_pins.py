@@ -347,3 +347,58 @@ def test_thread_count_does_not_change_results(nthreads):
     o2, s2 = oracle.kda_forward(q, k, v, g, b, nthreads=nthreads)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(s1, s2)
+
+
+# ---------------------------------------------------------------- output gate
+def _og_inputs(rng, rows=7, V=16):
+    return rng.standard_normal((rows, V)), rng.standard_normal((rows, V)), rng.uniform(0.5, 1.5, V)
+
+
+def test_output_gate_homogeneous_of_degree_zero_in_o():
+    """eps = 0: scaling a row of o by c > 0 leaves the output unchanged; c < 0 flips it."""
+    rng = np.random.default_rng(41)
+    o, g, w = _og_inputs(rng)
+    base = oracle.output_gate(o, g, w, eps=0.0)
+    np.testing.assert_allclose(oracle.output_gate(3.7 * o, g, w, eps=0.0), base, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(oracle.output_gate(-0.2 * o, g, w, eps=0.0), -base, rtol=1e-13, atol=1e-15)
+
+
+def test_output_gate_sigmoid_reflection():
+    """sigmoid(x) + sigmoid(-x) = 1 and sigmoid(x) / sigmoid(-x) = e^x: the outputs for
+    gate and -gate add up to the normed, weighted row and their ratio is e^gate."""
+    rng = np.random.default_rng(42)
+    o, g, w = _og_inputs(rng)
+    a = oracle.output_gate(o, g, w, eps=1e-3)
+    b = oracle.output_gate(o, -g, w, eps=1e-3)
+    full = oracle.output_gate(o, np.full_like(g, 60.0), w, eps=1e-3)  # sigmoid(60) = 1 in fp64
+    np.testing.assert_allclose(a + b, full, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(a / b, np.exp(g), rtol=1e-12)
+
+
+def test_output_gate_rows_have_unit_rms():
+    """eps = 0, weight 1, gate open: every output row has root-mean-square 1 (an RMS
+    norm over the V channels, not over their sum)."""
+    rng = np.random.default_rng(43)
+    for V in (16, 64, 128):
+        o = rng.standard_normal((5, V)) * rng.uniform(0.01, 100.0, (5, 1))
+        out = oracle.output_gate(o, np.full((5, V), 60.0), None, eps=0.0)
+        np.testing.assert_allclose(np.sqrt(np.mean(out * out, axis=-1)), 1.0, rtol=1e-13)
+
+
+def test_output_gate_channel_equivariance_and_weight_linearity():
+    """Permuting the channels of o, gate and weight permutes the output; the output is
+    linear in the weight; rows are independent of one another."""
+    rng = np.random.default_rng(44)
+    o, g, w = _og_inputs(rng)
+    base = oracle.output_gate(o, g, w)
+    perm = rng.permutation(o.shape[1])
+    np.testing.assert_allclose(oracle.output_gate(o[:, perm], g[:, perm], w[perm]), base[:, perm], rtol=1e-13)
+    np.testing.assert_allclose(oracle.output_gate(o, g, 2.5 * w), 2.5 * base, rtol=1e-13)
+    np.testing.assert_allclose(oracle.output_gate(o[::-1], g[::-1], w), base[::-1], rtol=1e-13)
+
+
+def test_output_gate_constant_row_closed_form():
+    """o = c (all V channels), gate 0, weight 1: out = c / sqrt(c^2 + eps) / 2."""
+    for c, eps in ((0.5, 0.25), (-2.0, 1e-6), (1e-3, 1e-6)):
+        out = oracle.output_gate(np.full((1, 8), c), np.zeros((1, 8)), None, eps=eps)
+        np.testing.assert_allclose(out, c / np.sqrt(c * c + eps) / 2.0, rtol=1e-14)
