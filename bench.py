@@ -433,6 +433,29 @@ def run_ours(args, world, rank, local):
                            "peak_kind": peak_kind}}
     del dd, state, qs, ks, vs, gs, bs
 
+    # ---- the layer's output gate on the prefill's o (4096 x 96 rows of 128):
+    # reads o fp32 and the bf16 gate, writes fp32
+    og_in = synth.output_gate_inputs((1, T, H, V), torch.bfloat16, 7 + 1000 * rank)
+    og_o, og_g, og_w = (og_in[k].to(dev) for k in ("o", "gate", "weight"))
+    og_out = torch.empty_like(og_o)
+
+    def ogstep():
+        kda.output_gate(og_o, og_g, og_w, out=og_out)
+
+    for _ in range(max(3, args.warmup)):
+        ogstep()
+    torch.cuda.synchronize()
+    barrier(world)
+    og_ms, ogper = time_launches(ogstep, max(10, args.steps), stream)
+    og_ms = max_over_ranks(og_ms, world) / max(10, args.steps)
+    og_bytes = T * H * V * (4 + 2 + 4) + V * 4
+    og_ach = og_bytes / (sum(ogper) / len(ogper) * 1e-3) / 1e9
+    out_gate = {"value": world * T / (og_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": og_ms,
+                "workload": "output gate on the prefill's o: 4096 x 96 rows of 128, fp32 o, bf16 gate, fp32 out",
+                "roofline": {"bound": "hbm", "achieved": og_ach, "peak": hbm, "unit": "GB/s", "frac": og_ach / hbm,
+                             "traffic": None, "algorithmic_bytes": og_bytes, "peak_kind": peak_kind}}
+    del og_in, og_o, og_g, og_w, og_out
+
     # ---- the other prefill workloads, each with its own roofline
     extra = {}
     for name in (["varlen"] if not args.skip_varlen else []) + (["long"] if not args.skip_long else []):
@@ -494,6 +517,7 @@ def run_ours(args, world, rank, local):
                      "kernel_ms": kernel_ms, "peak_kind": peak_kind, "kernels": kernels},
         "clocks": clk, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "decode": decode,
+        "output_gate": out_gate,
     }
     line.update(extra)
     if not args.no_cpu_baseline:

@@ -217,6 +217,35 @@ KDA_API kda_status kda_recurrent_step(const void *q, const void *k, const void *
                               int N, int H, int K, int V, void *o, kda_dtype o_dtype,
                               void *stream);
 
+/*
+ * kda_output_gate -- the layer's output gate on o ("kimi-k3-mlx" review,
+ * section "Attention is 93 layers ...": KDA carries a full-rank output gate;
+ * "NeMo AutoModel draft_kimi_k3", module description: K3's norms are RMS norms
+ * with the variance in fp32 and its output gates are sigmoid gates).  Per
+ * (token, head) row of V values:
+ *
+ *     out = o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)
+ *
+ *  o       [B, T, H, V] fp32 (the output of kda_chunk_fwd / kda_recurrent_step),
+ *          device, 16-byte aligned.
+ *  gate    [B, T, H, V], element type gate_dtype (the gate projection), device,
+ *          16-byte aligned.
+ *  weight  [V] fp32 shared by all heads, device, 16-byte aligned; NULL means ones.
+ *  eps     >= 0 (finite).
+ *  out     [B, T, H, V], element type out_dtype, device, 16-byte aligned.  It may
+ *          be o itself when out_dtype is KDA_F32 (in place); any other overlap
+ *          with o or gate is invalid.
+ *
+ * Sizes: B, T >= 0, H > 0, V in {64, 128}.  Returns KDA_ERR_INVALID_ARG for
+ * null or misaligned pointers (with B*T > 0), negative sizes, a negative or
+ * non-finite eps, or a bf16 out aliasing o; KDA_ERR_UNSUPPORTED for another V
+ * or dtype.  Nothing is launched when a check fails.  Stream-ordered on
+ * `stream`.
+ */
+KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype gate_dtype,
+                           const float *weight, float eps, int B, int T, int H, int V,
+                           void *out, kda_dtype out_dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

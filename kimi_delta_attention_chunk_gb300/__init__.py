@@ -14,6 +14,7 @@ from .kda import (  # noqa: F401
     chunk_fwd_noalloc,
     library_path,
     load_library,
+    output_gate,
     recurrent_step,
     trace_events,
 )

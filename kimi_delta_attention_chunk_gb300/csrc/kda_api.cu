@@ -177,4 +177,32 @@ kda_status kda_recurrent_step(const void* q, const void* k, const void* v, const
                                       resolve_scale(scale, K), state, N, H, o, st));
 }
 
+kda_status kda_output_gate(const float* o, const void* gate, kda_dtype gate_dtype, const float* weight,
+                           float eps, int B, int T, int H, int V, void* out, kda_dtype out_dtype,
+                           void* stream) {
+    if (B < 0 || T < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || isinf(eps)) return KDA_ERR_INVALID_ARG;
+    if (!head_size_ok(V)) return KDA_ERR_UNSUPPORTED;
+    if (!dtype_ok(gate_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * T * H;
+    if ((double)rows * V > 9.0e18) return KDA_ERR_INVALID_ARG;
+    if (rows == 0) return KDA_OK;
+    if (!o || !gate || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {o, gate, weight, out};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    // in place only for an fp32 out; no other overlap with the inputs
+    const char* ob = reinterpret_cast<const char*>(o);
+    const char* gb = reinterpret_cast<const char*>(gate);
+    const char* xb = reinterpret_cast<const char*>(out);
+    const size_t o_bytes = (size_t)rows * V * 4;
+    const size_t g_bytes = (size_t)rows * V * (gate_dtype == KDA_BF16 ? 2 : 4);
+    const size_t x_bytes = (size_t)rows * V * (out_dtype == KDA_BF16 ? 2 : 4);
+    const bool same = xb == ob && out_dtype == KDA_F32;
+    if (!same && xb < ob + o_bytes && ob < xb + x_bytes) return KDA_ERR_INVALID_ARG;
+    if (xb < gb + g_bytes && gb < xb + x_bytes) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::output_gate(gate_dtype, out_dtype, V, o, gate, weight, eps, rows, out,
+                                      (cudaStream_t)stream));
+}
+
 }  // extern "C"

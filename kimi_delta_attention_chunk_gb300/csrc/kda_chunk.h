@@ -60,4 +60,8 @@ cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const v
                         const void* k, const void* v, const void* g, const void* beta,
                         float scale, float* state, int N, int H, void* o, cudaStream_t st);
 
+// Output gate: out = o / sqrt(mean_V(o^2) + eps) * w * sigmoid(gate), rows of V.
+cudaError_t output_gate(kda_dtype gate_dt, kda_dtype out_dt, int V, const float* o, const void* gate,
+                        const float* w, float eps, int64_t rows, void* out, cudaStream_t st);
+
 }  // namespace kda

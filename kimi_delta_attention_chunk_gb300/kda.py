@@ -37,6 +37,7 @@ SIGNATURES = {
     "kda_trace_events": (None, [_vp, _vp, _vp]),
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
+    "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
 }
 
 
@@ -206,3 +207,25 @@ def recurrent_step(q, k, v, g, beta, state, scale: float | None = None, o_dtype=
                                 _stream(q.device))
     _check("kda_recurrent_step", st)
     return o
+
+
+def output_gate(o, gate, weight=None, eps: float = 1e-6, out_dtype=torch.float32, out=None):
+    """The layer's output gate, ``o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)``
+    per (token, head) row of V values.
+
+    o: [B,T,H,V] or [N,H,V] fp32; gate: same shape (bf16 or fp32); weight: [V] fp32
+    or None.  ``out`` may be ``o`` itself for an fp32 result.  Returns out.
+    """
+    lib = load_library()
+    if o.dim() == 3:
+        (B, T), (H, V) = (1, o.shape[0]), o.shape[1:]
+    else:
+        B, T, H, V = o.shape
+    if tuple(gate.shape) != tuple(o.shape):
+        raise ValueError(f"gate has shape {tuple(gate.shape)}, expected {tuple(o.shape)}")
+    if out is None:
+        out = torch.empty(o.shape, dtype=out_dtype, device=o.device)
+    st = lib.kda_output_gate(_ptr(o), _ptr(gate), _dt(gate), _ptr(weight), float(eps), B, T, H, V,
+                             _ptr(out), _dt(out), _stream(o.device))
+    _check("kda_output_gate", st)
+    return out

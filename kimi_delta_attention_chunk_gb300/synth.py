@@ -230,3 +230,16 @@ def workload_inputs(name: str) -> dict:
     lengths = varlen_lengths(w.seed, w.n_seqs) if w.n_seqs else None
     return direct_inputs(w.T, w.H, w.K, w.V, w.dtype, w.seed, B=w.B, lengths=lengths,
                          init_state=w.init_state)
+
+
+def output_gate_inputs(shape, gate_dtype: torch.dtype, seed: int) -> dict:
+    """Inputs of the layer's output gate: o fp32 ~ N(0,1) times a per-row scale
+    10^U(-2, 1) (rows of very different magnitude, as attention outputs have),
+    gate pre-activation ~ N(0,1) in ``gate_dtype``, weight [V] ~ U(0.5, 1.5) fp32."""
+    rng = _rng(seed)
+    V = shape[-1]
+    o = rng.standard_normal(shape, dtype=np.float32)
+    o *= (10.0 ** rng.uniform(-2.0, 1.0, tuple(shape[:-1]) + (1,))).astype(np.float32)
+    gate = rng.standard_normal(shape, dtype=np.float32)
+    w = rng.uniform(0.5, 1.5, V).astype(np.float32)
+    return {"o": _to(o, torch.float32), "gate": _to(gate, gate_dtype), "weight": _to(w, torch.float32)}

@@ -103,6 +103,29 @@ def test_decode_rejects_bad_arguments(lib):
     assert step(N=0, q=None) == 0   # nothing to do
 
 
+def test_output_gate_rejects_bad_arguments(lib):
+    big = ctypes.c_void_p(0x1000000)
+
+    def og(**kw):
+        a = dict(o=P, g=big, gdt=1, w=None, eps=1e-6, B=1, T=64, H=2, V=128, out=ctypes.c_void_p(0x2000000),
+                 odt=0)
+        a.update(kw)
+        return lib.kda_output_gate(a["o"], a["g"], a["gdt"], a["w"], a["eps"], a["B"], a["T"], a["H"],
+                                   a["V"], a["out"], a["odt"], None)
+    assert og(V=96) == UNSUPPORTED
+    assert og(gdt=4) == UNSUPPORTED
+    assert og(odt=9) == UNSUPPORTED
+    assert og(o=None) == INVALID_ARG
+    assert og(w=Pm) == INVALID_ARG
+    assert og(eps=-1.0) == INVALID_ARG
+    assert og(eps=float("inf")) == INVALID_ARG
+    assert og(H=0) == INVALID_ARG
+    assert og(out=P, odt=1) == INVALID_ARG                        # bf16 out over the fp32 o
+    assert og(out=ctypes.c_void_p(0x10000 + 1024)) == INVALID_ARG   # partial overlap with o
+    assert og(out=big) == INVALID_ARG                               # out over the gate
+    assert og(T=0, o=None, g=None, out=None) == 0                   # nothing to do
+
+
 def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
     b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
