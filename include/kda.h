@@ -246,6 +246,29 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
                            const float *weight, float eps, int B, int T, int H, int V,
                            void *out, kda_dtype out_dtype, void *stream);
 
+/*
+ * kda_state_compose -- one step of the prefix over segment transitions, for
+ * context-parallel prefill (the sequence split into consecutive segments, one
+ * per rank).  The recurrence is affine in the state: over a segment,
+ * S_end = M S_start + S_zero, with M = prod_t (I - beta_t k_t k_t^T) Diag(e^{g_t})
+ * (later tokens on the left; kda_chunk_fwd with v = 0 and initial state I gives
+ * M as its final state) and S_zero the segment's final state from a zero start.
+ * This call evaluates, for every head h,
+ *
+ *     out[h] = M[h] S[h] + A[h]        (K x K times K x V, fp32)
+ *
+ *  M    [H, K, K] fp32, device;  S, A, out  [H, K, V] fp32, device; all 16-byte
+ *       aligned.  A may be NULL (zero) or equal to out (accumulate in place);
+ *       out must not overlap M or S.
+ *  K, V in {64, 128}, H >= 0.
+ *
+ * Returns KDA_ERR_INVALID_ARG for null or misaligned pointers or a forbidden
+ * overlap, KDA_ERR_UNSUPPORTED for another K or V; nothing is launched then.
+ * Stream-ordered on `stream`.
+ */
+KDA_API kda_status kda_state_compose(const float *M, const float *S, const float *A, float *out,
+                             int H, int K, int V, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,5 +16,6 @@ from .kda import (  # noqa: F401
     load_library,
     output_gate,
     recurrent_step,
+    state_compose,
     trace_events,
 )

@@ -205,4 +205,27 @@ kda_status kda_output_gate(const float* o, const void* gate, kda_dtype gate_dtyp
                                       (cudaStream_t)stream));
 }
 
+kda_status kda_state_compose(const float* M, const float* S, const float* A, float* out, int H, int K, int V,
+                             void* stream) {
+    if (H < 0) return KDA_ERR_INVALID_ARG;
+    if (!head_size_ok(K) || !head_size_ok(V)) return KDA_ERR_UNSUPPORTED;
+    if (H == 0) return KDA_OK;
+    if (!M || !S || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {M, S, A, out};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const char* xb = reinterpret_cast<const char*>(out);
+    const size_t x_bytes = (size_t)H * K * V * 4;
+    const struct { const void* p; size_t n; } ins[] = {{M, (size_t)H * K * K * 4}, {S, x_bytes}};
+    for (const auto& in : ins) {
+        const char* b = reinterpret_cast<const char*>(in.p);
+        if (xb < b + in.n && b < xb + x_bytes) return KDA_ERR_INVALID_ARG;
+    }
+    if (A && A != out) {
+        const char* ab = reinterpret_cast<const char*>(A);
+        if (xb < ab + x_bytes && ab < xb + x_bytes) return KDA_ERR_INVALID_ARG;
+    }
+    return from_cuda(kda::state_compose(M, S, A, out, H, K, V, (cudaStream_t)stream));
+}
+
 }  // extern "C"

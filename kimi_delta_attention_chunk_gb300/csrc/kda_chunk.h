@@ -64,4 +64,8 @@ cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const v
 cudaError_t output_gate(kda_dtype gate_dt, kda_dtype out_dt, int V, const float* o, const void* gate,
                         const float* w, float eps, int64_t rows, void* out, cudaStream_t st);
 
+// out[h] = M[h] S[h] + A[h] (A may be null or out), K x K times K x V, fp32.
+cudaError_t state_compose(const float* M, const float* S, const float* A, float* out, int H, int K, int V,
+                          cudaStream_t st);
+
 }  // namespace kda

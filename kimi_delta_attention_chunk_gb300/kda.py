@@ -38,6 +38,7 @@ SIGNATURES = {
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
+    "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
 }
 
 
@@ -228,4 +229,19 @@ def output_gate(o, gate, weight=None, eps: float = 1e-6, out_dtype=torch.float32
     st = lib.kda_output_gate(_ptr(o), _ptr(gate), _dt(gate), _ptr(weight), float(eps), B, T, H, V,
                              _ptr(out), _dt(out), _stream(o.device))
     _check("kda_output_gate", st)
+    return out
+
+
+def state_compose(M, S, A=None, out=None):
+    """out[h] = M[h] @ S[h] + A[h] for every head: M [..., H, K, K], S and A
+    [..., H, K, V] fp32 (leading dims flattened into heads).  ``out`` may be A."""
+    lib = load_library()
+    K, V = S.shape[-2:]
+    H = S.numel() // (K * V)
+    if M.shape[-2:] != (K, K) or M.numel() != H * K * K:
+        raise ValueError(f"M has shape {tuple(M.shape)}")
+    if out is None:
+        out = torch.empty_like(S)
+    st = lib.kda_state_compose(_ptr(M), _ptr(S), _ptr(A), _ptr(out), H, K, V, _stream(S.device))
+    _check("kda_state_compose", st)
     return out

@@ -23,6 +23,13 @@ with gcc into ``oracle/_build/libkda_oracle.so`` on first use.  Functions:
   with ``A_log`` broadcast along the 128-wide channel axis and shared by all
   heads ("kimi-k3-mlx" review, "The A_log shape mismatch ...").
 * :func:`prologue` -- short_conv on q, k, v, then l2norm on q and k, then gate.
+* :func:`segment_transition`, :func:`state_compose` -- context parallelism
+  over consecutive segments of a sequence: the recurrence is affine in the
+  state, S_end = M S_start + S_zero with M the product of the per-token
+  factors ``(I - beta k k^T) Diag(e^g)`` (later tokens on the left), and the
+  prefix ``S_in(r+1) = M_r S_in(r) + S_zero_r`` ("ISEEKYAN/k3" README, on the
+  initial path without context parallelism; the affine form follows from the
+  recurrence above).
 * :func:`output_gate` -- the layer's output gate on o: per (token, head)
   ``o / sqrt(mean_v o^2 + eps) * w * sigmoid(gate)`` ("kimi-k3-mlx" review,
   "Attention is 93 layers ...": a full-rank output gate; "NeMo AutoModel
@@ -254,4 +261,30 @@ def output_gate(o, gate, weight=None, eps: float = 1e-6):
                                         o.size // V, V, float(eps), _ptr(out))
     if rc != 0:
         raise RuntimeError(f"kda_oracle_output_gate failed with status {rc}")
+    return out
+
+
+def segment_transition(k, g, beta):
+    """M = prod_t (I - beta_t k_t k_t^T) Diag(exp(g_t)) over a segment, later tokens
+    on the left, per head: k, g [T, H, K] (or [1, T, H, K]), beta [T, H] -> M [H, K, K]
+    float64 (explicit K x K products, numpy matmul)."""
+    k, g, beta = (_f64(a) for a in (k, g, beta))
+    if k.ndim == 4:
+        k, g, beta = k[0], g[0], beta[0]
+    T, H, K = k.shape
+    M = np.broadcast_to(np.eye(K), (H, K, K)).copy()
+    for t in range(T):
+        for h in range(H):
+            kt = k[t, h]
+            step = (np.eye(K) - beta[t, h] * np.outer(kt, kt)) * np.exp(g[t, h])[None, :]
+            M[h] = step @ M[h]
+    return M
+
+
+def state_compose(M, S, A=None):
+    """M @ S + A per head (numpy matmul in float64): M [..., K, K], S and A [..., K, V]."""
+    M, S = _f64(M), _f64(S)
+    out = np.matmul(M, S)
+    if A is not None:
+        out = out + _f64(A)
     return out

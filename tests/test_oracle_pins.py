@@ -402,3 +402,44 @@ def test_output_gate_constant_row_closed_form():
     for c, eps in ((0.5, 0.25), (-2.0, 1e-6), (1e-3, 1e-6)):
         out = oracle.output_gate(np.full((1, 8), c), np.zeros((1, 8)), None, eps=eps)
         np.testing.assert_allclose(out, c / np.sqrt(c * c + eps) / 2.0, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- segments (context parallelism)
+def test_segment_composition_equals_the_whole_sequence():
+    """Split a sequence into segments: the final state of the whole is reached by
+    S_in(r+1) = M_r S_in(r) + S_zero_r, with M_r the product of the per-token
+    factors and S_zero_r the segment's final state from a zero start; and the
+    segment's final state from S_in is exactly M_r S_in + S_zero_r."""
+    rng = np.random.default_rng(51)
+    T, H, K, V = 23, 2, 6, 4
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    _, s_all = oracle.kda_forward(q, k, v, g, b, initial_state=s0)
+    s_in = s0[0]
+    for a, e in ((0, 7), (7, 8), (8, 23)):
+        sl = slice(a, e)
+        _, s_zero = oracle.kda_forward(q[sl], k[sl], v[sl], g[sl], b[sl])
+        M = oracle.segment_transition(k[sl], g[sl], b[sl])
+        _, s_from = oracle.kda_forward(q[sl], k[sl], v[sl], g[sl], b[sl], initial_state=s_in[None])
+        s_next = oracle.state_compose(M, s_in, s_zero[0])
+        np.testing.assert_allclose(s_next, s_from[0], rtol=1e-12, atol=1e-12)
+        s_in = s_next
+    np.testing.assert_allclose(s_in, s_all[0], rtol=1e-12, atol=1e-12)
+
+
+def test_segment_transition_special_cases():
+    """beta = 0: M = Diag(exp(sum of g)); g = 0, beta = 1, one unit k: M = I - k k^T
+    (a projector: M M = M); an empty segment: M = I."""
+    rng = np.random.default_rng(52)
+    T, H, K = 5, 2, 4
+    _, k, _, g, _ = _rand(rng, T, H, K, 1)
+    M = oracle.segment_transition(k, g, np.zeros((T, H)))
+    for h in range(H):
+        np.testing.assert_allclose(M[h], np.diag(np.exp(g[:, h].sum(axis=0))), rtol=1e-13, atol=1e-15)
+    ku = k[:1] / np.linalg.norm(k[:1], axis=-1, keepdims=True)
+    P = oracle.segment_transition(ku, np.zeros_like(ku), np.ones((1, H)))
+    for h in range(H):
+        np.testing.assert_allclose(P[h], np.eye(K) - np.outer(ku[0, h], ku[0, h]), atol=1e-15)
+        np.testing.assert_allclose(P[h] @ P[h], P[h], atol=1e-14)
+    np.testing.assert_allclose(oracle.segment_transition(k[:0], g[:0], np.zeros((0, H))),
+                               np.broadcast_to(np.eye(K), (H, K, K)), atol=0)
