@@ -63,7 +63,7 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2, /* head size or dtype outside the supported set */
     KDA_ERR_WORKSPACE = 3,   /* device workspace unavailable (see kda_chunk_fwd, kda_chunk_fwd_noalloc) */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-    KDA_ERR_RANGE = 5,       /* reserved for input-range checks */
+    KDA_ERR_RANGE = 5,       /* an input lies outside its documented range (kda_check_range) */
     KDA_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
 } kda_status;
 
@@ -268,6 +268,24 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
  */
 KDA_API kda_status kda_state_compose(const float *M, const float *S, const float *A, float *out,
                              int H, int K, int V, void *stream);
+
+/*
+ * kda_check_range -- debug check of an input's documented range, e.g. the
+ * prefill's precondition that every log decay g lies in [-5, 0] (the K3
+ * gate_lower_bound, "kimi-k3-mlx" review, "Attention is 93 layers ...").
+ *
+ *  x       count elements of dtype, device.
+ *  status  caller-owned device int32: set to KDA_OK on the stream, then to
+ *          KDA_ERR_RANGE by the check if any element lies outside [lo, hi] or is
+ *          NaN.  The caller reads it after the stream work completes.
+ *
+ * Returns KDA_ERR_INVALID_ARG for a null x (count > 0), a null or misaligned
+ * (4-byte) status, a negative count or lo > hi; KDA_ERR_UNSUPPORTED for another
+ * dtype.  Stream-ordered and asynchronous: the call's own return value says
+ * nothing about the data.
+ */
+KDA_API kda_status kda_check_range(const void *x, kda_dtype dtype, int64_t count, float lo, float hi,
+                           int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -9,6 +9,7 @@ library is missing.
 from .kda import (  # noqa: F401
     KDAError,
     SIGNATURES,
+    check_range,
     chunk_fwd,
     chunk_fwd_fused,
     chunk_fwd_noalloc,

@@ -228,4 +228,14 @@ kda_status kda_state_compose(const float* M, const float* S, const float* A, flo
     return from_cuda(kda::state_compose(M, S, A, out, H, K, V, (cudaStream_t)stream));
 }
 
+kda_status kda_check_range(const void* x, kda_dtype dtype, int64_t count, float lo, float hi, int32_t* status,
+                           void* stream) {
+    if (!dtype_ok(dtype)) return KDA_ERR_UNSUPPORTED;
+    if (count < 0 || !(lo <= hi)) return KDA_ERR_INVALID_ARG;
+    if (!status || ((uintptr_t)status % 4)) return KDA_ERR_INVALID_ARG;
+    if (count > 0 && !x) return KDA_ERR_INVALID_ARG;
+    if (x && ((uintptr_t)x % (dtype == KDA_BF16 ? 2 : 4))) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::check_range(dtype, x, count, lo, hi, status, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -68,4 +68,8 @@ cudaError_t output_gate(kda_dtype gate_dt, kda_dtype out_dt, int V, const float*
 cudaError_t state_compose(const float* M, const float* S, const float* A, float* out, int H, int K, int V,
                           cudaStream_t st);
 
+// Sets *status (device) to KDA_OK, then to KDA_ERR_RANGE if any x is outside [lo, hi] or NaN.
+cudaError_t check_range(kda_dtype dt, const void* x, int64_t n, float lo, float hi, int32_t* status,
+                        cudaStream_t st);
+
 }  // namespace kda

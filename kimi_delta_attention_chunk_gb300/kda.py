@@ -39,6 +39,7 @@ SIGNATURES = {
                                 _vp]),
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
+    "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
 }
 
 
@@ -245,3 +246,21 @@ def state_compose(M, S, A=None, out=None):
     st = lib.kda_state_compose(_ptr(M), _ptr(S), _ptr(A), _ptr(out), H, K, V, _stream(S.device))
     _check("kda_state_compose", st)
     return out
+
+
+def check_range(x, lo: float = -5.0, hi: float = 0.0, status=None, sync: bool = True):
+    """Debug range check on the device (default: the log-decay precondition
+    g in [-5, 0]).  With ``sync`` the stream is synchronised and KDAError
+    (KDA_ERR_RANGE) is raised for an element outside [lo, hi] or NaN; without it
+    the device status word (int32 tensor, 0 or 5) is returned for the caller to
+    read later."""
+    lib = load_library()
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=x.device)
+    st = lib.kda_check_range(_ptr(x), _dt(x), x.numel(), float(lo), float(hi), _ptr(status),
+                             _stream(x.device))
+    _check("kda_check_range", st)
+    if sync:
+        code = int(status.item())
+        _check("kda_check_range", code)
+    return status

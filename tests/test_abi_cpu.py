@@ -126,6 +126,21 @@ def test_output_gate_rejects_bad_arguments(lib):
     assert og(T=0, o=None, g=None, out=None) == 0                   # nothing to do
 
 
+def test_check_range_rejects_bad_arguments(lib):
+    def chk(**kw):
+        a = dict(x=P, dt=1, n=100, lo=-5.0, hi=0.0, st=P)
+        a.update(kw)
+        return lib.kda_check_range(a["x"], a["dt"], a["n"], a["lo"], a["hi"], a["st"], None)
+    assert chk(dt=3) == UNSUPPORTED
+    assert chk(n=-1) == INVALID_ARG
+    assert chk(lo=1.0, hi=0.0) == INVALID_ARG
+    assert chk(lo=float("nan")) == INVALID_ARG
+    assert chk(st=None) == INVALID_ARG
+    assert chk(st=ctypes.c_void_p(0x10002)) == INVALID_ARG   # status word not 4-byte aligned
+    assert chk(x=None) == INVALID_ARG
+    assert chk(x=ctypes.c_void_p(0x10001)) == INVALID_ARG    # bf16 elements need 2-byte alignment
+
+
 def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
     b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
