@@ -2,9 +2,10 @@
 
 The compute lives in ``libkda.so`` (CUDA for sm_103a behind the C ABI declared
 in ``include/kda.h``); :mod:`.kda` is a thin ctypes binding that marshals
-torch tensors and the current stream into those calls.  Importing the package
-does not load the library; the first call does, and fails loudly if the
-library is missing.
+torch tensors and the current stream into those calls; :mod:`.cp` builds
+context-parallel prefill (a sequence split into segments, across ranks or on
+one device) from those calls.  Importing the package does not load the
+library; the first call does, and fails loudly if the library is missing.
 """
 from .kda import (  # noqa: F401
     KDAError,

@@ -146,3 +146,12 @@ def test_binding_refuses_cpu_tensors(lib):
     b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         kda.chunk_fwd(x, x, x, x, b)
+
+
+def test_segmented_driver_checks_its_cuts_on_the_host():
+    from kimi_delta_attention_chunk_gb300 import cp
+    x = torch.zeros(1, 100, 2, 128, dtype=torch.bfloat16)
+    b = torch.zeros(1, 100, 2, dtype=torch.bfloat16)
+    for bounds in ([0], [100], [50, 50], [60, 40]):
+        with pytest.raises(ValueError):
+            cp.chunk_fwd_segmented(x, x, x, x, b, bounds)
