@@ -28,8 +28,9 @@
 //
 // Operand precision: every operand that feeds o or the state directly is
 // split x = hi + lo into two bf16 values and multiplied as hi*hi + hi*lo +
-// lo*hi (about 16 significant bits); W and the correction W S use one bf16
-// term; v is exact in bf16.  Decay factors are running
+// lo*hi (about 16 significant bits); that includes W and S in the correction
+// W S (long, weakly gated sequences need both split); v is exact in bf16 for
+// direct inputs and split after the fused prologue.  Decay factors are running
 // products of e^{g} over exactly the tokens they span, built from
 // per-16-token-block prefix products (each >= e^-80 since g >= -5, so ratios
 // inside a block are safe) and block totals; nothing overflows and nothing
