@@ -925,8 +925,9 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (failed) break;
 
         // ---- (8) -W and Qs = scale q e^G, hi|lo, staged as the two merged B images
-        //      (hi where L lo was, lo in the dead T Diag(beta) / P region once P has
-        //      left it); U~ fp32 staged over (q e^G) once that is read -------------
+        //      (hi in the second half of the (q e^G) region, lo in the dead
+        //      T Diag(beta) / P region once P has left it); U~ fp32 staged over
+        //      (q e^G) once that is read --------------------------------------------
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
