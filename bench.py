@@ -453,7 +453,7 @@ def run_ours(args, world, rank, local):
     out_gate = {"value": world * T / (og_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": og_ms,
                 "workload": "output gate on the prefill's o: 4096 x 96 rows of 128, fp32 o, bf16 gate, fp32 out",
                 "roofline": {"bound": "hbm", "achieved": og_ach, "peak": hbm, "unit": "GB/s", "frac": og_ach / hbm,
-                             "traffic": None, "algorithmic_bytes": og_bytes, "peak_kind": peak_kind}}
+                             "traffic": recorded_traffic("output_gate_kernel/prefill"), "algorithmic_bytes": og_bytes, "peak_kind": peak_kind}}
     del og_in, og_o, og_g, og_w, og_out
 
     # ---- the other prefill workloads, each with its own roofline
@@ -541,6 +541,12 @@ def profile_case(args):
         for _ in range(args.profile_reps):
             kda.chunk_fwd_fused(d["q_raw"], d["k_raw"], d["v_raw"], d["gate_x"], d["beta"], d["conv_w"],
                                 d["A_log"], d["dt_bias"], scale=d["scale"], initial_state=d["initial_state"])
+    elif args.profile_case == "output_gate":
+        og = synth.output_gate_inputs((1, args.profile_T, args.profile_H, 128), torch.bfloat16, 7)
+        o, g, wt = (og[k].to(dev) for k in ("o", "gate", "weight"))
+        out = torch.empty_like(o)
+        for _ in range(args.profile_reps):
+            kda.output_gate(o, g, wt, out=out)
     else:
         w = synth.WORKLOADS["decode"]
         dec = synth.decode_inputs(w.B, w.H, w.K, w.V, args.profile_reps, w.dtype, w.seed)
@@ -554,7 +560,7 @@ def profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode", "output_gate"], default=None,
                     help="run a few launches of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-T", type=int, default=2048)
     ap.add_argument("--profile-H", type=int, default=16)
