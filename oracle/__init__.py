@@ -30,6 +30,10 @@ with gcc into ``oracle/_build/libkda_oracle.so`` on first use.  Functions:
   prefix ``S_in(r+1) = M_r S_in(r) + S_zero_r`` ("ISEEKYAN/k3" README, on the
   initial path without context parallelism; the affine form follows from the
   recurrence above).
+* :func:`kda_backward` -- gradients of <dO, o> + <dS_T, S_T> with respect to
+  q, k, v, g, beta and the initial state, by reverse mode through the same
+  recurrence, token by token (pinned by central finite differences, the T=1
+  closed forms and the adjoint identity of the map (v, S0) -> (o, S_T)).
 * :func:`output_gate` -- the layer's output gate on o: per (token, head)
   ``o / sqrt(mean_v o^2 + eps) * w * sigmoid(gate)`` ("kimi-k3-mlx" review,
   "Attention is 93 layers ...": a full-rank output gate; "NeMo AutoModel
@@ -99,6 +103,11 @@ def _load():
             lib.kda_oracle_output_gate.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                                    ctypes.c_double, _dp]
             lib.kda_oracle_output_gate.restype = ctypes.c_int
+            lib.kda_oracle_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64p, ctypes.c_int64,
+                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_double, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                                ctypes.c_int]
+            lib.kda_oracle_backward.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -287,4 +296,39 @@ def state_compose(M, S, A=None):
     out = np.matmul(M, S)
     if A is not None:
         out = out + _f64(A)
+    return out
+
+
+def kda_backward(q, k, v, g, beta, dO, dS_T=None, scale=None, initial_state=None, cu_seqlens=None,
+                 nthreads: int | None = None):
+    """Gradients of ``<dO, o> + <dS_T, S_T>`` through :func:`kda_forward` (same
+    shapes and conventions; dS_T [N, H, K, V] or None).  Returns a dict with dq,
+    dk, dv, dg, dbeta (input shapes) and dS0 ([N, H, K, V]), all float64."""
+    q, k, v, g, beta, dO = (_f64(a) for a in (q, k, v, g, beta, dO))
+    lead = q.shape[:-2]
+    H, K = q.shape[-2:]
+    V = v.shape[-1]
+    B, T = (lead if len(lead) == 2 else (1, lead[0]))
+    if cu_seqlens is not None and B != 1:
+        raise ValueError("cu_seqlens requires B == 1")
+    cu = _seqlens(cu_seqlens, B * T, B, T)
+    N = cu.shape[0] - 1
+    if dO.shape != lead + (H, V):
+        raise ValueError(f"dO has shape {dO.shape}")
+    s0 = None if initial_state is None else _f64(initial_state)
+    dst = None if dS_T is None else _f64(dS_T)
+    for name, a in (("initial_state", s0), ("dS_T", dst)):
+        if a is not None and a.shape != (N, H, K, V):
+            raise ValueError(f"{name} has shape {a.shape}, expected {(N, H, K, V)}")
+    if scale is None:
+        scale = float(K) ** -0.5
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v), "dg": np.zeros_like(g),
+           "dbeta": np.zeros_like(beta), "dS0": np.zeros((N, H, K, V))}
+    rc = _load().kda_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(s0) if s0 is not None else None, cu.ctypes.data_as(_i64p),
+                                     N, H, K, V, float(scale), _ptr(dO), _ptr(dst) if dst is not None else None,
+                                     _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                                     _ptr(out["dbeta"]), _ptr(out["dS0"]), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_backward failed with status {rc}")
     return out

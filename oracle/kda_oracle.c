@@ -269,3 +269,200 @@ int kda_oracle_output_gate(const double *o, const double *gate, const double *w,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Backward of the recurrence (reverse mode, token by token)                  */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Gradients of  L = <dO, o> + <dS_T, S_T>  with respect to q, k, v, g, beta and
+ * the initial state, through the recurrence above (same layouts; dO [Ttot, H,
+ * V], dS_T and dS_0 [N, H, K, V]).  Per token, with S' = Diag(e^{g_t}) S_{t-1},
+ * a = S'^T k_t, delta = beta_t (v_t - a) and S_t = S' + k_t delta^T, the
+ * reverse step from the state gradient dS (of S_t) is
+ *
+ *     dq_t   = scale S_t dO_t              dS    += scale q_t dO_t^T
+ *     ddelta = dS^T k_t                    dk_t   = dS delta
+ *     dbeta_t = ddelta . (v_t - a)         dv_t   = beta_t ddelta
+ *     da     = -beta_t ddelta              dS'    = dS + k_t da^T
+ *     dk_t  += S' da                       dg_t[c] = sum_x dS'[c, x] S'[c, x]
+ *     dS_{t-1} = Diag(e^{g_t}) dS'
+ *
+ * States are recomputed forward from checkpoints every 64 tokens.
+ */
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *s0, *dO, *dST;
+    const int64_t *cu;
+    int64_t N, H, K, V;
+    double scale;
+    double *dq, *dk, *dv, *dg, *dbeta, *ds0;
+    int tid, nthreads;
+    int status;
+} bwd_job;
+
+enum { BWD_BLOCK = 64 };
+
+/* One forward token: S <- Diag(e^g) S, then the delta update (kS scratch [V]). */
+static void fwd_token(const double *kt, const double *gt, const double *vt, double bt, int64_t K, int64_t V,
+                      double *S, double *kS)
+{
+    for (int64_t c = 0; c < K; ++c) {
+        const double ea = exp(gt[c]);
+        for (int64_t x = 0; x < V; ++x) S[c * V + x] *= ea;
+    }
+    for (int64_t x = 0; x < V; ++x) kS[x] = 0.0;
+    for (int64_t c = 0; c < K; ++c)
+        for (int64_t x = 0; x < V; ++x) kS[x] += S[c * V + x] * kt[c];
+    for (int64_t c = 0; c < K; ++c)
+        for (int64_t x = 0; x < V; ++x) S[c * V + x] += bt * kt[c] * (vt[x] - kS[x]);
+}
+
+static int bwd_chain(const bwd_job *j, int64_t n, int64_t h)
+{
+    const int64_t H = j->H, K = j->K, V = j->V, KV = K * V;
+    const int64_t t0 = j->cu[n], t1 = j->cu[n + 1], T = t1 - t0;
+    const int64_t nblk = (T + BWD_BLOCK - 1) / BWD_BLOCK;
+    double *ckpt = (double *)malloc(sizeof(double) * KV * (size_t)(nblk > 0 ? nblk : 1));
+    double *prev = (double *)malloc(sizeof(double) * KV * BWD_BLOCK);  /* S_{t-1} inside a block */
+    double *S = (double *)malloc(sizeof(double) * KV);
+    double *Sp = (double *)malloc(sizeof(double) * KV);
+    double *dS = (double *)malloc(sizeof(double) * KV);
+    double *vec = (double *)malloc(sizeof(double) * (size_t)(4 * V + K));
+    if (!ckpt || !prev || !S || !Sp || !dS || !vec) {
+        free(ckpt); free(prev); free(S); free(Sp); free(dS); free(vec);
+        return -2;
+    }
+    double *kS = vec, *delta = vec + V, *ddelta = vec + 2 * V, *da = vec + 3 * V;
+    (void)da;
+
+    /* forward: the state before each block */
+    if (j->s0) memcpy(S, j->s0 + (n * H + h) * KV, sizeof(double) * KV);
+    else memset(S, 0, sizeof(double) * KV);
+    for (int64_t b = 0; b < nblk; ++b) {
+        memcpy(ckpt + b * KV, S, sizeof(double) * KV);
+        const int64_t e = (b + 1) * BWD_BLOCK < T ? (b + 1) * BWD_BLOCK : T;
+        for (int64_t t = t0 + b * BWD_BLOCK; t < t0 + e; ++t)
+            fwd_token(j->k + (t * H + h) * K, j->g + (t * H + h) * K, j->v + (t * H + h) * V,
+                      j->beta[t * H + h], K, V, S, kS);
+    }
+
+    /* backward */
+    if (j->dST) memcpy(dS, j->dST + (n * H + h) * KV, sizeof(double) * KV);
+    else memset(dS, 0, sizeof(double) * KV);
+    for (int64_t b = nblk - 1; b >= 0; --b) {
+        const int64_t s = t0 + b * BWD_BLOCK;
+        const int64_t e = t0 + ((b + 1) * BWD_BLOCK < T ? (b + 1) * BWD_BLOCK : T);
+        memcpy(S, ckpt + b * KV, sizeof(double) * KV);
+        for (int64_t t = s; t < e; ++t) {
+            memcpy(prev + (t - s) * KV, S, sizeof(double) * KV);
+            fwd_token(j->k + (t * H + h) * K, j->g + (t * H + h) * K, j->v + (t * H + h) * V,
+                      j->beta[t * H + h], K, V, S, kS);
+        }
+        for (int64_t t = e - 1; t >= s; --t) {
+            const double *qt = j->q + (t * H + h) * K, *kt = j->k + (t * H + h) * K;
+            const double *gt = j->g + (t * H + h) * K, *vt = j->v + (t * H + h) * V;
+            const double *dot = j->dO + (t * H + h) * V;
+            const double bt = j->beta[t * H + h];
+            double *dqt = j->dq + (t * H + h) * K, *dkt = j->dk + (t * H + h) * K;
+            double *dvt = j->dv + (t * H + h) * V, *dgt = j->dg + (t * H + h) * K;
+            /* S' = Diag(e^g) S_{t-1}; a = S'^T k; delta = beta (v - a); S_t = S' + k delta^T */
+            const double *Sprev = prev + (t - s) * KV;
+            for (int64_t c = 0; c < K; ++c) {
+                const double ea = exp(gt[c]);
+                for (int64_t x = 0; x < V; ++x) Sp[c * V + x] = ea * Sprev[c * V + x];
+            }
+            for (int64_t x = 0; x < V; ++x) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < K; ++c) acc += kt[c] * Sp[c * V + x];
+                kS[x] = acc;
+                delta[x] = bt * (vt[x] - acc);
+            }
+            /* dq = scale S_t dO  (S_t = S' + k delta^T) */
+            for (int64_t c = 0; c < K; ++c) {
+                double acc = 0.0;
+                for (int64_t x = 0; x < V; ++x) acc += (Sp[c * V + x] + kt[c] * delta[x]) * dot[x];
+                dqt[c] = j->scale * acc;
+            }
+            /* dS += scale q dO^T */
+            for (int64_t c = 0; c < K; ++c)
+                for (int64_t x = 0; x < V; ++x) dS[c * V + x] += j->scale * qt[c] * dot[x];
+            /* ddelta = dS^T k;  dk = dS delta */
+            for (int64_t x = 0; x < V; ++x) {
+                double acc = 0.0;
+                for (int64_t c = 0; c < K; ++c) acc += dS[c * V + x] * kt[c];
+                ddelta[x] = acc;
+            }
+            for (int64_t c = 0; c < K; ++c) {
+                double acc = 0.0;
+                for (int64_t x = 0; x < V; ++x) acc += dS[c * V + x] * delta[x];
+                dkt[c] = acc;
+            }
+            /* dbeta = ddelta . (v - a); dv = beta ddelta; da = -beta ddelta */
+            double db = 0.0;
+            for (int64_t x = 0; x < V; ++x) {
+                db += ddelta[x] * (vt[x] - kS[x]);
+                dvt[x] = bt * ddelta[x];
+            }
+            j->dbeta[t * H + h] = db;
+            /* dS' = dS + k da^T (in place); dk += S' da; dg = rowsum(dS' * S') */
+            for (int64_t c = 0; c < K; ++c) {
+                double acc = 0.0;
+                for (int64_t x = 0; x < V; ++x) acc += Sp[c * V + x] * (-bt * ddelta[x]);
+                dkt[c] += acc;
+            }
+            for (int64_t c = 0; c < K; ++c) {
+                double acc = 0.0;
+                const double ea = exp(gt[c]);
+                for (int64_t x = 0; x < V; ++x) {
+                    const double d = dS[c * V + x] + kt[c] * (-bt * ddelta[x]);
+                    acc += d * Sp[c * V + x];
+                    dS[c * V + x] = ea * d; /* dS_{t-1} = Diag(e^g) dS' */
+                }
+                dgt[c] = acc;
+            }
+        }
+    }
+    if (j->ds0) memcpy(j->ds0 + (n * H + h) * KV, dS, sizeof(double) * KV);
+    free(ckpt); free(prev); free(S); free(Sp); free(dS); free(vec);
+    return 0;
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *j = (bwd_job *)arg;
+    const int64_t items = j->N * j->H;
+    for (int64_t it = j->tid; it < items; it += j->nthreads) {
+        const int rc = bwd_chain(j, it / j->H, it % j->H);
+        if (rc) { j->status = rc; break; }
+    }
+    return NULL;
+}
+
+/* Returns 0, -1 (invalid arguments), -2 (allocation) or -3 (threads). */
+int kda_oracle_backward(const double *q, const double *k, const double *v, const double *g,
+                        const double *beta, const double *initial_state, const int64_t *cu_seqlens,
+                        int64_t N, int64_t H, int64_t K, int64_t V, double scale, const double *dO,
+                        const double *dST, double *dq, double *dk, double *dv, double *dg, double *dbeta,
+                        double *ds0, int nthreads)
+{
+    if (!q || !k || !v || !g || !beta || !cu_seqlens || !dO || !dq || !dk || !dv || !dg || !dbeta ||
+        N < 0 || H <= 0 || K <= 0 || V <= 0)
+        return -1;
+    if (cu_seqlens[0] != 0) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > N * H && N * H > 0) nthreads = (int)(N * H);
+    bwd_job *jobs = (bwd_job *)calloc((size_t)nthreads, sizeof(bwd_job));
+    if (!jobs) return -2;
+    for (int i = 0; i < nthreads; ++i) {
+        bwd_job jb = {q, k, v, g, beta, initial_state, dO, dST, cu_seqlens, N, H, K, V, scale,
+                      dq, dk, dv, dg, dbeta, ds0, i, nthreads, 0};
+        jobs[i] = jb;
+    }
+    int rc = spawn(bwd_worker, jobs, sizeof(bwd_job), nthreads);
+    for (int i = 0; i < nthreads && rc == 0; ++i)
+        if (jobs[i].status) rc = jobs[i].status;
+    free(jobs);
+    return rc;
+}

@@ -36,6 +36,12 @@ MUTATIONS = {
     "output gate sigmoid sign": ("exp(-gate[r * V + c])", "exp(gate[r * V + c])"),
     "output weight dropped": ("(w ? w[c] : 1.0)", "1.0"),
     "output eps outside the root": ("sqrt(ss / (double)V + eps)", "(sqrt(ss / (double)V) + eps)"),
+    "backward: state gradient not decayed": ("dS[c * V + x] = ea * d;", "dS[c * V + x] = d;"),
+    "backward: erase term sign": ("const double d = dS[c * V + x] + kt[c] * (-bt * ddelta[x]);",
+                                  "const double d = dS[c * V + x] + kt[c] * (bt * ddelta[x]);"),
+    "backward: dq from the pre-update state": ("(Sp[c * V + x] + kt[c] * delta[x]) * dot[x]",
+                                               "Sp[c * V + x] * dot[x]"),
+    "backward: dbeta without the erase": ("db += ddelta[x] * (vt[x] - kS[x]);", "db += ddelta[x] * vt[x];"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and n != "test_thread_count_does_not_change_results"]
@@ -59,7 +65,7 @@ def test_pins_catch_mutation(tmp_path, name, monkeypatch):
     real = oracle._load()
     mutant = ctypes.CDLL(so)
     for fn in ("kda_oracle_forward", "kda_oracle_short_conv", "kda_oracle_l2norm", "kda_oracle_gate",
-               "kda_oracle_output_gate"):
+               "kda_oracle_output_gate", "kda_oracle_backward"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -443,3 +443,89 @@ def test_segment_transition_special_cases():
         np.testing.assert_allclose(P[h] @ P[h], P[h], atol=1e-14)
     np.testing.assert_allclose(oracle.segment_transition(k[:0], g[:0], np.zeros((0, H))),
                                np.broadcast_to(np.eye(K), (H, K, K)), atol=0)
+
+
+# ---------------------------------------------------------------- backward
+def _loss(q, k, v, g, b, s0, dO, dST, scale):
+    o, sT = oracle.kda_forward(q, k, v, g, b, scale=scale, initial_state=s0)
+    return float(np.sum(dO * o) + np.sum(dST * sT))
+
+
+def test_backward_matches_central_differences():
+    """Every gradient entry against a central difference of <dO, o> + <dS_T, S_T>
+    (step 1e-6 in fp64), on a tiny chain crossing a 64-token checkpoint block."""
+    rng = np.random.default_rng(91)
+    for T, K, V in ((5, 3, 2), (70, 2, 2)):
+        H = 1
+        q, k, v, g, b = _rand(rng, T, H, K, V)
+        s0 = rng.standard_normal((1, H, K, V))
+        dO = rng.standard_normal((T, H, V))
+        dST = rng.standard_normal((1, H, K, V))
+        scale = 0.7
+        gr = oracle.kda_backward(q, k, v, g, b, dO, dS_T=dST, scale=scale, initial_state=s0)
+        args = {"q": q, "k": k, "v": v, "g": g, "beta": b, "s0": s0}
+        names = {"q": "dq", "k": "dk", "v": "dv", "g": "dg", "beta": "dbeta", "s0": "dS0"}
+        step = 1e-6
+        for name, arr in args.items():
+            flat = arr.reshape(-1)
+            idx = range(flat.size) if flat.size <= 12 else rng.choice(flat.size, 12, replace=False)
+            for i in idx:
+                old = flat[i]
+                flat[i] = old + step
+                lp = _loss(q, k, v, g, b, s0, dO, dST, scale)
+                flat[i] = old - step
+                lm = _loss(q, k, v, g, b, s0, dO, dST, scale)
+                flat[i] = old
+                fd = (lp - lm) / (2 * step)
+                an = gr[names[name]].reshape(-1)[i]
+                assert abs(fd - an) <= 1e-6 * (1.0 + abs(fd)), (name, i, fd, an)
+
+
+def test_backward_single_token_closed_forms():
+    """T=1, S0=0, dS_T=0: o = scale beta (q.k) v, so dq = scale beta (v.dO) k,
+    dk = scale beta (v.dO) q, dv = scale beta (q.k) dO, dbeta = scale (q.k)(v.dO),
+    and dg = 0 (the decay acts on the zero state)."""
+    rng = np.random.default_rng(92)
+    K, V, scale = 4, 3, 0.5
+    q, k, v, g, b = _rand(rng, 1, 1, K, V)
+    dO = rng.standard_normal((1, 1, V))
+    gr = oracle.kda_backward(q, k, v, g, b, dO, scale=scale)
+    qk, vd, bt = float(q[0, 0] @ k[0, 0]), float(v[0, 0] @ dO[0, 0]), float(b[0, 0])
+    np.testing.assert_allclose(gr["dq"][0, 0], scale * bt * vd * k[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(gr["dk"][0, 0], scale * bt * vd * q[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(gr["dv"][0, 0], scale * bt * qk * dO[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(gr["dbeta"][0, 0], scale * qk * vd, rtol=1e-13)
+    np.testing.assert_allclose(gr["dg"][0, 0], 0.0, atol=1e-15)
+
+
+def test_backward_adjoint_identity():
+    """(o, S_T) is linear in (v, S0) for fixed q, k, g, beta, so for any (dO, dS_T)
+    <dO, o> + <dS_T, S_T> = <dv, v> + <dS0, S0>."""
+    rng = np.random.default_rng(93)
+    T, H, K, V = 40, 2, 5, 4
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    s0 = rng.standard_normal((1, H, K, V))
+    dO = rng.standard_normal((T, H, V))
+    dST = rng.standard_normal((1, H, K, V))
+    lhs = _loss(q, k, v, g, b, s0, dO, dST, K ** -0.5)
+    gr = oracle.kda_backward(q, k, v, g, b, dO, dS_T=dST, initial_state=s0)
+    rhs = float(np.sum(gr["dv"] * v) + np.sum(gr["dS0"] * s0))
+    assert abs(lhs - rhs) <= 1e-10 * (1.0 + abs(lhs))
+
+
+def test_backward_packed_equals_separate():
+    """Packed sequences: each sequence's gradients are those of its own chain."""
+    rng = np.random.default_rng(94)
+    lens = [3, 0, 9, 5]
+    T, H, K, V = sum(lens), 2, 3, 2
+    q, k, v, g, b = _rand(rng, T, H, K, V)
+    dO = rng.standard_normal((T, H, V))
+    s0 = rng.standard_normal((len(lens), H, K, V))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    gr = oracle.kda_backward(q, k, v, g, b, dO, initial_state=s0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        one = oracle.kda_backward(q[sl], k[sl], v[sl], g[sl], b[sl], dO[sl], initial_state=s0[n:n + 1])
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            np.testing.assert_allclose(gr[key][sl], one[key], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(gr["dS0"][n], one["dS0"][0], rtol=1e-13, atol=1e-15)
