@@ -287,6 +287,37 @@ KDA_API kda_status kda_state_compose(const float *M, const float *S, const float
 KDA_API kda_status kda_check_range(const void *x, kda_dtype dtype, int64_t count, float lo, float hi,
                            int32_t *status, void *stream);
 
+/*
+ * kda_recurrent_bwd -- gradients of  L = <dO, o> + <dS_T, S_T>  through the
+ * recurrence above (the backward of kda_chunk_fwd), for training.  Per token,
+ * with S' = Diag(e^{g_t}) S_{t-1}, a = S'^T k_t, delta = beta_t (v_t - a):
+ *
+ *     dq_t = scale S_t dO_t,  ddelta = dS^T k_t,  dv_t = beta_t ddelta,
+ *     dbeta_t = ddelta . (v_t - a),  dk_t = dS delta + S' da  (da = -beta_t ddelta),
+ *     dg_t[c] = sum_x (dS + k_t da^T)[c, x] S'[c, x],
+ *     dS_{t-1} = Diag(e^{g_t}) (dS + k_t da^T),  after dS += scale q_t dO_t^T,
+ *
+ * run token by token on the CUDA cores in fp32, one CTA per (sequence, head),
+ * with the state recomputed from checkpoints every 64 tokens.
+ *
+ *  q, k, v, g, beta, in_dtype, scale, initial_state, cu_seqlens, B, T, H, K, V, N:
+ *          as kda_chunk_fwd.
+ *  dO      [B, T, H, V] fp32, device.  dS_T [N, H, K, V] fp32 or NULL (zero).
+ *  dq, dk, dg [B, T, H, K], dv [B, T, H, V], dbeta [B, T, H]: fp32 outputs, device.
+ *  dS0     [N, H, K, V] fp32 or NULL (not written).
+ *
+ * The call takes a device workspace of 4*K*V*(ceil(len/64) + 64) bytes per
+ * (sequence, head) from the device's default stream-ordered memory pool for the
+ * duration of the call (KDA_ERR_WORKSPACE if it cannot be had).  Alignment and
+ * error rules as kda_chunk_fwd; dbeta needs 4-byte alignment.
+ */
+KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const void *g,
+                             const void *beta, kda_dtype in_dtype, float scale,
+                             const float *initial_state, const int32_t *cu_seqlens, int B, int T,
+                             int H, int K, int V, int N, const float *dO, const float *dS_T,
+                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,6 +11,7 @@ from .kda import (  # noqa: F401
     KDAError,
     SIGNATURES,
     check_range,
+    chunk_bwd,
     chunk_fwd,
     chunk_fwd_fused,
     chunk_fwd_noalloc,

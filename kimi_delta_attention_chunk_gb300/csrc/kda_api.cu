@@ -238,4 +238,30 @@ kda_status kda_check_range(const void* x, kda_dtype dtype, int64_t count, float 
     return from_cuda(kda::check_range(dtype, x, count, lo, hi, status, (cudaStream_t)stream));
 }
 
+kda_status kda_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                             kda_dtype in_dtype, float scale, const float* initial_state,
+                             const int32_t* cu_seqlens, int B, int T, int H, int K, int V, int N,
+                             const float* dO, const float* dS_T, float* dq, float* dk, float* dv, float* dg,
+                             float* dbeta, float* dS0, void* stream) {
+    kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H, K, V, N,
+                                dO, KDA_F32, nullptr);
+    if (s != KDA_OK) return s;
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens && (!dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {dS_T, dq, dk, dv, dg, dS0};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (dbeta && ((uintptr_t)dbeta % 4)) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H == 0) return KDA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t bytes = kda::recurrent_bwd_workspace(B, T, H, K, V, N, cu_seqlens != nullptr);
+    void* ws = nullptr;
+    if (bytes > 0 && cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return KDA_ERR_WORKSPACE;
+    const cudaError_t e = kda::recurrent_bwd(in_dtype, q, k, v, g, beta, resolve_scale(scale, K), initial_state,
+                                             cu_seqlens, B, T, H, K, V, N, dO, dS_T, dq, dk, dv, dg, dbeta, dS0,
+                                             ws, st);
+    const cudaError_t ef = ws ? cudaFreeAsync(ws, st) : cudaSuccess;
+    return from_cuda(e != cudaSuccess ? e : ef);
+}
+
 }  // extern "C"

@@ -72,4 +72,11 @@ cudaError_t state_compose(const float* M, const float* S, const float* A, float*
 cudaError_t check_range(kda_dtype dt, const void* x, int64_t n, float lo, float hi, int32_t* status,
                         cudaStream_t st);
 
+// Backward of the recurrence (CUDA cores, fp32): workspace bytes, and the launch.
+size_t recurrent_bwd_workspace(int B, int T, int H, int K, int V, int N, bool packed);
+cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, float scale, const float* s0, const int32_t* cu, int B, int T, int H,
+                          int K, int V, int N, const float* dO, const float* dST, float* dq, float* dk, float* dv,
+                          float* dg, float* dbeta, float* dS0, void* ws, cudaStream_t st);
+
 }  // namespace kda

@@ -40,6 +40,8 @@ SIGNATURES = {
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
     "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
+    "kda_recurrent_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
+                               _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp]),
 }
 
 
@@ -264,3 +266,28 @@ def check_range(x, lo: float = -5.0, hi: float = 0.0, status=None, sync: bool = 
         code = int(status.item())
         _check("kda_check_range", code)
     return status
+
+
+def chunk_bwd(q, k, v, g, beta, dO, dS_T=None, scale: float | None = None, initial_state=None,
+              cu_seqlens=None):
+    """Gradients of <dO, o> + <dS_T, S_T> through :func:`chunk_fwd` (same shapes;
+    dO fp32 [B,T,H,V], dS_T fp32 [N,H,K,V] or None).  Returns a dict of fp32
+    tensors dq, dk, dv, dg, dbeta and dS0 ([N,H,K,V])."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.device
+    f32 = torch.float32
+    out = {"dq": torch.empty((B, T, H, K), dtype=f32, device=dev),
+           "dk": torch.empty((B, T, H, K), dtype=f32, device=dev),
+           "dv": torch.empty((B, T, H, V), dtype=f32, device=dev),
+           "dg": torch.empty((B, T, H, K), dtype=f32, device=dev),
+           "dbeta": torch.empty((B, T, H), dtype=f32, device=dev),
+           "dS0": torch.empty((N, H, K, V), dtype=f32, device=dev)}
+    st = lib.kda_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q), float(scale or 0.0),
+                               _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(dO), _ptr(dS_T),
+                               _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                               _ptr(out["dbeta"]), _ptr(out["dS0"]), _stream(dev))
+    _check("kda_recurrent_bwd", st)
+    return out

@@ -141,6 +141,20 @@ def test_check_range_rejects_bad_arguments(lib):
     assert chk(x=ctypes.c_void_p(0x10001)) == INVALID_ARG    # bf16 elements need 2-byte alignment
 
 
+def test_backward_rejects_bad_arguments(lib):
+    def bwd(**kw):
+        a = dict(dq=P, dO=P, K=128, dt=1, dbeta=P)
+        a.update(kw)
+        return lib.kda_recurrent_bwd(P, P, P, P, P, a["dt"], 0.0, None, None, 1, 64, 2, a["K"], 128, 1, a["dO"],
+                                     None, a["dq"], P, P, P, a["dbeta"], None, None)
+    assert bwd(K=96) == UNSUPPORTED
+    assert bwd(dt=4) == UNSUPPORTED
+    assert bwd(dO=None) == INVALID_ARG
+    assert bwd(dq=None) == INVALID_ARG
+    assert bwd(dq=Pm) == INVALID_ARG
+    assert bwd(dbeta=ctypes.c_void_p(0x10002)) == INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
     b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
