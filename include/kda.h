@@ -21,8 +21,9 @@
  *    takes a device workspace for the duration of the call from a
  *    stream-ordered memory pool that the library owns (one per device, kept
  *    across calls for reuse); kda_chunk_fwd_noalloc uses a fixed array
- *    instead; nothing else allocates.  Calls from different host threads are
- *    safe.
+ *    instead; kda_recurrent_bwd takes its workspace from the device's default
+ *    stream-ordered pool; nothing else allocates.  Calls from different host
+ *    threads are safe.
  *  - Layouts are row-major and token-major, as the K3 gate tensor (B, T, 96, 128):
  *        q, k, g [B, T, H, K]    v [B, T, H, V]    beta [B, T, H]
  *        o [B, T, H, V]          states [N, H, K, V] (V contiguous, fp32)
