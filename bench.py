@@ -456,6 +456,36 @@ def run_ours(args, world, rank, local):
                              "traffic": recorded_traffic("output_gate_kernel/prefill"), "algorithmic_bytes": og_bytes, "peak_kind": peak_kind}}
     del og_in, og_o, og_g, og_w, og_out
 
+    # ---- the backward of the 4096-token prefill (token by token, fp32); a
+    # failure here is reported in its own line and does not stop the others
+    dO = torch.randn((1, T, H, V), generator=torch.Generator(device=dev).manual_seed(11 + rank), device=dev)
+
+    def bwstep():
+        kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO, scale=d["scale"])
+
+    bw_err = None
+    try:
+        bwstep()
+        torch.cuda.synchronize()
+    except Exception as exc:  # noqa: BLE001
+        bw_err = str(exc)[:200]
+    barrier(world)
+    if bw_err is None:
+        nb = 3
+        bw_ms, bwper = time_launches(bwstep, nb, stream)
+        bw_ms = max_over_ranks(bw_ms, world) / nb
+        bw_bytes = T * H * ((3 * K + V) * 2 + 2 + 4 * V + (3 * K + V) * 4 + 4)
+        bw_ach = bw_bytes / (sum(bwper) / len(bwper) * 1e-3) / 1e9
+        backward = {"value": world * T / (bw_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": bw_ms,
+                    "workload": "backward of the 4096-token prefill (dq, dk, dv, dg, dbeta, dS0), "
+                                "token by token in fp32",
+                    "roofline": {"bound": "hbm", "achieved": bw_ach, "peak": hbm, "unit": "GB/s",
+                                 "frac": bw_ach / hbm, "traffic": None, "algorithmic_bytes": bw_bytes,
+                                 "peak_kind": peak_kind}}
+    else:
+        backward = {"error": bw_err}
+    del dO
+
     # ---- the other prefill workloads, each with its own roofline
     extra = {}
     for name in (["varlen"] if not args.skip_varlen else []) + (["long"] if not args.skip_long else []):
@@ -518,6 +548,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "decode": decode,
         "output_gate": out_gate,
+        "backward": backward,
     }
     line.update(extra)
     if not args.no_cpu_baseline:
