@@ -34,7 +34,7 @@ recurrent_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
                      int V, const float* __restrict__ dO, const float* __restrict__ dST, float* __restrict__ dq,
                      float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg,
                      float* __restrict__ dbeta, float* __restrict__ dS0, float* __restrict__ ckpt,
-                     float* __restrict__ states) {
+                     float* __restrict__ states, int64_t max_blocks) {
     extern __shared__ float sm[];
     const int LD = V + 1;
     float* S = sm;                      // running state, then S' of the current token [K][LD]
@@ -65,6 +65,21 @@ recurrent_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
     const int64_t len = eos - bos;
     const int nblk = (int)((len + kBwdBlock - 1) / kBwdBlock);
     const int64_t KV = (int64_t)K * V;
+    if (ck0 + nblk > max_blocks) {
+        // offsets that overlap can need more checkpoints than the workspace holds:
+        // such a chain is not computed, its gradients are marked NaN
+        const float nan = __int_as_float(0x7fc00000);
+        for (int64_t i = tid; i < len * K; i += kBwdThreads) {
+            const int64_t t = bos + i / K;
+            const int64_t e = (t * H + h) * K + i % K;
+            dq[e] = nan; dk[e] = nan; dg[e] = nan;
+        }
+        for (int64_t i = tid; i < len * V; i += kBwdThreads) dv[((bos + i / V) * H + h) * V + i % V] = nan;
+        for (int64_t i = tid; i < len; i += kBwdThreads) dbeta[(bos + i) * H + h] = nan;
+        if (dS0)
+            for (int64_t e = tid; e < KV; e += kBwdThreads) dS0[((int64_t)n * H + h) * KV + e] = nan;
+        return;
+    }
     float* ck = ckpt + (ck0 * H + (int64_t)h * nblk) * KV;  // nblk checkpoints of this chain
     float* st = states + (int64_t)blockIdx.x * kBwdBlock * KV;
     const int64_t sbase = ((int64_t)n * H + h) * KV;
@@ -231,7 +246,7 @@ cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const v
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
             static_cast<const __nv_bfloat16*>(beta), scale, s0, cu, B, T, H, K, V, dO, dST, dq, dk, dv, dg, dbeta,
-            dS0, ckpt, states);
+            dS0, ckpt, states, blocks);
     } else {
         auto kern = recurrent_bwd_kernel<float>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -239,7 +254,7 @@ cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const v
         kern<<<(unsigned)chains, kBwdThreads, smem, st>>>(
             static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
             static_cast<const float*>(g), static_cast<const float*>(beta), scale, s0, cu, B, T, H, K, V, dO, dST,
-            dq, dk, dv, dg, dbeta, dS0, ckpt, states);
+            dq, dk, dv, dg, dbeta, dS0, ckpt, states, blocks);
     }
     return cudaGetLastError();
 }
