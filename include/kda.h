@@ -16,14 +16,22 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
- *    tensor-core prefill (kda_chunk_fwd with bf16 inputs and K = V = 128)
- *    takes a device workspace for the duration of the call from a
- *    stream-ordered memory pool that the library owns (one per device, kept
- *    across calls for reuse); kda_chunk_fwd_noalloc uses a fixed array
- *    instead; kda_recurrent_bwd takes its workspace from the device's default
- *    stream-ordered pool; nothing else allocates.  Calls from different host
- *    threads are safe.
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, and so is
+ *    every workspace: the library allocates no memory.  kda_chunk_fwd,
+ *    kda_chunk_fwd_fused and kda_recurrent_bwd take a caller-owned device
+ *    workspace of at least the size their *_workspace_size query returns
+ *    (16-byte aligned; the call owns it until its stream work completes, and
+ *    nothing in it needs to be initialised); a smaller one returns
+ *    KDA_ERR_WORKSPACE before anything is enqueued.  kda_chunk_fwd_noalloc
+ *    keeps its workspace in a fixed array inside the library instead.  Calls
+ *    from different host threads are safe.
+ *  - status: those three entry points also take an optional caller-owned
+ *    device int32 status word (4-byte aligned, or NULL).  The call sets it to
+ *    KDA_OK on its stream; a kernel that cannot complete sets it to an error
+ *    (KDA_ERR_TIMEOUT: a bounded device-side wait gave up; KDA_ERR_RANGE: the
+ *    backward skipped a sequence whose offsets are malformed).  The caller
+ *    reads it after the stream work completes, as for kda_check_range; the
+ *    call's return value only covers what the host can check.
  *  - Layouts are row-major and token-major, as the K3 gate tensor (B, T, 96, 128):
  *        q, k, g [B, T, H, K]    v [B, T, H, V]    beta [B, T, H]
  *        o [B, T, H, V]          states [N, H, K, V] (V contiguous, fp32)
@@ -62,10 +70,10 @@ typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, inconsistent B/N */
     KDA_ERR_UNSUPPORTED = 2, /* head size or dtype outside the supported set */
-    KDA_ERR_WORKSPACE = 3,   /* device workspace unavailable (see kda_chunk_fwd, kda_chunk_fwd_noalloc) */
+    KDA_ERR_WORKSPACE = 3,   /* workspace smaller than the call needs (see the *_workspace_size queries) */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-    KDA_ERR_RANGE = 5,       /* an input lies outside its documented range (kda_check_range) */
-    KDA_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up */
+    KDA_ERR_RANGE = 5,       /* an input lies outside its documented range (device status word) */
+    KDA_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up (device status word) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -77,15 +85,32 @@ KDA_API const char *kda_status_string(kda_status status);
 KDA_API int kda_abi_version(void);
 
 /*
+ * kda_chunk_fwd_workspace_size -- device workspace bytes that kda_chunk_fwd
+ * (and kda_chunk_fwd_fused) needs for these sizes; packed = 1 when cu_seqlens
+ * will be given.  For bf16 inputs with K = V = 128 (the tensor-core path):
+ *
+ *     ceil(4 * hdr / 1024) * 1024 + max_chunks * H * 147968 bytes,
+ *     max_chunks = B * ceil(T / 64)          (packed = 0; hdr = 0)
+ *     max_chunks = ceil(T / 64) + N           (packed = 1; hdr = 2 N + 1 + max_chunks)
+ *
+ * (a slot per 64-token chunk and head holding the chunk-local results as the
+ * state kernel's MMA operands, written by the first kernel and read by the
+ * second), and 0 when N * H = 0.  Every other path (fp32 inputs, K or V = 64)
+ * needs none: 0.  Invalid sizes also give 0; the entry point validates them.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N,
+                                            int packed);
+
+/*
  * kda_chunk_fwd -- chunked prefill.
  *
  * Computes the recurrence above for N independent sequences with a chunked
  * (64-token) algorithm: in-chunk gated products A = K K^T and P = Q K^T with
  * cumulative per-channel decay, a UT transform of the decayed keys, and the
  * state carried from chunk to chunk (tensor-core path: a chunk-local kernel
- * over all chunks at once, then one state chain per sequence and head with
- * the state in tensor memory).  Results equal the token-by-token
- * recurrence up to rounding.
+ * over all chunks at once, then one state chain per sequence and head with the
+ * state in tensor memory).  Results equal the token-by-token recurrence up to
+ * rounding.
  *
  *  q, k, g, v, beta   inputs as laid out above, element type in_dtype.
  *  scale              read-out scale; scale <= 0 selects K^-0.5.
@@ -105,17 +130,20 @@ KDA_API int kda_abi_version(void);
  *                     or NULL to skip.  May alias initial_state exactly (the
  *                     state is then updated in place); no other overlap is
  *                     allowed.
- *
- *  Workspace (bf16, K = V = 128): 147968 bytes per (chunk, head) slot for
- *  every 64-token chunk of every sequence (an upper bound of ceil(T / 64) + N
- *  chunks per head when cu_seqlens is given), returned to the pool when the
- *  call's work completes.  KDA_ERR_WORKSPACE if the pool cannot provide it.
+ *  workspace          device memory of workspace_bytes >= the size
+ *                     kda_chunk_fwd_workspace_size returns (16-byte aligned;
+ *                     may be NULL when that size is 0).  Calls whose stream
+ *                     work overlaps must not share a workspace.
+ *  status             optional device status word (see the conventions):
+ *                     KDA_ERR_TIMEOUT if a bounded wait inside the kernels gave
+ *                     up, in which case o and final_state are unspecified.
  */
 KDA_API kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                          const void *beta, kda_dtype in_dtype, float scale,
                          const float *initial_state, const int32_t *cu_seqlens,
                          int B, int T, int H, int K, int V, int N,
-                         void *o, kda_dtype o_dtype, float *final_state, void *stream);
+                         void *o, kda_dtype o_dtype, float *final_state,
+                         void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd without any memory allocation.
@@ -125,20 +153,22 @@ KDA_API kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, co
  * the middle of their work: a serving process that reserved all free HBM for
  * its own state pool at start-up, or a runtime whose memory is managed by a
  * custom allocator that the library does not know about.  kda_chunk_fwd takes
- * its workspace from a pool and would fail or compete for memory there.  This
- * entry point computes exactly what kda_chunk_fwd computes, with the same
- * arguments, but keeps its workspace in one fixed 64 MiB device array that
- * every GPU loading libkda.so holds until the process exits; it calls no
- * allocation routine.  The caller still passes all inputs and outputs.
+ * a workspace that someone has to allocate.  This entry point computes
+ * exactly what kda_chunk_fwd computes, with the same arguments minus the
+ * workspace and status word, but keeps its workspace in one fixed 64 MiB
+ * device array that every GPU loading libkda.so holds until the process
+ * exits; it calls no allocation routine.  The caller still passes all inputs
+ * and outputs.  A device-side wait that gives up is not reported (there is no
+ * status word); o and final_state are then unspecified.
  *
  *  - Supported: in_dtype KDA_BF16 with K = V = 128 (the tensor-core path);
  *    anything else returns KDA_ERR_UNSUPPORTED.
- *  - The workspace needed is 147968 bytes per (chunk, head) slot, with
- *    ceil(T / 64) * B slots per head without cu_seqlens and ceil(T / 64) + N
- *    with it (plus 4 * (2 N + 1 + slots per head) bytes, rounded up to 1 KiB,
- *    of chunk bookkeeping).  A call needing more than 64 MiB returns
- *    KDA_ERR_WORKSPACE before anything is enqueued (e.g. H = 96: T <= 256 for
- *    one sequence; H = 8: T <= 3584).
+ *  - The workspace needed is what kda_chunk_fwd_workspace_size returns:
+ *    147968 bytes per (chunk, head) slot, with ceil(T / 64) * B slots per head
+ *    without cu_seqlens and ceil(T / 64) + N with it (plus 4 * (2 N + 1 +
+ *    slots per head) bytes, rounded up to 1 KiB, of chunk bookkeeping).  A
+ *    call needing more than 64 MiB returns KDA_ERR_WORKSPACE before anything
+ *    is enqueued (e.g. H = 96: T <= 256 for one sequence; H = 8: T <= 3584).
  *  - The first call made on a device looks up the array's device address (a
  *    CUDA runtime call); make that first call before any stream capture.
  *  - Every call shares the one array and leaves its last contents there;
@@ -172,7 +202,8 @@ KDA_API kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const voi
  *                     element type in_dtype.
  *  conv_q, conv_k     fp32 [H*K][4];  conv_v fp32 [H*V][4]  (channel = h*D + c).
  *  A_log fp32 [K];  dt_bias fp32 [H*K].
- *  Everything else as for kda_chunk_fwd.
+ *  Everything else as for kda_chunk_fwd, including the workspace (the same
+ *  kda_chunk_fwd_workspace_size) and the status word.
  */
 KDA_API kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, const void *v_raw,
                                const void *gate_x, const void *beta, kda_dtype in_dtype,
@@ -181,7 +212,8 @@ KDA_API kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, con
                                float lower_bound, float l2_eps, float scale,
                                const float *initial_state, const int32_t *cu_seqlens,
                                int B, int T, int H, int K, int V, int N,
-                               void *o, kda_dtype o_dtype, float *final_state, void *stream);
+                               void *o, kda_dtype o_dtype, float *final_state,
+                               void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
  * kda_trace_events -- timing hook for the tensor-core prefill.
@@ -196,6 +228,31 @@ KDA_API kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, con
  * too.  The events belong to the caller.
  */
 KDA_API void kda_trace_events(void *begin, void *split, void *end);
+
+/*
+ * kda_set_wait_limit -- testing hook: how many times a bounded device-side
+ * wait of the tensor-core prefill polls before it gives up (0 restores the
+ * default, about a second).  Process-wide; read when a call launches its
+ * kernels.  With kda_inject_wait_timeout it makes a wait give up quickly, so
+ * that the status word's KDA_ERR_TIMEOUT path can be exercised without a
+ * fault: the kernels then skip the rest of their work, drain the copies and
+ * MMAs in flight, and exit normally.  (The pages have no counterpart: failure
+ * detection.)
+ */
+KDA_API void kda_set_wait_limit(uint32_t iterations);
+
+/*
+ * kda_inject_wait_timeout -- testing hook: the next kda_chunk_fwd,
+ * kda_chunk_fwd_fused or kda_chunk_fwd_noalloc call made by the calling host
+ * thread on the tensor-core path makes the first wait of one of its kernels
+ * (kernel = 1: the chunk-local kernel, in every CTA; 2: the state kernel's MMA
+ * issuer, in every CTA) a wait on an mbarrier that nothing arrives on.  That
+ * wait runs out after the kda_set_wait_limit polls, records KDA_ERR_TIMEOUT in
+ * the call's status word and the kernels take their give-up path (no fault, no
+ * trap).  The call consumes the setting; another kernel value clears it.
+ * (The pages have no counterpart: failure detection.)
+ */
+KDA_API void kda_inject_wait_timeout(int kernel);
 
 /*
  * kda_recurrent_step -- one decode token for each of N sequences.
@@ -307,17 +364,26 @@ KDA_API kda_status kda_check_range(const void *x, kda_dtype dtype, int64_t count
  *  dq, dk, dg [B, T, H, K], dv [B, T, H, V], dbeta [B, T, H]: fp32 outputs, device.
  *  dS0     [N, H, K, V] fp32 or NULL (not written).
  *
- * The call takes a device workspace of 4*K*V*(ceil(len/64) + 64) bytes per
- * (sequence, head) from the device's default stream-ordered memory pool for the
- * duration of the call (KDA_ERR_WORKSPACE if it cannot be had).  Alignment and
- * error rules as kda_chunk_fwd; dbeta needs 4-byte alignment.
+ * The caller passes a device workspace of at least
+ * kda_recurrent_bwd_workspace_size bytes (16-byte aligned):
+ * 4 * K * V * (max_blocks * H + 64 * N * H) with max_blocks = B * ceil(T / 64),
+ * or ceil(T / 64) + N with cu_seqlens (state checkpoints every 64 tokens, and
+ * 64 recomputed states per chain); KDA_ERR_WORKSPACE before anything is
+ * enqueued if it is smaller.  status: optional device word, KDA_ERR_RANGE if
+ * a sequence was skipped because malformed (overlapping) offsets would need
+ * more checkpoints than the workspace holds; its gradients are then NaN, and
+ * rows it shares with another sequence are unspecified.  Alignment and error
+ * rules as kda_chunk_fwd; dbeta needs 4-byte alignment.
  */
+KDA_API size_t kda_recurrent_bwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N,
+                                                int packed);
+
 KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v, const void *g,
                              const void *beta, kda_dtype in_dtype, float scale,
                              const float *initial_state, const int32_t *cu_seqlens, int B, int T,
                              int H, int K, int V, int N, const float *dO, const float *dS_T,
                              float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
-                             void *stream);
+                             void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

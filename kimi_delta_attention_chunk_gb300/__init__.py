@@ -10,15 +10,19 @@ library; the first call does, and fails loudly if the library is missing.
 from .kda import (  # noqa: F401
     KDAError,
     SIGNATURES,
+    bwd_workspace_size,
     check_range,
     chunk_bwd,
     chunk_fwd,
     chunk_fwd_fused,
     chunk_fwd_noalloc,
+    inject_wait_timeout,
     library_path,
     load_library,
     output_gate,
     recurrent_step,
+    set_wait_limit,
     state_compose,
     trace_events,
+    workspace_size,
 )

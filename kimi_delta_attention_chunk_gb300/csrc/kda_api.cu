@@ -7,7 +7,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 bool head_size_ok(int d) { return d == 64 || d == 128; }
 bool dtype_ok(kda_dtype d) { return d == KDA_F32 || d == KDA_BF16; }
@@ -59,6 +59,18 @@ kda_status check_common(const void* q, const void* k, const void* v, const void*
     return KDA_OK;
 }
 
+// A caller-owned workspace of at least the queried size (16-byte aligned) and an
+// optional 4-byte aligned device status word.
+kda_status check_workspace(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N, bool packed,
+                           const void* ws, size_t ws_bytes, const int32_t* status) {
+    if (status != nullptr && ((uintptr_t)status % 4)) return KDA_ERR_INVALID_ARG;
+    if (ws != nullptr && !kda_host::aligned16(ws)) return KDA_ERR_INVALID_ARG;
+    if (!kda::chunk_tc_supported(in_dtype, K, V)) return KDA_OK;
+    const size_t need = kda::chunk_tc_workspace(B, T, H, N, packed);
+    if (ws_bytes < need || (need > 0 && ws == nullptr)) return KDA_ERR_WORKSPACE;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -68,7 +80,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head size or dtype not supported";
-        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: device workspace could not be allocated, or the call needs more than kda_chunk_fwd_noalloc's fixed scratch holds";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: the workspace is smaller than the call needs (see the *_workspace_size queries), or the call needs more than kda_chunk_fwd_noalloc's fixed scratch holds";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
         case KDA_ERR_RANGE: return "KDA_ERR_RANGE: input out of range";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: device-side wait gave up";
@@ -78,13 +90,26 @@ const char* kda_status_string(kda_status s) {
 
 int kda_abi_version(void) { return kAbiVersion; }
 
+size_t kda_chunk_fwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N, int packed) {
+    if (B < 0 || T < 0 || H <= 0 || N < 0) return 0;
+    if (!kda::chunk_tc_supported(in_dtype, K, V)) return 0;
+    return kda::chunk_tc_workspace(B, T, H, N, packed != 0);
+}
+
+void kda_set_wait_limit(uint32_t iterations) { kda::set_wait_limit(iterations); }
+
+void kda_inject_wait_timeout(int kernel) { kda::inject_wait_timeout(kernel); }
+
 kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
                          const void* beta, kda_dtype in_dtype, float scale,
                          const float* initial_state, const int32_t* cu_seqlens, int B, int T,
                          int H, int K, int V, int N, void* o, kda_dtype o_dtype,
-                         float* final_state, void* stream) {
+                         float* final_state, void* workspace, size_t workspace_bytes, int32_t* status,
+                         void* stream) {
     kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H,
                                 K, V, N, o, o_dtype, final_state);
+    if (s != KDA_OK) return s;
+    s = check_workspace(in_dtype, B, T, H, K, V, N, cu_seqlens != nullptr, workspace, workspace_bytes, status);
     if (s != KDA_OK) return s;
     kda::ChunkParams p{};
     p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
@@ -95,8 +120,10 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
     p.o = o;
     p.final_state = final_state;
     cudaStream_t st = (cudaStream_t)stream;
-    if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc(o_dtype, p, st));
+    if (kda::chunk_tc_supported(in_dtype, K, V))
+        return from_cuda(kda::chunk_tc(o_dtype, p, workspace, workspace_bytes, status, st));
     kda::trace_set(nullptr, nullptr, nullptr);
+    if (status != nullptr && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return KDA_ERR_CUDA;
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, false, p, st));
 }
 
@@ -127,9 +154,12 @@ kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void*
                                float lower_bound, float l2_eps, float scale,
                                const float* initial_state, const int32_t* cu_seqlens, int B,
                                int T, int H, int K, int V, int N, void* o, kda_dtype o_dtype,
-                               float* final_state, void* stream) {
+                               float* final_state, void* workspace, size_t workspace_bytes,
+                               int32_t* status, void* stream) {
     kda_status s = check_common(q_raw, k_raw, v_raw, gate_x, beta, in_dtype, initial_state,
                                 cu_seqlens, B, T, H, K, V, N, o, o_dtype, final_state);
+    if (s != KDA_OK) return s;
+    s = check_workspace(in_dtype, B, T, H, K, V, N, cu_seqlens != nullptr, workspace, workspace_bytes, status);
     if (s != KDA_OK) return s;
     if (conv_act != 0 && conv_act != 1) return KDA_ERR_INVALID_ARG;
     if (!(l2_eps >= 0.f) || !(lower_bound <= 0.f) || isnan(lower_bound)) return KDA_ERR_INVALID_ARG;
@@ -152,8 +182,10 @@ kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void*
     p.lower_bound = lower_bound;
     p.l2_eps = l2_eps;
     cudaStream_t st = (cudaStream_t)stream;
-    if (kda::chunk_tc_supported(in_dtype, K, V)) return from_cuda(kda::chunk_tc_fused(o_dtype, p, st));
+    if (kda::chunk_tc_supported(in_dtype, K, V))
+        return from_cuda(kda::chunk_tc_fused(o_dtype, p, workspace, workspace_bytes, status, st));
     kda::trace_set(nullptr, nullptr, nullptr);
+    if (status != nullptr && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return KDA_ERR_CUDA;
     return from_cuda(kda::chunk_simt(in_dtype, o_dtype, K, V, true, p, st));
 }
 
@@ -238,11 +270,18 @@ kda_status kda_check_range(const void* x, kda_dtype dtype, int64_t count, float 
     return from_cuda(kda::check_range(dtype, x, count, lo, hi, status, (cudaStream_t)stream));
 }
 
+size_t kda_recurrent_bwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N, int packed) {
+    if (B < 0 || T < 0 || H <= 0 || N < 0 || !dtype_ok(in_dtype)) return 0;
+    if (!head_size_ok(K) || !head_size_ok(V)) return 0;
+    return kda::recurrent_bwd_workspace(B, T, H, K, V, N, packed != 0);
+}
+
 kda_status kda_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
                              kda_dtype in_dtype, float scale, const float* initial_state,
                              const int32_t* cu_seqlens, int B, int T, int H, int K, int V, int N,
                              const float* dO, const float* dS_T, float* dq, float* dk, float* dv, float* dg,
-                             float* dbeta, float* dS0, void* stream) {
+                             float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
+                             int32_t* status, void* stream) {
     kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H, K, V, N,
                                 dO, KDA_F32, nullptr);
     if (s != KDA_OK) return s;
@@ -252,16 +291,14 @@ kda_status kda_recurrent_bwd(const void* q, const void* k, const void* v, const 
     for (const void* p : ptrs)
         if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
     if (dbeta && ((uintptr_t)dbeta % 4)) return KDA_ERR_INVALID_ARG;
-    if ((int64_t)N * H == 0) return KDA_OK;
+    if (status != nullptr && ((uintptr_t)status % 4)) return KDA_ERR_INVALID_ARG;
+    const size_t bytes = (int64_t)N * H == 0 ? 0 : kda::recurrent_bwd_workspace(B, T, H, K, V, N, cu_seqlens != nullptr);
+    if (workspace_bytes < bytes || (bytes > 0 && workspace == nullptr)) return KDA_ERR_WORKSPACE;
+    if (workspace != nullptr && !kda_host::aligned16(workspace)) return KDA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
-    const size_t bytes = kda::recurrent_bwd_workspace(B, T, H, K, V, N, cu_seqlens != nullptr);
-    void* ws = nullptr;
-    if (bytes > 0 && cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return KDA_ERR_WORKSPACE;
-    const cudaError_t e = kda::recurrent_bwd(in_dtype, q, k, v, g, beta, resolve_scale(scale, K), initial_state,
-                                             cu_seqlens, B, T, H, K, V, N, dO, dS_T, dq, dk, dv, dg, dbeta, dS0,
-                                             ws, st);
-    const cudaError_t ef = ws ? cudaFreeAsync(ws, st) : cudaSuccess;
-    return from_cuda(e != cudaSuccess ? e : ef);
+    return from_cuda(kda::recurrent_bwd(in_dtype, q, k, v, g, beta, resolve_scale(scale, K), initial_state,
+                                        cu_seqlens, B, T, H, K, V, N, dO, dS_T, dq, dk, dv, dg, dbeta, dS0,
+                                        workspace, status, st));
 }
 
 }  // extern "C"

@@ -37,18 +37,32 @@ struct ChunkParams {
 cudaError_t chunk_simt(kda_dtype in_dt, kda_dtype out_dt, int K, int V, bool prologue,
                        const ChunkParams& p, cudaStream_t st);
 
-// Tensor-core chunk kernels (bf16 inputs, K = V = 128), workspace from the
-// library's stream-ordered pool.
+// Tensor-core chunk kernels (bf16 inputs, K = V = 128): the workspace bytes a
+// call needs, and the launch with a caller-owned workspace (cudaErrorMemoryAllocation
+// before anything is enqueued if ws_bytes is too small).  status (device, may be
+// null) is set to KDA_OK on the stream and to KDA_ERR_TIMEOUT by a kernel whose
+// bounded wait gave up.
 bool chunk_tc_supported(kda_dtype in_dt, int K, int V);
-cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+size_t chunk_tc_workspace(int B, int T, int H, int N, bool packed);
+cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, void* ws, size_t ws_bytes, int32_t* status,
+                     cudaStream_t st);
 // With the input prologue (p.q, p.k, p.v, p.g are the raw inputs).
-cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, void* ws, size_t ws_bytes, int32_t* status,
+                           cudaStream_t st);
 
 // The same with the workspace in a fixed device array of kFixedScratchBytes
 // (no allocation); cudaErrorMemoryAllocation, before anything is enqueued,
 // when the call needs more.
 constexpr size_t kFixedScratchBytes = (size_t)64 << 20;
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st);
+
+// Polls before a bounded device-side wait of the tensor-core prefill gives up
+// (0 = the default, about a second); read at each launch.
+void set_wait_limit(uint32_t iterations);
+// Testing: the next tensor-core prefill call on this host thread makes the
+// first wait of its chunk-local (1) or state (2) kernel one on an mbarrier that
+// nothing arrives on, so that it gives up; the call consumes the setting.
+void inject_wait_timeout(int kernel);
 
 // Events that the next tensor-core prefill call made on this host thread
 // records: before its first kernel, after the chunk-local kernel, after its
@@ -73,10 +87,12 @@ cudaError_t check_range(kda_dtype dt, const void* x, int64_t n, float lo, float 
                         cudaStream_t st);
 
 // Backward of the recurrence (CUDA cores, fp32): workspace bytes, and the launch.
+// status (device, may be null): KDA_ERR_RANGE when a chain was skipped because
+// malformed offsets would need more workspace than the call has.
 size_t recurrent_bwd_workspace(int B, int T, int H, int K, int V, int N, bool packed);
 cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const void* v, const void* g,
                           const void* beta, float scale, const float* s0, const int32_t* cu, int B, int T, int H,
                           int K, int V, int N, const float* dO, const float* dST, float* dq, float* dk, float* dv,
-                          float* dg, float* dbeta, float* dS0, void* ws, cudaStream_t st);
+                          float* dg, float* dbeta, float* dS0, void* ws, int32_t* status, cudaStream_t st);
 
 }  // namespace kda

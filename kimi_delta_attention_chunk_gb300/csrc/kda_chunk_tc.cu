@@ -39,8 +39,13 @@
 // Sources: "ISEEKYAN/k3" README (chunked KDA forward as the compute path);
 // "kimi-k3-mlx" review, "The A_log shape mismatch ..." (per-channel decay) and
 // "Attention is 93 layers ..." (gate lower bound -5, 96 heads of 128).
+// Every wait is bounded (a launch parameter, about a second by default).  A
+// wait that gives up records KDA_ERR_TIMEOUT in the caller's status word (when
+// one is given), the kernel leaves its loop, drains the copies and MMAs it has
+// in flight and exits; the affected outputs are unspecified.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kda_chunk.h"
@@ -48,12 +53,15 @@
 #include "kda_tc.cuh"
 
 namespace kda {
+
+std::atomic<uint32_t> g_wait_limit{0};
+
 namespace {
 
 constexpr int C = 64;
 constexpr int D = 128;   // K = V
 constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TMEM lanes
-constexpr uint32_t kWaitIter = 1u << 26;
+constexpr uint32_t kWaitIter = 1u << 26;   // default poll count of a bounded wait, and of the exit drains
 
 // ---- workspace slot of one (chunk, head), written by the local kernel --------
 constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qs hi] (bf16) as one B operand, MN-major
@@ -85,7 +93,15 @@ struct Plan {
     int cps;                   // chunks per sequence (dense only)
     int64_t max_chunks;        // number of workspace chunk slots (an upper bound when packed)
     uint8_t* slots;
+    int32_t* status;           // device status word (KDA_ERR_TIMEOUT on a wait that gave up), or null
+    uint32_t wait_iter;        // polls before a wait gives up
+    int inject;                // testing: 1 = the chunk-local kernel's, 2 = the state kernel's first wait
+                               //   is on an mbarrier that nothing arrives on (0 = none)
 };
+
+__device__ __forceinline__ void report_timeout(const Plan& pl) {
+    if (pl.status != nullptr) *reinterpret_cast<volatile int32_t*>(pl.status) = (int32_t)KDA_ERR_TIMEOUT;
+}
 
 struct Chunk {
     int64_t c0, eos;  // first token of the chunk, end of its sequence
@@ -145,7 +161,7 @@ constexpr uint32_t RT_LO = 96 * D * 2;
 constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals of e^g
 constexpr uint32_t SM_ITOT = SM_SMALL + 2048;    // fp32 [2][128] inverses of the totals of blocks 0, 2
 constexpr uint32_t SM_BETA = SM_SMALL + 3072;    // fp32 [64]
-constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base
+constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base, exit drain, testing
 constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
 // with the input prologue (raw q, k, v and gate input in the staging tiles):
 constexpr uint32_t SM_RED = SM_SMALL + 3456;     // fp32 [2][64][4] partial sums of squares of q, k rows
@@ -229,6 +245,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
+    uint64_t* bar_fin = bar_tma + 3;   // every MMA issued has completed (exit drain)
+    uint64_t* bar_never = bar_tma + 4; // testing: nothing arrives on it
     const int H = pl.H;
     const __nv_bfloat16* __restrict__ beta_g = reinterpret_cast<const __nv_bfloat16*>(beta_ptr);
 
@@ -236,6 +254,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     if (tid == 0) {
         tc::bar_init(bar_tma, 1);
         tc::bar_init(bar_mma, 1);
+        tc::bar_init(bar_fin, 1);
+        tc::bar_init(bar_never, 1);
         tc::bar_init_fence();
     }
     tc::fence_async_smem();
@@ -298,13 +318,19 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
         }
     };
-    // One warp polls the barrier; the others park at the CTA barrier.
+    // One warp polls the barrier; the others park at the CTA barrier.  A wait
+    // that gives up leaves its phase pending (the exit drains it) and sets failed
+    // in every thread.
+    bool inject = pl.inject == 1;
     auto wait_one = [&](uint64_t* bar, uint32_t& phase) {
         bool ok = true;
-        if (warp == 0) ok = tc::bar_wait(bar, phase, kWaitIter);
-        phase ^= 1;
-        failed = __syncthreads_or(failed || !ok);
+        if (warp == 0) ok = inject ? tc::bar_wait(bar_never, 0, pl.wait_iter) : tc::bar_wait(bar, phase, pl.wait_iter);
+        inject = false;
+        const bool gave_up = __syncthreads_or(!ok) != 0;
+        if (!gave_up) phase ^= 1;
+        failed = failed || gave_up;
         tc::fence_after();
+        return !gave_up;
     };
     auto mma_sync = [&]() { wait_one(bar_mma, mma_phase); };
     // Make generic-proxy smem writes and TMEM stores visible to the MMA issuer.
@@ -349,8 +375,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 
         // (the previous task's bulk stores read only the operand regions, which are
         // rewritten once they are done: see the wait before the A/P operands)
-        wait_one(bar_tma, tma_phase);
-        tma_pending = false;
+        if (wait_one(bar_tma, tma_phase)) tma_pending = false;
         if (failed) break;
         // the next task's byte count, posted long before its loads are issued (by
         // several threads, so none of them may complete the phase early)
@@ -975,6 +1000,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 
     if (failed) {
+        if (tid == 0) report_timeout(pl);
         // mark the slot of the task that could not finish (its e^{G_C} becomes NaN,
         // which poisons the state of that sequence), then drain a tile load in flight
         if (cur.valid && tid < 128)
@@ -983,6 +1009,12 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (tma_pending && tid == 0) tc::bar_wait(bar_tma, tma_phase, kWaitIter);
     }
     if (tid == kIssueTid) tc::bulk_wait();
+    // MMAs that a wait gave up on may still run: they complete before TMEM is released
+    if (warp == 0) {
+        tc::commit_w(bar_fin);
+        if (lane == 0) tc::bar_wait(bar_fin, 0, kWaitIter);
+        __syncwarp();
+    }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, TL_COLS);
@@ -1077,7 +1109,7 @@ constexpr int ISSUER = 16;
 constexpr uint32_t SS_KB = 2 * SLOT_IMG;    // [-W | Qs] images + e^{G_C} of two chunks, then Kbar
 constexpr uint32_t SS_UT = SS_KB + SLOT_KBP;//   and P, and U~, of one chunk
 constexpr uint32_t SS_BAR = SS_UT + 32768;  // img 0, img 1, u, o, s, ut, kb, uready, sready;
-constexpr uint32_t SS_TOTAL = SS_BAR + 128; //   tmem base; abort flag
+constexpr uint32_t SS_TOTAL = SS_BAR + 128; //   tmem base; abort flag; exit drain; testing
 static_assert(SS_TOTAL + 128 <= 232448, "shared memory");
 
 // ---- tensor memory map (columns) ----------------------------------------------
@@ -1107,6 +1139,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     uint64_t* bar_sready = bar_img + 8;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_img + 9);
     volatile int* abort_s = reinterpret_cast<volatile int*>(bar_img + 10);
+    uint64_t* bar_fin = bar_img + 11;   // every MMA issued has completed (exit drain)
+    uint64_t* bar_never = bar_img + 12; // testing: nothing arrives on it
     const float* ut_s = reinterpret_cast<const float*>(smem + SS_UT);   // U~ [64 r][128 v]
 
     const int H = pl.H;
@@ -1136,6 +1170,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     if (tid == 0) {
 #pragma unroll
         for (int b = 0; b < 7; ++b) tc::bar_init(bar_img + b, 1);
+        tc::bar_init(bar_fin, 1);
+        tc::bar_init(bar_never, 1);
         tc::bar_init(bar_uready, 16);
         tc::bar_init(bar_sready, 16);
         *abort_s = 0;
@@ -1148,7 +1184,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
 
     auto slot_of = [&](int64_t i) { return pl.slots + ((g0 + i) * H + h) * (int64_t)SLOT_BYTES; };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-        return tc::bar_wait_or_abort(bar, parity, kWaitIter, abort_s);
+        return tc::bar_wait_or_abort(bar, parity, pl.wait_iter, abort_s);
     };
     auto chunk_rows = [&](int64_t i) {
         const int64_t c0 = bos + i * C;
@@ -1199,7 +1235,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
         const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
         const uint32_t id_n64 = tc::idesc_bf16(128, 64);
         bool ok = true;
-        for (int64_t i = 0; i < nchunks; ++i) {
+        if (pl.inject == 2) ok = wait(bar_never, 0);
+        for (int64_t i = 0; i < nchunks && ok; ++i) {
             const uint32_t par = (uint32_t)(i & 1);
             if (!wait(bar_img + (i & 1), (uint32_t)((i >> 1) & 1))) { ok = false; break; }
             done = i + 1;
@@ -1267,10 +1304,15 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
         if (ok && nchunks > 0 && wait(bar_sready, (uint32_t)(nchunks & 1))) store_o(nchunks - 1);
         // drain loads that may still be in flight before the CTA exits
         if (*abort_s && lane == 0) {
+            report_timeout(pl);
             for (int64_t j = done; j < issued; ++j) tc::bar_wait(bar_img + (j & 1), (uint32_t)((j >> 1) & 1), kWaitIter);
             if (ut_issued > 0) tc::bar_wait(bar_ut, (uint32_t)((ut_issued - 1) & 1), kWaitIter);
             if (kb_issued > 0) tc::bar_wait(bar_kb, (uint32_t)((kb_issued - 1) & 1), kWaitIter);
         }
+        // MMAs that a wait gave up on may still run: they complete before TMEM is released
+        tc::commit_w(bar_fin);
+        if (lane == 0) tc::bar_wait(bar_fin, 0, kWaitIter);
+        __syncwarp();
         tc::bulk_wait();
     } else {
         // ================= TMEM epilogues =================
@@ -1448,85 +1490,87 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, bool halo =
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Library-owned stream-ordered memory pool, one per device, that keeps what it
-// has reserved (release threshold = unlimited), so repeated calls reuse it.
+// SM count of the current device, looked up once per device.
 constexpr int kMaxDevices = 64;
-std::mutex g_pool_mutex;
-cudaMemPool_t g_pool[kMaxDevices];
-bool g_pool_ready[kMaxDevices];
+std::mutex g_dev_mutex;
 int g_sm_count[kMaxDevices];
 
-cudaError_t device_pool(cudaMemPool_t* pool, int* sms) {
+cudaError_t device_sms(int* sms) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_pool_mutex);
-    if (!g_pool_ready[dev]) {
-        cudaMemPoolProps props{};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.handleTypes = cudaMemHandleTypeNone;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        e = cudaMemPoolCreate(&g_pool[dev], &props);
-        if (e != cudaSuccess) return e;
-        uint64_t keep = UINT64_MAX;
-        e = cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
-        if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_sm_count[dev] == 0) {
         e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        g_pool_ready[dev] = true;
     }
-    *pool = g_pool[dev];
     *sms = g_sm_count[dev];
     return cudaSuccess;
 }
 
 // Events that the next prefill call on this host thread records (timing hook).
 thread_local cudaEvent_t g_trace[3] = {nullptr, nullptr, nullptr};
+// Wait-timeout injection of the next prefill call on this host thread (testing hook).
+thread_local int g_inject = 0;
 
 void trace_record(cudaEvent_t ev, cudaStream_t st) {
     if (ev != nullptr) cudaEventRecord(ev, st);
 }
 
-// The prefill's kernels, with the workspace taken from the library's pool
-// (fixed_ws == nullptr) or from a caller-side buffer of fixed_bytes.
+// Workspace of one call: packed-sequence bookkeeping (chunk offsets, longest-
+// first order, chunk -> sequence map) rounded up to 1 KiB, then one slot per
+// (chunk, head).  max_chunks is exact without cu_seqlens and an upper bound
+// (ceil(T / 64) + N) with it.
+struct Layout {
+    int64_t max_chunks;
+    size_t hdr_bytes;
+    size_t bytes;
+};
+Layout layout(int B, int T, int H, int N, bool packed) {
+    Layout l{};
+    const int64_t cps = ((int64_t)T + C - 1) / C;
+    l.max_chunks = packed ? cps + N : (int64_t)B * cps;
+    const size_t hdr_ints = packed ? (size_t)(2 * (int64_t)N + 1) + (size_t)l.max_chunks : 0;
+    l.hdr_bytes = (hdr_ints * 4 + 1023) & ~size_t(1023);
+    l.bytes = l.hdr_bytes + (size_t)l.max_chunks * (size_t)H * SLOT_BYTES;
+    if ((int64_t)N * H == 0) l.bytes = 0;
+    return l;
+}
+
+// The prefill's kernels on a caller-owned workspace of ws_bytes.
 template <typename TOut>
-cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nullptr, size_t fixed_bytes = 0,
-                      int fixed_sms = 0, bool fused = false) {
+cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws_bytes, int32_t* status,
+                      bool fused) {
+    cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
+    g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (status != nullptr) {
+        e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t NH = (int64_t)p.N * p.H;
     if (NH == 0) return cudaSuccess;
     const bool packed = p.cu_seqlens != nullptr;
-    cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
-    g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
+    const Layout lo = layout(p.B, p.T, p.H, p.N, packed);
+    if (lo.bytes > ws_bytes || (lo.bytes > 0 && ws == nullptr)) return cudaErrorMemoryAllocation;
+    int sms = 0;
+    e = device_sms(&sms);
+    if (e != cudaSuccess) return e;
     Plan pl{};
     pl.cu_seqlens = p.cu_seqlens;
     pl.T = p.T;
     pl.H = p.H;
     pl.N = p.N;
     pl.cps = packed ? 0 : (p.T + C - 1) / C;
-    pl.max_chunks = packed ? ((int64_t)p.T + C - 1) / C + p.N : (int64_t)p.B * pl.cps;
-    const size_t hdr_ints = packed ? (size_t)(2 * (int64_t)p.N + 1) + (size_t)pl.max_chunks : 0;
-    const size_t hdr_bytes = (hdr_ints * 4 + 1023) & ~size_t(1023);
-    const size_t bytes = hdr_bytes + (size_t)pl.max_chunks * (size_t)p.H * SLOT_BYTES;
-
-    cudaError_t e = cudaSuccess;
-    int sms = fixed_sms;
-    void* ws = nullptr;
-    if (fixed_ws != nullptr) {
-        if (bytes > fixed_bytes) return cudaErrorMemoryAllocation;
-        ws = fixed_ws;
-    } else {
-        cudaMemPool_t pool;
-        e = device_pool(&pool, &sms);
-        if (e != cudaSuccess) return e;
-        if (bytes > 0) {
-            e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
-            if (e != cudaSuccess) return cudaErrorMemoryAllocation;
-        }
-    }
+    pl.max_chunks = lo.max_chunks;
+    pl.status = status;
+    const uint32_t lim = g_wait_limit.load(std::memory_order_relaxed);
+    pl.wait_iter = lim != 0 ? lim : kWaitIter;
+    pl.inject = g_inject;
+    g_inject = 0;
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
-    pl.slots = reinterpret_cast<uint8_t*>(ws) + hdr_bytes;
+    pl.slots = reinterpret_cast<uint8_t*>(ws) + lo.hdr_bytes;
     trace_record(trace[0], st);
     if (packed) {
         pl.chunk_off = hdr;
@@ -1536,10 +1580,11 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
                                               const_cast<int32_t*>(pl.chunk_off), const_cast<int32_t*>(pl.order),
                                               const_cast<int32_t*>(pl.chunk_seq));
         e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     const int64_t tasks = pl.max_chunks * p.H;
-    if (tasks >= ((int64_t)1 << 31)) e = cudaErrorInvalidValue;
-    if (e == cudaSuccess && tasks > 0) {
+    if (tasks >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    if (tasks > 0) {
         const int64_t rows = (int64_t)p.B * p.T;
         CUtensorMap mq, mk, mv, mg, hq, hk, hv;
         bool ok = make_map(&mq, p.q, rows, p.H) && make_map(&mk, p.k, rows, p.H) && make_map(&mv, p.v, rows, p.H) &&
@@ -1550,47 +1595,34 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
         } else {
             hq = mq; hk = mk; hv = mv;  // unused
         }
-        if (!ok) {
-            e = cudaErrorInvalidValue;
-        } else {
-            Prologue pro{};
-            pro.conv_q = p.conv_q; pro.conv_k = p.conv_k; pro.conv_v = p.conv_v;
-            pro.A_log = p.A_log; pro.dt_bias = p.dt_bias;
-            pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
-            auto kern = !fused ? chunk_local_kernel<false>
-                               : (p.conv_act == 1 ? chunk_local_kernel<true, true> : chunk_local_kernel<true, false>);
-            const int smem_bytes = (int)(fused ? SM_LOCAL_TOTAL_FUSED : SM_LOCAL_TOTAL) + 1024;  // + alignment slack
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-            if (e == cudaSuccess) {
-                const int64_t grid = tasks < sms ? tasks : sms;
-                kern<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, hq, hk, hv, p.beta, p.scale, pl, pro);
-                e = cudaGetLastError();
-                trace_record(trace[1], st);
-            }
-        }
+        if (!ok) return cudaErrorInvalidValue;
+        Prologue pro{};
+        pro.conv_q = p.conv_q; pro.conv_k = p.conv_k; pro.conv_v = p.conv_v;
+        pro.A_log = p.A_log; pro.dt_bias = p.dt_bias;
+        pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
+        auto kern = !fused ? chunk_local_kernel<false>
+                           : (p.conv_act == 1 ? chunk_local_kernel<true, true> : chunk_local_kernel<true, false>);
+        const int smem_bytes = (int)(fused ? SM_LOCAL_TOTAL_FUSED : SM_LOCAL_TOTAL) + 1024;  // + alignment slack
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = tasks < sms ? tasks : sms;
+        kern<<<(unsigned)grid, NT, smem_bytes, st>>>(mq, mk, mv, mg, hq, hk, hv, p.beta, p.scale, pl, pro);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        trace_record(trace[1], st);
     }
-    if (e == cudaSuccess) {
-        auto kern = chunk_state_kernel<TOut>;
-        const int smem_bytes = (int)SS_TOTAL + 128;
-        CUtensorMap mo;
-        const int64_t rows = (int64_t)p.B * p.T;
-        if (!make_out_map<TOut>(&mo, p.o, rows > 0 ? rows : 1, p.H)) {
-            e = cudaErrorInvalidValue;
-        } else {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-            if (e == cudaSuccess) {
-                kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(mo, p.initial_state, p.final_state,
-                                                           reinterpret_cast<TOut*>(p.o), pl);
-                e = cudaGetLastError();
-                trace_record(trace[2], st);
-            }
-        }
-    }
-    if (ws != nullptr && fixed_ws == nullptr) {
-        const cudaError_t ef = cudaFreeAsync(ws, st);
-        if (e == cudaSuccess) e = ef;
-    }
-    return e;
+    auto kern = chunk_state_kernel<TOut>;
+    const int smem_bytes = (int)SS_TOTAL + 128;
+    CUtensorMap mo;
+    const int64_t rows = (int64_t)p.B * p.T;
+    if (!make_out_map<TOut>(&mo, p.o, rows > 0 ? rows : 1, p.H)) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)NH, NT2, smem_bytes, st>>>(mo, p.initial_state, p.final_state, reinterpret_cast<TOut*>(p.o), pl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    trace_record(trace[2], st);
+    return cudaSuccess;
 }
 
 // ---- prefill without any allocation ---------------------------------------------
@@ -1600,9 +1632,8 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* fixed_ws = nu
 static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
 std::mutex g_fixed_mutex;
 void* g_fixed_ptr[kMaxDevices];
-int g_fixed_sms[kMaxDevices];
 
-cudaError_t fixed_scratch(void** ptr, int* sms) {
+cudaError_t fixed_scratch(void** ptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1612,12 +1643,9 @@ cudaError_t fixed_scratch(void** ptr, int* sms) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_fixed_scratch);
         if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&g_fixed_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
         g_fixed_ptr[dev] = p;
     }
     *ptr = g_fixed_ptr[dev];
-    *sms = g_fixed_sms[dev];
     return cudaSuccess;
 }
 
@@ -1625,29 +1653,36 @@ cudaError_t fixed_scratch(void** ptr, int* sms) {
 
 bool chunk_tc_supported(kda_dtype in_dt, int K, int V) { return in_dt == KDA_BF16 && K == D && V == D; }
 
+size_t chunk_tc_workspace(int B, int T, int H, int N, bool packed) { return layout(B, T, H, N, packed).bytes; }
+
 void trace_set(void* begin, void* split, void* end) {
     g_trace[0] = static_cast<cudaEvent_t>(begin);
     g_trace[1] = static_cast<cudaEvent_t>(split);
     g_trace[2] = static_cast<cudaEvent_t>(end);
 }
 
-cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
-    if (out_dt == KDA_F32) return launch_tc<float>(p, st);
-    return launch_tc<__nv_bfloat16>(p, st);
+void set_wait_limit(uint32_t iterations) { g_wait_limit.store(iterations, std::memory_order_relaxed); }
+
+void inject_wait_timeout(int kernel) { g_inject = (kernel == 1 || kernel == 2) ? kernel : 0; }
+
+cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, void* ws, size_t ws_bytes, int32_t* status,
+                     cudaStream_t st) {
+    if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, ws_bytes, status, false);
+    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false);
 }
 
-cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
-    if (out_dt == KDA_F32) return launch_tc<float>(p, st, nullptr, 0, 0, true);
-    return launch_tc<__nv_bfloat16>(p, st, nullptr, 0, 0, true);
+cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, void* ws, size_t ws_bytes, int32_t* status,
+                           cudaStream_t st) {
+    if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, ws_bytes, status, true);
+    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, true);
 }
 
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
     void* ws = nullptr;
-    int sms = 0;
-    const cudaError_t e = fixed_scratch(&ws, &sms);
+    const cudaError_t e = fixed_scratch(&ws);
     if (e != cudaSuccess) return e;
-    if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, kFixedScratchBytes, sms);
-    return launch_tc<__nv_bfloat16>(p, st, ws, kFixedScratchBytes, sms);
+    if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, kFixedScratchBytes, nullptr, false);
+    return launch_tc<__nv_bfloat16>(p, st, ws, kFixedScratchBytes, nullptr, false);
 }
 
 }  // namespace kda

@@ -34,7 +34,7 @@ recurrent_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
                      int V, const float* __restrict__ dO, const float* __restrict__ dST, float* __restrict__ dq,
                      float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg,
                      float* __restrict__ dbeta, float* __restrict__ dS0, float* __restrict__ ckpt,
-                     float* __restrict__ states, int64_t max_blocks) {
+                     float* __restrict__ states, int64_t max_blocks, int32_t* __restrict__ status) {
     extern __shared__ float sm[];
     const int LD = V + 1;
     float* S = sm;                      // running state, then S' of the current token [K][LD]
@@ -67,7 +67,10 @@ recurrent_bwd_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
     const int64_t KV = (int64_t)K * V;
     if (ck0 + nblk > max_blocks) {
         // offsets that overlap can need more checkpoints than the workspace holds:
-        // such a chain is not computed, its gradients are marked NaN
+        // such a chain is not computed, its gradients are marked NaN (rows that a
+        // computed chain shares with it may be overwritten by that chain) and the
+        // status word says KDA_ERR_RANGE
+        if (tid == 0 && status != nullptr) *reinterpret_cast<volatile int32_t*>(status) = (int32_t)KDA_ERR_RANGE;
         const float nan = __int_as_float(0x7fc00000);
         for (int64_t i = tid; i < len * K; i += kBwdThreads) {
             const int64_t t = bos + i / K;
@@ -230,7 +233,11 @@ size_t recurrent_bwd_workspace(int B, int T, int H, int K, int V, int N, bool pa
 cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const void* v, const void* g,
                           const void* beta, float scale, const float* s0, const int32_t* cu, int B, int T, int H,
                           int K, int V, int N, const float* dO, const float* dST, float* dq, float* dk, float* dv,
-                          float* dg, float* dbeta, float* dS0, void* ws, cudaStream_t st) {
+                          float* dg, float* dbeta, float* dS0, void* ws, int32_t* status, cudaStream_t st) {
+    if (status != nullptr) {
+        const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     float* ckpt = static_cast<float*>(ws);
@@ -246,7 +253,7 @@ cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const v
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
             static_cast<const __nv_bfloat16*>(beta), scale, s0, cu, B, T, H, K, V, dO, dST, dq, dk, dv, dg, dbeta,
-            dS0, ckpt, states, blocks);
+            dS0, ckpt, states, blocks, status);
     } else {
         auto kern = recurrent_bwd_kernel<float>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -254,7 +261,7 @@ cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const v
         kern<<<(unsigned)chains, kBwdThreads, smem, st>>>(
             static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
             static_cast<const float*>(g), static_cast<const float*>(beta), scale, s0, cu, B, T, H, K, V, dO, dST,
-            dq, dk, dv, dg, dbeta, dS0, ckpt, states, blocks);
+            dq, dk, dv, dg, dbeta, dS0, ckpt, states, blocks, status);
     }
     return cudaGetLastError();
 }

@@ -175,7 +175,34 @@ __device__ __forceinline__ bool bar_wait_or_abort(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// ---- named barriers (ids 1..15; count a multiple of 32) ----------------------
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// A named barrier that also returns whether any participating thread passed
+// pred = true (the same answer in every thread).
+__device__ __forceinline__ bool named_any(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // ---- TMA -------------------------------------------------------------------
+// Prefetch of one tensor-map box into L2 (no shared memory written).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+// Prefetch of a contiguous range into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
     asm volatile(

@@ -24,24 +24,29 @@ _STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "
 
 # (name, restype, argtypes) of every exported symbol of include/kda.h
 _vp, _fp, _i32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
-_i, _f = ctypes.c_int, ctypes.c_float
+_i, _f, _sz, _u32 = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint32
 SIGNATURES = {
     "kda_status_string": (ctypes.c_char_p, [_i]),
     "kda_abi_version": (_i, []),
+    "kda_chunk_fwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "kda_chunk_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
-                           _vp, _i, _fp, _vp]),
+                           _vp, _i, _fp, _vp, _sz, _i32p, _vp]),
     "kda_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i,
                                    _i, _vp, _i, _fp, _vp]),
     "kda_chunk_fwd_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _fp, _fp, _f, _f,
-                                 _f, _fp, _i32p, _i, _i, _i, _i, _i, _i, _vp, _i, _fp, _vp]),
+                                 _f, _fp, _i32p, _i, _i, _i, _i, _i, _i, _vp, _i, _fp, _vp, _sz, _i32p,
+                                 _vp]),
     "kda_trace_events": (None, [_vp, _vp, _vp]),
+    "kda_set_wait_limit": (None, [_u32]),
+    "kda_inject_wait_timeout": (None, [_i]),
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
     "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
+    "kda_recurrent_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "kda_recurrent_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
-                               _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp]),
+                               _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _i32p, _vp]),
 }
 
 
@@ -102,13 +107,61 @@ def _check(fn: str, status: int):
         raise KDAError(fn, status)
 
 
+def _dt_of(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return KDA_BF16
+    if dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {dtype}")
+
+
+def workspace_size(in_dtype, B: int, T: int, H: int, K: int, V: int, N: int, packed: bool) -> int:
+    """Device workspace bytes ``kda_chunk_fwd`` / ``kda_chunk_fwd_fused`` need."""
+    return int(load_library().kda_chunk_fwd_workspace_size(_dt_of(in_dtype), B, T, H, K, V, N, int(packed)))
+
+
+def bwd_workspace_size(in_dtype, B: int, T: int, H: int, K: int, V: int, N: int, packed: bool) -> int:
+    """Device workspace bytes ``kda_recurrent_bwd`` needs."""
+    return int(load_library().kda_recurrent_bwd_workspace_size(_dt_of(in_dtype), B, T, H, K, V, N, int(packed)))
+
+
+def _workspace(nbytes: int, device, workspace):
+    """The caller's workspace tensor (checked), or a fresh uint8 one of nbytes."""
+    if workspace is None:
+        if nbytes == 0:
+            return None, 0
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, "
+                         f"the call needs {nbytes}")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def set_wait_limit(iterations: int = 0):
+    """Testing hook: polls before a bounded device-side wait of the tensor-core
+    prefill gives up (0 restores the default)."""
+    load_library().kda_set_wait_limit(int(iterations))
+
+
+def inject_wait_timeout(kernel: int):
+    """Testing hook: the next tensor-core prefill call on this thread makes the
+    first wait of its chunk-local (1) or state (2) kernel one that nothing
+    completes, so that it gives up and reports KDA_ERR_TIMEOUT."""
+    load_library().kda_inject_wait_timeout(int(kernel))
+
+
 def chunk_fwd(q, k, v, g, beta, scale: float | None = None, initial_state=None, cu_seqlens=None,
-              output_final_state: bool = True, o_dtype=torch.float32, o=None, final_state=None):
+              output_final_state: bool = True, o_dtype=torch.float32, o=None, final_state=None,
+              workspace=None, status=None):
     """Chunked KDA prefill.  q, k, g: [B,T,H,K]; v: [B,T,H,V]; beta: [B,T,H].
 
     Returns (o [B,T,H,V] in ``o_dtype``, final_state [N,H,K,V] fp32 or None).
     ``cu_seqlens`` (int32 [N+1], on the device) packs N sequences into B == 1.
     ``final_state`` may be the ``initial_state`` tensor itself (in-place update).
+    ``workspace``: a device tensor of at least :func:`workspace_size` bytes (a
+    fresh one from torch's allocator when None).  ``status``: an optional device
+    int32 tensor that receives the call's device-side status (0, or 6 =
+    KDA_ERR_TIMEOUT when a bounded wait gave up); read it after the stream work.
     """
     lib = load_library()
     B, T, H, K = q.shape
@@ -118,9 +171,12 @@ def chunk_fwd(q, k, v, g, beta, scale: float | None = None, initial_state=None, 
         o = torch.empty((B, T, H, V), dtype=o_dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _workspace(workspace_size(q.dtype, B, T, H, K, V, N, cu_seqlens is not None), q.device,
+                              workspace)
     st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q),
                            float(scale or 0.0), _ptr(initial_state), _ptr(cu_seqlens),
-                           B, T, H, K, V, N, _ptr(o), _dt(o), _ptr(final_state), _stream(q.device))
+                           B, T, H, K, V, N, _ptr(o), _dt(o), _ptr(final_state), _ptr(ws), ws_bytes,
+                           _ptr(status), _stream(q.device))
     _check("kda_chunk_fwd", st)
     return o, final_state
 
@@ -151,11 +207,12 @@ def chunk_fwd_fused(q_raw, k_raw, v_raw, gate_x, beta, conv_w, A_log, dt_bias,
                     scale: float | None = None, initial_state=None, cu_seqlens=None,
                     lower_bound: float = -5.0, l2_eps: float = 1e-6, conv_act: int = 0,
                     output_final_state: bool = True, o_dtype=torch.float32, o=None,
-                    final_state=None):
+                    final_state=None, workspace=None, status=None):
     """Chunked prefill with the fused prologue (short conv, L2-norm, gate).
 
     conv_w: a sequence (conv_q [H*K,4], conv_k [H*K,4], conv_v [H*V,4]) of fp32
-    tensors, or one [3, H*D, 4] tensor whose leading rows are used.
+    tensors, or one [3, H*D, 4] tensor whose leading rows are used.  ``workspace``
+    and ``status`` as for :func:`chunk_fwd`.
     """
     lib = load_library()
     B, T, H, K = q_raw.shape
@@ -171,11 +228,14 @@ def chunk_fwd_fused(q_raw, k_raw, v_raw, gate_x, beta, conv_w, A_log, dt_bias,
         o = torch.empty((B, T, H, V), dtype=o_dtype, device=q_raw.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q_raw.device)
+    ws, ws_bytes = _workspace(workspace_size(q_raw.dtype, B, T, H, K, V, N, cu_seqlens is not None),
+                              q_raw.device, workspace)
     st = lib.kda_chunk_fwd_fused(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(gate_x), _ptr(beta),
                                  _dt(q_raw), _ptr(cq), _ptr(ck), _ptr(cv), int(conv_act), _ptr(A_log),
                                  _ptr(dt_bias), float(lower_bound), float(l2_eps), float(scale or 0.0),
                                  _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(o),
-                                 _dt(o), _ptr(final_state), _stream(q_raw.device))
+                                 _dt(o), _ptr(final_state), _ptr(ws), ws_bytes, _ptr(status),
+                                 _stream(q_raw.device))
     _check("kda_chunk_fwd_fused", st)
     return o, final_state
 
@@ -269,10 +329,13 @@ def check_range(x, lo: float = -5.0, hi: float = 0.0, status=None, sync: bool = 
 
 
 def chunk_bwd(q, k, v, g, beta, dO, dS_T=None, scale: float | None = None, initial_state=None,
-              cu_seqlens=None):
+              cu_seqlens=None, workspace=None, status=None):
     """Gradients of <dO, o> + <dS_T, S_T> through :func:`chunk_fwd` (same shapes;
     dO fp32 [B,T,H,V], dS_T fp32 [N,H,K,V] or None).  Returns a dict of fp32
-    tensors dq, dk, dv, dg, dbeta and dS0 ([N,H,K,V])."""
+    tensors dq, dk, dv, dg, dbeta and dS0 ([N,H,K,V]).  ``workspace`` (at least
+    :func:`bwd_workspace_size` bytes) and ``status`` as for :func:`chunk_fwd`
+    (the status word reads 5 = KDA_ERR_RANGE when malformed offsets made the
+    call skip a sequence)."""
     lib = load_library()
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -285,9 +348,12 @@ def chunk_bwd(q, k, v, g, beta, dO, dS_T=None, scale: float | None = None, initi
            "dg": torch.empty((B, T, H, K), dtype=f32, device=dev),
            "dbeta": torch.empty((B, T, H), dtype=f32, device=dev),
            "dS0": torch.empty((N, H, K, V), dtype=f32, device=dev)}
+    ws, ws_bytes = _workspace(bwd_workspace_size(q.dtype, B, T, H, K, V, N, cu_seqlens is not None), dev,
+                              workspace)
     st = lib.kda_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q), float(scale or 0.0),
                                _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(dO), _ptr(dS_T),
                                _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
-                               _ptr(out["dbeta"]), _ptr(out["dS0"]), _stream(dev))
+                               _ptr(out["dbeta"]), _ptr(out["dS0"]), _ptr(ws), ws_bytes, _ptr(status),
+                               _stream(dev))
     _check("kda_recurrent_bwd", st)
     return out

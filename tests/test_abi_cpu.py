@@ -14,7 +14,8 @@ from kimi_delta_attention_chunk_gb300 import build as kbuild
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "kda.h")
 
-INVALID_ARG, UNSUPPORTED = 1, 2
+INVALID_ARG, UNSUPPORTED, WORKSPACE = 1, 2, 3
+SLOT = 147968  # workspace bytes per (chunk, head) of the tensor-core prefill
 
 
 def declared_symbols():
@@ -54,9 +55,13 @@ P = ctypes.c_void_p(0x10000)
 Pm = ctypes.c_void_p(0x10008)  # misaligned
 
 
+BIG_WS = ctypes.c_void_p(0x40000000)  # fake workspace address
+
+
 def chunk(lib, *, q=P, k=P, v=P, g=P, beta=P, dt=1, s0=None, cu=None, B=1, T=64, H=2, K=128, V=128,
-          N=1, o=P, odt=0, sT=None):
-    return lib.kda_chunk_fwd(q, k, v, g, beta, dt, 0.0, s0, cu, B, T, H, K, V, N, o, odt, sT, None)
+          N=1, o=P, odt=0, sT=None, ws=BIG_WS, ws_bytes=1 << 30, status=None):
+    return lib.kda_chunk_fwd(q, k, v, g, beta, dt, 0.0, s0, cu, B, T, H, K, V, N, o, odt, sT, ws, ws_bytes,
+                             status, None)
 
 
 def test_chunk_rejects_bad_arguments(lib):
@@ -72,6 +77,34 @@ def test_chunk_rejects_bad_arguments(lib):
     assert chunk(lib, B=2, N=1) == INVALID_ARG          # N must equal B without cu_seqlens
     assert chunk(lib, B=2, N=3, cu=P) == INVALID_ARG    # packed sequences need B == 1
     assert chunk(lib, s0=ctypes.c_void_p(0x100000), sT=ctypes.c_void_p(0x100000 + 4096)) == INVALID_ARG
+    assert chunk(lib, status=ctypes.c_void_p(0x10002)) == INVALID_ARG   # status word not 4-byte aligned
+    assert chunk(lib, ws=Pm) == INVALID_ARG                             # workspace not 16-byte aligned
+
+
+def test_workspace_size_formula(lib):
+    """The size query gives the documented formula: a 147968-byte slot per
+    64-token chunk and head, plus the packed-sequence bookkeeping rounded up to
+    1 KiB; the CUDA-core path (fp32 or a head size of 64) needs none."""
+    ws = lib.kda_chunk_fwd_workspace_size
+    assert ws(1, 1, 4096, 96, 128, 128, 1, 0) == 64 * 96 * SLOT
+    assert ws(1, 2, 333, 3, 128, 128, 2, 0) == 2 * 6 * 3 * SLOT
+    assert ws(1, 1, 0, 3, 128, 128, 1, 0) == 0
+    assert ws(1, 1, 64, 4, 128, 128, 0, 1) == 0        # N * H == 0
+    # packed: max_chunks = ceil(T / 64) + N, bookkeeping 4 * (2 N + 1 + max_chunks) bytes
+    T, N, H = 68645, 16, 96
+    mc = -(-T // 64) + N
+    hdr = -(-(4 * (2 * N + 1 + mc)) // 1024) * 1024
+    assert ws(1, 1, T, H, 128, 128, N, 1) == hdr + mc * H * SLOT
+    assert ws(0, 1, 4096, 96, 128, 128, 1, 0) == 0     # fp32 inputs: CUDA-core path
+    assert ws(1, 1, 4096, 96, 64, 128, 1, 0) == 0      # K = 64: CUDA-core path
+    assert ws(1, -1, 4096, 96, 128, 128, 1, 0) == 0    # invalid sizes
+
+
+def test_chunk_rejects_a_small_workspace_before_launching(lib):
+    need = lib.kda_chunk_fwd_workspace_size(1, 1, 64, 2, 128, 128, 1, 0)
+    assert need == 2 * SLOT
+    assert chunk(lib, ws_bytes=need - 1) == WORKSPACE
+    assert chunk(lib, ws=None, ws_bytes=0) == WORKSPACE
 
 
 def test_fused_rejects_bad_arguments(lib):
@@ -80,13 +113,14 @@ def test_fused_rejects_bad_arguments(lib):
         a.update(kw)
         return lib.kda_chunk_fwd_fused(P, P, P, P, P, 1, a["cq"], a["ck"], a["cv"], a["conv_act"], a["A"],
                                        a["db"], a["lb"], a["eps"], 0.0, None, None, 1, 64, 2, a["K"], 128, 1,
-                                       P, 0, None, None)
+                                       P, 0, None, a.get("ws", BIG_WS), a.get("wsb", 1 << 30), None, None)
     assert fused(conv_act=2) == INVALID_ARG
     assert fused(lb=1.0) == INVALID_ARG
     assert fused(eps=-1.0) == INVALID_ARG
     assert fused(A=None) == INVALID_ARG
     assert fused(cv=Pm) == INVALID_ARG
     assert fused(K=80) == UNSUPPORTED
+    assert fused(wsb=1000) == WORKSPACE
 
 
 def test_decode_rejects_bad_arguments(lib):
@@ -146,13 +180,18 @@ def test_backward_rejects_bad_arguments(lib):
         a = dict(dq=P, dO=P, K=128, dt=1, dbeta=P)
         a.update(kw)
         return lib.kda_recurrent_bwd(P, P, P, P, P, a["dt"], 0.0, None, None, 1, 64, 2, a["K"], 128, 1, a["dO"],
-                                     None, a["dq"], P, P, P, a["dbeta"], None, None)
+                                     None, a["dq"], P, P, P, a["dbeta"], None, a.get("ws", BIG_WS),
+                                     a.get("wsb", 1 << 30), a.get("st", None), None)
     assert bwd(K=96) == UNSUPPORTED
     assert bwd(dt=4) == UNSUPPORTED
     assert bwd(dO=None) == INVALID_ARG
     assert bwd(dq=None) == INVALID_ARG
     assert bwd(dq=Pm) == INVALID_ARG
     assert bwd(dbeta=ctypes.c_void_p(0x10002)) == INVALID_ARG
+    need = lib.kda_recurrent_bwd_workspace_size(1, 1, 64, 2, 128, 128, 1, 0)
+    assert need == 4 * 128 * 128 * (1 * 2 + 64 * 2)
+    assert bwd(wsb=need - 1) == WORKSPACE
+    assert bwd(st=ctypes.c_void_p(0x10001)) == INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -45,6 +45,26 @@ def test_prefill_4096_tokens_96_heads():
     assert eo <= TOL_BF16 and es <= TOL_BF16, (eo, es)
 
 
+def test_prefill_512_tokens_every_one_of_96_heads():
+    """Every head of a 96-head prefill against the oracle, element by element:
+    the persistent chunk-local kernel hands (chunk, head) tasks to CTAs by
+    chunk * H + h, so a mapping fault confined to some heads would show here
+    (8 chunks x 96 heads = 768 tasks: every CTA runs several)."""
+    inp = synth.direct_inputs(512, 96, 128, 128, torch.bfloat16, seed=11, init_state=True)
+    d = to_dev(inp)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    o, sT = kda.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                          initial_state=d["initial_state"], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, s_ref = oracle.kda_forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
+                                      initial_state=inp["initial_state"])
+    for h in range(96):
+        eo = rel_err(o[:, :, h].cpu(), o_ref[:, :, h])
+        es = rel_err(sT[:, h].cpu(), s_ref[:, h])
+        assert eo <= TOL_BF16 and es <= TOL_BF16, (h, eo, es)
+
+
 def test_varlen_16_sequences():
     inp = synth.workload_inputs("varlen")
     d = to_dev(inp)
