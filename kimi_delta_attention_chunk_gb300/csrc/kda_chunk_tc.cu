@@ -242,6 +242,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     float* itot_s = reinterpret_cast<float*>(smem + SM_ITOT);   // [2][128]
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
     float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][128], swizzled
+    float* pfx_s = reinterpret_cast<float*>(smem + SM_KST);     // [4][128] block-total products (passes 3-4,
+    float* sfx_s = pfx_s + 512;                                  //   in the image staging, free until pass 8)
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -500,7 +502,6 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_st_wait();
         }
         if (bt >= 0 && bt < C) beta_s[bt] = __uint_as_float((uint32_t)beta_r << 16);
-        if (tid == kIssueTid) tc::bulk_wait_read();  // last task's stores left the operand regions
         __syncthreads();
 
         if constexpr (FUSED) {
@@ -602,6 +603,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tc::tmem_st8(tm + lane_base(warp) + TL_LL + 16 * wg + 8 * h16, ll);
             }
         }
+        // the last task's bulk stores have read the image regions (Rt below, then the
+        // block-total tables and (q e^G)) before they are overwritten
+        if (tid == kIssueTid) tc::bulk_wait_read();
+        __syncthreads();
 #pragma unroll
         for (int R = 0; R < 2; ++R) {
             const int nrows = 32 * (R + 1);  // columns j of this block's products
@@ -682,8 +687,16 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_st8(tm + lane_base(warp) + TL_KTH + jb / 2, kh);
             tc::tmem_st8(tm + lane_base(warp) + TL_KTL + jb / 2, kl);
             if constexpr (!FUSED) tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vv);
-            if (tid < 128)
-                reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * tot_s[384 + c];
+            // per (block, channel): the totals of the blocks before it (prefix) and this
+            // block's total times those after it (suffix), read by pass (4)
+            {
+                const float t3v = tot_s[384 + c];
+                const float sfx = jblk == 0 ? t0v * t1v * t2v * t3v
+                                            : (jblk == 1 ? t1v * t2v * t3v : (jblk == 2 ? t2v * t3v : t3v));
+                pfx_s[jblk * 128 + c] = pf;
+                sfx_s[jblk * 128 + c] = sfx;
+                if (tid < 128) reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * t3v;
+            }
         }
         tc::tmem_st_wait();
 
@@ -697,22 +710,15 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const int item = tid + NT * kk;
                 const int r = ((item >> 7) << 3) | (item & 7);
                 const int J = r >> 4;
-                // products of the block totals before (pf) and after (sf) block J
-                float pf[8], sf[8], tj[8], t[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) { pf[u] = 1.f; sf[u] = 1.f; }
-                for (int J2 = 0; J2 < 4; ++J2) {
-                    ld_tot8(J2, 8 * cg, t);
-                    if (J2 == J) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) tj[u] = t[u];
-                    } else if (J2 < J) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) pf[u] *= t[u];
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) sf[u] *= t[u];
-                    }
+                // products of the block totals before block J (pf) and from it on (sf)
+                float pf[8], sf[8];
+                {
+                    const float4 a0 = *reinterpret_cast<const float4*>(pfx_s + J * 128 + 8 * cg);
+                    const float4 a1 = *reinterpret_cast<const float4*>(pfx_s + J * 128 + 8 * cg + 4);
+                    const float4 b0 = *reinterpret_cast<const float4*>(sfx_s + J * 128 + 8 * cg);
+                    const float4 b1 = *reinterpret_cast<const float4*>(sfx_s + J * 128 + 8 * cg + 4);
+                    pf[0] = a0.x; pf[1] = a0.y; pf[2] = a0.z; pf[3] = a0.w; pf[4] = a1.x; pf[5] = a1.y; pf[6] = a1.z; pf[7] = a1.w;
+                    sf[0] = b0.x; sf[1] = b0.y; sf[2] = b0.z; sf[3] = b0.w; sf[4] = b1.x; sf[5] = b1.y; sf[6] = b1.z; sf[7] = b1.w;
                 }
                 float q[8], k[8], pr[8], fq[8], fk[8];
                 ld8(true, r, 8 * cg, q);
@@ -721,7 +727,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     fq[u] = q[u] * (pf[u] * pr[u]);
-                    fk[u] = k[u] * (sf[u] * __fdividef(tj[u], pr[u]));
+                    fk[u] = k[u] * __fdividef(sf[u], pr[u]);
                 }
                 *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg)) = make_float4(fq[0], fq[1], fq[2], fq[3]);
                 *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg + 4)) = make_float4(fq[4], fq[5], fq[6], fq[7]);
