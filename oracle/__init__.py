@@ -34,6 +34,11 @@ with gcc into ``oracle/_build/libkda_oracle.so`` on first use.  Functions:
   q, k, v, g, beta and the initial state, by reverse mode through the same
   recurrence, token by token (pinned by central finite differences, the T=1
   closed forms and the adjoint identity of the map (v, S0) -> (o, S_T)).
+* :func:`gate_proj` -- the projections ahead of the gate, per token:
+  ``gate_x = f_b (f_a x)`` (the low-rank forget gate; its input to
+  :func:`gate`) and ``beta = sigmoid(b_proj x)`` ("kimi-k3-mlx" review,
+  "Attention is 93 layers ...": low-rank forget gate through f_a and f_b;
+  "The A_log shape mismatch ...": b_proj is [96, H]).
 * :func:`output_gate` -- the layer's output gate on o: per (token, head)
   ``o / sqrt(mean_v o^2 + eps) * w * sigmoid(gate)`` ("kimi-k3-mlx" review,
   "Attention is 93 layers ...": a full-rank output gate; "NeMo AutoModel
@@ -46,8 +51,11 @@ case, linearity in (v, S0), the Householder norm invariant, padding tokens,
 a hand-worked golden fixture, and library routines for the prologue
 (``numpy.convolve``, ``numpy.linalg.norm``, ``numpy.logaddexp``); for the output
 gate, degree-0 homogeneity in o, the sigmoid reflection, unit RMS of the normed
-rows, per-channel equivariance and the constant-row closed form.  No function
-here is "parity unpinned".
+rows, per-channel equivariance and the constant-row closed form; for the gate
+projections, the rank-1 outer-product closed form, brute-force sums on tiny
+shapes written as Python loops, beta = 1/2 for b_proj = 0, the sigmoid
+reflection, and linearity of gate_x in x.  No function here is "parity
+unpinned".
 """
 from __future__ import annotations
 
@@ -103,6 +111,9 @@ def _load():
             lib.kda_oracle_output_gate.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                                    ctypes.c_double, _dp]
             lib.kda_oracle_output_gate.restype = ctypes.c_int
+            lib.kda_oracle_gate_proj.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _dp, _dp]
+            lib.kda_oracle_gate_proj.restype = ctypes.c_int
             lib.kda_oracle_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64p, ctypes.c_int64,
                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                 ctypes.c_double, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
@@ -271,6 +282,29 @@ def output_gate(o, gate, weight=None, eps: float = 1e-6):
     if rc != 0:
         raise RuntimeError(f"kda_oracle_output_gate failed with status {rc}")
     return out
+
+
+def gate_proj(x, f_a, f_b, b_proj):
+    """The forget gate's input and beta from the layer input (plain fp64 loops):
+    per token, ``gate_x = f_b (f_a x)`` with the low-rank activation ``f_a x``
+    kept unrounded, and ``beta = sigmoid(b_proj x)``.
+
+    x: [..., D]; f_a [R, D]; f_b [HK, R]; b_proj [NH, D].  Returns float64
+    (gate_x [..., HK], beta [..., NH]).
+    """
+    x, fa, fb, bp = (_f64(a) for a in (x, f_a, f_b, b_proj))
+    D = x.shape[-1]
+    R, HK, NH = fa.shape[0], fb.shape[0], bp.shape[0]
+    if fa.shape != (R, D) or fb.shape != (HK, R) or bp.shape != (NH, D):
+        raise ValueError("f_a must be [R, D], f_b [HK, R] and b_proj [NH, D]")
+    rows = x.size // D
+    gx = np.zeros(x.shape[:-1] + (HK,))
+    beta = np.zeros(x.shape[:-1] + (NH,))
+    rc = _load().kda_oracle_gate_proj(_ptr(x), _ptr(fa), _ptr(fb), _ptr(bp), rows, D, R, HK, NH, _ptr(gx),
+                                      _ptr(beta))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_gate_proj failed with status {rc}")
+    return gx, beta
 
 
 def segment_transition(k, g, beta):

@@ -271,6 +271,53 @@ int kda_oracle_output_gate(const double *o, const double *gate, const double *w,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Projections ahead of the gate                                              */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The forget gate's input and beta from the layer input x ("kimi-k3-mlx"
+ * review, "Attention is 93 layers ...": a low-rank forget gate through f_a and
+ * f_b; "The A_log shape mismatch ...": b_proj is [96, H], H = 7168).  Per row
+ * (token) of x [rows, D]:
+ *
+ *     y       = f_a x                      f_a [R, D]   (the low-rank activation, kept in fp64)
+ *     gate_x  = f_b y                      f_b [HK, R]  (the input of the gate)
+ *     beta    = 1 / (1 + exp(-(b_proj x))) b_proj [NH, D]
+ *
+ * gate_x: [rows, HK], beta: [rows, NH].  Plain loops, one row at a time.
+ */
+int kda_oracle_gate_proj(const double *x, const double *f_a, const double *f_b, const double *b_proj,
+                         int64_t rows, int64_t D, int64_t R, int64_t HK, int64_t NH, double *gate_x,
+                         double *beta)
+{
+    if (!x || !f_a || !f_b || !b_proj || !gate_x || !beta || rows < 0 || D <= 0 || R <= 0 || HK <= 0 ||
+        NH <= 0)
+        return -1;
+    double *y = (double *)malloc((size_t)R * sizeof(double));
+    if (!y) return -2;
+    for (int64_t t = 0; t < rows; ++t) {
+        const double *xt = x + t * D;
+        for (int64_t i = 0; i < R; ++i) {
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += f_a[i * D + d] * xt[d];
+            y[i] = acc;
+        }
+        for (int64_t j = 0; j < HK; ++j) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < R; ++i) acc += f_b[j * R + i] * y[i];
+            gate_x[t * HK + j] = acc;
+        }
+        for (int64_t h = 0; h < NH; ++h) {
+            double z = 0.0;
+            for (int64_t d = 0; d < D; ++d) z += b_proj[h * D + d] * xt[d];
+            beta[t * NH + h] = 1.0 / (1.0 + exp(-z));
+        }
+    }
+    free(y);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Backward of the recurrence (reverse mode, token by token)                  */
 /* ------------------------------------------------------------------------- */
 

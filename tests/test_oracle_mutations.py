@@ -42,6 +42,11 @@ MUTATIONS = {
     "backward: dq from the pre-update state": ("(Sp[c * V + x] + kt[c] * delta[x]) * dot[x]",
                                                "Sp[c * V + x] * dot[x]"),
     "backward: dbeta without the erase": ("db += ddelta[x] * (vt[x] - kS[x]);", "db += ddelta[x] * vt[x];"),
+    "gate projection: f_b transposed": ("acc += f_b[j * R + i] * y[i];", "acc += f_b[i * HK + j] * y[i];"),
+    "gate projection: low-rank step skipped": ("acc += f_a[i * D + d] * xt[d];", "acc += xt[d];"),
+    "gate projection: b_proj transposed": ("z += b_proj[h * D + d] * xt[d];", "z += b_proj[d * NH + h] * xt[d];"),
+    "gate projection: sigmoid sign": ("beta[t * NH + h] = 1.0 / (1.0 + exp(-z));",
+                                      "beta[t * NH + h] = 1.0 / (1.0 + exp(z));"),
 }
 
 PINS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_") and n != "test_thread_count_does_not_change_results"]
@@ -65,7 +70,7 @@ def test_pins_catch_mutation(tmp_path, name, monkeypatch):
     real = oracle._load()
     mutant = ctypes.CDLL(so)
     for fn in ("kda_oracle_forward", "kda_oracle_short_conv", "kda_oracle_l2norm", "kda_oracle_gate",
-               "kda_oracle_output_gate", "kda_oracle_backward"):
+               "kda_oracle_output_gate", "kda_oracle_backward", "kda_oracle_gate_proj"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)

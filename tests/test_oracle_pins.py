@@ -529,3 +529,68 @@ def test_backward_packed_equals_separate():
         for key in ("dq", "dk", "dv", "dg", "dbeta"):
             np.testing.assert_allclose(gr[key][sl], one[key], rtol=1e-13, atol=1e-15)
         np.testing.assert_allclose(gr["dS0"][n], one["dS0"][0], rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- gate projections
+def _proj_inputs(rng, D, R, HK, NH, rows):
+    return (rng.standard_normal((rows, D)), rng.standard_normal((R, D)), rng.standard_normal((HK, R)),
+            rng.standard_normal((NH, D)))
+
+
+def test_gate_proj_rank_one_is_an_outer_product():
+    # f_a = a^T (one row), f_b = b (one column): gate_x_t = (a . x_t) b
+    rng = np.random.default_rng(31)
+    x, a, b, bp = _proj_inputs(rng, 7, 1, 6, 3, 4)
+    gx, _ = oracle.gate_proj(x, a, b, bp)
+    for t in range(4):
+        s = 0.0
+        for d in range(7):
+            s += a[0, d] * x[t, d]
+        for j in range(6):
+            assert abs(gx[t, j] - s * b[j, 0]) <= 1e-12 * (1.0 + abs(s * b[j, 0]))
+
+
+def test_gate_proj_brute_force_loops():
+    rng = np.random.default_rng(32)
+    D, R, HK, NH, rows = 5, 3, 4, 2, 3
+    x, fa, fb, bp = _proj_inputs(rng, D, R, HK, NH, rows)
+    gx, beta = oracle.gate_proj(x, fa, fb, bp)
+    for t in range(rows):
+        y = [sum(fa[i, d] * x[t, d] for d in range(D)) for i in range(R)]
+        for j in range(HK):
+            ref = sum(fb[j, i] * y[i] for i in range(R))
+            assert abs(gx[t, j] - ref) <= 1e-12 * (1.0 + abs(ref))
+        for h in range(NH):
+            z = sum(bp[h, d] * x[t, d] for d in range(D))
+            ref = np.exp(z) / (np.exp(z) + 1.0)   # the other form of the logistic function
+            assert abs(beta[t, h] - ref) <= 1e-14
+
+
+def test_gate_proj_beta_special_cases():
+    rng = np.random.default_rng(33)
+    x, fa, fb, bp = _proj_inputs(rng, 6, 2, 4, 3, 5)
+    _, half = oracle.gate_proj(x, fa, fb, np.zeros_like(bp))
+    assert np.all(half == 0.5)
+    _, b1 = oracle.gate_proj(x, fa, fb, bp)
+    _, b2 = oracle.gate_proj(x, fa, fb, -bp)
+    np.testing.assert_allclose(b1 + b2, 1.0, rtol=0, atol=1e-15)   # sigmoid(-z) = 1 - sigmoid(z)
+    assert np.all((b1 > 0.0) & (b1 < 1.0))
+
+
+def test_gate_proj_is_linear_in_x_and_row_local():
+    rng = np.random.default_rng(34)
+    x1, fa, fb, bp = _proj_inputs(rng, 6, 3, 5, 2, 4)
+    x2 = rng.standard_normal(x1.shape)
+    g1, _ = oracle.gate_proj(x1, fa, fb, bp)
+    g2, _ = oracle.gate_proj(x2, fa, fb, bp)
+    g12, _ = oracle.gate_proj(x1 + 2.5 * x2, fa, fb, bp)
+    np.testing.assert_allclose(g12, g1 + 2.5 * g2, rtol=1e-12, atol=1e-12)
+    perm = np.array([2, 0, 3, 1])
+    gp, bperm = oracle.gate_proj(x1[perm], fa, fb, bp)
+    _, b1 = oracle.gate_proj(x1, fa, fb, bp)
+    np.testing.assert_array_equal(gp, g1[perm])
+    np.testing.assert_array_equal(bperm, b1[perm])
+    # leading dimensions are rows: [B, T, D] -> [B, T, HK] and [B, T, NH]
+    g3, b3 = oracle.gate_proj(x1.reshape(2, 2, 6), fa, fb, bp)
+    assert g3.shape == (2, 2, 5) and b3.shape == (2, 2, 2)
+    np.testing.assert_array_equal(g3.reshape(4, 5), g1)
