@@ -463,6 +463,44 @@ def run_ours(args, world, rank, local):
                              "traffic": recorded_traffic("output_gate_kernel/prefill"), "algorithmic_bytes": og_bytes, "peak_kind": peak_kind}}
     del og_in, og_o, og_g, og_w, og_out
 
+    # ---- the projections ahead of the gate for the same 4096 tokens: x [4096, 7168]
+    # -> gate_x [4096, 96*128] and beta [4096, 96] (rank-128 f_a/f_b, b_proj)
+    GD, GR = 7168, 128
+    gp_in = {k: v.to(dev) for k, v in synth.gate_proj_inputs(1, T, GD, GR, H * K, H, 9 + 1000 * rank).items()}
+    gp_gx = torch.empty((1, T, H * K), dtype=torch.bfloat16, device=dev)
+    gp_beta = torch.empty((1, T, H), dtype=torch.bfloat16, device=dev)
+    gp_ws = torch.empty(kda.gate_proj_workspace_size(1, T, GR), dtype=torch.uint8, device=dev)
+    gp_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def gpstep():
+        kda.gate_proj(gp_in["x"], gp_in["f_a"], gp_in["f_b"], gp_in["b_proj"], gate_x=gp_gx, beta=gp_beta,
+                      workspace=gp_ws, status=gp_status)
+
+    for _ in range(max(3, args.warmup)):
+        gpstep()
+    torch.cuda.synchronize()
+    barrier(world)
+    gp_n = max(10, args.steps)
+    gp_ms, gpper = time_launches(gpstep, gp_n, stream)
+    if int(gp_status.item()) != 0:
+        raise RuntimeError(f"gate projection reported device status {int(gp_status.item())}")
+    gp_ms = max_over_ranks(gp_ms, world) / gp_n
+    gp_bytes = 2 * (T * GD + GR * GD + H * GD + H * K * GR + T * H * K + T * H)
+    gp_flops = 2 * T * (GD * (GR + H) + GR * H * K)
+    gp_call = sum(gpper) / len(gpper)
+    gp_ach = gp_bytes / (gp_call * 1e-3) / 1e9
+    gate_proj = {"value": world * T / (gp_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": gp_ms,
+                 "workload": "gate projections for the prefill's 4096 tokens: x [4096, 7168] bf16, rank-128 "
+                             "f_a/f_b to gate_x [4096, 96*128], b_proj + sigmoid to beta [4096, 96], bf16 out",
+                 "gpu_launches": 2 * gp_n,
+                 "tensor_tflops": gp_flops / (gp_call * 1e-3) / 1e12,
+                 "roofline": {"bound": "hbm", "achieved": gp_ach, "peak": hbm, "unit": "GB/s", "frac": gp_ach / hbm,
+                              "traffic": recorded_traffic("gate_proj/prefill"), "algorithmic_bytes": gp_bytes,
+                              "peak_kind": peak_kind,
+                              "note": "both kernels of one call; algorithmic bytes exclude the y round trip "
+                                      "through the workspace (4 MB)"}}
+    del gp_in, gp_gx, gp_beta, gp_ws
+
     # ---- the backward of the 4096-token prefill (token by token, fp32); a
     # failure here is reported in its own line and does not stop the others
     dO = torch.randn((1, T, H, V), generator=torch.Generator(device=dev).manual_seed(11 + rank), device=dev)
@@ -562,6 +600,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "decode": decode,
         "output_gate": out_gate,
+        "gate_proj": gate_proj,
         "backward": backward,
     }
     line.update(extra)
@@ -586,6 +625,11 @@ def profile_case(args):
         for _ in range(args.profile_reps):
             kda.chunk_fwd_fused(d["q_raw"], d["k_raw"], d["v_raw"], d["gate_x"], d["beta"], d["conv_w"],
                                 d["A_log"], d["dt_bias"], scale=d["scale"], initial_state=d["initial_state"])
+    elif args.profile_case == "gate_proj":
+        gp = {k: v.to(dev) for k, v in synth.gate_proj_inputs(1, args.profile_T, 7168, 128, args.profile_H * 128,
+                                                               args.profile_H, 9).items()}
+        for _ in range(args.profile_reps):
+            kda.gate_proj(gp["x"], gp["f_a"], gp["f_b"], gp["b_proj"])
     elif args.profile_case == "output_gate":
         og = synth.output_gate_inputs((1, args.profile_T, args.profile_H, 128), torch.bfloat16, 7)
         o, g, wt = (og[k].to(dev) for k in ("o", "gate", "weight"))
@@ -605,7 +649,7 @@ def profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode", "output_gate"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode", "output_gate", "gate_proj"], default=None,
                     help="run a few launches of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-T", type=int, default=2048)
     ap.add_argument("--profile-H", type=int, default=16)

@@ -305,6 +305,49 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
                            void *out, kda_dtype out_dtype, void *stream);
 
 /*
+ * kda_gate_proj -- the projections that produce kda_chunk_fwd_fused's gate_x
+ * and beta from the layer input ("kimi-k3-mlx" review, section "Attention is
+ * 93 layers ...": a low-rank forget gate through f_a and f_b; section "The
+ * A_log shape mismatch ...": b_proj is [96, H] with H = 7168 the model width).
+ * Per token t (a row of x):
+ *
+ *     y_t      = f_a x_t                   (fp32, not rounded to bf16)
+ *     gate_x_t = f_b y_t
+ *     beta_t   = 1 / (1 + exp(-(b_proj x_t)))
+ *
+ * Both GEMMs run on the tensor cores with fp32 accumulation; y is carried into
+ * the second as a bf16 pair (hi + lo) so that its rounding does not reach
+ * gate_x.  The pages give no rank for f_a/f_b; R = 128 (the head size) is the
+ * model's, R = 64 is also accepted.
+ *
+ *  x       [B, T, D] bf16, device.
+ *  f_a     [R, D] bf16;  f_b [HK, R] bf16;  b_proj [NH, D] bf16; device.
+ *  gate_x  [B, T, HK] bf16 out, device (HK = H * K: kda_chunk_fwd_fused's
+ *          gate_x [B, T, H, K]).
+ *  beta    [B, T, NH] bf16 out, device (NH = H: kda_chunk_fwd_fused's beta).
+ *  dtype   KDA_BF16 (anything else: KDA_ERR_UNSUPPORTED).
+ *  workspace   device, 16-byte aligned, at least kda_gate_proj_workspace_size
+ *          bytes (y between the two kernels); owned by the caller and in use
+ *          until the call's work on `stream` has completed.
+ *  status  optional device int32 (4-byte aligned): set to KDA_OK on the stream,
+ *          then to KDA_ERR_TIMEOUT if a bounded wait inside a kernel gave up
+ *          (the outputs are then incomplete).
+ *
+ * Sizes: B, T >= 0 with B * T < 2^31; D > 0 a multiple of 64; R in {64, 128};
+ * NH > 0 a multiple of 16 with R + NH <= 256; HK > 0 a multiple of 256.
+ * Every pointer 16-byte aligned.  Returns KDA_ERR_INVALID_ARG for null or
+ * misaligned pointers (with B * T > 0), negative sizes or outputs that overlap
+ * an input, the workspace or each other; KDA_ERR_UNSUPPORTED for sizes outside
+ * the set above; KDA_ERR_WORKSPACE for a workspace that is too small.  Nothing
+ * is launched when a check fails.  Stream-ordered on `stream`.
+ */
+KDA_API size_t kda_gate_proj_workspace_size(int B, int T, int R);
+KDA_API kda_status kda_gate_proj(const void *x, const void *f_a, const void *f_b, const void *b_proj,
+                                 kda_dtype dtype, int B, int T, int D, int R, int HK, int NH,
+                                 void *gate_x, void *beta, void *workspace, size_t workspace_bytes,
+                                 int32_t *status, void *stream);
+
+/*
  * kda_state_compose -- one step of the prefix over segment transitions, for
  * context-parallel prefill (the sequence split into consecutive segments, one
  * per rank).  The recurrence is affine in the state: over a segment,

@@ -16,6 +16,8 @@ from .kda import (  # noqa: F401
     chunk_fwd,
     chunk_fwd_fused,
     chunk_fwd_noalloc,
+    gate_proj,
+    gate_proj_workspace_size,
     inject_wait_timeout,
     library_path,
     load_library,

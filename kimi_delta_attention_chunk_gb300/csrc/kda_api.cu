@@ -237,6 +237,43 @@ kda_status kda_output_gate(const float* o, const void* gate, kda_dtype gate_dtyp
                                       (cudaStream_t)stream));
 }
 
+size_t kda_gate_proj_workspace_size(int B, int T, int R) {
+    if (B < 0 || T < 0 || (R != 64 && R != 128)) return 0;
+    return kda::gate_proj_workspace((int64_t)B * T, R);
+}
+
+kda_status kda_gate_proj(const void* x, const void* f_a, const void* f_b, const void* b_proj, kda_dtype dtype,
+                         int B, int T, int D, int R, int HK, int NH, void* gate_x, void* beta, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream) {
+    if (B < 0 || T < 0 || D <= 0 || R <= 0 || HK <= 0 || NH <= 0) return KDA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)B * T;
+    if (rows > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 || !kda::gate_proj_supported(D, R, HK, NH)) return KDA_ERR_UNSUPPORTED;
+    if (status != nullptr && ((uintptr_t)status % 4)) return KDA_ERR_INVALID_ARG;
+    if (rows > 0) {
+        const void* ptrs[] = {x, f_a, f_b, b_proj, gate_x, beta};
+        for (const void* p : ptrs)
+            if (!p || !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+        const size_t need = kda::gate_proj_workspace(rows, R);
+        if (workspace_bytes < need || workspace == nullptr) return KDA_ERR_WORKSPACE;
+        if (!kda_host::aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+        // the outputs and the workspace overlap nothing else
+        struct Span { const char* p; size_t n; };
+        const Span in[] = {{(const char*)x, (size_t)rows * D * 2}, {(const char*)f_a, (size_t)R * D * 2},
+                           {(const char*)f_b, (size_t)HK * R * 2}, {(const char*)b_proj, (size_t)NH * D * 2}};
+        const Span out[] = {{(const char*)gate_x, (size_t)rows * HK * 2}, {(const char*)beta, (size_t)rows * NH * 2},
+                            {(const char*)workspace, need}};
+        for (int i = 0; i < 3; ++i) {
+            for (const Span& a : in)
+                if (out[i].p < a.p + a.n && a.p < out[i].p + out[i].n) return KDA_ERR_INVALID_ARG;
+            for (int j = i + 1; j < 3; ++j)
+                if (out[i].p < out[j].p + out[j].n && out[j].p < out[i].p + out[i].n) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    return from_cuda(kda::gate_proj(x, f_a, f_b, b_proj, rows, D, R, HK, NH, gate_x, beta, workspace, status,
+                                    (cudaStream_t)stream));
+}
+
 kda_status kda_state_compose(const float* M, const float* S, const float* A, float* out, int H, int K, int V,
                              void* stream) {
     if (H < 0) return KDA_ERR_INVALID_ARG;

@@ -59,6 +59,8 @@ cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaS
 // Polls before a bounded device-side wait of the tensor-core prefill gives up
 // (0 = the default, about a second); read at each launch.
 void set_wait_limit(uint32_t iterations);
+// The current setting (0 = the default).
+uint32_t wait_limit();
 // Testing: the next tensor-core prefill call on this host thread makes the
 // first wait of its chunk-local (1) or state (2) kernel one on an mbarrier that
 // nothing arrives on, so that it gives up; the call consumes the setting.
@@ -77,6 +79,15 @@ cudaError_t decode_step(kda_dtype in_dt, kda_dtype out_dt, int K, int V, const v
 // Output gate: out = o / sqrt(mean_V(o^2) + eps) * w * sigmoid(gate), rows of V.
 cudaError_t output_gate(kda_dtype gate_dt, kda_dtype out_dt, int V, const float* o, const void* gate,
                         const float* w, float eps, int64_t rows, void* out, cudaStream_t st);
+
+// Projections ahead of the gate: gate_x = f_b (f_a x), beta = sigmoid(b_proj x),
+// bf16 in and out, y = f_a x kept in ws as a bf16 hi/lo pair (gate_proj_workspace
+// bytes).  status as for chunk_tc.
+bool gate_proj_supported(int D, int R, int HK, int NH);
+size_t gate_proj_workspace(int64_t rows, int R);
+cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const void* b_proj, int64_t rows, int D,
+                      int R, int HK, int NH, void* gate_x, void* beta, void* ws, int32_t* status,
+                      cudaStream_t st);
 
 // out[h] = M[h] S[h] + A[h] (A may be null or out), K x K times K x V, fp32.
 cudaError_t state_compose(const float* M, const float* S, const float* A, float* out, int H, int K, int V,

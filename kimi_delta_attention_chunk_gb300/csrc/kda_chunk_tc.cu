@@ -55,6 +55,7 @@
 namespace kda {
 
 std::atomic<uint32_t> g_wait_limit{0};
+uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 namespace {
 

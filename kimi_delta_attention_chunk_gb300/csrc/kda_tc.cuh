@@ -25,6 +25,21 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of
+// 128 bytes (64 bf16 along K) XOR-swizzled in 16-byte units by row mod 8, as a
+// TMA box with CU_TENSOR_MAP_SWIZZLE_128B lays them out; 8-row groups 1024 bytes
+// apart (SBO).  The tile must start on a 1024-byte boundary; within a row, K
+// advances by moving the start address (32 bytes per 16 elements).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;             // leading byte offset: not used with this swizzle
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 operands and fp32 accumulation.
 // b_mn: B operand stored MN-major (N contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool neg_a = false, bool b_mn = false) {
@@ -210,6 +225,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+// Tiled TMA store shared -> global (2D) in the calling thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a

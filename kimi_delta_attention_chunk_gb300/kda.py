@@ -42,6 +42,8 @@ SIGNATURES = {
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
+    "kda_gate_proj_workspace_size": (_sz, [_i, _i, _i]),
+    "kda_gate_proj": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _i32p, _vp]),
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
     "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
     "kda_recurrent_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
@@ -293,6 +295,39 @@ def output_gate(o, gate, weight=None, eps: float = 1e-6, out_dtype=torch.float32
                              _ptr(out), _dt(out), _stream(o.device))
     _check("kda_output_gate", st)
     return out
+
+
+def gate_proj_workspace_size(B: int, T: int, R: int) -> int:
+    """Device workspace bytes ``kda_gate_proj`` needs (y = f_a x between its kernels)."""
+    return int(load_library().kda_gate_proj_workspace_size(B, T, R))
+
+
+def gate_proj(x, f_a, f_b, b_proj, gate_x=None, beta=None, workspace=None, status=None):
+    """The projections ahead of the gate: ``gate_x = f_b (f_a x)`` and
+    ``beta = sigmoid(b_proj x)`` per token, bf16 in and out.
+
+    x: [B,T,D] (or [T,D]); f_a [R,D]; f_b [HK,R]; b_proj [NH,D].  Returns
+    (gate_x [B,T,HK], beta [B,T,NH]), the shapes ``chunk_fwd_fused`` takes as
+    [B,T,H,K] and [B,T,H].  ``workspace``/``status`` as for :func:`chunk_fwd`.
+    """
+    lib = load_library()
+    xs = x if x.dim() == 3 else x.unsqueeze(0)
+    B, T, D = xs.shape
+    R, HK, NH = f_a.shape[0], f_b.shape[0], b_proj.shape[0]
+    if tuple(f_a.shape) != (R, D) or tuple(f_b.shape) != (HK, R) or tuple(b_proj.shape) != (NH, D):
+        raise ValueError("f_a must be [R, D], f_b [HK, R] and b_proj [NH, D]")
+    for t in (f_a, f_b, b_proj):
+        if t.dtype != x.dtype:
+            raise TypeError("x, f_a, f_b and b_proj must share one dtype")
+    if gate_x is None:
+        gate_x = torch.empty((B, T, HK), dtype=x.dtype, device=x.device)
+    if beta is None:
+        beta = torch.empty((B, T, NH), dtype=x.dtype, device=x.device)
+    ws, ws_bytes = _workspace(gate_proj_workspace_size(B, T, R), x.device, workspace)
+    st = lib.kda_gate_proj(_ptr(xs), _ptr(f_a), _ptr(f_b), _ptr(b_proj), _dt(x), B, T, D, R, HK, NH,
+                           _ptr(gate_x), _ptr(beta), _ptr(ws), ws_bytes, _ptr(status), _stream(x.device))
+    _check("kda_gate_proj", st)
+    return gate_x, beta
 
 
 def state_compose(M, S, A=None, out=None):

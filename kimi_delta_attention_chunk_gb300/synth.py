@@ -243,3 +243,18 @@ def output_gate_inputs(shape, gate_dtype: torch.dtype, seed: int) -> dict:
     gate = rng.standard_normal(shape, dtype=np.float32)
     w = rng.uniform(0.5, 1.5, V).astype(np.float32)
     return {"o": _to(o, torch.float32), "gate": _to(gate, gate_dtype), "weight": _to(w, torch.float32)}
+
+
+def gate_proj_inputs(B: int, T: int, D: int, R: int, HK: int, NH: int, seed: int,
+                     dtype: torch.dtype = torch.bfloat16) -> dict:
+    """Inputs of the projections ahead of the gate: the layer input x [B,T,D] ~ N(0,1)
+    (a normalised hidden state) and weights drawn with fan-in scaling, f_a [R,D] and
+    b_proj [NH,D] ~ N(0, 1/D), f_b [HK,R] ~ N(0, 1/R), so that f_a x, f_b (f_a x) and
+    b_proj x all have unit variance.  Drawn in the order x, f_a, f_b, b_proj."""
+    rng = _rng(seed)
+    x = _normal(rng, (B * T, D), dtype).view(B, T, D)
+    f_a = _normal(rng, (R, D), dtype, std=D ** -0.5)
+    f_b = _normal(rng, (HK, R), dtype, std=R ** -0.5)
+    b_proj = _normal(rng, (NH, D), dtype, std=D ** -0.5)
+    return {"x": x, "f_a": f_a, "f_b": f_b, "b_proj": b_proj}
+

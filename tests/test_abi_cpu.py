@@ -194,6 +194,41 @@ def test_backward_rejects_bad_arguments(lib):
     assert bwd(st=ctypes.c_void_p(0x10001)) == INVALID_ARG
 
 
+def test_gate_proj_rejects_bad_arguments(lib):
+    # fake, disjoint, 16-byte aligned addresses (x [B*T, D], weights, outputs)
+    X, FA, FB, BP = (ctypes.c_void_p(a) for a in (0x10000000, 0x20000000, 0x30000000, 0x40000000))
+    GX, BE, WS = (ctypes.c_void_p(a) for a in (0x50000000, 0x60000000, 0x70000000))
+
+    def gp(**kw):
+        a = dict(x=X, fa=FA, fb=FB, bp=BP, dt=1, B=1, T=300, D=7168, R=128, HK=12288, NH=96, gx=GX, be=BE,
+                 ws=WS, wsb=1 << 30, st=None)
+        a.update(kw)
+        return lib.kda_gate_proj(a["x"], a["fa"], a["fb"], a["bp"], a["dt"], a["B"], a["T"], a["D"], a["R"],
+                                 a["HK"], a["NH"], a["gx"], a["be"], a["ws"], a["wsb"], a["st"], None)
+    need = lib.kda_gate_proj_workspace_size(1, 300, 128)
+    assert need == 300 * 128 * 2 * 2                      # y as bf16 hi and lo
+    assert lib.kda_gate_proj_workspace_size(1, 300, 96) == 0
+    assert gp(dt=0) == UNSUPPORTED                        # bf16 only
+    assert gp(D=7000) == UNSUPPORTED                      # D a multiple of 64
+    assert gp(R=96) == UNSUPPORTED
+    assert gp(NH=100) == UNSUPPORTED                      # NH a multiple of 16
+    assert gp(R=128, NH=144) == UNSUPPORTED               # R + NH > 256
+    assert gp(HK=12000) == UNSUPPORTED                    # HK a multiple of 256
+    assert gp(B=-1) == INVALID_ARG
+    assert gp(D=0) == INVALID_ARG
+    assert gp(B=1 << 16, T=1 << 16) == INVALID_ARG        # more than 2^31 - 1 tokens
+    assert gp(x=None) == INVALID_ARG
+    assert gp(fb=Pm) == INVALID_ARG
+    assert gp(be=ctypes.c_void_p(0x60000008)) == INVALID_ARG
+    assert gp(st=ctypes.c_void_p(0x10002)) == INVALID_ARG
+    assert gp(wsb=need - 1) == WORKSPACE
+    assert gp(ws=None) == WORKSPACE
+    assert gp(gx=ctypes.c_void_p(0x10000000 + 4096)) == INVALID_ARG   # gate_x over x
+    assert gp(be=ctypes.c_void_p(0x50000000 + 1024)) == INVALID_ARG   # beta over gate_x
+    assert gp(ws=ctypes.c_void_p(0x20000000)) == INVALID_ARG          # workspace over f_a
+    assert gp(T=0, x=None, gx=None, be=None, ws=None, wsb=0) == 0    # nothing to do
+
+
 def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16)
     b = torch.zeros(1, 64, 2, dtype=torch.bfloat16)
