@@ -17,9 +17,9 @@
 //   chunk_local_kernel   persistent, one (chunk, head) task at a time per CTA:
 //                        A, P, T, W, U~, Kbar = k e^{G_C - G}, scale (q e^G) and
 //                        e^{G_C}, written to a per-(chunk, head) workspace slot
-//                        (the MMA operands already in their shared-memory
-//                        layout, so the next kernel fetches them with bulk
-//                        copies)
+//                        straight from registers (the MMA operands already in
+//                        their shared-memory layout, so the next kernel fetches
+//                        them with bulk copies)
 //   chunk_state_kernel   one CTA per (sequence, head): the fp32 state lives in
 //                        tensor memory as S^T for the whole sequence; per chunk
 //                        [U^T | O^T] = [U~^T | 0] + S^T [-W | scale q e^G]^T,
@@ -65,12 +65,13 @@ constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TME
 constexpr uint32_t kWaitIter = 1u << 26;   // default poll count of a bounded wait, and of the exit drains
 
 // ---- workspace slot of one (chunk, head), written by the local kernel --------
-constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qs hi] (bf16) as one B operand, MN-major
-                                        //   (n = r for -W, n = 64 + r for Qs = scale q e^G; k = c)
+constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qs hi] (bf16) as one B operand, MN-major stored
+                                        //   n-group by n-group (n = r for -W, n = 64 + r for
+                                        //   Qs = scale q e^G; k = c): -W the first 16 KB, Qs the rest
 constexpr uint32_t SLOT_WQL = 32768;    // [-W lo | Qs lo], same layout
 constexpr uint32_t SLOT_EGC = 65536;    // e^{G_C} fp32 [128]
 constexpr uint32_t SLOT_IMG = 66048;    // bytes of the images above (one shared-memory copy)
-constexpr uint32_t SLOT_KH = 66048;     // Kbar hi as B operand, MN-major (n = c, k = r)
+constexpr uint32_t SLOT_KH = 66048;     // Kbar hi as B operand [128 c][64 r], K-major
 constexpr uint32_t SLOT_KL = 82432;     // Kbar lo
 constexpr uint32_t SLOT_P = 98816;      // scale P hi | lo, B operand [64 r][64 j] K-major
 constexpr uint32_t SLOT_KBP = 49152;    // bytes of Kbar and P (one shared-memory copy)
@@ -78,9 +79,6 @@ constexpr uint32_t SLOT_UT = 115200;    // U~ fp32 [64 r][128 v]
 constexpr uint32_t SLOT_BYTES = 147968;
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
-// (q e^G) fp32 [64 r][128 c] in shared memory: float4 column f of row r stored at
-// f ^ (r % 8), so both the row-blocked writes and the column reads are conflict-free
-__device__ __forceinline__ int qt_idx(int r, int c) { return r * 128 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
 
 // Work description shared by the kernels.  Sequences are either B dense rows
 // of T tokens (cu_seqlens == nullptr) or packed by cu_seqlens; chunks are
@@ -144,18 +142,14 @@ __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
 
 // ---- shared memory map (bytes) ----------------------------------------------
 constexpr uint32_t SM_STG = 0;             // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
-constexpr uint32_t SM_OPA = 65536;         // 64 KB: (q e^G) fp32 [64][128] (float4 columns
-constexpr uint32_t SM_QT = SM_OPA;         //   XOR-swizzled by row), later U~ staged for its store;
-constexpr uint32_t SM_KST = SM_OPA + 32768;//   the staged [-W | Qs hi] image
-constexpr uint32_t SM_OPB = 131072;        // 48 KB, A/P phase: Rt hi|lo (B op [96 j][128 c]); then
+constexpr uint32_t SM_OPB = 65536;         // 48 KB, A/P phase: Rt hi|lo (B op [96 j][128 c]); then
 constexpr uint32_t SM_TB = SM_OPB;         //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
-constexpr uint32_t SM_PB = SM_OPB + 16384; //   P hi|lo, B op [64 r][64 j] K-major
-constexpr uint32_t SM_PRE = 180224;        // fp32 [64][PRE_LD] in-block prefix products of e^g,
+constexpr uint32_t SM_PRE = 114688;        // fp32 [64][PRE_LD] in-block prefix products of e^g,
 constexpr int PRE_LD = 132;                //   later Diag(beta) A and T as fp32 [64][MAT_LD] each
 constexpr int MAT_LD = 68;
 constexpr uint32_t SM_AF = SM_PRE;
 constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
-constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 215040
+constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 149504
 // A/P operands of both row blocks R: L rows 64 R + i (i < 32: k rows, else q rows of
 // block R) in TMEM, Rt rows j (block 0, j < 32) and 32 + j (block 1, j < 64) in SM_OPB
 constexpr uint32_t RT_LO = 96 * D * 2;
@@ -188,9 +182,9 @@ constexpr uint32_t TL_VTL = 320;   // v^T lo (bf16 pairs), with the prologue (v 
 constexpr uint32_t TL_LH = 352;    // A/P A operand [L_0; L_1] hi (bf16 pairs) [128 i][64]
 constexpr uint32_t TL_LL = 416;    // its lo
 constexpr uint32_t TL_COLS = 512;
-// Thread that issues the bulk stores (and the first task's tile loads).  While warps
-// 0 and 1 (scheduler partitions 0 and 1) invert the diagonal blocks of T, the warps of
-// partitions 2 and 3, this one among them, issue the next task's tile loads.
+// Thread that issues the first task's tile loads and posts each next task's byte
+// count; it and the next 63 fetch beta.  (The next task's tile loads are spread over
+// lane 0 of the warps of scheduler partitions 2 and 3.)
 constexpr int kIssueTid = 320;
 
 // Input prologue ("kimi-k3-mlx" review: short convolution of kernel size 4 on
@@ -242,9 +236,6 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     float* tot_s = reinterpret_cast<float*>(smem + SM_TOT);     // [4][128]
     float* itot_s = reinterpret_cast<float*>(smem + SM_ITOT);   // [2][128]
     float* pre_s = reinterpret_cast<float*>(smem + SM_PRE);     // [64][PRE_LD]
-    float* qt_s = reinterpret_cast<float*>(smem + SM_QT);       // [64][128], swizzled
-    float* pfx_s = reinterpret_cast<float*>(smem + SM_KST);     // [4][128] block-total products (passes 3-4,
-    float* sfx_s = pfx_s + 512;                                  //   in the image staging, free until pass 8)
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -376,8 +367,6 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const int64_t next_task = task + gridDim.x;
         const Chunk nxt = decode_task(pl, next_task);
 
-        // (the previous task's bulk stores read only the operand regions, which are
-        // rewritten once they are done: see the wait before the A/P operands)
         if (wait_one(bar_tma, tma_phase)) tma_pending = false;
         if (failed) break;
         // the next task's byte count, posted long before its loads are issued (by
@@ -407,10 +396,15 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 for (int i = 0; i < 8; ++i) x[i] = 0.f;
             }
         };
-        // one channel of k
+        // one channel of k, of q
         auto ld_k = [&](int r, int c) {
             float x = ld_bf(ks, r, c);
             if constexpr (FUSED) x += ld_bf(gs, r, c);
+            return x;
+        };
+        auto ld_q = [&](int r, int c) {
+            float x = ld_bf(qs, r, c);
+            if constexpr (FUSED) x += ld_bf(vs, r, c);
             return x;
         };
         auto ld_pre8 = [&](int r, int c, float* x) {
@@ -604,8 +598,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 tc::tmem_st8(tm + lane_base(warp) + TL_LL + 16 * wg + 8 * h16, ll);
             }
         }
-        // the last task's bulk stores have read the image regions (Rt below, then the
-        // block-total tables and (q e^G)) before they are overwritten
+        // the last task's -W bulk stores have read the operand region before Rt overwrites it
         if (tid == kIssueTid) tc::bulk_wait_read();
         __syncthreads();
 #pragma unroll
@@ -662,81 +655,70 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tc::commit_w(bar_mma);
         }
-        // ---- (3) (k e^G)^T and v^T into TMEM (lane = channel / value column) and
-        //      e^{G_C} out, while the A/P MMAs run ---------------------------------
+        // ---- (3) per channel and 16-token block, while the A/P MMAs run: (k e^G)^T
+        //      and v^T into TMEM (lane = channel / value column); the slot's
+        //      Qs = scale q e^G (the second half of the merged image) and
+        //      Kbar = k e^{G_C - G} (K-major), hi|lo, and e^{G_C}, stored straight
+        //      from registers: a thread's 8 consecutive tokens of one channel are one
+        //      16-byte unit of both layouts, and a warp's 32 channels 512 (Qs) or four
+        //      runs of 128 (Kbar) contiguous bytes
         {
             const int c = (warp & 3) * 32 + lane;
-            const int jb = (warp >> 2) * 16;  // warpgroup w covers tokens [16 w, 16 w + 16)
-            const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c];
-            // product of the block totals before this warpgroup's 16-token block
-            const int jblk = warp >> 2;
+            const int jblk = warp >> 2, jb = 16 * jblk;  // warpgroup w covers tokens [16 w, 16 w + 16)
+            const float t0v = tot_s[c], t1v = tot_s[128 + c], t2v = tot_s[256 + c], t3v = tot_s[384 + c];
+            // products of the block totals before this block (pf) and from it on (sf)
             const float pf = jblk == 0 ? 1.f : (jblk == 1 ? t0v : (jblk == 2 ? t0v * t1v : t0v * t1v * t2v));
-            uint32_t kh[8], kl[8], vv[8];
+            const float sf = jblk == 0 ? t0v * t1v * t2v * t3v
+                                       : (jblk == 1 ? t1v * t2v * t3v : (jblk == 2 ? t2v * t3v : t3v));
+            // two halves of 8 tokens, each stored as soon as it is done
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = jb + 2 * i;
-                const float k0 = j < L ? ld_k(j, c) : 0.f;
-                const float k1 = j + 1 < L ? ld_k(j + 1, c) : 0.f;
-                tc::split2(k0 * pf * pre_s[j * PRE_LD + c], k1 * pf * pre_s[(j + 1) * PRE_LD + c], kh[i], kl[i]);
-                if constexpr (!FUSED) {
-                    const __nv_bfloat16 z = __float2bfloat16(0.f);
-                    const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
-                    const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
-                    vv[i] = tc::pack_bf16(v0, v1);
+            for (int h8 = 0; h8 < 2; ++h8) {
+                uint32_t kh[4], kl[4], vv[4];
+                float fq[8], fk[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = jb + 8 * h8 + 2 * i;
+                    const float p0 = pre_s[j * PRE_LD + c], p1 = pre_s[(j + 1) * PRE_LD + c];
+                    const float k0 = j < L ? ld_k(j, c) : 0.f;
+                    const float k1 = j + 1 < L ? ld_k(j + 1, c) : 0.f;
+                    const float q0 = j < L ? ld_q(j, c) : 0.f;
+                    const float q1 = j + 1 < L ? ld_q(j + 1, c) : 0.f;
+                    const float e0 = pf * p0, e1 = pf * p1;   // e^{G_j}, e^{G_{j+1}}
+                    tc::split2(k0 * e0, k1 * e1, kh[i], kl[i]);
+                    fq[2 * i] = q0 * (scale * e0);
+                    fq[2 * i + 1] = q1 * (scale * e1);
+                    fk[2 * i] = k0 * __fdividef(sf, p0);
+                    fk[2 * i + 1] = k1 * __fdividef(sf, p1);
+                    if constexpr (!FUSED) {
+                        const __nv_bfloat16 z = __float2bfloat16(0.f);
+                        const __nv_bfloat16 v0 = j < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j, c)) : z;
+                        const __nv_bfloat16 v1 = j + 1 < L ? *reinterpret_cast<const __nv_bfloat16*>(vs + tc::swz128(j + 1, c)) : z;
+                        vv[i] = tc::pack_bf16(v0, v1);
+                    }
                 }
+                uint4 hi, lo;
+                tc::split8(fq, hi, lo);
+                *reinterpret_cast<uint4*>(slot + SLOT_WQH + tc::mnmaj_ng(C + jb + 8 * h8, c, D)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_WQL + tc::mnmaj_ng(C + jb + 8 * h8, c, D)) = lo;
+                tc::split8(fk, hi, lo);
+                *reinterpret_cast<uint4*>(slot + SLOT_KH + tc::kmaj(c, jb + 8 * h8, C)) = hi;
+                *reinterpret_cast<uint4*>(slot + SLOT_KL + tc::kmaj(c, jb + 8 * h8, C)) = lo;
+                tc::tmem_st4(tm + lane_base(warp) + TL_KTH + jb / 2 + 4 * h8, kh);
+                tc::tmem_st4(tm + lane_base(warp) + TL_KTL + jb / 2 + 4 * h8, kl);
+                if constexpr (!FUSED) tc::tmem_st4(tm + lane_base(warp) + TL_VT + jb / 2 + 4 * h8, vv);
             }
-            tc::tmem_st8(tm + lane_base(warp) + TL_KTH + jb / 2, kh);
-            tc::tmem_st8(tm + lane_base(warp) + TL_KTL + jb / 2, kl);
-            if constexpr (!FUSED) tc::tmem_st8(tm + lane_base(warp) + TL_VT + jb / 2, vv);
-            // per (block, channel): the totals of the blocks before it (prefix) and this
-            // block's total times those after it (suffix), read by pass (4)
-            {
-                const float t3v = tot_s[384 + c];
-                const float sfx = jblk == 0 ? t0v * t1v * t2v * t3v
-                                            : (jblk == 1 ? t1v * t2v * t3v : (jblk == 2 ? t2v * t3v : t3v));
-                pfx_s[jblk * 128 + c] = pf;
-                sfx_s[jblk * 128 + c] = sfx;
-                if (tid < 128) reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * t3v;
-            }
+            if (tid < 128) reinterpret_cast<float*>(slot + SLOT_EGC)[c] = t0v * t1v * t2v * t3v;
         }
         tc::tmem_st_wait();
+        // (the staging tiles are consumed: the next task's loads may overwrite them)
+        tc::fence_async_smem();
 
         mma_sync();
         if (failed) break;
-
-        // ---- (4) (q e^G) fp32 into shared memory, Kbar = k e^{G_C - G} hi|lo out ----
-        {
-#pragma unroll 1
-            for (int kk = 0; kk < 2; ++kk) {
-                const int item = tid + NT * kk;
-                const int r = ((item >> 7) << 3) | (item & 7);
-                const int J = r >> 4;
-                // products of the block totals before block J (pf) and from it on (sf)
-                float pf[8], sf[8];
-                {
-                    const float4 a0 = *reinterpret_cast<const float4*>(pfx_s + J * 128 + 8 * cg);
-                    const float4 a1 = *reinterpret_cast<const float4*>(pfx_s + J * 128 + 8 * cg + 4);
-                    const float4 b0 = *reinterpret_cast<const float4*>(sfx_s + J * 128 + 8 * cg);
-                    const float4 b1 = *reinterpret_cast<const float4*>(sfx_s + J * 128 + 8 * cg + 4);
-                    pf[0] = a0.x; pf[1] = a0.y; pf[2] = a0.z; pf[3] = a0.w; pf[4] = a1.x; pf[5] = a1.y; pf[6] = a1.z; pf[7] = a1.w;
-                    sf[0] = b0.x; sf[1] = b0.y; sf[2] = b0.z; sf[3] = b0.w; sf[4] = b1.x; sf[5] = b1.y; sf[6] = b1.z; sf[7] = b1.w;
-                }
-                float q[8], k[8], pr[8], fq[8], fk[8];
-                ld8(true, r, 8 * cg, q);
-                ld8(false, r, 8 * cg, k);
-                ld_pre8(r, 8 * cg, pr);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    fq[u] = q[u] * (pf[u] * pr[u]);
-                    fk[u] = k[u] * __fdividef(sf[u], pr[u]);
-                }
-                *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg)) = make_float4(fq[0], fq[1], fq[2], fq[3]);
-                *reinterpret_cast<float4*>(qt_s + qt_idx(r, 8 * cg + 4)) = make_float4(fq[4], fq[5], fq[6], fq[7]);
-                uint4 hi, lo;
-                tc::split8(fk, hi, lo);
-                *reinterpret_cast<uint4*>(slot + SLOT_KH + tc::mnmaj(8 * cg, r, D)) = hi;
-                *reinterpret_cast<uint4*>(slot + SLOT_KL + tc::mnmaj(8 * cg, r, D)) = lo;
-            }
+        if (nxt.valid) {
+            issue_tma_spread(nxt);
+            beta_r = fetch_beta(nxt);
+            tma_pending = true;
         }
 
         // ---- (5) A/P out of TMEM: Diag(beta) A -> fp32, P -> hi/lo operand ---------
@@ -770,8 +752,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 if (is_q) {
                     uint4 hi, lo;
                     tc::split8(v, hi, lo);
-                    *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, j0 + 8 * g8, C)) = hi;
-                    *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, j0 + 8 * g8, C)) = lo;
+                    *reinterpret_cast<uint4*>(slot + SLOT_P + tc::kmaj(r, j0 + 8 * g8, C)) = hi;
+                    *reinterpret_cast<uint4*>(slot + SLOT_P + 8192 + tc::kmaj(r, j0 + 8 * g8, C)) = lo;
                 } else {
                     *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 8 * g8) = make_float4(v[0], v[1], v[2], v[3]);
                     *reinterpret_cast<float4*>(Af + r * MAT_LD + j0 + 8 * g8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
@@ -779,12 +761,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             // P rows of block 0 are zero in columns 32..63 (the P operand spans all 64)
             if (R == 0 && is_q) {
-                *reinterpret_cast<uint4*>(smem + SM_PB + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(smem + SM_PB + 8192 + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(slot + SLOT_P + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(slot + SLOT_P + 8192 + tc::kmaj(r, 32 + j0, C)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        // (the staging tiles are consumed)
-        tc::fence_async_smem();
         __syncthreads();
 
         // ---- (6) T = (I + Diag(beta) A)^{-1} ----------------------------------------
@@ -821,16 +801,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) T[(16 * blk + r) * MAT_LD + 16 * blk + col] = x[r];
-            } else if ((warp & 2) != 0) {
-                // scale P out; prefetch the next task into the consumed staging
-                if (tid == kIssueTid) {
-                    tc::bulk_store(slot + SLOT_P, smem + SM_PB, 16384);
-                    tc::bulk_commit();
-                }
-                if (nxt.valid) issue_tma_spread(nxt);
-                if (nxt.valid) beta_r = fetch_beta(nxt);
             }
-            if (nxt.valid) tma_pending = true;
             __syncthreads();
             // off-diagonal blocks, as two 32 x 32 halves T11 (tokens 0..31) and T22
             // (32..63): first the lower 16 x 16 block inside each half,
@@ -952,14 +923,12 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tc::commit_w(bar_mma);
         }
-        if (tid == kIssueTid) tc::bulk_wait_read();  // P has left its staging
         mma_sync();
         if (failed) break;
 
-        // ---- (8) -W and Qs = scale q e^G, hi|lo, staged as the two merged B images
-        //      (hi in the second half of the (q e^G) region, lo in the dead
-        //      T Diag(beta) / P region once P has left it); U~ fp32 staged over
-        //      (q e^G) once that is read --------------------------------------------
+        // ---- (8) -W hi|lo (the first half of the merged image) staged in the dead
+        //      operand region for two bulk stores; U~ fp32 [64 r][128 v] straight from
+        //      TMEM to the slot (a warp's 32 value columns are 128 contiguous bytes) --
         {
             const int x = (warp & 3) * 32 + lane;  // channel c of W^T, value column v of U~^T
             const int rb = (warp >> 2) * 16;
@@ -967,38 +936,25 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_ld16(tm + lane_base(warp) + TL_AW + rb, a);
             tc::tmem_ld16(tm + lane_base(warp) + TL_AU + rb, b);
             tc::tmem_ld_wait();
-            uint8_t* bh_s = smem + SM_KST;
-            uint8_t* bl_s = smem + SM_OPB;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
-                // -W (the 8 consecutive r of a core-matrix row)
-                float w[8], qs[8];
+                float w[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) w[u] = -__uint_as_float(a[8 * g8 + u]);
                 uint4 hi, lo;
                 tc::split8(w, hi, lo);
-                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) = hi;
-                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(rb + 8 * g8, x, 2 * C)) = lo;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) qs[u] = scale * qt_s[qt_idx(rb + 8 * g8 + u, x)];
-                tc::split8(qs, hi, lo);
-                *reinterpret_cast<uint4*>(bh_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = hi;
-                *reinterpret_cast<uint4*>(bl_s + tc::mnmaj(C + rb + 8 * g8, x, 2 * C)) = lo;
+                *reinterpret_cast<uint4*>(smem + SM_OPB + tc::mnmaj_ng(rb + 8 * g8, x, D)) = hi;
+                *reinterpret_cast<uint4*>(smem + SM_OPB + 16384 + tc::mnmaj_ng(rb + 8 * g8, x, D)) = lo;
             }
-            __syncthreads();
-            float* ut = reinterpret_cast<float*>(smem + SM_QT);
+            float* ut = reinterpret_cast<float*>(slot + SLOT_UT);
 #pragma unroll
             for (int i = 0; i < 16; ++i) ut[(rb + i) * D + x] = __uint_as_float(b[i]);
         }
         tc::fence_async_smem();
-        tc::fence_before();
         __syncthreads();
-        tc::fence_after();
         if (tid == kIssueTid) {
-            tc::bulk_store(slot + SLOT_UT, smem + SM_QT, 32768);
-            tc::bulk_commit();
-            tc::bulk_store(slot + SLOT_WQH, smem + SM_KST, 32768);
-            tc::bulk_store(slot + SLOT_WQL, smem + SM_OPB, 32768);
+            tc::bulk_store(slot + SLOT_WQH, smem + SM_OPB, 16384);
+            tc::bulk_store(slot + SLOT_WQL, smem + SM_OPB + 16384, 16384);
             tc::bulk_commit();
         }
 
@@ -1240,6 +1196,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
         }
         if (nchunks > 1) { issue_img(1); issued = 2; }
         const uint32_t id_n128_bmn = tc::idesc_bf16(128, 128, false, true);
+        const uint32_t id_n128 = tc::idesc_bf16(128, 128);
         const uint32_t id_n64 = tc::idesc_bf16(128, 64);
         bool ok = true;
         if (pl.inject == 2) ok = wait(bar_never, 0);
@@ -1254,11 +1211,11 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             const uint32_t img = tc::smem_u32(smem + (i & 1) * SLOT_IMG);
             // [U^T | O^T] = S^T [-W | Qs]^T with both operands split hi|lo:
             //   S_hi [-W hi | Qs hi] + S_lo [-W hi | Qs hi] + S_hi [-W lo | Qs lo]
-            const uint64_t bh = tc::sdesc(img + SLOT_WQH, 2 * C * 16, 128);
-            const uint64_t bl = tc::sdesc(img + SLOT_WQL, 2 * C * 16, 128);
+            const uint64_t bh = tc::sdesc(img + SLOT_WQH, 128, D * 16);
+            const uint64_t bl = tc::sdesc(img + SLOT_WQL, 128, D * 16);
 #pragma unroll
             for (int ks_ = 0; ks_ < D / 16; ++ks_) {
-                const uint32_t off = ks_ * 2 * 2 * C * 16;
+                const uint32_t off = ks_ * 256;
                 tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bh, off), id_n128_bmn, ks_ > 0);
                 tc::mma_ts_w(tm + TS_AU, tm + TS_SL + ks_ * 8, tc::dadv(bh, off), id_n128_bmn, 1);
                 tc::mma_ts_w(tm + TS_AU, tm + TS_SH + ks_ * 8, tc::dadv(bl, off), id_n128_bmn, 1);
@@ -1276,16 +1233,16 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
             if (!wait(bar_uready, par) || !wait(bar_kb, par)) { ok = false; break; }
             tc::fence_after();
             const uint32_t kb = tc::smem_u32(smem + SS_KB);
-            const uint64_t khd = tc::sdesc(kb, D * 16, 128), kld = tc::sdesc(kb + 16384, D * 16, 128);
+            const uint64_t khd = tc::sdesc(kb, 128, C * 16), kld = tc::sdesc(kb + 16384, 128, C * 16);
             const uint64_t phd = tc::sdesc(kb + (SLOT_P - SLOT_KH), 128, C * 16);
             const uint64_t pld = tc::sdesc(kb + (SLOT_P - SLOT_KH) + 8192, 128, C * 16);
 #pragma unroll
             for (int ks_ = 0; ks_ < C / 16; ++ks_) {
                 const uint32_t uh = tm + TS_UH + ks_ * 8, ul = tm + TS_UL + ks_ * 8;
-                const uint64_t bh2 = tc::dadv(khd, ks_ * 2 * D * 16), bl2 = tc::dadv(kld, ks_ * 2 * D * 16);
-                tc::mma_ts_w(tm + TS_S, uh, bh2, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TS_S, uh, bl2, id_n128_bmn, 1);
-                tc::mma_ts_w(tm + TS_S, ul, bh2, id_n128_bmn, 1);
+                const uint64_t bh2 = tc::dadv(khd, ks_ * 256), bl2 = tc::dadv(kld, ks_ * 256);
+                tc::mma_ts_w(tm + TS_S, uh, bh2, id_n128, 1);
+                tc::mma_ts_w(tm + TS_S, uh, bl2, id_n128, 1);
+                tc::mma_ts_w(tm + TS_S, ul, bh2, id_n128, 1);
             }
             tc::commit_w(bar_s);
 #pragma unroll

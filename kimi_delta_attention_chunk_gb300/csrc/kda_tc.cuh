@@ -142,6 +142,10 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]));
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- mbarriers -------------------------------------------------------------
@@ -286,6 +290,14 @@ __device__ __forceinline__ uint32_t kmaj(int row, int k, int Kd) {
 // SBO = 128 (next 8 n), LBO = Nd * 16 (next 8 k).
 __device__ __forceinline__ uint32_t mnmaj(int n, int k, int Nd) {
     return (uint32_t)((k >> 3) * (Nd * 16) + (n >> 3) * 128 + (k & 7) * 16 + (n & 7) * 2);
+}
+
+// Byte offset of element (n, k) in an MN-major, no-swizzle operand stored
+// n-group by n-group: the core matrices (8 k-rows of 8 consecutive n) of one
+// group of 8 n follow each other along K (LBO = 128), groups Kd * 16 bytes apart
+// (SBO), so any run of whole n-groups is one contiguous range.
+__device__ __forceinline__ uint32_t mnmaj_ng(int n, int k, int Kd) {
+    return (uint32_t)((n >> 3) * (Kd * 16) + (k >> 3) * 128 + (k & 7) * 16 + (n & 7) * 2);
 }
 
 // Element (r, c) of a [rows][128] bf16 tile loaded by TMA as two 64-column
