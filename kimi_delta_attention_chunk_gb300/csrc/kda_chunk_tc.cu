@@ -144,12 +144,12 @@ __device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
 constexpr uint32_t SM_STG = 0;             // 64 KB: q | k | v | g tiles, [64][128] bf16, 128B-swizzled halves
 constexpr uint32_t SM_OPB = 65536;         // 48 KB, A/P phase: Rt hi|lo (B op [96 j][128 c]); then
 constexpr uint32_t SM_TB = SM_OPB;         //   (T Diag beta) hi|lo, B op [64 r][64 j] K-major
-constexpr uint32_t SM_PRE = 114688;        // fp32 [64][PRE_LD] in-block prefix products of e^g,
-constexpr int PRE_LD = 132;                //   later Diag(beta) A and T as fp32 [64][MAT_LD] each
+constexpr uint32_t SM_PRE = 114688;        // fp32 [64][PRE_LD] in-block prefix products of e^g
+constexpr int PRE_LD = 132;
 constexpr int MAT_LD = 68;
-constexpr uint32_t SM_AF = SM_PRE;
-constexpr uint32_t SM_TF = SM_PRE + 64 * MAT_LD * 4;
-constexpr uint32_t SM_SMALL = SM_PRE + 64 * 2 * MAT_LD * 4;   // 149504
+constexpr uint32_t SM_AF = SM_PRE + 64 * PRE_LD * 4;   // Diag(beta) A, fp32 [64][MAT_LD]
+constexpr uint32_t SM_TF = SM_AF + 64 * MAT_LD * 4;    // T, fp32 [64][MAT_LD]
+constexpr uint32_t SM_SMALL = SM_TF + 64 * MAT_LD * 4;  // 183296
 // A/P operands of both row blocks R: L rows 64 R + i (i < 32: k rows, else q rows of
 // block R) in TMEM, Rt rows j (block 0, j < 32) and 32 + j (block 1, j < 64) in SM_OPB
 constexpr uint32_t RT_LO = 96 * D * 2;
@@ -166,7 +166,6 @@ constexpr uint32_t SM_DTB = SM_CONV + 6144;      // fp32 [128] this head's dt_bi
 constexpr uint32_t SM_ALOG = SM_DTB + 512;       // fp32 [128] A_log
 constexpr uint32_t SM_LOCAL_TOTAL_FUSED = SM_ALOG + 512;
 constexpr uint32_t PRO_TX = 6 * 384 + 6144 + 512 + 512;   // prologue bytes per task load
-static_assert(64 * PRE_LD * 4 <= 2 * 64 * MAT_LD * 4, "prefix array fits the A/T region");
 static_assert(SM_LOCAL_TOTAL + 1024 <= 232448, "shared memory");
 static_assert(SM_RED >= SM_LOCAL_TOTAL && SM_HALO % 128 == 0, "prologue regions");
 static_assert(SM_LOCAL_TOTAL_FUSED + 1024 <= 232448, "shared memory with the prologue");
@@ -350,6 +349,43 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         return b;
     };
 
+    // (1) for one (channel c, 16-token block J) of a task with Ln tokens: the in-block
+    // prefix products of e^g (1 past the sequence end) and the block total
+    auto prefix_item = [&](int c, int J, int Ln) {
+        const uint8_t* gs = smem + SM_STG + 49152;
+        auto g_at = [&](int r) {
+            return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gs + tc::swz128(r, c)));
+        };
+        float eg[16];
+        if constexpr (FUSED) {
+            // g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias)), in base 2:
+            //   g log2(e) = max(lower_bound log2(e), -exp(A_log) sp2(y)),  y = (gate_x + dt_bias) log2(e),
+            //   sp2(y) = log2(1 + 2^y) = max(y, 0) + log2(1 + 2^-|y|)
+            // (three special-function operations per element, no branch)
+            const float ea = __expf(reinterpret_cast<const float*>(smem + SM_ALOG)[c]);
+            const float db = reinterpret_cast<const float*>(smem + SM_DTB)[c];
+            const float lb2 = pro.lower_bound * kLog2e;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float y = (g_at(16 * J + u) + db) * kLog2e;
+                const float sp2 = fmaxf(y, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(y)));
+                eg[u] = 16 * J + u < Ln ? ex2_approx(fmaxf(lb2, -ea * sp2)) : 1.f;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) eg[u] = 16 * J + u < Ln ? __expf(g_at(16 * J + u)) : 1.f;
+        }
+        float run = 1.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            run *= eg[u];
+            pre_s[(16 * J + u) * PRE_LD + c] = run;
+        }
+        tot_s[J * 128 + c] = run;
+        if ((J & 1) == 0) itot_s[(J >> 1) * 128 + c] = __fdividef(1.f, run);
+    };
+    bool pre_done = false;  // the current task's prefix pass has run
+
     int64_t task = blockIdx.x;
     Chunk cur = decode_task(pl, task);
     unsigned short beta_r = 0;
@@ -367,8 +403,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const int64_t next_task = task + gridDim.x;
         const Chunk nxt = decode_task(pl, next_task);
 
-        if (wait_one(bar_tma, tma_phase)) tma_pending = false;
-        if (failed) break;
+        if (!pre_done) {
+            if (wait_one(bar_tma, tma_phase)) tma_pending = false;
+            if (failed) break;
+        }
         // the next task's byte count, posted long before its loads are issued (by
         // several threads, so none of them may complete the phase early)
         if (tid == kIssueTid && nxt.valid) tc::bar_expect_tx(bar_tma, 4u * 16384u + (FUSED ? PRO_TX : 0u));
@@ -440,37 +478,9 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             else return y;
         };
 
-        // ---- (1) in-block prefix products of e^g, block totals --------------------
-        {
-            const int c = tid & 127, J = tid >> 7;  // block J of channel c
-            float eg[16];  // e^g (1 past the sequence end)
-            if constexpr (FUSED) {
-                // g = max(lower_bound, -exp(A_log) softplus(gate_x + dt_bias)), in base 2:
-                //   g log2(e) = max(lower_bound log2(e), -exp(A_log) sp2(y)),  y = (gate_x + dt_bias) log2(e),
-                //   sp2(y) = log2(1 + 2^y) = max(y, 0) + log2(1 + 2^-|y|)
-                // (three special-function operations per element, no branch)
-                const float ea = __expf(reinterpret_cast<const float*>(smem + SM_ALOG)[c]);
-                const float db = reinterpret_cast<const float*>(smem + SM_DTB)[c];
-                const float lb2 = pro.lower_bound * kLog2e;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float y = (ld_bf(gs, 16 * J + u, c) + db) * kLog2e;
-                    const float sp2 = fmaxf(y, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(y)));
-                    eg[u] = 16 * J + u < L ? ex2_approx(fmaxf(lb2, -ea * sp2)) : 1.f;
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 16; ++u) eg[u] = 16 * J + u < L ? __expf(ld_bf(gs, 16 * J + u, c)) : 1.f;
-            }
-            float run = 1.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                run *= eg[u];
-                pre_s[(16 * J + u) * PRE_LD + c] = run;
-            }
-            tot_s[J * 128 + c] = run;
-            if ((J & 1) == 0) itot_s[(J >> 1) * 128 + c] = __fdividef(1.f, run);
-        }
+        // ---- (1) in-block prefix products of e^g, block totals (for the first task;
+        //      every later task's ran while the previous task inverted T) ----------
+        if (!pre_done) prefix_item(tid & 127, tid >> 7, L);
         if constexpr (FUSED) {
             // v = act(conv4(v_raw)): this thread's value column, 16 tokens, as hi|lo
             // pairs into TMEM (lane = value column)
@@ -767,10 +777,12 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         }
         __syncthreads();
 
-        // ---- (6) T = (I + Diag(beta) A)^{-1} ----------------------------------------
-        {
-            const float* N = reinterpret_cast<const float*>(smem + SM_AF);
-            float* T = reinterpret_cast<float*>(smem + SM_TF);
+        // ---- (6) T = (I + Diag(beta) A)^{-1} on warps 0..3 (named barrier 1), while
+        //      warps 4..15 wait for the next task's tiles and run its prefix pass ------
+        bool nxt_ok = true;
+        const float* N = reinterpret_cast<const float*>(smem + SM_AF);
+        float* T = reinterpret_cast<float*>(smem + SM_TF);
+        if (warp < 4) {
             float* Y = reinterpret_cast<float*>(smem + SM_TB);  // scratch: [2][16][16] then [32][32]
             // (blocks above the diagonal are never written; the operand build masks them)
             // diagonal blocks: one thread per column of each 16 x 16 block (warps 0, 1),
@@ -802,7 +814,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int r = 0; r < 16; ++r) T[(16 * blk + r) * MAT_LD + 16 * blk + col] = x[r];
             }
-            __syncthreads();
+            tc::named_sync(1, 128);
             // off-diagonal blocks, as two 32 x 32 halves T11 (tokens 0..31) and T22
             // (32..63): first the lower 16 x 16 block inside each half,
             //   T_{2p+1,2p} = -T_{2p+1,2p+1} (N_{2p+1,2p} T_{2p,2p}),   p = 0, 1,
@@ -811,7 +823,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 // one thread per (p, row a, 4 columns): 128 items
                 const int pp = tid >> 6, a = (tid >> 2) & 15, b4 = tid & 3;
                 const int R = 2 * pp + 1, J = 2 * pp;
-                if (tid < 128) {
+                {
                     const float* nrow = N + (16 * R + a) * MAT_LD + 16 * J;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -826,8 +838,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     }
                     *reinterpret_cast<float4*>(Y + (pp << 8) + (a << 4) + 4 * b4) = acc;
                 }
-                __syncthreads();
-                if (tid < 128) {
+                tc::named_sync(1, 128);
+                {
                     const float* trow = T + (16 * R + a) * MAT_LD + 16 * R;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -839,14 +851,14 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     *reinterpret_cast<float4*>(T + (16 * R + a) * MAT_LD + 16 * J + 4 * b4) =
                         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
-                __syncthreads();
+                tc::named_sync(1, 128);
             }
             {
                 // one thread per (rows a and a + 16, 4 columns) of a 32 x 32 block:
                 // 128 items, each loaded row serving two outputs
                 float* X = Y + 512;
                 const int a = tid >> 3, b4 = tid & 7;
-                if (tid < 128) {
+                {
                     const float* n0 = N + (32 + a) * MAT_LD;
                     const float* n1 = N + (48 + a) * MAT_LD;
                     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
@@ -865,8 +877,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     *reinterpret_cast<float4*>(X + a * 32 + 4 * b4) = acc0;
                     *reinterpret_cast<float4*>(X + (a + 16) * 32 + 4 * b4) = acc1;
                 }
-                __syncthreads();
-                if (tid < 128) {
+                tc::named_sync(1, 128);
+                {
                     // T22 is zero above its diagonal blocks: row a < 16 stops at column 16
                     const float* t0 = T + (32 + a) * MAT_LD + 32;
                     const float* t1 = T + (48 + a) * MAT_LD + 32;
@@ -887,8 +899,29 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     *reinterpret_cast<float4*>(T + (32 + a) * MAT_LD + 4 * b4) = make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w);
                     *reinterpret_cast<float4*>(T + (48 + a) * MAT_LD + 4 * b4) = make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w);
                 }
-                __syncthreads();
             }
+        } else if (nxt.valid) {
+            bool ok = true;
+            if (warp == 4) ok = tc::bar_wait(bar_tma, tma_phase, pl.wait_iter);
+            nxt_ok = !tc::named_any(2, NT - 128, !ok);
+            if (nxt_ok) {
+                tc::fence_after();
+                const int Ln = (nxt.eos - nxt.c0 < (int64_t)C) ? (int)(nxt.eos - nxt.c0) : C;
+                for (int item = tid - 128; item < 4 * 128; item += NT - 128) prefix_item(item & 127, item >> 7, Ln);
+            }
+        }
+        {
+            // join: T is complete, and the next task's tiles have landed (or a wait gave up)
+            const bool gave_up = __syncthreads_or(!nxt_ok) != 0;
+            if (nxt.valid && !gave_up) {
+                tma_phase ^= 1;
+                tma_pending = false;
+            }
+            failed = failed || gave_up;
+            pre_done = nxt.valid && !gave_up;
+            if (failed) break;
+        }
+        {
             // T Diag(beta) -> hi/lo B operand [64 r][64 j], K-major
             for (int item = tid; item < 64 * 8; item += NT) {
                 const int r = ((item >> 6) << 3) | (item & 7);
