@@ -317,8 +317,10 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
  *
  * Both GEMMs run on the tensor cores with fp32 accumulation; y is carried into
  * the second as a bf16 pair (hi + lo) so that its rounding does not reach
- * gate_x.  The pages give no rank for f_a/f_b; R = 128 (the head size) is the
- * model's, R = 64 is also accepted.
+ * gate_x.  The first GEMM is split along D into up to 8 ranges whose fp32
+ * partial sums are added in a fixed order, so results do not depend on
+ * scheduling.  The pages give no rank for f_a/f_b; R = 128 (the head size) is
+ * the model's, R = 64 is also accepted.
  *
  *  x       [B, T, D] bf16, device.
  *  f_a     [R, D] bf16;  f_b [HK, R] bf16;  b_proj [NH, D] bf16; device.
@@ -327,8 +329,11 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
  *  beta    [B, T, NH] bf16 out, device (NH = H: kda_chunk_fwd_fused's beta).
  *  dtype   KDA_BF16 (anything else: KDA_ERR_UNSUPPORTED).
  *  workspace   device, 16-byte aligned, at least kda_gate_proj_workspace_size
- *          bytes (y between the two kernels); owned by the caller and in use
- *          until the call's work on `stream` has completed.
+ *          bytes: y as bf16 hi and lo (4 R bytes per token) and the fp32 partial
+ *          sums of [f_a x | b_proj x] (4 S (R + NH) bytes per token, S the number of
+ *          ranges: min(8, D / 64, max(1, 128 / ceil(B T / 128))), made exact so that
+ *          none is empty); owned by the caller and in use until the call's work on
+ *          `stream` has completed.  0 for invalid sizes.
  *  status  optional device int32 (4-byte aligned): set to KDA_OK on the stream,
  *          then to KDA_ERR_TIMEOUT if a bounded wait inside a kernel gave up
  *          (the outputs are then incomplete).
@@ -341,7 +346,7 @@ KDA_API kda_status kda_output_gate(const float *o, const void *gate, kda_dtype g
  * the set above; KDA_ERR_WORKSPACE for a workspace that is too small.  Nothing
  * is launched when a check fails.  Stream-ordered on `stream`.
  */
-KDA_API size_t kda_gate_proj_workspace_size(int B, int T, int R);
+KDA_API size_t kda_gate_proj_workspace_size(int B, int T, int D, int R, int NH);
 KDA_API kda_status kda_gate_proj(const void *x, const void *f_a, const void *f_b, const void *b_proj,
                                  kda_dtype dtype, int B, int T, int D, int R, int HK, int NH,
                                  void *gate_x, void *beta, void *workspace, size_t workspace_bytes,

@@ -237,9 +237,9 @@ kda_status kda_output_gate(const float* o, const void* gate, kda_dtype gate_dtyp
                                       (cudaStream_t)stream));
 }
 
-size_t kda_gate_proj_workspace_size(int B, int T, int R) {
-    if (B < 0 || T < 0 || (R != 64 && R != 128)) return 0;
-    return kda::gate_proj_workspace((int64_t)B * T, R);
+size_t kda_gate_proj_workspace_size(int B, int T, int D, int R, int NH) {
+    if (B < 0 || T < 0 || (R != 64 && R != 128) || NH <= 0 || R + NH > 256) return 0;
+    return kda::gate_proj_workspace((int64_t)B * T, D, R, NH);
 }
 
 kda_status kda_gate_proj(const void* x, const void* f_a, const void* f_b, const void* b_proj, kda_dtype dtype,
@@ -254,7 +254,7 @@ kda_status kda_gate_proj(const void* x, const void* f_a, const void* f_b, const 
         const void* ptrs[] = {x, f_a, f_b, b_proj, gate_x, beta};
         for (const void* p : ptrs)
             if (!p || !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
-        const size_t need = kda::gate_proj_workspace(rows, R);
+        const size_t need = kda::gate_proj_workspace(rows, D, R, NH);
         if (workspace_bytes < need || workspace == nullptr) return KDA_ERR_WORKSPACE;
         if (!kda_host::aligned16(workspace)) return KDA_ERR_INVALID_ARG;
         // the outputs and the workspace overlap nothing else

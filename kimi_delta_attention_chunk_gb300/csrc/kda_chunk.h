@@ -81,10 +81,10 @@ cudaError_t output_gate(kda_dtype gate_dt, kda_dtype out_dt, int V, const float*
                         const float* w, float eps, int64_t rows, void* out, cudaStream_t st);
 
 // Projections ahead of the gate: gate_x = f_b (f_a x), beta = sigmoid(b_proj x),
-// bf16 in and out, y = f_a x kept in ws as a bf16 hi/lo pair (gate_proj_workspace
-// bytes).  status as for chunk_tc.
+// bf16 in and out; ws (gate_proj_workspace bytes) holds the split-K partial sums of
+// f_a x and b_proj x and y = f_a x as a bf16 hi/lo pair.  status as for chunk_tc.
 bool gate_proj_supported(int D, int R, int HK, int NH);
-size_t gate_proj_workspace(int64_t rows, int R);
+size_t gate_proj_workspace(int64_t rows, int D, int R, int NH);
 cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const void* b_proj, int64_t rows, int D,
                       int R, int HK, int NH, void* gate_x, void* beta, void* ws, int32_t* status,
                       cudaStream_t st);

@@ -42,7 +42,7 @@ SIGNATURES = {
     "kda_recurrent_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i, _i, _i, _i, _vp, _i,
                                 _vp]),
     "kda_output_gate": (_i, [_fp, _vp, _i, _fp, _f, _i, _i, _i, _i, _vp, _i, _vp]),
-    "kda_gate_proj_workspace_size": (_sz, [_i, _i, _i]),
+    "kda_gate_proj_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "kda_gate_proj": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _i32p, _vp]),
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
     "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
@@ -297,9 +297,10 @@ def output_gate(o, gate, weight=None, eps: float = 1e-6, out_dtype=torch.float32
     return out
 
 
-def gate_proj_workspace_size(B: int, T: int, R: int) -> int:
-    """Device workspace bytes ``kda_gate_proj`` needs (y = f_a x between its kernels)."""
-    return int(load_library().kda_gate_proj_workspace_size(B, T, R))
+def gate_proj_workspace_size(B: int, T: int, D: int, R: int, NH: int) -> int:
+    """Device workspace bytes ``kda_gate_proj`` needs (the split partial sums and
+    y = f_a x between its kernels)."""
+    return int(load_library().kda_gate_proj_workspace_size(B, T, D, R, NH))
 
 
 def gate_proj(x, f_a, f_b, b_proj, gate_x=None, beta=None, workspace=None, status=None):
@@ -323,7 +324,7 @@ def gate_proj(x, f_a, f_b, b_proj, gate_x=None, beta=None, workspace=None, statu
         gate_x = torch.empty((B, T, HK), dtype=x.dtype, device=x.device)
     if beta is None:
         beta = torch.empty((B, T, NH), dtype=x.dtype, device=x.device)
-    ws, ws_bytes = _workspace(gate_proj_workspace_size(B, T, R), x.device, workspace)
+    ws, ws_bytes = _workspace(gate_proj_workspace_size(B, T, D, R, NH), x.device, workspace)
     st = lib.kda_gate_proj(_ptr(xs), _ptr(f_a), _ptr(f_b), _ptr(b_proj), _dt(x), B, T, D, R, HK, NH,
                            _ptr(gate_x), _ptr(beta), _ptr(ws), ws_bytes, _ptr(status), _stream(x.device))
     _check("kda_gate_proj", st)

@@ -205,9 +205,13 @@ def test_gate_proj_rejects_bad_arguments(lib):
         a.update(kw)
         return lib.kda_gate_proj(a["x"], a["fa"], a["fb"], a["bp"], a["dt"], a["B"], a["T"], a["D"], a["R"],
                                  a["HK"], a["NH"], a["gx"], a["be"], a["ws"], a["wsb"], a["st"], None)
-    need = lib.kda_gate_proj_workspace_size(1, 300, 128)
-    assert need == 300 * 128 * 2 * 2                      # y as bf16 hi and lo
-    assert lib.kda_gate_proj_workspace_size(1, 300, 96) == 0
+    need = lib.kda_gate_proj_workspace_size(1, 300, 7168, 128, 96)
+    # y as bf16 hi and lo, and the fp32 partial sums of 8 ranges of D (3 tiles of 128 tokens)
+    assert need == 300 * 128 * 2 * 2 + 8 * 224 * 300 * 4
+    # 64 tiles: 2 ranges; D = 64: a single range
+    assert lib.kda_gate_proj_workspace_size(1, 8192, 7168, 128, 96) == 8192 * (512 + 2 * 224 * 4)
+    assert lib.kda_gate_proj_workspace_size(1, 300, 64, 128, 96) == 300 * (512 + 224 * 4)
+    assert lib.kda_gate_proj_workspace_size(1, 300, 7168, 96, 96) == 0
     assert gp(dt=0) == UNSUPPORTED                        # bf16 only
     assert gp(D=7000) == UNSUPPORTED                      # D a multiple of 64
     assert gp(R=96) == UNSUPPORTED
