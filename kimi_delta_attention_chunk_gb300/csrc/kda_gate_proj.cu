@@ -39,10 +39,12 @@ constexpr int GM = 128;            // tokens per tile (TMEM lanes)
 constexpr int GK = 64;             // K elements per 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kThreads = 192;      // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr int kThreadsFB = 320;    // the second product: warps 2..9 share the epilogue
 constexpr uint32_t kWaitDefault = 1u << 26;
 constexpr uint32_t kTileA = GM * GK * 2;   // 16 KB: [128 rows][64] bf16
 constexpr int kMaxSplit = 8;
 constexpr int GN2 = 128;           // channels per tile of the second product
+constexpr int kRingB = 3;          // f_b tiles in flight in the second product
 constexpr int kFinRows = 32;       // tokens per CTA of the finishing kernel
 constexpr int kFinCols = 16;       // columns of [y | z] per CTA of the finishing kernel
 constexpr int kThreadsFin = 256;
@@ -218,13 +220,13 @@ gate_proj_finish_kernel(const float* __restrict__ part, int S, int rows, int R, 
 
 // ---- gate_x = (y_hi + y_lo) f_b^T ----------------------------------------------------
 // One CTA: the 128-token tile blockIdx.x and the channel tiles [t0, t0 + nt) of GN2 each.
-// Shared memory: A hi | A lo ([128][R] each: R/64 swizzle atoms of 16 KB), a two-stage
-// ring of f_b tiles ([128][R]), two output stagings ([128][128] bf16 as two 16 KB atoms).
+// Shared memory: A hi | A lo ([128][R] each: R/64 swizzle atoms of 16 KB), a ring of
+// kRingB f_b tiles ([128][R]), two output stagings ([128][128] bf16 as two 16 KB atoms).
 __host__ __device__ __forceinline__ uint32_t fb_smem_bytes(int R) {
-    return (uint32_t)(R / GK) * kTileA * 2 + 2u * (uint32_t)(R / GK) * kTileA + 2u * 2u * kTileA;
+    return (uint32_t)(R / GK) * kTileA * 2 + (uint32_t)kRingB * (uint32_t)(R / GK) * kTileA + 2u * 2u * kTileA;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFB, 1)
 gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_constant__ CUtensorMap myl,
                     const __grid_constant__ CUtensorMap mfb, const __grid_constant__ CUtensorMap mout, int R,
                     int ntiles, int per_cta, int32_t* status, uint32_t wait_iter) {
@@ -234,16 +236,16 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
     const int na = R / GK;
     uint8_t* ah = smem;
     uint8_t* al = ah + na * kTileA;
-    uint8_t* bring = al + na * kTileA;              // [2 stages][na][16 KB]
-    uint8_t* ostg = bring + 2 * na * kTileA;        // [2][2 atoms][16 KB]
+    uint8_t* bring = al + na * kTileA;              // [kRingB stages][na][16 KB]
+    uint8_t* ostg = bring + kRingB * na * kTileA;   // [2][2 atoms][16 KB]
     uint64_t* a_full = reinterpret_cast<uint64_t*>(ostg + 4 * kTileA);
-    uint64_t* b_full = a_full + 1;    // [2]
-    uint64_t* b_empty = a_full + 3;   // [2]
-    uint64_t* t_full = a_full + 5;    // [2]
-    uint64_t* t_empty = a_full + 7;   // [2]
-    uint64_t* fin = a_full + 9;
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(a_full + 10);
-    volatile int* abort_s = reinterpret_cast<volatile int*>(a_full + 11);
+    uint64_t* b_full = a_full + 1;              // [kRingB]
+    uint64_t* b_empty = b_full + kRingB;        // [kRingB]
+    uint64_t* t_full = b_empty + kRingB;        // [2]
+    uint64_t* t_empty = t_full + 2;             // [2]
+    uint64_t* fin = t_empty + 2;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(fin + 2);
     const int m0 = blockIdx.x * GM;
     const int t0 = blockIdx.y * per_cta;
     const int nt = min(per_cta, ntiles - t0);   // >= 1: the host leaves no CTA empty
@@ -251,11 +253,13 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
     if (warp == 0) tc::tmem_alloc(tmem_base_s, 2 * GN2);
     if (tid == 0) {
         tc::bar_init(a_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kRingB; ++i) {
             tc::bar_init(b_full + i, 1);
             tc::bar_init(b_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             tc::bar_init(t_full + i, 1);
-            tc::bar_init(t_empty + i, 4);   // one arrival per epilogue warp
+            tc::bar_init(t_empty + i, 8);   // one arrival per epilogue warp
         }
         tc::bar_init(fin, 1);
         *abort_s = 0;
@@ -278,9 +282,9 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < nt; ++i) {
-                const int st = i & 1;
-                if (i >= 2) {
-                    ok = wait(b_empty + st, (uint32_t)(((i >> 1) - 1) & 1));
+                const int st = i % kRingB;
+                if (i >= kRingB) {
+                    ok = wait(b_empty + st, (uint32_t)(((i / kRingB) - 1) & 1));
                     if (!ok) break;
                 }
                 tc::bar_expect_tx(b_full + st, (uint32_t)na * kTileA);
@@ -291,8 +295,8 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
             if (!ok) report(status);
             // every load issued lands before the CTA exits
             tc::bar_wait(a_full, 0, kWaitDefault);
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                tc::bar_wait(b_full + (i & 1), (uint32_t)((i >> 1) & 1), kWaitDefault);
+            for (int i = issued > kRingB ? issued - kRingB : 0; i < issued; ++i)
+                tc::bar_wait(b_full + i % kRingB, (uint32_t)((i / kRingB) & 1), kWaitDefault);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -300,8 +304,8 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
         const uint32_t id = tc::idesc_bf16(GM, GN2);
         bool ok = wait(a_full, 0);
         for (int i = 0; ok && i < nt; ++i) {
-            const int b = i & 1;
-            ok = wait(b_full + b, (uint32_t)((i >> 1) & 1));
+            const int b = i & 1, st = i % kRingB;
+            ok = wait(b_full + st, (uint32_t)((i / kRingB) & 1));
             if (!ok) break;
             if (i >= 2) {
                 // the epilogue has read this accumulator's previous tile
@@ -311,7 +315,7 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
             tc::fence_after();
             const uint32_t d = tm + (uint32_t)(b * GN2);
             const uint32_t hb = tc::smem_u32(ah), lb = tc::smem_u32(al);
-            const uint32_t bb = tc::smem_u32(bring + b * na * kTileA);
+            const uint32_t bb = tc::smem_u32(bring + st * na * kTileA);
             for (int a = 0; a < na; ++a) {
 #pragma unroll
                 for (int kk = 0; kk < GK / 16; ++kk) {
@@ -321,7 +325,7 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
                     tc::mma_ss_w(d, tc::sdesc_sw128(lb + off), bd, id, 1);
                 }
             }
-            tc::commit_w(b_empty + b);   // the f_b stage is free once these MMAs are done
+            tc::commit_w(b_empty + st);  // the f_b stage is free once these MMAs are done
             tc::commit_w(t_full + b);    // and the accumulator is ready
         }
         if (!ok && lane == 0) report(status);
@@ -329,21 +333,24 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
         if (lane == 0) tc::bar_wait(fin, 0, kWaitDefault);   // every MMA issued has completed
         __syncwarp();
     } else {
-        // ---- epilogue: TMEM -> bf16 staging (128-byte swizzle) -> two TMA stores ---
-        const int et = tid - 64;                 // 0..127
+        // ---- epilogue: TMEM -> bf16 staging (128-byte swizzle) -> two TMA stores;
+        //      warp w reads TMEM lanes 32 (w % 4).. and the 64 columns of staging atom
+        //      (w - 2) / 4 ---------------------------------------------------------
+        const int et = tid - 64;                 // 0..255
         const int r = (warp & 3) * 32 + lane;    // the row this thread's TMEM lane holds
+        const int c0 = ((warp - 2) >> 2) * GK;
         for (int i = 0; i < nt; ++i) {
             const int b = i & 1;
             // staging b is free once the stores of tile i - 2 have read it
             if (et == 0) tc::bulk_wait_read_1();
             const bool ok = wait(t_full + b, (uint32_t)((i >> 1) & 1));
-            if (tc::named_any(1, 128, !ok)) {
+            if (tc::named_any(1, kThreadsFB - 64, !ok)) {
                 if (et == 0) report(status);
                 break;
             }
             tc::fence_after();
             uint8_t* stg = ostg + b * 2 * kTileA;
-            for (int c = 0; c < GN2; c += 16) {
+            for (int c = c0; c < c0 + GK; c += 16) {
                 uint32_t a[16];
                 tc::tmem_ld16(tm + lane_base(warp) + (uint32_t)(b * GN2 + c), a);
                 tc::tmem_ld_wait();
@@ -361,7 +368,7 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
             __syncwarp();
             if (lane == 0) tc::bar_arrive(t_empty + b);
             tc::fence_async_smem();
-            tc::named_sync(1, 128);
+            tc::named_sync(1, kThreadsFB - 64);
             if (et == 0) {
                 tc::tma_store_2d(&mout, stg, (t0 + i) * GN2, m0);
                 tc::tma_store_2d(&mout, stg + kTileA, (t0 + i) * GN2 + GK, m0);
@@ -491,9 +498,11 @@ cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const voi
         const int per_cta = (ntiles + ng - 1) / ng;
         ng = (ntiles + per_cta - 1) / per_cta;  // no CTA without a tile
         const int smem = (int)(fb_smem_bytes(R) + 128 + 1024);
+        static_assert(2 * 2 * kTileA + kRingB * 2 * kTileA + 2 * 2 * kTileA + 128 + 1024 <= 232448,
+                      "shared memory of the second product");
         e = cudaFuncSetAttribute(gate_proj_fb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        gate_proj_fb_kernel<<<dim3(mt, (unsigned)ng), kThreads, smem, st>>>(myh, myl, mfb, mout, R, ntiles, per_cta,
+        gate_proj_fb_kernel<<<dim3(mt, (unsigned)ng), kThreadsFB, smem, st>>>(myh, myl, mfb, mout, R, ntiles, per_cta,
                                                                             status, wait_iter);
         e = cudaGetLastError();
     }
