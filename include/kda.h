@@ -433,6 +433,39 @@ KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v
                              float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
                              void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
+/*
+ * kda_chunk_bwd -- the same gradients (of L = <dO, o> + <dS_T, S_T>), chunk by
+ * chunk (the backward of the chunked form in "ISEEKYAN/k3" README's chunked KDA
+ * forward; the per-channel decay of "kimi-k3-mlx" review, "The A_log shape
+ * mismatch ...").  For bf16 inputs with K = V = 128 it runs the tensor-core
+ * prefill once more, keeping the state that enters every 64-token chunk and the
+ * chunk's operands (W, q e^G, k e^{G_C - G}, P, U~, e^{G_C}), then carries the
+ * state gradient backwards chunk by chunk,
+ *
+ *     dU = scale P^T dO + Kb dS',   dS = scale (q e^G)^T dO + Diag(e^{G_C}) dS' - W^T dU,
+ *
+ * and forms every chunk's dq, dk, dv, dg, dbeta in parallel from (S, dU, dS', dO)
+ * (fp32 on the CUDA cores).  Other dtypes and head sizes take kda_recurrent_bwd.
+ *
+ * Arguments, outputs and rules as kda_recurrent_bwd.  The caller passes a device
+ * workspace of at least kda_chunk_bwd_workspace_size bytes (16-byte aligned): for
+ * the chunked path kda_chunk_fwd_workspace_size + 2 B T H V (o, bf16) + 4 slots
+ * (K V + K V + 64 V) with slots = max_chunks * H (the entering states, dS' and dU
+ * of every chunk), each part rounded up to 256 bytes; for the other sizes
+ * kda_recurrent_bwd_workspace_size.  status: optional device word, KDA_ERR_TIMEOUT
+ * if a bounded wait of the forward's kernels gave up (the gradients are then
+ * unspecified).
+ */
+KDA_API size_t kda_chunk_bwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N,
+                                            int packed);
+KDA_API kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g,
+                                 const void *beta, kda_dtype in_dtype, float scale,
+                                 const float *initial_state, const int32_t *cu_seqlens,
+                                 int B, int T, int H, int K, int V, int N, const float *dO,
+                                 const float *dS_T, float *dq, float *dk, float *dv, float *dg,
+                                 float *dbeta, float *dS0, void *workspace, size_t workspace_bytes,
+                                 int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

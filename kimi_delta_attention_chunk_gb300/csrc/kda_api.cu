@@ -338,4 +338,42 @@ kda_status kda_recurrent_bwd(const void* q, const void* k, const void* v, const 
                                         workspace, status, st));
 }
 
+size_t kda_chunk_bwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N, int packed) {
+    if (B < 0 || T < 0 || H <= 0 || N < 0 || !dtype_ok(in_dtype)) return 0;
+    if (!head_size_ok(K) || !head_size_ok(V)) return 0;
+    if (kda::chunk_bwd_supported(in_dtype, K, V)) return kda::chunk_bwd_workspace(B, T, H, N, packed != 0);
+    return kda::recurrent_bwd_workspace(B, T, H, K, V, N, packed != 0);
+}
+
+kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                         kda_dtype in_dtype, float scale, const float* initial_state, const int32_t* cu_seqlens,
+                         int B, int T, int H, int K, int V, int N, const float* dO, const float* dS_T, float* dq,
+                         float* dk, float* dv, float* dg, float* dbeta, float* dS0, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream) {
+    if (!kda::chunk_bwd_supported(in_dtype, K, V))
+        return kda_recurrent_bwd(q, k, v, g, beta, in_dtype, scale, initial_state, cu_seqlens, B, T, H, K, V, N, dO,
+                                 dS_T, dq, dk, dv, dg, dbeta, dS0, workspace, workspace_bytes, status, stream);
+    kda_status s = check_common(q, k, v, g, beta, in_dtype, initial_state, cu_seqlens, B, T, H, K, V, N,
+                                dO, KDA_F32, nullptr);
+    if (s != KDA_OK) return s;
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens && (!dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {dS_T, dq, dk, dv, dg, dS0};
+    for (const void* p : ptrs)
+        if (p && !kda_host::aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (dbeta && ((uintptr_t)dbeta % 4)) return KDA_ERR_INVALID_ARG;
+    if (status != nullptr && ((uintptr_t)status % 4)) return KDA_ERR_INVALID_ARG;
+    const size_t bytes = kda::chunk_bwd_workspace(B, T, H, N, cu_seqlens != nullptr);
+    if (workspace_bytes < bytes || (bytes > 0 && workspace == nullptr)) return KDA_ERR_WORKSPACE;
+    if (workspace != nullptr && !kda_host::aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+    kda::ChunkParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.scale = resolve_scale(scale, K);
+    p.initial_state = initial_state;
+    p.cu_seqlens = cu_seqlens;
+    p.B = B; p.T = T; p.H = H; p.N = N;
+    return from_cuda(kda::chunk_bwd(p, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace, workspace_bytes, status,
+                                    (cudaStream_t)stream));
+}
+
 }  // extern "C"

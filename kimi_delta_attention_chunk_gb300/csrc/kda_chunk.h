@@ -106,4 +106,13 @@ cudaError_t recurrent_bwd(kda_dtype in_dt, const void* q, const void* k, const v
                           int K, int V, int N, const float* dO, const float* dST, float* dq, float* dk, float* dv,
                           float* dg, float* dbeta, float* dS0, void* ws, int32_t* status, cudaStream_t st);
 
+// Chunked backward (bf16 inputs, K = V = 128) on the forward's per-chunk operands:
+// workspace bytes, and the launch (cudaErrorMemoryAllocation, before anything is
+// enqueued, if ws_bytes is too small); status as for chunk_tc.
+bool chunk_bwd_supported(kda_dtype in_dt, int K, int V);
+size_t chunk_bwd_workspace(int B, int T, int H, int N, bool packed);
+cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, float* dq, float* dk, float* dv,
+                      float* dg, float* dbeta, float* dS0, void* ws, size_t ws_bytes, int32_t* status,
+                      cudaStream_t st);
+
 }  // namespace kda

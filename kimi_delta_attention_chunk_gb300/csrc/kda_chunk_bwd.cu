@@ -1,0 +1,627 @@
+// Chunked backward of the KDA prefill (bf16 inputs, K = V = 128), built on the
+// forward's per-chunk operands.  Gradients of L = <dO, o> + <dS_T, S_T> with
+// respect to q, k, v, g, beta and the initial state.  Per chunk of C = 64
+// tokens with entering state S (the forward's chunk algebra: G the in-chunk
+// cumulative log-decay, X = k e^G, Xq = q e^G, Kb = k e^{G_C - G},
+// A = tril(X (k e^-G)^T, -1), P = tril(Xq (k e^-G)^T), T = (I + Diag(beta) A)^{-1},
+// W = T Diag(beta) X, U~ = T Diag(beta) v, U = U~ - W S,
+// O = scale (Xq S + P U), S' = Diag(e^{G_C}) S + Kb^T U), the reverse step from
+// the gradient dS' of S' is
+//
+//     dU = scale P^T dO + Kb dS'
+//     dS = scale Xq^T dO + Diag(e^{G_C}) dS' - W^T dU
+//
+// and the chunk's input gradients follow from (S, dU, dS', dO) alone:
+//
+//     dXq = scale dO S^T + dP Y,  dP = scale tril(dO U^T),  dKb = U dS'^T,  dW = -dU S^T
+//     dT = dW (Diag(beta) X)^T + dU (Diag(beta) v)^T,  dM = -T^T dT T^T,  dA = Diag(beta) tril(dM, -1)
+//     dbeta = rowsum(dM A) + rowsum((T^T dW) X) + rowsum((T^T dU) v),  dv = Diag(beta) T^T dU
+//     then the gated products back to k, q and G, and dg = the reverse cumulative sum of dG.
+//
+// Kernels, on the caller's stream:
+//   the forward (chunk_tc_forward_states): the tensor-core prefill, also writing the
+//       state entering every chunk; its workspace slots keep W, Qs = scale Xq, Kb,
+//       scale P, U~ and e^{G_C} per (chunk, head);
+//   bwd_chain_kernel: one CTA per (sequence, head) carries dS backwards through the
+//       chunks (the first two lines above, fp32 on the CUDA cores, operands read
+//       from the slots) and stores dS' and dU of every chunk;
+//   bwd_chunk_kernel: one CTA per (chunk, head) task forms dq, dk, dv, dg, dbeta.
+#include "kda_chunk.h"
+#include "kda_chunk_plan.cuh"
+#include "kda_common.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace {
+
+using namespace cplan;
+
+constexpr int kChainThreads = 512;
+constexpr int LDX = D + 4;   // fp32 rows of 128 values, padded
+constexpr int LDR = C + 4;   // fp32 rows of 64 values, padded
+
+// bf16 hi + lo at the same offset of two images -> 8 floats
+__device__ __forceinline__ void hilo8(const uint8_t* hi, const uint8_t* lo, float* x) {
+    float a[8], b[8];
+    tc::unpack8(*reinterpret_cast<const uint4*>(hi), a);
+    tc::unpack8(*reinterpret_cast<const uint4*>(lo), b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = a[i] + b[i];
+}
+
+// ---- reverse chain --------------------------------------------------------------
+// Shared memory (fp32): dSp [128][LDX] (the gradient of the state after the chunk),
+// dO, dU, Wn = -W, Qs [64][LDX] each (Qs over KbT once dU is formed), P [64][LDR],
+// KbT [128][LDR] (Kb transposed), e^{G_C} [128].
+constexpr uint32_t BC_DSP = 0;
+constexpr uint32_t BC_DO = BC_DSP + D * LDX * 4;
+constexpr uint32_t BC_DU = BC_DO + C * LDX * 4;
+constexpr uint32_t BC_WN = BC_DU + C * LDX * 4;
+constexpr uint32_t BC_P = BC_WN + C * LDX * 4;
+constexpr uint32_t BC_KB = BC_P + C * LDR * 4;   // KbT [128][LDR], later Qs [64][LDX]
+constexpr uint32_t BC_EGC = BC_KB + D * LDR * 4;
+constexpr uint32_t BC_TOTAL = BC_EGC + D * 4;
+static_assert(C * LDX <= D * LDR, "Qs fits the KbT region");
+static_assert(BC_TOTAL <= 232448, "shared memory of the chain kernel");
+
+__global__ void __launch_bounds__(kChainThreads, 1)
+bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __restrict__ dST,
+                 float* __restrict__ dS0, float* __restrict__ dsp_out, float* __restrict__ du_out) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float* dSp = reinterpret_cast<float*>(smem + BC_DSP);
+    float* dOs = reinterpret_cast<float*>(smem + BC_DO);
+    float* dUs = reinterpret_cast<float*>(smem + BC_DU);
+    float* Wn = reinterpret_cast<float*>(smem + BC_WN);
+    float* Ps = reinterpret_cast<float*>(smem + BC_P);
+    float* KbT = reinterpret_cast<float*>(smem + BC_KB);
+    float* Qs = KbT;
+    float* egc = reinterpret_cast<float*>(smem + BC_EGC);
+    const int tid = threadIdx.x;
+    const Chain chn = chain_of(pl, blockIdx.x);
+    const int H = pl.H, h = chn.h;
+    const int64_t sbase = ((int64_t)chn.n * H + h) * D * D;
+
+    for (int e = tid; e < D * D; e += kChainThreads)
+        dSp[(e >> 7) * LDX + (e & 127)] = dST != nullptr ? dST[sbase + e] : 0.f;
+
+    for (int64_t i = chn.nchunks - 1; i >= 0; --i) {
+        const int64_t c0 = chn.bos + i * C;
+        const int L = (chn.eos - c0 < (int64_t)C) ? (int)(chn.eos - c0) : C;
+        const int64_t task = (chn.g0 + i) * H + h;
+        const uint8_t* slot = pl.slots + task * (int64_t)SLOT_BYTES;
+        __syncthreads();   // the previous chunk's readers are done
+        // dO rows of the chunk (0 past the sequence end)
+        for (int f = tid; f < C * (D / 4); f += kChainThreads) {
+            const int r = f >> 5, x4 = (f & 31) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < L) v = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + x4);
+            *reinterpret_cast<float4*>(dOs + r * LDX + x4) = v;
+        }
+        // scale P [r][j] (K-major [64 r][64 j]): one 16-byte unit = 8 consecutive j of a row
+        for (int u = tid; u < C * 8; u += kChainThreads) {
+            const int r = ((u >> 6) << 3) | (u & 7), jg = (u >> 3) & 7;
+            float x[8];
+            hilo8(slot + SLOT_P + u * 16, slot + SLOT_P + 8192 + u * 16, x);
+            *reinterpret_cast<float4*>(Ps + r * LDR + 8 * jg) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(Ps + r * LDR + 8 * jg + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+        // Kb (K-major [128 c][64 r]): a unit = 8 consecutive r of a channel c -> KbT[c][r]
+        for (int u = tid; u < D * 8; u += kChainThreads) {
+            const int c = ((u >> 6) << 3) | (u & 7), rg = (u >> 3) & 7;
+            float x[8];
+            hilo8(slot + SLOT_KH + u * 16, slot + SLOT_KL + u * 16, x);
+            *reinterpret_cast<float4*>(KbT + c * LDR + 8 * rg) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(KbT + c * LDR + 8 * rg + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+        // -W (the first half of the merged image, n-group major: a unit = 8 consecutive
+        // rows r of a channel c)
+        for (int u = tid; u < 8 * D; u += kChainThreads) {
+            const int c = u & 127, ng = u >> 7;
+            float x[8];
+            hilo8(slot + SLOT_WQH + u * 16, slot + SLOT_WQL + u * 16, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Wn[(8 * ng + e) * LDX + c] = x[e];
+        }
+        if (tid < D) egc[tid] = reinterpret_cast<const float*>(slot + SLOT_EGC)[tid];
+        __syncthreads();
+
+        // the gradient of the state after this chunk, for the chunk's own gradients
+        {
+            float* dst = dsp_out + task * (int64_t)(D * D);
+            for (int f = tid; f < D * (D / 4); f += kChainThreads) {
+                const int c = f >> 5, x4 = (f & 31) * 4;
+                *reinterpret_cast<float4*>(dst + c * D + x4) = *reinterpret_cast<const float4*>(dSp + c * LDX + x4);
+            }
+        }
+        // dU = (scale P)^T dO + Kb dSp: rows 4 rg.., columns 4 cg..
+        {
+            const int rg = tid >> 5, cg = tid & 31;
+            float acc[4][4] = {};
+#pragma unroll 4
+            for (int j = 0; j < C; ++j) {
+                const float4 a = *reinterpret_cast<const float4*>(Ps + j * LDR + 4 * rg);
+                const float4 b = *reinterpret_cast<const float4*>(dOs + j * LDX + 4 * cg);
+                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[p][q] += av[p] * bv[q];
+            }
+#pragma unroll 4
+            for (int c = 0; c < D; ++c) {
+                const float4 a = *reinterpret_cast<const float4*>(KbT + c * LDR + 4 * rg);
+                const float4 b = *reinterpret_cast<const float4*>(dSp + c * LDX + 4 * cg);
+                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[p][q] += av[p] * bv[q];
+            }
+            float* gdu = du_out + task * (int64_t)(C * D);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float4 v = make_float4(acc[p][0], acc[p][1], acc[p][2], acc[p][3]);
+                *reinterpret_cast<float4*>(dUs + (4 * rg + p) * LDX + 4 * cg) = v;
+                *reinterpret_cast<float4*>(gdu + (4 * rg + p) * D + 4 * cg) = v;
+            }
+        }
+        __syncthreads();   // KbT is read; dU is complete
+        // Qs = scale Xq (the second half of the merged image) over KbT
+        for (int u = tid; u < 8 * D; u += kChainThreads) {
+            const int c = u & 127, ng = u >> 7;
+            float x[8];
+            hilo8(slot + SLOT_WQH + 16384 + u * 16, slot + SLOT_WQL + 16384 + u * 16, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Qs[(8 * ng + e) * LDX + c] = x[e];
+        }
+        __syncthreads();
+        // dSp <- Diag(e^{G_C}) dSp + Qs^T dO + (-W)^T dU: rows c = 4 rg.., columns x = 8 cg..
+        {
+            const int rg = tid >> 4, cg = tid & 15;
+            float acc[4][8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float e = egc[4 * rg + p];
+                const float4 s0 = *reinterpret_cast<const float4*>(dSp + (4 * rg + p) * LDX + 8 * cg);
+                const float4 s1 = *reinterpret_cast<const float4*>(dSp + (4 * rg + p) * LDX + 8 * cg + 4);
+                acc[p][0] = e * s0.x; acc[p][1] = e * s0.y; acc[p][2] = e * s0.z; acc[p][3] = e * s0.w;
+                acc[p][4] = e * s1.x; acc[p][5] = e * s1.y; acc[p][6] = e * s1.z; acc[p][7] = e * s1.w;
+            }
+#pragma unroll 2
+            for (int r = 0; r < C; ++r) {
+                const float4 a = *reinterpret_cast<const float4*>(Qs + r * LDX + 4 * rg);
+                const float4 b0 = *reinterpret_cast<const float4*>(dOs + r * LDX + 8 * cg);
+                const float4 b1 = *reinterpret_cast<const float4*>(dOs + r * LDX + 8 * cg + 4);
+                const float4 w = *reinterpret_cast<const float4*>(Wn + r * LDX + 4 * rg);
+                const float4 u0 = *reinterpret_cast<const float4*>(dUs + r * LDX + 8 * cg);
+                const float4 u1 = *reinterpret_cast<const float4*>(dUs + r * LDX + 8 * cg + 4);
+                const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w.x, w.y, w.z, w.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[p][q] += av[p] * bv[q] + wv[p] * uv[q];
+            }
+            // (each thread reads and writes only its own elements of dSp here)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                *reinterpret_cast<float4*>(dSp + (4 * rg + p) * LDX + 8 * cg) =
+                    make_float4(acc[p][0], acc[p][1], acc[p][2], acc[p][3]);
+                *reinterpret_cast<float4*>(dSp + (4 * rg + p) * LDX + 8 * cg + 4) =
+                    make_float4(acc[p][4], acc[p][5], acc[p][6], acc[p][7]);
+            }
+        }
+    }
+    __syncthreads();
+    if (dS0 != nullptr)
+        for (int e = tid; e < D * D; e += kChainThreads) dS0[sbase + e] = dSp[(e >> 7) * LDX + (e & 127)];
+}
+
+// ---- chunk-parallel gradients ------------------------------------------------------
+constexpr int kChunkThreads = 512;
+constexpr int kBwdCtas = 152;   // persistent CTAs of the chunk kernel (the workspace holds a scratch area for each)
+constexpr int MR = C * D;       // floats of a [64][128] matrix
+constexpr int MQ = C * C;       // floats of a [64][64] matrix
+// Per-CTA scratch (fp32, in the workspace; offsets in floats).  KRF holds, for each
+// 16-token row block b, k_j e^{G_m - G_j} (m = the token before block b; 0 for j
+// past block b).
+enum : int {
+    SC_K = 0, SC_Q = SC_K + MR, SC_V = SC_Q + MR, SC_DO = SC_V + MR, SC_WN = SC_DO + MR,
+    SC_PRE = SC_WN + MR, SC_EA = SC_PRE + MR, SC_KL = SC_EA + MR, SC_QL = SC_KL + MR,
+    SC_KRF = SC_QL + MR,
+    SC_U = SC_KRF + 4 * MR, SC_DXQ = SC_U + MR, SC_DW = SC_DXQ + MR, SC_DKB = SC_DW + MR,
+    SC_DBK = SC_DKB + MR, SC_DBV = SC_DBK + MR, SC_XB = SC_DBV + MR, SC_VB = SC_XB + MR,
+    SC_GB = SC_VB + MR, SC_GF = SC_GB + MR, SC_GC = SC_GF + MR, SC_PART = SC_GC + MR, SC_DG = SC_PART + MR,
+    SC_DP = SC_DG + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
+    SC_DM = SC_TMP + MQ, SC_DA = SC_DM + MQ,
+    SC_TOTAL = SC_DA + MQ
+};
+// shared memory of the chunk kernel: the GEMM staging area, then small vectors
+constexpr int GEMM_FLOATS = 128 * 68 + 4 * 128 * 68;   // the largest staging (the gated A product)
+constexpr uint32_t BK_TOT = GEMM_FLOATS * 4;            // tot [4][128]
+constexpr uint32_t BK_BETA = BK_TOT + 4 * D * 4;        // beta [64]
+constexpr uint32_t BK_DEC = BK_BETA + C * 4;            // dEC [128]
+constexpr uint32_t BK_EC = BK_DEC + D * 4;              // e^{G_C} [128]
+constexpr uint32_t BK_TOTAL = BK_EC + D * 4;
+static_assert(BK_TOTAL <= 232448, "shared memory of the chunk kernel");
+
+// C[M x N] (row-major, ldc) = alpha op(A) op(B) (+ C when acc), fp32, by the whole CTA:
+// op(A)(m, k) = A[m lda + k] (ta false) or A[k lda + m]; op(B)(k, n) = B[k ldb + n] (tb
+// false) or B[n ldb + k]; with bblk != 0 the B of the output rows [16 b, 16 b + 16) is
+// B + b bblk.  Both operands are staged in shared memory k-major; a thread computes 4 x 4
+// outputs.  The operands are in global memory (this CTA's scratch or the inputs).
+template <int M, int N, int K>
+__device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
+                                      bool tb, int bblk, float alpha, bool acc, float* sm) {
+    constexpr int LA = M + 4, LB = N + 4;
+    float* As = sm;
+    float* Bs = sm + K * LA;
+    const int nb = bblk != 0 ? M / 16 : 1;
+    const int tid = threadIdx.x;
+    __syncthreads();   // the previous readers of the staging area and writers of the operands are done
+    for (int i = tid; i < M * K; i += kChunkThreads) {
+        const int m = ta ? i % M : i / K, k = ta ? i / M : i % K;
+        As[k * LA + m] = ta ? A[(int64_t)k * lda + m] : A[(int64_t)m * lda + k];
+    }
+    for (int b = 0; b < nb; ++b) {
+        const float* Bb = B + (int64_t)b * bblk;
+        float* Bsb = Bs + b * K * LB;
+        for (int i = tid; i < K * N; i += kChunkThreads) {
+            const int k = tb ? i % K : i / N, n = tb ? i / K : i % N;
+            Bsb[k * LB + n] = tb ? Bb[(int64_t)n * ldb + k] : Bb[(int64_t)k * ldb + n];
+        }
+    }
+    __syncthreads();
+    constexpr int TN = N / 4;
+    for (int t = tid; t < (M / 4) * TN; t += kChunkThreads) {
+        const int tm = t / TN, tn = t % TN;
+        const float* Bsb = Bs + (bblk != 0 ? ((4 * tm) >> 4) * K * LB : 0);
+        float a4[4][4] = {};
+#pragma unroll 4
+        for (int k = 0; k < K; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(As + k * LA + 4 * tm);
+            const float4 b = *reinterpret_cast<const float4*>(Bsb + k * LB + 4 * tn);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a4[p][q] += av[p] * bv[q];
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float* cr = Cm + (int64_t)(4 * tm + p) * ldc + 4 * tn;
+            float4 v = make_float4(alpha * a4[p][0], alpha * a4[p][1], alpha * a4[p][2], alpha * a4[p][3]);
+            if (acc) {
+                const float4 o = *reinterpret_cast<const float4*>(cr);
+                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *reinterpret_cast<float4*>(cr) = v;
+        }
+    }
+    __syncthreads();   // C is complete
+}
+
+template <typename TIn>
+__device__ __forceinline__ float ld_in(const TIn* p) { return to_f32<TIn>(*p); }
+
+// One (chunk, head) task per CTA at a time: the chunk's dq, dk, dv, dg, dbeta from the
+// entering state S, the gradient dS' of the state after it, dU and dO, plus the
+// forward's W and U~ (slot), all in fp32.  Decay factors are formed per 16-token row
+// block from products over exactly the tokens they span (never e^{-G} alone).
+__global__ void __launch_bounds__(kChunkThreads, 1)
+bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                 const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+                 const __nv_bfloat16* __restrict__ beta, float scale, const float* __restrict__ dO,
+                 const float* __restrict__ states, const float* __restrict__ dsp, const float* __restrict__ du,
+                 float* __restrict__ scratch, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+                 float* __restrict__ dg, float* __restrict__ dbeta) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float* gsm = reinterpret_cast<float*>(smem);
+    float* tot = reinterpret_cast<float*>(smem + BK_TOT);
+    float* bs = reinterpret_cast<float*>(smem + BK_BETA);
+    float* dec = reinterpret_cast<float*>(smem + BK_DEC);
+    float* ec = reinterpret_cast<float*>(smem + BK_EC);
+    const int tid = threadIdx.x;
+    const int H = pl.H;
+    float* sc = scratch + (int64_t)blockIdx.x * SC_TOTAL;
+    float* K_ = sc + SC_K;
+    float* Q_ = sc + SC_Q;
+    float* V_ = sc + SC_V;
+    float* DO_ = sc + SC_DO;
+    float* WN = sc + SC_WN;
+    float* PRE = sc + SC_PRE;
+    float* EA = sc + SC_EA;
+    float* KL = sc + SC_KL;
+    float* QL = sc + SC_QL;
+    float* KRF = sc + SC_KRF;
+    float* U = sc + SC_U;
+    float* DXQ = sc + SC_DXQ;
+    float* DW = sc + SC_DW;
+    float* DKB = sc + SC_DKB;
+    float* DBK = sc + SC_DBK;
+    float* DBV = sc + SC_DBV;
+    float* XB = sc + SC_XB;
+    float* VB = sc + SC_VB;
+    float* GB = sc + SC_GB;
+    float* GF = sc + SC_GF;
+    float* GC = sc + SC_GC;
+    float* PART = sc + SC_PART;
+    float* DGm = sc + SC_DG;
+    float* DP = sc + SC_DP;
+    float* Am = sc + SC_A;
+    float* Tm = sc + SC_T;
+    float* DT = sc + SC_DT;
+    float* TMP = sc + SC_TMP;
+    float* DM = sc + SC_DM;
+    float* DA = sc + SC_DA;
+    const int64_t ntasks = pl.max_chunks * H;
+
+    for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
+        const Chunk ch = decode_task(pl, task);
+        if (!ch.valid) continue;
+        const int h = ch.h;
+        const int64_t c0 = ch.c0;
+        const int L = (ch.eos - c0 < (int64_t)C) ? (int)(ch.eos - c0) : C;
+        const uint8_t* slot = pl.slots + task * (int64_t)SLOT_BYTES;
+        const float* S = states + task * (int64_t)(D * D);
+        const float* DSP = dsp + task * (int64_t)(D * D);
+        const float* DU = du + task * (int64_t)(C * D);
+        __syncthreads();   // the previous task is done with the scratch
+
+        // ---- inputs (0 past the sequence end), prefix products, -W, U~ -----------------
+        for (int e = tid; e < MR; e += kChunkThreads) {
+            const int r = e >> 7, c = e & 127;
+            const bool ok = r < L;
+            const int64_t ti = ((c0 + r) * H + h) * D + c;
+            K_[e] = ok ? ld_in(k + ti) : 0.f;
+            Q_[e] = ok ? ld_in(q + ti) : 0.f;
+            V_[e] = ok ? ld_in(v + ti) : 0.f;
+            DO_[e] = ok ? dO[ti] : 0.f;
+            U[e] = reinterpret_cast<const float*>(slot + SLOT_UT)[e];
+        }
+        if (tid < C) bs[tid] = tid < L ? ld_in(beta + (c0 + tid) * H + h) : 0.f;
+        {
+            const int c = tid & 127, J = tid >> 7;
+            float run = 1.f;
+            for (int u = 0; u < 16; ++u) {
+                const int r = 16 * J + u;
+                const float eg = r < L ? __expf(ld_in(g + ((c0 + r) * H + h) * D + c)) : 1.f;
+                run *= eg;
+                PRE[r * D + c] = run;
+            }
+            tot[J * D + c] = run;
+        }
+        for (int u = tid; u < 8 * D; u += kChunkThreads) {
+            const int c = u & 127, ng = u >> 7;
+            float x[8];
+            hilo8(slot + SLOT_WQH + u * 16, slot + SLOT_WQL + u * 16, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) WN[(8 * ng + e) * D + c] = x[e];
+        }
+        __syncthreads();
+        if (tid < D) ec[tid] = tot[tid] * tot[D + tid] * tot[2 * D + tid] * tot[3 * D + tid];
+        // derived operands
+        for (int e = tid; e < MR; e += kChunkThreads) {
+            const int r = e >> 7, c = e & 127, B = r >> 4;
+            const float pr = PRE[e];
+            float before = 1.f;
+            for (int b = 0; b < B; ++b) before *= tot[b * D + c];
+            const float ea = before * pr;   // e^{G_r}
+            EA[e] = ea;
+            KL[e] = K_[e] * pr;
+            QL[e] = Q_[e] * pr;
+            XB[e] = bs[r] * K_[e] * ea;
+            VB[e] = bs[r] * V_[e];
+            // k_r e^{G_m(b) - G_r} for the row blocks b >= B (0 for b < B)
+            float f = 1.f / pr;   // within its own block
+            for (int b = 0; b < 4; ++b) {
+                float val = 0.f;
+                if (b == B) {
+                    val = f;
+                } else if (b > B) {
+                    float t = tot[B * D + c] / pr;
+                    for (int b2 = B + 1; b2 < b; ++b2) t *= tot[b2 * D + c];
+                    val = t;
+                }
+                KRF[b * MR + e] = K_[e] * val;
+            }
+        }
+
+        // ---- the products with S, dS', U ----------------------------------------------------
+        cta_gemm<C, D, D>(U, D, WN, D, false, S, D, false, 0, 1.f, true, gsm);        // U = U~ - W S
+        cta_gemm<C, D, D>(DXQ, D, DO_, D, false, S, D, true, 0, scale, false, gsm);   // scale dO S^T
+        cta_gemm<C, D, D>(DW, D, DU, D, false, S, D, true, 0, -1.f, false, gsm);      // -dU S^T
+        cta_gemm<C, D, D>(DKB, D, U, D, false, DSP, D, true, 0, 1.f, false, gsm);     // U dS'^T
+        cta_gemm<C, C, D>(DP, C, DO_, D, false, U, D, true, 0, scale, false, gsm);    // scale dO U^T
+        {
+            // dEC[c] = sum_x dS'[c][x] S[c][x]: four threads per channel
+            const int c = tid >> 2, part = tid & 3;
+            float a = 0.f;
+            for (int x = part * 32; x < part * 32 + 32; ++x) a += DSP[c * D + x] * S[c * D + x];
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            if (part == 0) dec[c] = a;
+        }
+        // A: the gated k k^T product per row block (strictly lower)
+        cta_gemm<C, C, D>(Am, C, KL, D, false, KRF, D, true, MR, 1.f, false, gsm);
+        for (int e = tid; e < MQ; e += kChunkThreads) {
+            const int r = e >> 6, j = e & 63;
+            if (j >= r) Am[e] = 0.f;
+            if (j > r) DP[e] = 0.f;
+        }
+        __syncthreads();
+        // T = (I + Diag(beta) A)^{-1}: eight threads per column, rows in order
+        {
+            const int j = tid >> 3, part = tid & 7;
+            for (int r = 0; r < C; ++r) {
+                float a = 0.f;
+                for (int i = j + part; i < r; i += 8) a += bs[r] * Am[r * C + i] * Tm[i * C + j];
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                a += __shfl_xor_sync(0xffffffffu, a, 4);
+                if (part == 0) Tm[r * C + j] = r == j ? 1.f : (r < j ? 0.f : -a);
+                __syncwarp();
+            }
+        }
+        // dT = dW (Diag(beta) X)^T + dU (Diag(beta) v)^T;  dBk = T^T dW;  dBv = T^T dU;
+        // dM = -T^T dT T^T
+        cta_gemm<C, C, D>(DT, C, DW, D, false, XB, D, true, 0, 1.f, false, gsm);
+        cta_gemm<C, C, D>(DT, C, DU, D, false, VB, D, true, 0, 1.f, true, gsm);
+        cta_gemm<C, D, C>(DBK, D, Tm, C, true, DW, D, false, 0, 1.f, false, gsm);
+        cta_gemm<C, D, C>(DBV, D, Tm, C, true, DU, D, false, 0, 1.f, false, gsm);
+        cta_gemm<C, C, C>(TMP, C, DT, C, false, Tm, C, true, 0, 1.f, false, gsm);
+        cta_gemm<C, C, C>(DM, C, Tm, C, true, TMP, C, false, 0, -1.f, false, gsm);
+        for (int e = tid; e < MQ; e += kChunkThreads) {
+            const int r = e >> 6, j = e & 63;
+            DA[e] = j < r ? bs[r] * DM[e] : 0.f;
+        }
+        // dbeta = rowsum(dM A) + rowsum(dBk X) + rowsum(dBv v);  dv = Diag(beta) dBv
+        {
+            const int r = tid >> 3, part = tid & 7;
+            float a = 0.f;
+            for (int j = part; j < C; j += 8) a += DM[r * C + j] * Am[r * C + j];
+            for (int c = part; c < D; c += 8) a += DBK[r * D + c] * K_[r * D + c] * EA[r * D + c] + DBV[r * D + c] * V_[r * D + c];
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            if (part == 0 && r < L) dbeta[(c0 + r) * H + h] = a;
+        }
+        for (int e = tid; e < MR; e += kChunkThreads) {
+            const int r = e >> 7, c = e & 127;
+            if (r < L) dv[((c0 + r) * H + h) * D + c] = bs[r] * DBV[e];
+        }
+        // the gated back-products
+        cta_gemm<C, D, C>(GB, D, DA, C, false, KRF, D, false, MR, 1.f, false, gsm);   // (dA Y) e^G / Lf
+        cta_gemm<C, D, C>(GF, D, DP, C, false, KRF, D, false, MR, 1.f, false, gsm);   // (dP Y) e^G / Lf
+        for (int e = tid; e < MR; e += kChunkThreads) GC[e] = 0.f;
+        for (int b = 0; b < 4; ++b) {
+            // rows j of block-b contributions: sum_{r in b} dA[r][j] kL[r] and dP[r][j] qL[r],
+            // times e^{G_m(b) - G_j}
+            for (int pass = 0; pass < 2; ++pass) {
+                cta_gemm<C, D, 16>(PART, D, (pass == 0 ? DA : DP) + 16 * b * C, C, true,
+                                   (pass == 0 ? KL : QL) + 16 * b * D, D, false, 0, 1.f, false, gsm);
+                for (int e = tid; e < MR; e += kChunkThreads) {
+                    // e^{G_m(b) - G_j} (0 for j past block b)
+                    const int j = e >> 7, c = e & 127, B = j >> 4;
+                    const float pr = PRE[e];
+                    float f = 0.f;
+                    if (B == b) {
+                        f = 1.f / pr;
+                    } else if (B < b) {
+                        f = tot[B * D + c] / pr;
+                        for (int b2 = B + 1; b2 < b; ++b2) f *= tot[b2 * D + c];
+                    }
+                    GC[e] += PART[e] * f;
+                }
+            }
+        }
+        __syncthreads();
+        // ---- dq, dk, dG ----------------------------------------------------------------------
+        for (int e = tid; e < MR; e += kChunkThreads) {
+            const int r = e >> 7, c = e & 127, B = r >> 4;
+            const float pr = PRE[e], ea = EA[e], kk = K_[e], qq = Q_[e];
+            float after = 1.f;   // e^{G_C - G_r}
+            for (int b = B + 1; b < 4; ++b) after *= tot[b * D + c];
+            const float kbf = tot[B * D + c] / pr * after;
+            const float dxe = bs[r] * DBK[e] * ea + GB[e] * pr;   // dX e^G
+            const float dye = GC[e];                                // dY e^{-G}
+            const float dqq = DXQ[e] * ea + GF[e] * pr;             // dXq e^G
+            const float dkb = DKB[e];
+            const float dkk = dxe + dye + dkb * kbf;
+            DGm[e] = kk * dxe - kk * dye + qq * dqq - dkb * kk * kbf;
+            if (r < L) {
+                const int64_t o = ((c0 + r) * H + h) * D + c;
+                dq[o] = dqq;
+                dk[o] = dkk;
+            }
+        }
+        __syncthreads();
+        // dg: reverse cumulative sum over the chunk's tokens; the last row also takes
+        // dEC e^{G_C} + sum_r dKb Kb
+        if (tid < D) {
+            const int c = tid;
+            float colsum = 0.f;
+            for (int r = 0; r < C; ++r) {
+                const int B = r >> 4;
+                float after = 1.f;
+                for (int b = B + 1; b < 4; ++b) after *= tot[b * D + c];
+                colsum += DKB[r * D + c] * K_[r * D + c] * (tot[B * D + c] / PRE[r * D + c] * after);
+            }
+            float acc = dec[c] * ec[c] + colsum;
+            for (int r = C - 1; r >= 0; --r) {
+                acc += DGm[r * D + c];
+                if (r < L) dg[((c0 + r) * H + h) * D + c] = acc;
+            }
+        }
+    }
+}
+
+// Workspace of the chunked backward: the forward's (bookkeeping and slots), o as
+// bf16, then per (chunk slot, head) the entering state, dS' and dU.
+struct BwdLayout {
+    size_t fwd, o, states, dsp, du, scratch, total;
+};
+BwdLayout bwd_layout(int B, int T, int H, int N, bool packed) {
+    BwdLayout l{};
+    const int64_t cps = ((int64_t)T + C - 1) / C;
+    const int64_t max_chunks = packed ? cps + N : (int64_t)B * cps;
+    const size_t slots = (size_t)max_chunks * (size_t)H;
+    l.fwd = (chunk_tc_workspace(B, T, H, N, packed) + 255) & ~size_t(255);
+    l.o = (((size_t)B * (size_t)T * (size_t)H * D * 2) + 255) & ~size_t(255);
+    l.states = slots * D * D * 4;
+    l.dsp = l.states;
+    l.du = slots * C * D * 4;
+    l.scratch = (size_t)kBwdCtas * SC_TOTAL * 4;
+    l.total = (int64_t)N * H == 0 ? 0 : l.fwd + l.o + l.states + l.dsp + l.du + l.scratch;
+    return l;
+}
+
+}  // namespace
+
+bool chunk_bwd_supported(kda_dtype in_dt, int K, int V) { return in_dt == KDA_BF16 && K == D && V == D; }
+
+size_t chunk_bwd_workspace(int B, int T, int H, int N, bool packed) { return bwd_layout(B, T, H, N, packed).total; }
+
+cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, float* dq, float* dk, float* dv,
+                      float* dg, float* dbeta, float* dS0, void* ws, size_t ws_bytes, int32_t* status,
+                      cudaStream_t st) {
+    const BwdLayout lo = bwd_layout(p.B, p.T, p.H, p.N, p.cu_seqlens != nullptr);
+    if ((int64_t)p.N * p.H == 0) {
+        if (status != nullptr) return cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        return cudaSuccess;
+    }
+    if (ws == nullptr || ws_bytes < lo.total) return cudaErrorMemoryAllocation;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint8_t* fwd = base;
+    void* o = base + lo.fwd;
+    float* states = reinterpret_cast<float*>(base + lo.fwd + lo.o);
+    float* dsp = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states);
+    float* du = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.dsp);
+    float* scratch = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.dsp + lo.du);
+    ChunkParams fp = p;
+    fp.o = o;
+    fp.final_state = nullptr;
+    Plan pl{};
+    cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, &pl, status, st);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BC_TOTAL);
+    if (e != cudaSuccess) return e;
+    bwd_chain_kernel<<<(unsigned)((int64_t)p.N * p.H), kChainThreads, BC_TOTAL, st>>>(pl, dO, dST, dS0, dsp, du);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t tasks = pl.max_chunks * p.H;
+    if (tasks > 0) {
+        e = cudaFuncSetAttribute(bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BK_TOTAL);
+        if (e != cudaSuccess) return e;
+        const unsigned grid = (unsigned)(tasks < kBwdCtas ? tasks : kBwdCtas);
+        bwd_chunk_kernel<<<grid, kChunkThreads, BK_TOTAL, st>>>(
+            pl, static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
+            static_cast<const __nv_bfloat16*>(p.v), static_cast<const __nv_bfloat16*>(p.g),
+            static_cast<const __nv_bfloat16*>(p.beta), p.scale, dO, states, dsp, du, scratch, dq, dk, dv, dg, dbeta);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace kda

@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "kda_chunk.h"
+#include "kda_chunk_plan.cuh"
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
 
@@ -59,82 +60,12 @@ uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 namespace {
 
-constexpr int C = 64;
-constexpr int D = 128;   // K = V
+using namespace cplan;
+
 constexpr int NT = 512;  // 16 warps: four warpgroups, each covering all 128 TMEM lanes
 constexpr uint32_t kWaitIter = 1u << 26;   // default poll count of a bounded wait, and of the exit drains
 
-// ---- workspace slot of one (chunk, head), written by the local kernel --------
-constexpr uint32_t SLOT_WQH = 0;        // [-W hi | Qs hi] (bf16) as one B operand, MN-major stored
-                                        //   n-group by n-group (n = r for -W, n = 64 + r for
-                                        //   Qs = scale q e^G; k = c): -W the first 16 KB, Qs the rest
-constexpr uint32_t SLOT_WQL = 32768;    // [-W lo | Qs lo], same layout
-constexpr uint32_t SLOT_EGC = 65536;    // e^{G_C} fp32 [128]
-constexpr uint32_t SLOT_IMG = 66048;    // bytes of the images above (one shared-memory copy)
-constexpr uint32_t SLOT_KH = 66048;     // Kbar hi as B operand [128 c][64 r], K-major
-constexpr uint32_t SLOT_KL = 82432;     // Kbar lo
-constexpr uint32_t SLOT_P = 98816;      // scale P hi | lo, B operand [64 r][64 j] K-major
-constexpr uint32_t SLOT_KBP = 49152;    // bytes of Kbar and P (one shared-memory copy)
-constexpr uint32_t SLOT_UT = 115200;    // U~ fp32 [64 r][128 v]
-constexpr uint32_t SLOT_BYTES = 147968;
-
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
-
-// Work description shared by the kernels.  Sequences are either B dense rows
-// of T tokens (cu_seqlens == nullptr) or packed by cu_seqlens; chunks are
-// numbered sequence by sequence (global chunk index gc), slots by gc * H + h.
-struct Plan {
-    const int32_t* cu_seqlens;
-    const int32_t* chunk_off;  // [N + 1] first global chunk of each sequence (packed only)
-    const int32_t* order;      // [N] sequences longest first (packed only; nullptr = identity)
-    const int32_t* chunk_seq;  // [max_chunks] sequence of each global chunk, -1 past the end
-    int T, H, N;
-    int cps;                   // chunks per sequence (dense only)
-    int64_t max_chunks;        // number of workspace chunk slots (an upper bound when packed)
-    uint8_t* slots;
-    int32_t* status;           // device status word (KDA_ERR_TIMEOUT on a wait that gave up), or null
-    uint32_t wait_iter;        // polls before a wait gives up
-    int inject;                // testing: 1 = the chunk-local kernel's, 2 = the state kernel's first wait
-                               //   is on an mbarrier that nothing arrives on (0 = none)
-};
-
-__device__ __forceinline__ void report_timeout(const Plan& pl) {
-    if (pl.status != nullptr) *reinterpret_cast<volatile int32_t*>(pl.status) = (int32_t)KDA_ERR_TIMEOUT;
-}
-
-struct Chunk {
-    int64_t c0, eos;  // first token of the chunk, end of its sequence
-    int64_t bos;      // first token of its sequence
-    int64_t gc;       // global chunk index
-    int h;
-    bool valid;
-};
-
-// (the host keeps the number of tasks below 2^31, so the divisions are 32-bit)
-__device__ __forceinline__ Chunk decode_task(const Plan& pl, int64_t task) {
-    Chunk ch{};
-    ch.valid = false;
-    if (task >= pl.max_chunks * pl.H) return ch;
-    const uint32_t t = (uint32_t)task, H = (uint32_t)pl.H;
-    const uint32_t gc = t / H;
-    ch.gc = gc;
-    ch.h = (int)(t - gc * H);
-    if (pl.cu_seqlens == nullptr) {
-        const uint32_t cps = (uint32_t)pl.cps;
-        const uint32_t n = gc / cps, j = gc - n * cps;
-        ch.bos = (int64_t)n * pl.T;
-        ch.c0 = ch.bos + (int64_t)j * C;
-        ch.eos = ch.bos + pl.T;
-    } else {
-        const int n = pl.chunk_seq[gc];
-        if (n < 0) return ch;
-        ch.bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
-        ch.c0 = ch.bos + (int64_t)(gc - (uint32_t)pl.chunk_off[n]) * C;
-        ch.eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
-    }
-    ch.valid = true;
-    return ch;
-}
 
 // ============================================================================
 // Chunk-local kernel
@@ -1118,7 +1049,8 @@ constexpr uint32_t TS_UH = 384;   // U^T hi (bf16 pairs) [128 v][32]
 constexpr uint32_t TS_UL = 416;   // U^T lo
 constexpr uint32_t TS_COLS = 512;
 
-template <typename TOut>
+// STATES: also write the state entering every chunk to pl.states_out (for the backward).
+template <typename TOut, bool STATES = false>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restrict__ initial_state,
                    float* __restrict__ final_state, TOut* __restrict__ o, const Plan pl) {
@@ -1140,27 +1072,9 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
     const float* ut_s = reinterpret_cast<const float*>(smem + SS_UT);   // U~ [64 r][128 v]
 
     const int H = pl.H;
-    const int h = blockIdx.x % H;
-    const int rank = blockIdx.x / H;
-    int n;
-    int64_t bos, eos, g0, nchunks;
-    if (pl.cu_seqlens == nullptr) {
-        n = rank;
-        bos = (int64_t)n * pl.T;
-        eos = bos + pl.T;
-        g0 = (int64_t)n * pl.cps;
-        nchunks = pl.cps;
-    } else {
-        n = pl.order != nullptr ? pl.order[rank] : rank;
-        bos = min(max((int)pl.cu_seqlens[n], 0), pl.T);
-        eos = min(max((int)pl.cu_seqlens[n + 1], 0), pl.T);
-        if (eos < bos) eos = bos;
-        // (offsets that overlap can need more chunks than the workspace holds:
-        //  those are left out, never read past the end)
-        g0 = min((int64_t)pl.chunk_off[n], pl.max_chunks);
-        nchunks = min((int64_t)pl.chunk_off[n + 1], pl.max_chunks) - g0;
-        if (nchunks < 0) nchunks = 0;
-    }
+    const Chain chn = chain_of(pl, blockIdx.x);
+    const int h = chn.h, n = chn.n;
+    const int64_t bos = chn.bos, eos = chn.eos, g0 = chn.g0, nchunks = chn.nchunks;
 
     if (warp == 0) tc::tmem_alloc(tmem_base_s, TS_COLS);
     if (tid == 0) {
@@ -1363,6 +1277,15 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc, s0);
                 tc::tmem_ld16(tm + lane_base(warp) + TS_S + cc + 16, s1);
                 tc::tmem_ld_wait();
+                if constexpr (STATES) {
+                    // the state entering this chunk, S[c][x] (a warp's 32 lanes are 32 consecutive x)
+                    float* so = pl.states_out + ((g0 + i) * H + h) * (int64_t)(D * D) + x;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        so[(int64_t)(cc + j) * D] = __uint_as_float(s0[j]);
+                        so[(int64_t)(cc + 16 + j) * D] = __uint_as_float(s1[j]);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     s0[j] = __float_as_uint(__uint_as_float(s0[j]) * eg[j]);
@@ -1535,10 +1458,12 @@ Layout layout(int B, int T, int H, int N, bool packed) {
     return l;
 }
 
-// The prefill's kernels on a caller-owned workspace of ws_bytes.
+// The prefill's kernels on a caller-owned workspace of ws_bytes.  With states_out the
+// state kernel also writes the state entering every chunk there; plan_out receives
+// the work plan (both for the backward).
 template <typename TOut>
 cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws_bytes, int32_t* status,
-                      bool fused) {
+                      bool fused, float* states_out = nullptr, Plan* plan_out = nullptr) {
     cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
     g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
     cudaError_t e = cudaSuccess;
@@ -1566,6 +1491,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws
     pl.wait_iter = lim != 0 ? lim : kWaitIter;
     pl.inject = g_inject;
     g_inject = 0;
+    pl.states_out = states_out;
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
     pl.slots = reinterpret_cast<uint8_t*>(ws) + lo.hdr_bytes;
     trace_record(trace[0], st);
@@ -1608,7 +1534,8 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws
         if (e != cudaSuccess) return e;
         trace_record(trace[1], st);
     }
-    auto kern = chunk_state_kernel<TOut>;
+    if (plan_out != nullptr) *plan_out = pl;
+    auto kern = states_out != nullptr ? chunk_state_kernel<TOut, true> : chunk_state_kernel<TOut, false>;
     const int smem_bytes = (int)SS_TOTAL + 128;
     CUtensorMap mo;
     const int64_t rows = (int64_t)p.B * p.T;
@@ -1672,6 +1599,11 @@ cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, void* ws, siz
                            cudaStream_t st) {
     if (out_dt == KDA_F32) return launch_tc<float>(p, st, ws, ws_bytes, status, true);
     return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, true);
+}
+
+cudaError_t chunk_tc_forward_states(const ChunkParams& p, void* ws, size_t ws_bytes, float* states_out,
+                                    cplan::Plan* plan_out, int32_t* status, cudaStream_t st) {
+    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false, states_out, plan_out);
 }
 
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {

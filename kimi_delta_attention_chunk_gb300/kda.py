@@ -47,6 +47,9 @@ SIGNATURES = {
     "kda_state_compose": (_i, [_fp, _fp, _fp, _fp, _i, _i, _i, _vp]),
     "kda_check_range": (_i, [_vp, _i, ctypes.c_int64, _f, _f, _vp, _vp]),
     "kda_recurrent_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "kda_chunk_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "kda_chunk_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
+                           _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _i32p, _vp]),
     "kda_recurrent_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _f, _fp, _i32p, _i, _i, _i, _i, _i, _i,
                                _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _i32p, _vp]),
 }
@@ -122,9 +125,13 @@ def workspace_size(in_dtype, B: int, T: int, H: int, K: int, V: int, N: int, pac
     return int(load_library().kda_chunk_fwd_workspace_size(_dt_of(in_dtype), B, T, H, K, V, N, int(packed)))
 
 
-def bwd_workspace_size(in_dtype, B: int, T: int, H: int, K: int, V: int, N: int, packed: bool) -> int:
-    """Device workspace bytes ``kda_recurrent_bwd`` needs."""
-    return int(load_library().kda_recurrent_bwd_workspace_size(_dt_of(in_dtype), B, T, H, K, V, N, int(packed)))
+def bwd_workspace_size(in_dtype, B: int, T: int, H: int, K: int, V: int, N: int, packed: bool,
+                       token_by_token: bool = False) -> int:
+    """Device workspace bytes ``kda_chunk_bwd`` (or, with ``token_by_token``,
+    ``kda_recurrent_bwd``) needs."""
+    lib = load_library()
+    fn = lib.kda_recurrent_bwd_workspace_size if token_by_token else lib.kda_chunk_bwd_workspace_size
+    return int(fn(_dt_of(in_dtype), B, T, H, K, V, N, int(packed)))
 
 
 def _workspace(nbytes: int, device, workspace):
@@ -365,13 +372,15 @@ def check_range(x, lo: float = -5.0, hi: float = 0.0, status=None, sync: bool = 
 
 
 def chunk_bwd(q, k, v, g, beta, dO, dS_T=None, scale: float | None = None, initial_state=None,
-              cu_seqlens=None, workspace=None, status=None):
+              cu_seqlens=None, workspace=None, status=None, token_by_token: bool = False):
     """Gradients of <dO, o> + <dS_T, S_T> through :func:`chunk_fwd` (same shapes;
     dO fp32 [B,T,H,V], dS_T fp32 [N,H,K,V] or None).  Returns a dict of fp32
     tensors dq, dk, dv, dg, dbeta and dS0 ([N,H,K,V]).  ``workspace`` (at least
     :func:`bwd_workspace_size` bytes) and ``status`` as for :func:`chunk_fwd`
     (the status word reads 5 = KDA_ERR_RANGE when malformed offsets made the
-    call skip a sequence)."""
+    token-by-token path skip a sequence).  ``kda_chunk_bwd`` runs by default
+    (chunk by chunk for bf16 with K = V = 128); ``token_by_token`` calls
+    ``kda_recurrent_bwd``."""
     lib = load_library()
     B, T, H, K = q.shape
     V = v.shape[-1]
@@ -384,12 +393,13 @@ def chunk_bwd(q, k, v, g, beta, dO, dS_T=None, scale: float | None = None, initi
            "dg": torch.empty((B, T, H, K), dtype=f32, device=dev),
            "dbeta": torch.empty((B, T, H), dtype=f32, device=dev),
            "dS0": torch.empty((N, H, K, V), dtype=f32, device=dev)}
-    ws, ws_bytes = _workspace(bwd_workspace_size(q.dtype, B, T, H, K, V, N, cu_seqlens is not None), dev,
-                              workspace)
-    st = lib.kda_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q), float(scale or 0.0),
-                               _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(dO), _ptr(dS_T),
-                               _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
-                               _ptr(out["dbeta"]), _ptr(out["dS0"]), _ptr(ws), ws_bytes, _ptr(status),
-                               _stream(dev))
-    _check("kda_recurrent_bwd", st)
+    ws, ws_bytes = _workspace(bwd_workspace_size(q.dtype, B, T, H, K, V, N, cu_seqlens is not None,
+                                                 token_by_token), dev, workspace)
+    name = "kda_recurrent_bwd" if token_by_token else "kda_chunk_bwd"
+    st = getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dt(q), float(scale or 0.0),
+                            _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N, _ptr(dO), _ptr(dS_T),
+                            _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                            _ptr(out["dbeta"]), _ptr(out["dS0"]), _ptr(ws), ws_bytes, _ptr(status),
+                            _stream(dev))
+    _check(name, st)
     return out

@@ -1,7 +1,8 @@
-"""kda_recurrent_bwd against the oracle's reverse-mode backward of the
-recurrence: every gradient (dq, dk, dv, dg, dbeta, dS0), element by element,
-bf16 and fp32 inputs, dense and packed sequences, with and without an initial
-state and a final-state gradient."""
+"""The backward against the oracle's reverse-mode backward of the recurrence:
+every gradient (dq, dk, dv, dg, dbeta, dS0), element by element, bf16 and fp32
+inputs, dense and packed sequences, with and without an initial state and a
+final-state gradient.  kda_chunk_bwd (chunk by chunk for bf16 with K = V = 128,
+token by token otherwise) and kda_recurrent_bwd (token by token) both."""
 import numpy as np
 import pytest
 import torch
@@ -14,11 +15,12 @@ from tests.kda_testutil import TOL_BF16, TOL_F32, rel_err, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def check(d, dO, dST, tol):
+def check(d, dO, dST, tol, token_by_token=False):
     dd = to_dev(d)
     got = kda.chunk_bwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dO.cuda(),
                         dS_T=None if dST is None else dST.cuda(), scale=d["scale"],
-                        initial_state=dd["initial_state"], cu_seqlens=dd["cu_seqlens"])
+                        initial_state=dd["initial_state"], cu_seqlens=dd["cu_seqlens"],
+                        token_by_token=token_by_token)
     torch.cuda.synchronize()
     lead = d["q"].shape[:2]
     flat = (lambda x: x[0]) if d["cu_seqlens"] is not None else (lambda x: x)
@@ -32,12 +34,50 @@ def check(d, dO, dST, tol):
     assert got["dq"].shape[:2] == lead
 
 
-def test_bf16_dense_with_state_gradient():
+@pytest.mark.parametrize("token_by_token", [False, True])
+def test_bf16_dense_with_state_gradient(token_by_token):
+    # three chunks, the last one ragged
     d = synth.direct_inputs(150, 2, 128, 128, torch.bfloat16, seed=111, init_state=True)
     gen = torch.Generator().manual_seed(1)
     dO = torch.randn(1, 150, 2, 128, generator=gen)
     dST = torch.randn(1, 2, 128, 128, generator=gen)
+    check(d, dO, dST, TOL_BF16, token_by_token)
+
+
+def test_bf16_chunked_packed_sequences():
+    # lengths 1, exactly one chunk, ragged, empty, several chunks
+    lengths = [1, 64, 100, 0, 130]
+    d = synth.direct_inputs(sum(lengths), 3, 128, 128, torch.bfloat16, seed=114, init_state=True, lengths=lengths)
+    gen = torch.Generator().manual_seed(4)
+    dO = torch.randn(1, sum(lengths), 3, 128, generator=gen)
+    dST = torch.randn(len(lengths), 3, 128, 128, generator=gen)
     check(d, dO, dST, TOL_BF16)
+
+
+def test_bf16_chunked_two_dense_rows_no_state():
+    d = synth.direct_inputs(256, 4, 128, 128, torch.bfloat16, seed=115, B=2)
+    dO = torch.randn(2, 256, 4, 128, generator=torch.Generator().manual_seed(5))
+    check(d, dO, None, TOL_BF16)
+
+
+def test_bf16_chunked_full_size_on_sampled_heads():
+    # the 4096-token, 96-head workload through the chunked path; the oracle's reverse
+    # mode on two of the heads (the heads are independent)
+    T, H = 4096, 96
+    d = synth.direct_inputs(T, H, 128, 128, torch.bfloat16, seed=116)
+    dO = torch.randn(1, T, H, 128, generator=torch.Generator().manual_seed(6))
+    dd = to_dev(d)
+    got = kda.chunk_bwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dO.cuda(), scale=d["scale"])
+    torch.cuda.synchronize()
+    for h in (0, 77):
+        sl = lambda x: x[0, :, h:h + 1]  # noqa: E731
+        ref = oracle.kda_backward(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), d["beta"][0, :, h:h + 1],
+                                  sl(dO), scale=d["scale"])
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            e = rel_err(got[key][0, :, h:h + 1], ref[key])
+            assert e <= TOL_BF16, f"head {h} {key}: err {e:.3e}"
+        e = rel_err(got["dS0"][:, h:h + 1], ref["dS0"])
+        assert e <= TOL_BF16, f"head {h} dS0: err {e:.3e}"
 
 
 def test_fp32_packed_sequences():
