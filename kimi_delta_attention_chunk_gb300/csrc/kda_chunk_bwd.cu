@@ -232,8 +232,8 @@ enum : int {
     SC_KRF = SC_QL + MR,
     SC_U = SC_KRF + 4 * MR, SC_DXQ = SC_U + MR, SC_DW = SC_DXQ + MR, SC_DKB = SC_DW + MR,
     SC_DBK = SC_DKB + MR, SC_DBV = SC_DBK + MR, SC_XB = SC_DBV + MR, SC_VB = SC_XB + MR,
-    SC_GB = SC_VB + MR, SC_GF = SC_GB + MR, SC_GC = SC_GF + MR, SC_PART = SC_GC + MR, SC_DG = SC_PART + MR,
-    SC_DP = SC_DG + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
+    SC_GB = SC_VB + MR, SC_GF = SC_GB + MR, SC_GC = SC_GF + MR, SC_PART = SC_GC + MR,
+    SC_DP = SC_PART + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
     SC_DM = SC_TMP + MQ, SC_DA = SC_DM + MQ,
     SC_TOTAL = SC_DA + MQ
 };
@@ -245,6 +245,36 @@ constexpr uint32_t BK_DEC = BK_BETA + C * 4;            // dEC [128]
 constexpr uint32_t BK_EC = BK_DEC + D * 4;              // e^{G_C} [128]
 constexpr uint32_t BK_TOTAL = BK_EC + D * 4;
 static_assert(BK_TOTAL <= 232448, "shared memory of the chunk kernel");
+
+// A [R][CO] fp32 matrix in global memory (row stride ld, 16-byte aligned rows) into
+// shared memory: dst[r][c] (TR false) or dst[c][r] (TR true), row stride ldd.  Float4
+// loads, four of them in flight per thread before their stores.
+template <int R, int CO, bool TR>
+__device__ __forceinline__ void stage(const float* src, int ld, float* dst, int ldd) {
+    constexpr int NV = R * (CO / 4);
+    for (int i0 = threadIdx.x; i0 < NV; i0 += 4 * kChunkThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kChunkThreads;
+            if (i < NV) v[u] = *reinterpret_cast<const float4*>(src + (int64_t)(i / (CO / 4)) * ld + 4 * (i % (CO / 4)));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kChunkThreads;
+            if (i >= NV) break;
+            const int r = i / (CO / 4), c = 4 * (i % (CO / 4));
+            if (TR) {
+                dst[(c + 0) * ldd + r] = v[u].x;
+                dst[(c + 1) * ldd + r] = v[u].y;
+                dst[(c + 2) * ldd + r] = v[u].z;
+                dst[(c + 3) * ldd + r] = v[u].w;
+            } else {
+                *reinterpret_cast<float4*>(dst + r * ldd + c) = v[u];
+            }
+        }
+    }
+}
 
 // C[M x N] (row-major, ldc) = alpha op(A) op(B) (+ C when acc), fp32, by the whole CTA:
 // op(A)(m, k) = A[m lda + k] (ta false) or A[k lda + m]; op(B)(k, n) = B[k ldb + n] (tb
@@ -258,23 +288,17 @@ __device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int ld
     float* As = sm;
     float* Bs = sm + K * LA;
     const int nb = bblk != 0 ? M / 16 : 1;
-    const int tid = threadIdx.x;
     __syncthreads();   // the previous readers of the staging area and writers of the operands are done
-    for (int i = tid; i < M * K; i += kChunkThreads) {
-        const int m = ta ? i % M : i / K, k = ta ? i / M : i % K;
-        As[k * LA + m] = ta ? A[(int64_t)k * lda + m] : A[(int64_t)m * lda + k];
-    }
+    // As[k][m]: A is stored m-major (rows m) unless ta; Bs[k][n]: B is stored k-major unless tb
+    if (ta) stage<K, M, false>(A, lda, As, LA);
+    else stage<M, K, true>(A, lda, As, LA);
     for (int b = 0; b < nb; ++b) {
-        const float* Bb = B + (int64_t)b * bblk;
-        float* Bsb = Bs + b * K * LB;
-        for (int i = tid; i < K * N; i += kChunkThreads) {
-            const int k = tb ? i % K : i / N, n = tb ? i / K : i % N;
-            Bsb[k * LB + n] = tb ? Bb[(int64_t)n * ldb + k] : Bb[(int64_t)k * ldb + n];
-        }
+        if (tb) stage<N, K, true>(B + (int64_t)b * bblk, ldb, Bs + b * K * LB, LB);
+        else stage<K, N, false>(B + (int64_t)b * bblk, ldb, Bs + b * K * LB, LB);
     }
     __syncthreads();
     constexpr int TN = N / 4;
-    for (int t = tid; t < (M / 4) * TN; t += kChunkThreads) {
+    for (int t = threadIdx.x; t < (M / 4) * TN; t += kChunkThreads) {
         const int tm = t / TN, tn = t % TN;
         const float* Bsb = Bs + (bblk != 0 ? ((4 * tm) >> 4) * K * LB : 0);
         float a4[4][4] = {};
@@ -347,7 +371,6 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* GF = sc + SC_GF;
     float* GC = sc + SC_GC;
     float* PART = sc + SC_PART;
-    float* DGm = sc + SC_DG;
     float* DP = sc + SC_DP;
     float* Am = sc + SC_A;
     float* Tm = sc + SC_T;
@@ -451,18 +474,24 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             if (j > r) DP[e] = 0.f;
         }
         __syncthreads();
-        // T = (I + Diag(beta) A)^{-1}: eight threads per column, rows in order
+        // T = (I + Diag(beta) A)^{-1} in shared memory: eight threads per column, rows in order
         {
+            float* Ns = gsm;               // Diag(beta) A [64][65]
+            float* Ts = gsm + C * (C + 1); // T [64][65]
+            for (int e = tid; e < MQ; e += kChunkThreads) Ns[(e >> 6) * (C + 1) + (e & 63)] = bs[e >> 6] * Am[e];
+            __syncthreads();
             const int j = tid >> 3, part = tid & 7;
             for (int r = 0; r < C; ++r) {
                 float a = 0.f;
-                for (int i = j + part; i < r; i += 8) a += bs[r] * Am[r * C + i] * Tm[i * C + j];
+                for (int i = j + part; i < r; i += 8) a += Ns[r * (C + 1) + i] * Ts[i * (C + 1) + j];
                 a += __shfl_xor_sync(0xffffffffu, a, 1);
                 a += __shfl_xor_sync(0xffffffffu, a, 2);
                 a += __shfl_xor_sync(0xffffffffu, a, 4);
-                if (part == 0) Tm[r * C + j] = r == j ? 1.f : (r < j ? 0.f : -a);
+                if (part == 0) Ts[r * (C + 1) + j] = r == j ? 1.f : (r < j ? 0.f : -a);
                 __syncwarp();
             }
+            __syncthreads();
+            for (int e = tid; e < MQ; e += kChunkThreads) Tm[e] = Ts[(e >> 6) * (C + 1) + (e & 63)];
         }
         // dT = dW (Diag(beta) X)^T + dU (Diag(beta) v)^T;  dBk = T^T dW;  dBv = T^T dU;
         // dM = -T^T dT T^T
@@ -529,7 +558,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             const float dqq = DXQ[e] * ea + GF[e] * pr;             // dXq e^G
             const float dkb = DKB[e];
             const float dkk = dxe + dye + dkb * kbf;
-            DGm[e] = kk * dxe - kk * dye + qq * dqq - dkb * kk * kbf;
+            gsm[e] = kk * dxe - kk * dye + qq * dqq - dkb * kk * kbf;   // dG
+            gsm[MR + e] = dkb * kk * kbf;                              // dKb Kb
             if (r < L) {
                 const int64_t o = ((c0 + r) * H + h) * D + c;
                 dq[o] = dqq;
@@ -542,15 +572,10 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         if (tid < D) {
             const int c = tid;
             float colsum = 0.f;
-            for (int r = 0; r < C; ++r) {
-                const int B = r >> 4;
-                float after = 1.f;
-                for (int b = B + 1; b < 4; ++b) after *= tot[b * D + c];
-                colsum += DKB[r * D + c] * K_[r * D + c] * (tot[B * D + c] / PRE[r * D + c] * after);
-            }
+            for (int r = 0; r < C; ++r) colsum += gsm[MR + r * D + c];
             float acc = dec[c] * ec[c] + colsum;
             for (int r = C - 1; r >= 0; --r) {
-                acc += DGm[r * D + c];
+                acc += gsm[r * D + c];
                 if (r < L) dg[((c0 + r) * H + h) * D + c] = acc;
             }
         }
