@@ -223,47 +223,70 @@ constexpr int kChunkThreads = 512;
 constexpr int kBwdCtas = 152;   // persistent CTAs of the chunk kernel (the workspace holds a scratch area for each)
 constexpr int MR = C * D;       // floats of a [64][128] matrix
 constexpr int MQ = C * C;       // floats of a [64][64] matrix
-// Per-CTA scratch (fp32, in the workspace; offsets in floats).  KRF holds, for each
-// 16-token row block b, k_j e^{G_m - G_j} (m = the token before block b; 0 for j
-// past block b).
+// Per-CTA scratch (fp32, in the workspace; offsets in floats).  [dW | dU] and
+// [dBk | dBv] are [64][256] (the two side by side).
 enum : int {
     SC_K = 0, SC_Q = SC_K + MR, SC_V = SC_Q + MR, SC_DO = SC_V + MR, SC_WN = SC_DO + MR,
     SC_PRE = SC_WN + MR, SC_EA = SC_PRE + MR, SC_KL = SC_EA + MR, SC_QL = SC_KL + MR,
-    SC_KRF = SC_QL + MR,
-    SC_U = SC_KRF + 4 * MR, SC_DXQ = SC_U + MR, SC_DW = SC_DXQ + MR, SC_DKB = SC_DW + MR,
-    SC_DBK = SC_DKB + MR, SC_DBV = SC_DBK + MR, SC_XB = SC_DBV + MR, SC_VB = SC_XB + MR,
-    SC_GB = SC_VB + MR, SC_GF = SC_GB + MR, SC_GC = SC_GF + MR, SC_PART = SC_GC + MR,
-    SC_DP = SC_PART + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
+    SC_U = SC_QL + MR, SC_DXQ = SC_U + MR, SC_DWU = SC_DXQ + MR, SC_DKB = SC_DWU + 2 * MR,
+    SC_DBKV = SC_DKB + MR, SC_XVB = SC_DBKV + 2 * MR, SC_GB = SC_XVB + 2 * MR, SC_GF = SC_GB + MR,
+    SC_GC = SC_GF + MR,
+    SC_DP = SC_GC + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
     SC_DM = SC_TMP + MQ, SC_DA = SC_DM + MQ,
     SC_TOTAL = SC_DA + MQ
 };
-// shared memory of the chunk kernel: the GEMM staging area, then small vectors
+// shared memory of the chunk kernel: the GEMM staging area, then small tables
 constexpr int GEMM_FLOATS = 128 * 68 + 4 * 128 * 68;   // the largest staging (the gated A product)
-constexpr uint32_t BK_TOT = GEMM_FLOATS * 4;            // tot [4][128]
-constexpr uint32_t BK_BETA = BK_TOT + 4 * D * 4;        // beta [64]
+constexpr uint32_t BK_TOT = GEMM_FLOATS * 4;            // tot [4][128]: e^g products over each 16-token block
+constexpr uint32_t BK_PT = BK_TOT + 4 * D * 4;          // ptot [4 B][4 b][128]: prod of tot over blocks [B, b)
+constexpr uint32_t BK_BETA = BK_PT + 16 * D * 4;        // beta [64]
 constexpr uint32_t BK_DEC = BK_BETA + C * 4;            // dEC [128]
 constexpr uint32_t BK_EC = BK_DEC + D * 4;              // e^{G_C} [128]
 constexpr uint32_t BK_TOTAL = BK_EC + D * 4;
 static_assert(BK_TOTAL <= 232448, "shared memory of the chunk kernel");
 
-// A [R][CO] fp32 matrix in global memory (row stride ld, 16-byte aligned rows) into
-// shared memory: dst[r][c] (TR false) or dst[c][r] (TR true), row stride ldd.  Float4
-// loads, four of them in flight per thread before their stores.
+// The float4 unit i of an [R][CO] matrix -> its row r and first column c.  For a
+// transposed store (TR), each warp covers eight consecutive rows of four column
+// groups, which keeps the scattered shared-memory stores free of most conflicts.
 template <int R, int CO, bool TR>
-__device__ __forceinline__ void stage(const float* src, int ld, float* dst, int ldd) {
+__device__ __forceinline__ void unit_rc(int i, int& r, int& c) {
+    if (TR) {
+        const int rest = i >> 3;
+        c = 4 * (rest % (CO / 4));
+        r = (rest / (CO / 4)) * 8 + (i & 7);
+    } else {
+        r = i / (CO / 4);
+        c = 4 * (i % (CO / 4));
+    }
+}
+
+// An [R][CO] fp32 matrix in global memory (row stride ld, 16-byte aligned rows) into
+// shared memory, each float4 passed through f(r, c, v) first: dst[r][c] (TR false) or
+// dst[c][r] (TR true), row stride ldd.  Four float4 loads in flight per thread.
+struct Ident {
+    __device__ __forceinline__ void operator()(int, int, float4&) const {}
+};
+template <int R, int CO, bool TR, typename F = Ident>
+__device__ __forceinline__ void stage(const float* src, int ld, float* dst, int ldd, F f = F()) {
     constexpr int NV = R * (CO / 4);
     for (int i0 = threadIdx.x; i0 < NV; i0 += 4 * kChunkThreads) {
         float4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * kChunkThreads;
-            if (i < NV) v[u] = *reinterpret_cast<const float4*>(src + (int64_t)(i / (CO / 4)) * ld + 4 * (i % (CO / 4)));
+            if (i < NV) {
+                int r, c;
+                unit_rc<R, CO, TR>(i, r, c);
+                v[u] = *reinterpret_cast<const float4*>(src + (int64_t)r * ld + c);
+            }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * kChunkThreads;
             if (i >= NV) break;
-            const int r = i / (CO / 4), c = 4 * (i % (CO / 4));
+            int r, c;
+            unit_rc<R, CO, TR>(i, r, c);
+            f(r, c, v[u]);
             if (TR) {
                 dst[(c + 0) * ldd + r] = v[u].x;
                 dst[(c + 1) * ldd + r] = v[u].y;
@@ -276,31 +299,23 @@ __device__ __forceinline__ void stage(const float* src, int ld, float* dst, int 
     }
 }
 
-// C[M x N] (row-major, ldc) = alpha op(A) op(B) (+ C when acc), fp32, by the whole CTA:
-// op(A)(m, k) = A[m lda + k] (ta false) or A[k lda + m]; op(B)(k, n) = B[k ldb + n] (tb
-// false) or B[n ldb + k]; with bblk != 0 the B of the output rows [16 b, 16 b + 16) is
-// B + b bblk.  Both operands are staged in shared memory k-major; a thread computes 4 x 4
-// outputs.  The operands are in global memory (this CTA's scratch or the inputs).
-template <int M, int N, int K>
-__device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
-                                      bool tb, int bblk, float alpha, bool acc, float* sm) {
+// C[M x N] (row-major, ldc) = alpha A B (+ C when acc), fp32, by the whole CTA, with
+// the operands staged into shared memory by the caller's functions: sa(As, LA) writes
+// As[k][m], sb(Bs, LB, b) writes Bs[k][n] for B variant b (nb of them: with nb = 4 the
+// output rows [16 b, 16 b + 16) use variant b).  A thread computes 4 x 4 outputs.
+template <int M, int N, int K, typename SA, typename SB>
+__device__ __forceinline__ void cta_mm(float* Cm, int ldc, SA sa, SB sb, int nb, float alpha, bool acc, float* sm) {
     constexpr int LA = M + 4, LB = N + 4;
     float* As = sm;
     float* Bs = sm + K * LA;
-    const int nb = bblk != 0 ? M / 16 : 1;
     __syncthreads();   // the previous readers of the staging area and writers of the operands are done
-    // As[k][m]: A is stored m-major (rows m) unless ta; Bs[k][n]: B is stored k-major unless tb
-    if (ta) stage<K, M, false>(A, lda, As, LA);
-    else stage<M, K, true>(A, lda, As, LA);
-    for (int b = 0; b < nb; ++b) {
-        if (tb) stage<N, K, true>(B + (int64_t)b * bblk, ldb, Bs + b * K * LB, LB);
-        else stage<K, N, false>(B + (int64_t)b * bblk, ldb, Bs + b * K * LB, LB);
-    }
+    sa(As, LA);
+    for (int b = 0; b < nb; ++b) sb(Bs + b * K * LB, LB, b);
     __syncthreads();
     constexpr int TN = N / 4;
     for (int t = threadIdx.x; t < (M / 4) * TN; t += kChunkThreads) {
         const int tm = t / TN, tn = t % TN;
-        const float* Bsb = Bs + (bblk != 0 ? ((4 * tm) >> 4) * K * LB : 0);
+        const float* Bsb = Bs + (nb > 1 ? ((4 * tm) >> 4) * K * LB : 0);
         float a4[4][4] = {};
 #pragma unroll 4
         for (int k = 0; k < K; ++k) {
@@ -326,13 +341,88 @@ __device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int ld
     __syncthreads();   // C is complete
 }
 
+// The plain case: op(A)(m, k) = A[m lda + k] (ta false) or A[k lda + m]; op(B)(k, n) =
+// B[k ldb + n] (tb false) or B[n ldb + k].
+template <int M, int N, int K>
+__device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
+                                      bool tb, float alpha, bool acc, float* sm) {
+    cta_mm<M, N, K>(
+        Cm, ldc,
+        [&](float* As, int LA) {
+            if (ta) stage<K, M, false>(A, lda, As, LA);
+            else stage<M, K, true>(A, lda, As, LA);
+        },
+        [&](float* Bs, int LB, int) {
+            if (tb) stage<N, K, true>(B, ldb, Bs, LB);
+            else stage<K, N, false>(B, ldb, Bs, LB);
+        },
+        1, alpha, acc, sm);
+}
+
 template <typename TIn>
 __device__ __forceinline__ float ld_in(const TIn* p) { return to_f32<TIn>(*p); }
+
+// Decay factors of the gated products, applied while staging (see bwd_chunk_kernel):
+// Krf(b): k_j e^{G_m(b) - G_j}, 0 for j past block b (staging k, rows j)
+struct Krf {
+    const float* pre;
+    const float* ptot;
+    int b;
+    __device__ __forceinline__ void operator()(int j, int c, float4& x) const {
+        const int B = j >> 4;
+        if (B > b) {
+            x = make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
+        const float4 pr = *reinterpret_cast<const float4*>(pre + j * D + c);
+        const float* pt = ptot + (B * 4 + b) * D + c;
+        x.x *= pt[0] / pr.x; x.y *= pt[1] / pr.y; x.z *= pt[2] / pr.z; x.w *= pt[3] / pr.w;
+    }
+};
+// Alp(Bo): a_r e^{G_r - G_m(b(r))} times the block totals over [Bo, b(r)), 0 for rows
+// before block Bo (staging k e^{G - G_m} or q e^{G - G_m}, rows r)
+struct Alp {
+    const float* ptot;
+    int Bo;
+    __device__ __forceinline__ void operator()(int r, int c, float4& x) const {
+        const int b = r >> 4;
+        if (b < Bo) {
+            x = make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
+        const float* pt = ptot + (Bo * 4 + b) * D + c;
+        x.x *= pt[0]; x.y *= pt[1]; x.z *= pt[2]; x.w *= pt[3];
+    }
+};
+
+// A[r][j] = sum_c kL[r][c] Krf(b(r))(k)[j][c]: the gated k k^T product (before masking)
+__device__ __noinline__ void gated_kk(float* Am, const float* KL, const float* K_, const float* pre, const float* ptot,
+                                      float* sm) {
+    cta_mm<C, C, D>(
+        Am, C, [&](float* As, int LA) { stage<C, D, true>(KL, D, As, LA); },
+        [&](float* Bs, int LB, int b) { stage<C, D, true>(K_, D, Bs, LB, Krf{pre, ptot, b}); }, 4, 1.f, false, sm);
+}
+// out[r][c] = sum_j M[r][j] Krf(b(r))(k)[j][c]
+__device__ __noinline__ void gated_rows(float* out, const float* M, const float* K_, const float* pre,
+                                        const float* ptot, float* sm) {
+    cta_mm<C, D, C>(
+        out, D, [&](float* As, int LA) { stage<C, C, true>(M, C, As, LA); },
+        [&](float* Bs, int LB, int b) { stage<C, D, false>(K_, D, Bs, LB, Krf{pre, ptot, b}); }, 4, 1.f, false, sm);
+}
+// out[j][c] (+)= sum_r M[r][j] Alp(b(j))(aL)[r][c]
+__device__ __noinline__ void gated_cols(float* out, const float* M, const float* aL, const float* ptot, bool acc,
+                                        float* sm) {
+    cta_mm<C, D, C>(
+        out, D, [&](float* As, int LA) { stage<C, C, false>(M, C, As, LA); },
+        [&](float* Bs, int LB, int b) { stage<C, D, false>(aL, D, Bs, LB, Alp{ptot, b}); }, 4, 1.f, acc, sm);
+}
 
 // One (chunk, head) task per CTA at a time: the chunk's dq, dk, dv, dg, dbeta from the
 // entering state S, the gradient dS' of the state after it, dU and dO, plus the
 // forward's W and U~ (slot), all in fp32.  Decay factors are formed per 16-token row
-// block from products over exactly the tokens they span (never e^{-G} alone).
+// block from products over exactly the tokens they span (never e^{-G} alone):
+// e^{G_r - G_m(b)} = pre_r for a row r of block b (m(b) the token before the block),
+// e^{G_m(b) - G_j} = ptot[B(j)][b] / pre_j for j up to the end of block b.
 __global__ void __launch_bounds__(kChunkThreads, 1)
 bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
@@ -343,6 +433,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     extern __shared__ __align__(16) uint8_t smem[];
     float* gsm = reinterpret_cast<float*>(smem);
     float* tot = reinterpret_cast<float*>(smem + BK_TOT);
+    float* ptot = reinterpret_cast<float*>(smem + BK_PT);
     float* bs = reinterpret_cast<float*>(smem + BK_BETA);
     float* dec = reinterpret_cast<float*>(smem + BK_DEC);
     float* ec = reinterpret_cast<float*>(smem + BK_EC);
@@ -358,19 +449,15 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* EA = sc + SC_EA;
     float* KL = sc + SC_KL;
     float* QL = sc + SC_QL;
-    float* KRF = sc + SC_KRF;
     float* U = sc + SC_U;
     float* DXQ = sc + SC_DXQ;
-    float* DW = sc + SC_DW;
+    float* DWU = sc + SC_DWU;    // [dW | dU] [64][256]
     float* DKB = sc + SC_DKB;
-    float* DBK = sc + SC_DBK;
-    float* DBV = sc + SC_DBV;
-    float* XB = sc + SC_XB;
-    float* VB = sc + SC_VB;
+    float* DBKV = sc + SC_DBKV;  // [dBk | dBv] [64][256]
+    float* XVB = sc + SC_XVB;    // [Diag(beta) X | Diag(beta) v] [64][256]
     float* GB = sc + SC_GB;
     float* GF = sc + SC_GF;
     float* GC = sc + SC_GC;
-    float* PART = sc + SC_PART;
     float* DP = sc + SC_DP;
     float* Am = sc + SC_A;
     float* Tm = sc + SC_T;
@@ -390,18 +477,37 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         const float* S = states + task * (int64_t)(D * D);
         const float* DSP = dsp + task * (int64_t)(D * D);
         const float* DU = du + task * (int64_t)(C * D);
-        __syncthreads();   // the previous task is done with the scratch
+        __syncthreads();   // the previous task is done with the scratch and the tables
 
-        // ---- inputs (0 past the sequence end), prefix products, -W, U~ -----------------
-        for (int e = tid; e < MR; e += kChunkThreads) {
-            const int r = e >> 7, c = e & 127;
-            const bool ok = r < L;
+        // ---- inputs (0 past the sequence end), U~ and dU, prefix products, -W ----------
+        for (int u = tid; u < MR / 8; u += kChunkThreads) {
+            const int r = u >> 4, c = 8 * (u & 15);
             const int64_t ti = ((c0 + r) * H + h) * D + c;
-            K_[e] = ok ? ld_in(k + ti) : 0.f;
-            Q_[e] = ok ? ld_in(q + ti) : 0.f;
-            V_[e] = ok ? ld_in(v + ti) : 0.f;
-            DO_[e] = ok ? dO[ti] : 0.f;
-            U[e] = reinterpret_cast<const float*>(slot + SLOT_UT)[e];
+            float kx[8], qx[8], vx[8];
+            if (r < L) {
+                tc::unpack8(*reinterpret_cast<const uint4*>(k + ti), kx);
+                tc::unpack8(*reinterpret_cast<const uint4*>(q + ti), qx);
+                tc::unpack8(*reinterpret_cast<const uint4*>(v + ti), vx);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kx[e] = qx[e] = vx[e] = 0.f;
+            }
+            const int o = r * D + c;
+            *reinterpret_cast<float4*>(K_ + o) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+            *reinterpret_cast<float4*>(K_ + o + 4) = make_float4(kx[4], kx[5], kx[6], kx[7]);
+            *reinterpret_cast<float4*>(Q_ + o) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+            *reinterpret_cast<float4*>(Q_ + o + 4) = make_float4(qx[4], qx[5], qx[6], qx[7]);
+            *reinterpret_cast<float4*>(V_ + o) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+            *reinterpret_cast<float4*>(V_ + o + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
+        }
+        for (int u = tid; u < MR / 4; u += kChunkThreads) {
+            const int r = u >> 5, c = 4 * (u & 31);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < L) x = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c);
+            *reinterpret_cast<float4*>(DO_ + r * D + c) = x;
+            *reinterpret_cast<float4*>(U + r * D + c) =
+                *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(slot + SLOT_UT) + r * D + c);
+            *reinterpret_cast<float4*>(DWU + r * 2 * D + D + c) = *reinterpret_cast<const float4*>(DU + r * D + c);
         }
         if (tid < C) bs[tid] = tid < L ? ld_in(beta + (c0 + tid) * H + h) : 0.f;
         {
@@ -423,51 +529,62 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             for (int e = 0; e < 8; ++e) WN[(8 * ng + e) * D + c] = x[e];
         }
         __syncthreads();
-        if (tid < D) ec[tid] = tot[tid] * tot[D + tid] * tot[2 * D + tid] * tot[3 * D + tid];
-        // derived operands
-        for (int e = tid; e < MR; e += kChunkThreads) {
-            const int r = e >> 7, c = e & 127, B = r >> 4;
-            const float pr = PRE[e];
-            float before = 1.f;
-            for (int b = 0; b < B; ++b) before *= tot[b * D + c];
-            const float ea = before * pr;   // e^{G_r}
-            EA[e] = ea;
-            KL[e] = K_[e] * pr;
-            QL[e] = Q_[e] * pr;
-            XB[e] = bs[r] * K_[e] * ea;
-            VB[e] = bs[r] * V_[e];
-            // k_r e^{G_m(b) - G_r} for the row blocks b >= B (0 for b < B)
-            float f = 1.f / pr;   // within its own block
-            for (int b = 0; b < 4; ++b) {
-                float val = 0.f;
-                if (b == B) {
-                    val = f;
-                } else if (b > B) {
-                    float t = tot[B * D + c] / pr;
-                    for (int b2 = B + 1; b2 < b; ++b2) t *= tot[b2 * D + c];
-                    val = t;
+        if (tid < D) {
+            const int c = tid;
+            ec[c] = tot[c] * tot[D + c] * tot[2 * D + c] * tot[3 * D + c];
+            for (int B = 0; B < 4; ++B) {
+                float p = 1.f;
+                for (int b = 0; b < 4; ++b) {
+                    ptot[(B * 4 + b) * D + c] = b >= B ? p : 0.f;
+                    if (b >= B) p *= tot[b * D + c];
                 }
-                KRF[b * MR + e] = K_[e] * val;
             }
+        }
+        // derived operands: e^{G_r}, a e^{G_r - G_m(b(r))}, Diag(beta) X, Diag(beta) v
+        for (int u = tid; u < MR / 4; u += kChunkThreads) {
+            const int r = u >> 5, c = 4 * (u & 31), B = r >> 4;
+            const float4 pr = *reinterpret_cast<const float4*>(PRE + r * D + c);
+            const float4 kx = *reinterpret_cast<const float4*>(K_ + r * D + c);
+            const float4 qx = *reinterpret_cast<const float4*>(Q_ + r * D + c);
+            const float4 vx = *reinterpret_cast<const float4*>(V_ + r * D + c);
+            float4 bf = make_float4(1.f, 1.f, 1.f, 1.f);
+            for (int b = 0; b < B; ++b) {
+                bf.x *= tot[b * D + c]; bf.y *= tot[b * D + c + 1]; bf.z *= tot[b * D + c + 2]; bf.w *= tot[b * D + c + 3];
+            }
+            const float4 ea = make_float4(bf.x * pr.x, bf.y * pr.y, bf.z * pr.z, bf.w * pr.w);
+            const float br = bs[r];
+            *reinterpret_cast<float4*>(EA + r * D + c) = ea;
+            *reinterpret_cast<float4*>(KL + r * D + c) = make_float4(kx.x * pr.x, kx.y * pr.y, kx.z * pr.z, kx.w * pr.w);
+            *reinterpret_cast<float4*>(QL + r * D + c) = make_float4(qx.x * pr.x, qx.y * pr.y, qx.z * pr.z, qx.w * pr.w);
+            *reinterpret_cast<float4*>(XVB + r * 2 * D + c) =
+                make_float4(br * kx.x * ea.x, br * kx.y * ea.y, br * kx.z * ea.z, br * kx.w * ea.w);
+            *reinterpret_cast<float4*>(XVB + r * 2 * D + D + c) = make_float4(br * vx.x, br * vx.y, br * vx.z, br * vx.w);
         }
 
         // ---- the products with S, dS', U ----------------------------------------------------
-        cta_gemm<C, D, D>(U, D, WN, D, false, S, D, false, 0, 1.f, true, gsm);        // U = U~ - W S
-        cta_gemm<C, D, D>(DXQ, D, DO_, D, false, S, D, true, 0, scale, false, gsm);   // scale dO S^T
-        cta_gemm<C, D, D>(DW, D, DU, D, false, S, D, true, 0, -1.f, false, gsm);      // -dU S^T
-        cta_gemm<C, D, D>(DKB, D, U, D, false, DSP, D, true, 0, 1.f, false, gsm);     // U dS'^T
-        cta_gemm<C, C, D>(DP, C, DO_, D, false, U, D, true, 0, scale, false, gsm);    // scale dO U^T
+        cta_gemm<C, D, D>(U, D, WN, D, false, S, D, false, 1.f, true, gsm);              // U = U~ - W S
+        cta_gemm<C, D, D>(DXQ, D, DO_, D, false, S, D, true, scale, false, gsm);         // scale dO S^T
+        cta_gemm<C, D, D>(DWU, 2 * D, DU, D, false, S, D, true, -1.f, false, gsm);       // dW = -dU S^T
+        cta_gemm<C, D, D>(DKB, D, U, D, false, DSP, D, true, 1.f, false, gsm);           // U dS'^T
+        cta_gemm<C, C, D>(DP, C, DO_, D, false, U, D, true, scale, false, gsm);          // scale dO U^T
         {
-            // dEC[c] = sum_x dS'[c][x] S[c][x]: four threads per channel
+            // dEC[c] = sum_x dS'[c][x] S[c][x]: four threads per channel, eight float4 each
             const int c = tid >> 2, part = tid & 3;
+            float4 a4[8], b4[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                a4[i] = *reinterpret_cast<const float4*>(DSP + c * D + part * 32 + 4 * i);
+                b4[i] = *reinterpret_cast<const float4*>(S + c * D + part * 32 + 4 * i);
+            }
             float a = 0.f;
-            for (int x = part * 32; x < part * 32 + 32; ++x) a += DSP[c * D + x] * S[c * D + x];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a += a4[i].x * b4[i].x + a4[i].y * b4[i].y + a4[i].z * b4[i].z + a4[i].w * b4[i].w;
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             if (part == 0) dec[c] = a;
         }
         // A: the gated k k^T product per row block (strictly lower)
-        cta_gemm<C, C, D>(Am, C, KL, D, false, KRF, D, true, MR, 1.f, false, gsm);
+        gated_kk(Am, KL, K_, PRE, ptot, gsm);
         for (int e = tid; e < MQ; e += kChunkThreads) {
             const int r = e >> 6, j = e & 63;
             if (j >= r) Am[e] = 0.f;
@@ -476,8 +593,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         __syncthreads();
         // T = (I + Diag(beta) A)^{-1} in shared memory: eight threads per column, rows in order
         {
-            float* Ns = gsm;               // Diag(beta) A [64][65]
-            float* Ts = gsm + C * (C + 1); // T [64][65]
+            float* Ns = gsm;                // Diag(beta) A [64][65]
+            float* Ts = gsm + C * (C + 1);  // T [64][65]
             for (int e = tid; e < MQ; e += kChunkThreads) Ns[(e >> 6) * (C + 1) + (e & 63)] = bs[e >> 6] * Am[e];
             __syncthreads();
             const int j = tid >> 3, part = tid & 7;
@@ -493,14 +610,12 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             __syncthreads();
             for (int e = tid; e < MQ; e += kChunkThreads) Tm[e] = Ts[(e >> 6) * (C + 1) + (e & 63)];
         }
-        // dT = dW (Diag(beta) X)^T + dU (Diag(beta) v)^T;  dBk = T^T dW;  dBv = T^T dU;
+        // dT = [dW | dU] [Diag(beta) X | Diag(beta) v]^T;  [dBk | dBv] = T^T [dW | dU];
         // dM = -T^T dT T^T
-        cta_gemm<C, C, D>(DT, C, DW, D, false, XB, D, true, 0, 1.f, false, gsm);
-        cta_gemm<C, C, D>(DT, C, DU, D, false, VB, D, true, 0, 1.f, true, gsm);
-        cta_gemm<C, D, C>(DBK, D, Tm, C, true, DW, D, false, 0, 1.f, false, gsm);
-        cta_gemm<C, D, C>(DBV, D, Tm, C, true, DU, D, false, 0, 1.f, false, gsm);
-        cta_gemm<C, C, C>(TMP, C, DT, C, false, Tm, C, true, 0, 1.f, false, gsm);
-        cta_gemm<C, C, C>(DM, C, Tm, C, true, TMP, C, false, 0, -1.f, false, gsm);
+        cta_gemm<C, C, 2 * D>(DT, C, DWU, 2 * D, false, XVB, 2 * D, true, 1.f, false, gsm);
+        cta_gemm<C, 2 * D, C>(DBKV, 2 * D, Tm, C, true, DWU, 2 * D, false, 1.f, false, gsm);
+        cta_gemm<C, C, C>(TMP, C, DT, C, false, Tm, C, true, 1.f, false, gsm);
+        cta_gemm<C, C, C>(DM, C, Tm, C, true, TMP, C, false, -1.f, false, gsm);
         for (int e = tid; e < MQ; e += kChunkThreads) {
             const int r = e >> 6, j = e & 63;
             DA[e] = j < r ? bs[r] * DM[e] : 0.f;
@@ -510,60 +625,45 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             const int r = tid >> 3, part = tid & 7;
             float a = 0.f;
             for (int j = part; j < C; j += 8) a += DM[r * C + j] * Am[r * C + j];
-            for (int c = part; c < D; c += 8) a += DBK[r * D + c] * K_[r * D + c] * EA[r * D + c] + DBV[r * D + c] * V_[r * D + c];
+            for (int c = part; c < D; c += 8)
+                a += DBKV[r * 2 * D + c] * K_[r * D + c] * EA[r * D + c] + DBKV[r * 2 * D + D + c] * V_[r * D + c];
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             a += __shfl_xor_sync(0xffffffffu, a, 4);
             if (part == 0 && r < L) dbeta[(c0 + r) * H + h] = a;
         }
-        for (int e = tid; e < MR; e += kChunkThreads) {
-            const int r = e >> 7, c = e & 127;
-            if (r < L) dv[((c0 + r) * H + h) * D + c] = bs[r] * DBV[e];
-        }
-        // the gated back-products
-        cta_gemm<C, D, C>(GB, D, DA, C, false, KRF, D, false, MR, 1.f, false, gsm);   // (dA Y) e^G / Lf
-        cta_gemm<C, D, C>(GF, D, DP, C, false, KRF, D, false, MR, 1.f, false, gsm);   // (dP Y) e^G / Lf
-        for (int e = tid; e < MR; e += kChunkThreads) GC[e] = 0.f;
-        for (int b = 0; b < 4; ++b) {
-            // rows j of block-b contributions: sum_{r in b} dA[r][j] kL[r] and dP[r][j] qL[r],
-            // times e^{G_m(b) - G_j}
-            for (int pass = 0; pass < 2; ++pass) {
-                cta_gemm<C, D, 16>(PART, D, (pass == 0 ? DA : DP) + 16 * b * C, C, true,
-                                   (pass == 0 ? KL : QL) + 16 * b * D, D, false, 0, 1.f, false, gsm);
-                for (int e = tid; e < MR; e += kChunkThreads) {
-                    // e^{G_m(b) - G_j} (0 for j past block b)
-                    const int j = e >> 7, c = e & 127, B = j >> 4;
-                    const float pr = PRE[e];
-                    float f = 0.f;
-                    if (B == b) {
-                        f = 1.f / pr;
-                    } else if (B < b) {
-                        f = tot[B * D + c] / pr;
-                        for (int b2 = B + 1; b2 < b; ++b2) f *= tot[b2 * D + c];
-                    }
-                    GC[e] += PART[e] * f;
-                }
+        for (int u = tid; u < MR / 4; u += kChunkThreads) {
+            const int r = u >> 5, c = 4 * (u & 31);
+            if (r < L) {
+                const float4 x = *reinterpret_cast<const float4*>(DBKV + r * 2 * D + D + c);
+                const float br = bs[r];
+                *reinterpret_cast<float4*>(dv + ((c0 + r) * H + h) * D + c) =
+                    make_float4(br * x.x, br * x.y, br * x.z, br * x.w);
             }
         }
-        __syncthreads();
+        // the gated back-products: GB = (dA k e^{G_m - G_j}) per row block, GF the same with
+        // dP (both times e^{G_r - G_m} later); GC = the transposed ones with kL and qL (times
+        // 1 / pre_j later)
+        gated_rows(GB, DA, K_, PRE, ptot, gsm);
+        gated_rows(GF, DP, K_, PRE, ptot, gsm);
+        gated_cols(GC, DA, KL, ptot, false, gsm);
+        gated_cols(GC, DP, QL, ptot, true, gsm);
+
         // ---- dq, dk, dG ----------------------------------------------------------------------
         for (int e = tid; e < MR; e += kChunkThreads) {
             const int r = e >> 7, c = e & 127, B = r >> 4;
             const float pr = PRE[e], ea = EA[e], kk = K_[e], qq = Q_[e];
-            float after = 1.f;   // e^{G_C - G_r}
-            for (int b = B + 1; b < 4; ++b) after *= tot[b * D + c];
-            const float kbf = tot[B * D + c] / pr * after;
-            const float dxe = bs[r] * DBK[e] * ea + GB[e] * pr;   // dX e^G
-            const float dye = GC[e];                                // dY e^{-G}
-            const float dqq = DXQ[e] * ea + GF[e] * pr;             // dXq e^G
+            const float kbf = ptot[(B * 4 + 3) * D + c] * tot[3 * D + c] / pr;   // e^{G_C - G_r}
+            const float dxe = bs[r] * DBKV[r * 2 * D + c] * ea + GB[e] * pr;  // dX e^G
+            const float dye = GC[e] / pr;                                       // dY e^{-G}
+            const float dqq = DXQ[e] * ea + GF[e] * pr;                         // dXq e^G
             const float dkb = DKB[e];
-            const float dkk = dxe + dye + dkb * kbf;
             gsm[e] = kk * dxe - kk * dye + qq * dqq - dkb * kk * kbf;   // dG
             gsm[MR + e] = dkb * kk * kbf;                              // dKb Kb
             if (r < L) {
                 const int64_t o = ((c0 + r) * H + h) * D + c;
                 dq[o] = dqq;
-                dk[o] = dkk;
+                dk[o] = dxe + dye + dkb * kbf;
             }
         }
         __syncthreads();
