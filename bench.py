@@ -522,15 +522,25 @@ def run_ours(args, world, rank, local):
         bw_ms, bwper = time_launches(bwstep, nb, stream)
         bw_ms = max_over_ranks(bw_ms, world) / nb
         bw_bytes = T * H * ((3 * K + V) * 2 + 2 + 4 * V + (3 * K + V) * 4 + 4)
-        bw_ach = bw_bytes / (sum(bwper) / len(bwper) * 1e-3) / 1e9
+        bw_call = sum(bwper) / len(bwper)
+        bw_gbs = bw_bytes / (bw_call * 1e-3) / 1e9
+        # fp32 multiply-adds of the chunked backward's CUDA-core kernels per (64-token chunk, head):
+        # the reverse chain (dU, dS) and the chunk kernel (its 17 products), as launched
+        chunks = (T + 63) // 64 * H
+        bw_flops = 2 * chunks * (64 * 128 * 192 + 2 * 128 * 128 * 64 + 9961472)
+        # fp32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the sampled maximum SM clock
+        alu_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * (
+            clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+        bw_tf = bw_flops / (bw_call * 1e-3) / 1e12
         backward = {"value": world * T / (bw_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": bw_ms,
-                    "workload": "backward of the 4096-token prefill (dq, dk, dv, dg, dbeta, dS0), "
-                                "token by token in fp32",
-                    "roofline": {"bound": "latency", "achieved": bw_ach, "peak": hbm, "unit": "GB/s",
-                                 "frac": bw_ach / hbm, "traffic": None, "algorithmic_bytes": bw_bytes,
-                                 "peak_kind": peak_kind,
-                                 "note": "a serial token-by-token chain per (sequence, head): bound by its "
-                                         "latency, not by HBM; frac is against HBM for scale only"}}
+                    "workload": "backward of the 4096-token prefill (dq, dk, dv, dg, dbeta, dS0): the "
+                                "tensor-core prefill again keeping every chunk's state, a reverse chain "
+                                "carrying dS, chunk-parallel gradients (fp32 CUDA cores)",
+                    "gpu_launches": 4 * nb,
+                    "roofline": {"bound": "alu", "achieved": bw_tf, "peak": alu_peak, "unit": "TFLOP/s",
+                                 "frac": bw_tf / alu_peak, "traffic": None, "algorithmic_flops": bw_flops,
+                                 "peak_kind": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
+                                 "algorithmic_bytes": bw_bytes, "hbm_gbs": bw_gbs, "hbm_frac": bw_gbs / hbm}}
     else:
         backward = {"error": bw_err or "failed on another rank"}
     del dO, bws
@@ -630,6 +640,12 @@ def profile_case(args):
                                                                args.profile_H, 9).items()}
         for _ in range(args.profile_reps):
             kda.gate_proj(gp["x"], gp["f_a"], gp["f_b"], gp["b_proj"])
+    elif args.profile_case == "bwd":
+        d = synth.device_inputs("prefill", dev)
+        dO = torch.randn(d["q"].shape[:3] + (d["v"].shape[-1],), device=dev,
+                         generator=torch.Generator(device=dev).manual_seed(11))
+        for _ in range(args.profile_reps):
+            kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO, scale=d["scale"])
     elif args.profile_case == "output_gate":
         og = synth.output_gate_inputs((1, args.profile_T, args.profile_H, 128), torch.bfloat16, 7)
         o, g, wt = (og[k].to(dev) for k in ("o", "gate", "weight"))
@@ -649,7 +665,7 @@ def profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode", "output_gate", "gate_proj"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "fused", "decode", "output_gate", "gate_proj", "bwd"], default=None,
                     help="run a few launches of one kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-T", type=int, default=2048)
     ap.add_argument("--profile-H", type=int, default=16)
