@@ -87,7 +87,7 @@ constexpr uint32_t RT_LO = 96 * D * 2;
 constexpr uint32_t SM_TOT = SM_SMALL;            // fp32 [4][128] block totals of e^g
 constexpr uint32_t SM_ITOT = SM_SMALL + 2048;    // fp32 [2][128] inverses of the totals of blocks 0, 2
 constexpr uint32_t SM_BETA = SM_SMALL + 3072;    // fp32 [64]
-constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tma, mma), tmem base, exit drain, testing
+constexpr uint32_t SM_BAR = SM_BETA + 256;       // barriers (tiles, mma), tmem base, exit drain, testing, g tile
 constexpr uint32_t SM_LOCAL_TOTAL = SM_BAR + 64;
 // with the input prologue (raw q, k, v and gate input in the staging tiles):
 constexpr uint32_t SM_RED = SM_SMALL + 3456;     // fp32 [2][64][4] partial sums of squares of q, k rows
@@ -171,6 +171,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_tma + 2);
     uint64_t* bar_fin = bar_tma + 3;   // every MMA issued has completed (exit drain)
     uint64_t* bar_never = bar_tma + 4; // testing: nothing arrives on it
+    uint64_t* bar_g = bar_tma + 5;     // the g tile, loaded one task ahead of q, k, v (without the prologue)
     const int H = pl.H;
     const __nv_bfloat16* __restrict__ beta_g = reinterpret_cast<const __nv_bfloat16*>(beta_ptr);
 
@@ -180,6 +181,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         tc::bar_init(bar_mma, 1);
         tc::bar_init(bar_fin, 1);
         tc::bar_init(bar_never, 1);
+        tc::bar_init(bar_g, 1);
         tc::bar_init_fence();
     }
     tc::fence_async_smem();
@@ -188,18 +190,31 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     tc::fence_after();
     const uint32_t tm = *tmem_base_s;
 
-    uint32_t tma_phase = 0, mma_phase = 0;
+    uint32_t tma_phase = 0, mma_phase = 0, g_phase = 0;
     bool failed = false;
-    bool tma_pending = false;
+    bool tma_pending = false, g_pending = false;
 
+    // Without the prologue the g tile has a barrier of its own: its only reader is
+    // the prefix pass, which for task n + 1 runs during task n's T inverse, so the
+    // tile of task n + 1 is requested when task n starts and has landed by the
+    // time that pass needs it.  (With the prologue the g tile later holds the lo
+    // half of k, so all four tiles travel together.)
+    constexpr uint32_t kTileTx = FUSED ? 4u * 16384u + PRO_TX : 3u * 16384u;
+    auto issue_g = [&](const Chunk& ch) {
+        tc::bar_expect_tx(bar_g, 16384u);
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+            tc::tma_load_3d(smem + SM_STG + 3 * 16384 + half * 8192, &mg, half * 64, ch.h, (int)ch.c0, bar_g);
+    };
     auto issue_tma = [&](const Chunk& ch) {
-        tc::bar_expect_tx(bar_tma, 4u * 16384u + (FUSED ? PRO_TX : 0u));
+        tc::bar_expect_tx(bar_tma, kTileTx);
         const CUtensorMap* maps[4] = {&mq, &mk, &mv, &mg};
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
+        for (int t = 0; t < (FUSED ? 4 : 3); ++t)
 #pragma unroll
             for (int half = 0; half < 2; ++half)
                 tc::tma_load_3d(smem + SM_STG + t * 16384 + half * 8192, maps[t], half * 64, ch.h, (int)ch.c0, bar_tma);
+        if constexpr (!FUSED) issue_g(ch);
         if constexpr (FUSED) {
             // the 3 raw rows before the chunk (row -3 and up; rows before the tensor
             // arrive as zeros, rows of another sequence are masked when used)
@@ -219,10 +234,11 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     };
     // The same, spread over lane 0 of the warps of scheduler partitions 2 and 3 (one
     // tile each, the prologue's extra loads round-robin), for a task whose byte count
-    // bar_tma already expects.
+    // bar_tma already expects (the g tile only with the prologue).
     auto issue_tma_spread = [&](const Chunk& ch) {
         if ((warp & 2) == 0 || lane != 0) return;
         const int i = ((warp >> 2) << 1) | (warp & 1);
+        if (!FUSED && i >= 6) return;
         const CUtensorMap* mp = i < 2 ? &mq : (i < 4 ? &mk : (i < 6 ? &mv : &mg));
         tc::tma_load_3d(smem + SM_STG + (i >> 1) * 16384 + (i & 1) * 8192, mp, (i & 1) * 64, ch.h, (int)ch.c0,
                         bar_tma);
@@ -315,7 +331,49 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         tot_s[J * 128 + c] = run;
         if ((J & 1) == 0) itot_s[(J >> 1) * 128 + c] = __fdividef(1.f, run);
     };
-    bool pre_done = false;  // the current task's prefix pass has run
+    // (2a) the A/P A operand L in TMEM for one item (16 channels: [16 item, 16 item
+    // + 16) of every stack row of this warp's lane quadrant) of a task with Lr
+    // tokens: lane quadrant q4 holds the k rows (even q4) or q rows (odd q4) of row
+    // block R = q4 / 2; e^{G_r - G_mid} = pre_r / tot_{2R} before the block centre,
+    // pre_r after it
+    auto build_L = [&](int item, int Lr) {
+        const int q4 = warp & 3, R = q4 >> 1;
+        const int r = 32 * R + lane;
+        const bool first = (lane & 16) == 0;  // r in the first 16-token block of R
+        const uint8_t* src = smem + SM_STG + ((q4 & 1) != 0 ? 0 : 16384);
+        uint32_t lh[8], ll[8];
+#pragma unroll
+        for (int g8 = 0; g8 < 2; ++g8) {
+            const int c = 16 * item + 8 * g8;
+            float x[8], pr[8], it[8];
+            if (r < Lr) {
+                tc::unpack8(*reinterpret_cast<const uint4*>(src + tc::swz128(r, c)), x);
+                if constexpr (FUSED) {
+                    float y[8];
+                    tc::unpack8(*reinterpret_cast<const uint4*>(src + 32768 + tc::swz128(r, c)), y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] += y[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = 0.f;
+            }
+            const float4 p0 = *reinterpret_cast<const float4*>(pre_s + r * PRE_LD + c);
+            const float4 p1 = *reinterpret_cast<const float4*>(pre_s + r * PRE_LD + c + 4);
+            pr[0] = p0.x; pr[1] = p0.y; pr[2] = p0.z; pr[3] = p0.w; pr[4] = p1.x; pr[5] = p1.y; pr[6] = p1.z; pr[7] = p1.w;
+            const float4 a = *reinterpret_cast<const float4*>(itot_s + R * 128 + c);
+            const float4 b = *reinterpret_cast<const float4*>(itot_s + R * 128 + c + 4);
+            it[0] = a.x; it[1] = a.y; it[2] = a.z; it[3] = a.w; it[4] = b.x; it[5] = b.y; it[6] = b.z; it[7] = b.w;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                tc::split2(x[2 * u] * (first ? pr[2 * u] * it[2 * u] : pr[2 * u]),
+                           x[2 * u + 1] * (first ? pr[2 * u + 1] * it[2 * u + 1] : pr[2 * u + 1]),
+                           lh[4 * g8 + u], ll[4 * g8 + u]);
+        }
+        tc::tmem_st8(tm + lane_base(warp) + TL_LH + 8 * item, lh);
+        tc::tmem_st8(tm + lane_base(warp) + TL_LL + 8 * item, ll);
+    };
+    bool pre_done = false;  // the current task's prefix pass (and, without the prologue, its L operand) has run
 
     int64_t task = blockIdx.x;
     Chunk cur = decode_task(pl, task);
@@ -323,6 +381,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     if (cur.valid) {
         if (tid == kIssueTid) issue_tma(cur);
         tma_pending = true;
+        g_pending = !FUSED;
         beta_r = fetch_beta(cur);
     }
 
@@ -337,10 +396,18 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         if (!pre_done) {
             if (wait_one(bar_tma, tma_phase)) tma_pending = false;
             if (failed) break;
+            if constexpr (!FUSED) {
+                if (wait_one(bar_g, g_phase)) g_pending = false;
+                if (failed) break;
+            }
+        } else if (!FUSED && nxt.valid) {
+            // (the last task's T-inverse window has read this task's g tile)
+            if (tid == kIssueTid) issue_g(nxt);
+            g_pending = true;
         }
         // the next task's byte count, posted long before its loads are issued (by
         // several threads, so none of them may complete the phase early)
-        if (tid == kIssueTid && nxt.valid) tc::bar_expect_tx(bar_tma, 4u * 16384u + (FUSED ? PRO_TX : 0u));
+        if (tid == kIssueTid && nxt.valid) tc::bar_expect_tx(bar_tma, kTileTx);
 
         uint8_t* qs = smem + SM_STG;
         uint8_t* ks = smem + SM_STG + 16384;
@@ -438,7 +505,12 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_st_wait();
         }
         if (bt >= 0 && bt < C) beta_s[bt] = __uint_as_float((uint32_t)beta_r << 16);
+        if (!FUSED && !pre_done) tc::fence_async_smem();   // (the g tile is read: the next one may land)
         __syncthreads();
+        if (!FUSED && !pre_done && nxt.valid) {
+            if (tid == kIssueTid) issue_g(nxt);
+            g_pending = true;
+        }
 
         if constexpr (FUSED) {
             // q, k = l2norm(act(conv4(raw))) over the 128 channels of each row, written
@@ -509,35 +581,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         // Both blocks' operands are stacked (L rows 64 R + i, Rt rows of block 1 after
         // those of block 0) and multiplied in one M = 128, N = 96 round; the two
         // off-diagonal products of the stack are not used.
-        {
-            // L (A operand, TMEM lane = stack row 64 R + i): lane quadrant q4 holds the
-            // k rows (even q4) or q rows (odd q4) of block R = q4 / 2, warpgroup wg the
-            // channels [32 wg, 32 wg + 32); e^{G_r - G_mid} = pre_r / tot_{2R} before the
-            // centre, pre_r after it
-            const int q4 = warp & 3, wg = warp >> 2, R = q4 >> 1;
-            const int r = 32 * R + lane;
-            const bool first = (lane & 16) == 0;  // r in the first 16-token block of R
+        // (Without the prologue, L was built while the last task's W/U MMAs ran.)
+        if (FUSED || !pre_done) {
 #pragma unroll 1
-            for (int h16 = 0; h16 < 2; ++h16) {
-                uint32_t lh[8], ll[8];
-#pragma unroll
-                for (int g8 = 0; g8 < 2; ++g8) {
-                    const int c = 32 * wg + 16 * h16 + 8 * g8;
-                    float x[8], pr[8], it[8];
-                    ld8((q4 & 1) != 0, r, c, x);
-                    ld_pre8(r, c, pr);
-                    const float4 a = *reinterpret_cast<const float4*>(itot_s + R * 128 + c);
-                    const float4 b = *reinterpret_cast<const float4*>(itot_s + R * 128 + c + 4);
-                    it[0] = a.x; it[1] = a.y; it[2] = a.z; it[3] = a.w; it[4] = b.x; it[5] = b.y; it[6] = b.z; it[7] = b.w;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        tc::split2(x[2 * u] * (first ? pr[2 * u] * it[2 * u] : pr[2 * u]),
-                                   x[2 * u + 1] * (first ? pr[2 * u + 1] * it[2 * u + 1] : pr[2 * u + 1]),
-                                   lh[4 * g8 + u], ll[4 * g8 + u]);
-                }
-                tc::tmem_st8(tm + lane_base(warp) + TL_LH + 16 * wg + 8 * h16, lh);
-                tc::tmem_st8(tm + lane_base(warp) + TL_LL + 16 * wg + 8 * h16, ll);
-            }
+            for (int it = 0; it < 2; ++it) build_L(2 * (warp >> 2) + it, L);
         }
         // the last task's -W bulk stores have read the operand region before Rt overwrites it
         if (tid == kIssueTid) tc::bulk_wait_read();
@@ -833,12 +880,21 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
         } else if (nxt.valid) {
             bool ok = true;
-            if (warp == 4) ok = tc::bar_wait(bar_tma, tma_phase, pl.wait_iter);
+            if (warp == 4) ok = FUSED ? tc::bar_wait(bar_tma, tma_phase, pl.wait_iter)
+                                      : tc::bar_wait(bar_g, g_phase, pl.wait_iter);
             nxt_ok = !tc::named_any(2, NT - 128, !ok);
+            const int Ln = (nxt.eos - nxt.c0 < (int64_t)C) ? (int)(nxt.eos - nxt.c0) : C;
             if (nxt_ok) {
                 tc::fence_after();
-                const int Ln = (nxt.eos - nxt.c0 < (int64_t)C) ? (int)(nxt.eos - nxt.c0) : C;
                 for (int item = tid - 128; item < 4 * 128; item += NT - 128) prefix_item(item & 127, item >> 7, Ln);
+                if constexpr (!FUSED) tc::fence_async_smem();   // (the g tile is read: the next one may land)
+            }
+            if constexpr (!FUSED) {
+                // the q, k, v tiles (their L operand is built while the W/U MMAs run)
+                if (nxt_ok) {
+                    if (warp == 4) ok = tc::bar_wait(bar_tma, tma_phase, pl.wait_iter);
+                    nxt_ok = !tc::named_any(2, NT - 128, !ok);
+                }
             }
         }
         {
@@ -847,6 +903,10 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (nxt.valid && !gave_up) {
                 tma_phase ^= 1;
                 tma_pending = false;
+                if constexpr (!FUSED) {
+                    g_phase ^= 1;
+                    g_pending = false;
+                }
             }
             failed = failed || gave_up;
             pre_done = nxt.valid && !gave_up;
@@ -886,6 +946,14 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 if constexpr (FUSED) tc::mma_ts_w(tm + TL_AU, tm + TL_VTL + ks_ * 8, bh, id_n64, 1);
             }
             tc::commit_w(bar_mma);
+        }
+        if (!FUSED && pre_done) {
+            // meanwhile the next task's L operand (its A/P MMAs' TMEM is free)
+            tc::fence_after();
+            const int Ln = (nxt.eos - nxt.c0 < (int64_t)C) ? (int)(nxt.eos - nxt.c0) : C;
+#pragma unroll 1
+            for (int it = 0; it < 2; ++it) build_L(2 * (warp >> 2) + it, Ln);
+            tc::tmem_st_wait();
         }
         mma_sync();
         if (failed) break;
@@ -934,6 +1002,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             reinterpret_cast<float*>(pl.slots + ((int64_t)cur.gc * H + cur.h) * (int64_t)SLOT_BYTES + SLOT_EGC)[tid] =
                 __int_as_float(0x7fc00000);
         if (tma_pending && tid == 0) tc::bar_wait(bar_tma, tma_phase, kWaitIter);
+        if (g_pending && tid == 0) tc::bar_wait(bar_g, g_phase, kWaitIter);
     }
     if (tid == kIssueTid) tc::bulk_wait();
     // MMAs that a wait gave up on may still run: they complete before TMEM is released
