@@ -20,12 +20,14 @@
 //
 // Kernels, on the caller's stream:
 //   the forward (chunk_tc_forward_states): the tensor-core prefill, also writing the
-//       state entering every chunk; its workspace slots keep W, Qs = scale Xq, Kb,
-//       scale P, U~ and e^{G_C} per (chunk, head);
+//       state entering every chunk and each chunk's A and T; its workspace slots keep
+//       W, Qs = scale Xq, Kb, scale P, U~ and e^{G_C} per (chunk, head);
 //   bwd_chain_kernel: one CTA per (sequence, head) carries dS backwards through the
 //       chunks (the first two lines above, fp32 on the CUDA cores, operands read
 //       from the slots) and stores dS' and dU of every chunk;
-//   bwd_chunk_kernel: one CTA per (chunk, head) task forms dq, dk, dv, dg, dbeta.
+//   bwd_chunk_kernel: one CTA per (chunk, head) task forms dq, dk, dv, dg, dbeta; its
+//       products are tensor-core rounds (tcgen05, operands split hi | lo into bf16,
+//       fp32 accumulators in tensor memory) on operands staged from a per-CTA scratch.
 #include "kda_chunk.h"
 #include "kda_chunk_plan.cuh"
 #include "kda_common.cuh"
@@ -231,43 +233,63 @@ enum : int {
     SC_U = SC_QL + MR, SC_DXQ = SC_U + MR, SC_DWU = SC_DXQ + MR, SC_DKB = SC_DWU + 2 * MR,
     SC_DBKV = SC_DKB + MR, SC_XVB = SC_DBKV + 2 * MR, SC_GB = SC_XVB + 2 * MR, SC_GF = SC_GB + MR,
     SC_GC = SC_GF + MR,
-    SC_DP = SC_GC + MR, SC_A = SC_DP + MQ, SC_T = SC_A + MQ, SC_DT = SC_T + MQ, SC_TMP = SC_DT + MQ,
+    SC_DP = SC_GC + MR, SC_DT = SC_DP + MQ, SC_TMP = SC_DT + MQ,
     SC_DM = SC_TMP + MQ, SC_DA = SC_DM + MQ,
     SC_TOTAL = SC_DA + MQ
 };
-// shared memory of the chunk kernel: the GEMM staging area, then small tables
-constexpr int GEMM_FLOATS = 128 * 68 + 4 * 128 * 68;   // the largest staging (the gated A product)
-constexpr uint32_t BK_TOT = GEMM_FLOATS * 4;            // tot [4][128]: e^g products over each 16-token block
+static_assert(SC_TOTAL * 4 == 770048, "the per-CTA scratch size stated in kda.h");
+// Shared memory of the chunk kernel: the operand images of one tensor-core round
+// (bf16 hi | lo), then small tables and the MMA barriers.
+constexpr uint32_t OP_BYTES = 160 * 1024;               // the largest round: A 128 x 64 + 4 B variants 128 x 64
+constexpr uint32_t BK_TOT = OP_BYTES;                   // tot [4][128]: e^g products over each 16-token block
 constexpr uint32_t BK_PT = BK_TOT + 4 * D * 4;          // ptot [4 B][4 b][128]: prod of tot over blocks [B, b)
 constexpr uint32_t BK_BETA = BK_PT + 16 * D * 4;        // beta [64]
 constexpr uint32_t BK_DEC = BK_BETA + C * 4;            // dEC [128]
 constexpr uint32_t BK_EC = BK_DEC + D * 4;              // e^{G_C} [128]
-constexpr uint32_t BK_TOTAL = BK_EC + D * 4;
+constexpr uint32_t BK_BAR = BK_EC + D * 4;              // MMA barrier, exit barrier, TMEM base
+constexpr uint32_t BK_TOTAL = BK_BAR + 64;
 static_assert(BK_TOTAL <= 232448, "shared memory of the chunk kernel");
+static_assert(2 * C * (C + 1) * 4 <= OP_BYTES && 2 * MR * 4 <= OP_BYTES, "scratch uses of the operand area");
 
-// The float4 unit i of an [R][CO] matrix -> its row r and first column c.  For a
-// transposed store (TR), each warp covers eight consecutive rows of four column
-// groups, which keeps the scattered shared-memory stores free of most conflicts.
-template <int R, int CO, bool TR>
+// The float4 unit i of an [R][CO] matrix -> its row r and first column c: each warp
+// covers eight consecutive rows of four consecutive column groups, so that the
+// operand stores below fill whole 128-byte runs.
+template <int R, int CO>
 __device__ __forceinline__ void unit_rc(int i, int& r, int& c) {
-    if (TR) {
-        const int rest = i >> 3;
-        c = 4 * (rest % (CO / 4));
-        r = (rest / (CO / 4)) * 8 + (i & 7);
-    } else {
-        r = i / (CO / 4);
-        c = 4 * (i % (CO / 4));
-    }
+    const int rest = i >> 3;
+    c = 4 * (rest % (CO / 4));
+    r = (rest / (CO / 4)) * 8 + (i & 7);
 }
 
-// An [R][CO] fp32 matrix in global memory (row stride ld, 16-byte aligned rows) into
-// shared memory, each float4 passed through f(r, c, v) first: dst[r][c] (TR false) or
-// dst[c][r] (TR true), row stride ldd.  Four float4 loads in flight per thread.
 struct Ident {
     __device__ __forceinline__ void operator()(int, int, float4&) const {}
 };
-template <int R, int CO, bool TR, typename F = Ident>
-__device__ __forceinline__ void stage(const float* src, int ld, float* dst, int ldd, F f = F()) {
+struct OneVariant {
+    __device__ __forceinline__ int operator()(int) const { return 0; }
+};
+
+// ---- tensor-core rounds ------------------------------------------------------------
+// An operand image is [rows][Kd] bf16 without swizzle: 8-row groups Kd * 16 bytes
+// apart, groups of 8 k 128 bytes apart; inside a 16-byte core-matrix row either 8
+// consecutive k of one operand row (K-major) or 8 consecutive operand rows of one k
+// (MN-major).  Both take the descriptor strides (128, Kd * 16), and 16 k further on
+// is 256 bytes further.  Each product is formed as hi hi + hi lo + lo hi of the
+// operands split x = hi + lo into bf16 (about 16 significant bits), accumulated in
+// fp32 in tensor memory.
+__device__ __forceinline__ uint32_t op_off(int row, int k, int Kd, bool mn) {
+    return (uint32_t)((row >> 3) * (Kd * 16) + (k >> 3) * 128 +
+                      (mn ? (k & 7) * 16 + (row & 7) * 2 : (row & 7) * 16 + (k & 7) * 2));
+}
+
+// An [R][CO] fp32 matrix in global memory (row stride ld) into an operand image, each
+// float4 passed through f(r + r_off, c + c_off, v) first (its coordinates in the
+// whole matrix).  KROW: the matrix rows are operand rows row0 + r and its columns
+// are k (K-major image); else its rows are k and its columns operand rows row0 + c
+// (MN-major image).  Four float4 loads in flight per thread.
+template <int R, int CO, bool KROW, typename F = Ident>
+__device__ __forceinline__ void stage_op(const float* src, int ld, uint8_t* hi, uint8_t* lo, int Kd, int row0,
+                                         int r_off = 0, int c_off = 0, F f = F()) {
+    static_assert(R % 8 == 0 && CO % 4 == 0, "operand tile");
     constexpr int NV = R * (CO / 4);
     for (int i0 = threadIdx.x; i0 < NV; i0 += 4 * kChunkThreads) {
         float4 v[4];
@@ -276,7 +298,7 @@ __device__ __forceinline__ void stage(const float* src, int ld, float* dst, int 
             const int i = i0 + u * kChunkThreads;
             if (i < NV) {
                 int r, c;
-                unit_rc<R, CO, TR>(i, r, c);
+                unit_rc<R, CO>(i, r, c);
                 v[u] = *reinterpret_cast<const float4*>(src + (int64_t)r * ld + c);
             }
         }
@@ -285,82 +307,136 @@ __device__ __forceinline__ void stage(const float* src, int ld, float* dst, int 
             const int i = i0 + u * kChunkThreads;
             if (i >= NV) break;
             int r, c;
-            unit_rc<R, CO, TR>(i, r, c);
-            f(r, c, v[u]);
-            if (TR) {
-                dst[(c + 0) * ldd + r] = v[u].x;
-                dst[(c + 1) * ldd + r] = v[u].y;
-                dst[(c + 2) * ldd + r] = v[u].z;
-                dst[(c + 3) * ldd + r] = v[u].w;
-            } else {
-                *reinterpret_cast<float4*>(dst + r * ldd + c) = v[u];
-            }
+            unit_rc<R, CO>(i, r, c);
+            f(r + r_off, c + c_off, v[u]);
+            uint2 h, l;
+            tc::split2(v[u].x, v[u].y, h.x, l.x);
+            tc::split2(v[u].z, v[u].w, h.y, l.y);
+            const uint32_t o = KROW ? op_off(row0 + r, c, Kd, false) : op_off(row0 + c, r, Kd, true);
+            *reinterpret_cast<uint2*>(hi + o) = h;
+            *reinterpret_cast<uint2*>(lo + o) = l;
         }
     }
 }
+// Operand rows [row0, 128) of an image set to zero (one contiguous range per half).
+__device__ __forceinline__ void zero_rows(uint8_t* hi, uint8_t* lo, int Kd, int row0) {
+    const int b0 = (row0 >> 3) * Kd * 16, n = (16 - (row0 >> 3)) * Kd * 16;
+    for (int i = threadIdx.x * 16; i < n; i += kChunkThreads * 16) {
+        *reinterpret_cast<uint4*>(hi + b0 + i) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(lo + b0 + i) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
 
-// C[M x N] (row-major, ldc) = alpha A B (+ C when acc), fp32, by the whole CTA, with
-// the operands staged into shared memory by the caller's functions: sa(As, LA) writes
-// As[k][m], sb(Bs, LB, b) writes Bs[k][n] for B variant b (nb of them: with nb = 4 the
-// output rows [16 b, 16 b + 16) use variant b).  A thread computes 4 x 4 outputs.
-template <int M, int N, int K, typename SA, typename SB>
-__device__ __forceinline__ void cta_mm(float* Cm, int ldc, SA sa, SB sb, int nb, float alpha, bool acc, float* sm) {
-    constexpr int LA = M + 4, LB = N + 4;
-    float* As = sm;
-    float* Bs = sm + K * LA;
-    __syncthreads();   // the previous readers of the staging area and writers of the operands are done
-    sa(As, LA);
-    for (int b = 0; b < nb; ++b) sb(Bs + b * K * LB, LB, b);
+// The tensor-memory accumulators and the barrier of the rounds.
+struct Tc {
+    uint8_t* op;        // operand area
+    uint32_t tm;        // TMEM base (512 columns)
+    uint64_t* bar;      // MMA completion
+    uint32_t phase;
+    uint32_t wait_iter;
+    bool failed;
+};
+
+// One round: D_b (+)= A B_b^T for the NB variants b (TMEM columns [b N, b N + N)),
+// M = 128 rows, K = Kd; sa(a_hi, a_lo) writes A [128][Kd], sb(b_hi, b_lo, b) B_b
+// [N][Kd].  acc: add to what the accumulators hold.  False if the wait gave up.
+template <int N, int NB, bool A_MN, bool B_MN, typename SA, typename SB>
+__device__ __forceinline__ bool tc_round(Tc& t, int Kd, bool acc, SA sa, SB sb) {
+    static_assert(N % 16 == 0 && N >= 16 && N <= 256 && N * NB <= 512, "accumulator shape");
+    const int warp = threadIdx.x >> 5;
+    uint8_t* a_hi = t.op;
+    uint8_t* a_lo = a_hi + 128 * Kd * 2;
+    uint8_t* b_base = a_hi + 128 * Kd * 4;
+    const int bstride = N * Kd * 4;
+    tc::fence_before();
+    __syncthreads();   // the last round's MMAs and epilogue are done with the operand area and TMEM
+    sa(a_hi, a_lo);
+    for (int b = 0; b < NB; ++b) sb(b_base + b * bstride, b_base + b * bstride + N * Kd * 2, b);
+    tc::fence_async_smem();
+    tc::fence_before();
     __syncthreads();
-    constexpr int TN = N / 4;
-    for (int t = threadIdx.x; t < (M / 4) * TN; t += kChunkThreads) {
-        const int tm = t / TN, tn = t % TN;
-        const float* Bsb = Bs + (nb > 1 ? ((4 * tm) >> 4) * K * LB : 0);
-        float a4[4][4] = {};
-#pragma unroll 4
-        for (int k = 0; k < K; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(As + k * LA + 4 * tm);
-            const float4 b = *reinterpret_cast<const float4*>(Bsb + k * LB + 4 * tn);
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) a4[p][q] += av[p] * bv[q];
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float* cr = Cm + (int64_t)(4 * tm + p) * ldc + 4 * tn;
-            float4 v = make_float4(alpha * a4[p][0], alpha * a4[p][1], alpha * a4[p][2], alpha * a4[p][3]);
-            if (acc) {
-                const float4 o = *reinterpret_cast<const float4*>(cr);
-                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+    tc::fence_after();
+    if (warp == 0) {
+        constexpr uint32_t id = tc::idesc_bf16(128, N, false, B_MN, A_MN);
+        const uint32_t ah = tc::smem_u32(a_hi), al = tc::smem_u32(a_lo);
+        for (int b = 0; b < NB; ++b) {
+            const uint32_t bh = tc::smem_u32(b_base + b * bstride), bl = bh + N * Kd * 2;
+            const uint32_t d = t.tm + (uint32_t)(b * N);
+            for (int ks = 0; ks < Kd / 16; ++ks) {
+                const uint32_t o = ks * 256;
+                const uint64_t dah = tc::sdesc(ah + o, 128, Kd * 16), dal = tc::sdesc(al + o, 128, Kd * 16);
+                const uint64_t dbh = tc::sdesc(bh + o, 128, Kd * 16), dbl = tc::sdesc(bl + o, 128, Kd * 16);
+                tc::mma_ss_w(d, dah, dbh, id, (acc || ks > 0) ? 1u : 0u);
+                tc::mma_ss_w(d, dah, dbl, id, 1u);
+                tc::mma_ss_w(d, dal, dbh, id, 1u);
             }
-            *reinterpret_cast<float4*>(cr) = v;
         }
+        tc::commit_w(t.bar);
     }
-    __syncthreads();   // C is complete
+    bool ok = true;
+    if (warp == 0) ok = tc::bar_wait(t.bar, t.phase, t.wait_iter);
+    const bool gave_up = __syncthreads_or(!ok) != 0;
+    if (!gave_up) t.phase ^= 1;
+    t.failed = t.failed || gave_up;
+    tc::fence_after();
+    return !gave_up;
 }
 
-// The plain case: op(A)(m, k) = A[m lda + k] (ta false) or A[k lda + m]; op(B)(k, n) =
-// B[k ldb + n] (tb false) or B[n ldb + k].
-template <int M, int N, int K>
-__device__ __noinline__ void cta_gemm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* B, int ldb,
-                                      bool tb, float alpha, bool acc, float* sm) {
-    cta_mm<M, N, K>(
-        Cm, ldc,
-        [&](float* As, int LA) {
-            if (ta) stage<K, M, false>(A, lda, As, LA);
-            else stage<M, K, true>(A, lda, As, LA);
-        },
-        [&](float* Bs, int LB, int) {
-            if (tb) stage<N, K, true>(B, ldb, Bs, LB);
-            else stage<K, N, false>(B, ldb, Bs, LB);
-        },
-        1, alpha, acc, sm);
+// Epilogue of a round: row r < rows of D_{vsel(r)} (vsel constant over 16 rows), the
+// N columns split over the four warpgroups, 16 at a time: epi(r, c0, v[16]); called
+// by every thread, it returns once all the outputs are written.
+template <int N, int NB, typename VS, typename EPI>
+__device__ __forceinline__ void tc_epi(const Tc& t, int rows, VS vsel, EPI epi) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, wg = warp >> 2;
+    constexpr int CW = N / 4;
+    static_assert(CW % 16 == 0, "columns per warpgroup");
+    if (32 * q < rows) {
+        const int r = 32 * q + lane;
+        const uint32_t base = t.tm + ((uint32_t)(32 * q) << 16);
+        const int b0 = NB > 1 ? vsel(32 * q) : 0, b1 = NB > 1 ? vsel(32 * q + 16) : 0;
+#pragma unroll 1
+        for (int c0 = wg * CW; c0 < (wg + 1) * CW; c0 += 16) {
+            uint32_t u[16];
+            tc::tmem_ld16(base + (uint32_t)(b0 * N + c0), u);
+            if (NB > 1 && b1 != b0) {
+                uint32_t w[16];
+                tc::tmem_ld16(base + (uint32_t)(b1 * N + c0), w);
+                tc::tmem_ld_wait();
+                if (lane >= 16)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) u[e] = w[e];
+            } else {
+                tc::tmem_ld_wait();
+            }
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(u[e]);
+            epi(r, c0, v);
+        }
+    }
+    tc::fence_before();
+    __syncthreads();   // the outputs are complete
+}
+
+// C[c0 .. c0 + 16) of a row = alpha v (+ what it holds when acc)
+__device__ __forceinline__ void put16(float* cr, const float* v, float alpha, bool acc) {
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        float4 x = make_float4(alpha * v[e], alpha * v[e + 1], alpha * v[e + 2], alpha * v[e + 3]);
+        if (acc) {
+            const float4 o = *reinterpret_cast<const float4*>(cr + e);
+            x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
+        }
+        *reinterpret_cast<float4*>(cr + e) = x;
+    }
 }
 
 template <typename TIn>
 __device__ __forceinline__ float ld_in(const TIn* p) { return to_f32<TIn>(*p); }
+__device__ __forceinline__ void ld4(const float* p, float* x) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
 
 // Decay factors of the gated products, applied while staging (see bwd_chunk_kernel):
 // Krf(b): k_j e^{G_m(b) - G_j}, 0 for j past block b (staging k, rows j)
@@ -395,28 +471,6 @@ struct Alp {
     }
 };
 
-// A[r][j] = sum_c kL[r][c] Krf(b(r))(k)[j][c]: the gated k k^T product (before masking)
-__device__ __noinline__ void gated_kk(float* Am, const float* KL, const float* K_, const float* pre, const float* ptot,
-                                      float* sm) {
-    cta_mm<C, C, D>(
-        Am, C, [&](float* As, int LA) { stage<C, D, true>(KL, D, As, LA); },
-        [&](float* Bs, int LB, int b) { stage<C, D, true>(K_, D, Bs, LB, Krf{pre, ptot, b}); }, 4, 1.f, false, sm);
-}
-// out[r][c] = sum_j M[r][j] Krf(b(r))(k)[j][c]
-__device__ __noinline__ void gated_rows(float* out, const float* M, const float* K_, const float* pre,
-                                        const float* ptot, float* sm) {
-    cta_mm<C, D, C>(
-        out, D, [&](float* As, int LA) { stage<C, C, true>(M, C, As, LA); },
-        [&](float* Bs, int LB, int b) { stage<C, D, false>(K_, D, Bs, LB, Krf{pre, ptot, b}); }, 4, 1.f, false, sm);
-}
-// out[j][c] (+)= sum_r M[r][j] Alp(b(j))(aL)[r][c]
-__device__ __noinline__ void gated_cols(float* out, const float* M, const float* aL, const float* ptot, bool acc,
-                                        float* sm) {
-    cta_mm<C, D, C>(
-        out, D, [&](float* As, int LA) { stage<C, C, false>(M, C, As, LA); },
-        [&](float* Bs, int LB, int b) { stage<C, D, false>(aL, D, Bs, LB, Alp{ptot, b}); }, 4, 1.f, acc, sm);
-}
-
 // One (chunk, head) task per CTA at a time: the chunk's dq, dk, dv, dg, dbeta from the
 // entering state S, the gradient dS' of the state after it, dU and dO, plus the
 // forward's W and U~ (slot), all in fp32.  Decay factors are formed per 16-token row
@@ -427,7 +481,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
                  const __nv_bfloat16* __restrict__ beta, float scale, const float* __restrict__ dO,
-                 const float* __restrict__ states, const float* __restrict__ dsp, const float* __restrict__ du,
+                 const float* __restrict__ states, const float* __restrict__ at, const float* __restrict__ dsp,
+                 const float* __restrict__ du,
                  float* __restrict__ scratch, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                  float* __restrict__ dg, float* __restrict__ dbeta) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -437,8 +492,21 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* bs = reinterpret_cast<float*>(smem + BK_BETA);
     float* dec = reinterpret_cast<float*>(smem + BK_DEC);
     float* ec = reinterpret_cast<float*>(smem + BK_EC);
+    uint64_t* bar_mma = reinterpret_cast<uint64_t*>(smem + BK_BAR);
+    uint64_t* bar_fin = bar_mma + 1;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_mma + 2);
     const int tid = threadIdx.x;
     const int H = pl.H;
+    if ((tid >> 5) == 0) tc::tmem_alloc(tmem_base_s, 512);
+    if (tid == 0) {
+        tc::bar_init(bar_mma, 1);
+        tc::bar_init(bar_fin, 1);
+        tc::bar_init_fence();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    Tc t{smem, *tmem_base_s, bar_mma, 0u, pl.wait_iter, false};
     float* sc = scratch + (int64_t)blockIdx.x * SC_TOTAL;
     float* K_ = sc + SC_K;
     float* Q_ = sc + SC_Q;
@@ -459,8 +527,6 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* GF = sc + SC_GF;
     float* GC = sc + SC_GC;
     float* DP = sc + SC_DP;
-    float* Am = sc + SC_A;
-    float* Tm = sc + SC_T;
     float* DT = sc + SC_DT;
     float* TMP = sc + SC_TMP;
     float* DM = sc + SC_DM;
@@ -477,6 +543,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         const float* S = states + task * (int64_t)(D * D);
         const float* DSP = dsp + task * (int64_t)(D * D);
         const float* DU = du + task * (int64_t)(C * D);
+        const float* Am = at + task * (int64_t)(2 * MQ);   // A (strictly lower), from the forward
+        const float* Tm = Am + MQ;                          // T, from the forward
         __syncthreads();   // the previous task is done with the scratch and the tables
 
         // ---- inputs (0 past the sequence end), U~ and dU, prefix products, -W ----------
@@ -511,13 +579,19 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         }
         if (tid < C) bs[tid] = tid < L ? ld_in(beta + (c0 + tid) * H + h) : 0.f;
         {
+            // (the block's 16 gate values are loaded first, all in flight together)
             const int c = tid & 127, J = tid >> 7;
-            float run = 1.f;
+            float gv[16];
+#pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int r = 16 * J + u;
-                const float eg = r < L ? __expf(ld_in(g + ((c0 + r) * H + h) * D + c)) : 1.f;
-                run *= eg;
-                PRE[r * D + c] = run;
+                gv[u] = r < L ? ld_in(g + ((c0 + r) * H + h) * D + c) : 0.f;
+            }
+            float run = 1.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                run *= 16 * J + u < L ? __expf(gv[u]) : 1.f;
+                PRE[(16 * J + u) * D + c] = run;
             }
             tot[J * D + c] = run;
         }
@@ -561,12 +635,41 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             *reinterpret_cast<float4*>(XVB + r * 2 * D + D + c) = make_float4(br * vx.x, br * vx.y, br * vx.z, br * vx.w);
         }
 
-        // ---- the products with S, dS', U ----------------------------------------------------
-        cta_gemm<C, D, D>(U, D, WN, D, false, S, D, false, 1.f, true, gsm);              // U = U~ - W S
-        cta_gemm<C, D, D>(DXQ, D, DO_, D, false, S, D, true, scale, false, gsm);         // scale dO S^T
-        cta_gemm<C, D, D>(DWU, 2 * D, DU, D, false, S, D, true, -1.f, false, gsm);       // dW = -dU S^T
-        cta_gemm<C, D, D>(DKB, D, U, D, false, DSP, D, true, 1.f, false, gsm);           // U dS'^T
-        cta_gemm<C, C, D>(DP, C, DO_, D, false, U, D, true, scale, false, gsm);          // scale dO U^T
+        // ---- the products with S, dS', U (tensor-core rounds) ----------------------------
+        // U = U~ + (-W) S
+        tc_round<D, 1, false, true>(
+            t, D, false,
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, D, true>(WN, D, hi, lo, D, 0); zero_rows(hi, lo, D, C); },
+            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<D, D, false>(S, D, hi, lo, D, 0); });
+        if (t.failed) break;
+        tc_epi<D, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(U + r * D + c0, x, 1.f, true); });
+        // [dO; dU] [S; U]^T: scale dO S^T, dW = -dU S^T, scale dO U^T (dU U^T unused)
+        tc_round<D + C, 1, false, false>(
+            t, D, false,
+            [&](uint8_t* hi, uint8_t* lo) {
+                stage_op<C, D, true>(DO_, D, hi, lo, D, 0);
+                stage_op<C, D, true>(DU, D, hi, lo, D, C);
+            },
+            [&](uint8_t* hi, uint8_t* lo, int) {
+                stage_op<D, D, true>(S, D, hi, lo, D, 0);
+                stage_op<C, D, true>(U, D, hi, lo, D, D);
+            });
+        if (t.failed) break;
+        tc_epi<D + C, 1>(t, 2 * C, OneVariant{}, [&](int r, int c0, const float* x) {
+            if (r < C) {
+                if (c0 < D) put16(DXQ + r * D + c0, x, scale, false);
+                else put16(DP + r * C + (c0 - D), x, scale, false);
+            } else if (c0 < D) {
+                put16(DWU + (r - C) * 2 * D + c0, x, -1.f, false);
+            }
+        });
+        // U dS'^T
+        tc_round<D, 1, false, false>(
+            t, D, false,
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, D, true>(U, D, hi, lo, D, 0); zero_rows(hi, lo, D, C); },
+            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<D, D, true>(DSP, D, hi, lo, D, 0); });
+        if (t.failed) break;
+        tc_epi<D, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DKB + r * D + c0, x, 1.f, false); });
         {
             // dEC[c] = sum_x dS'[c][x] S[c][x]: four threads per channel, eight float4 each
             const int c = tid >> 2, part = tid & 3;
@@ -583,39 +686,41 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             if (part == 0) dec[c] = a;
         }
-        // A: the gated k k^T product per row block (strictly lower)
-        gated_kk(Am, KL, K_, PRE, ptot, gsm);
         for (int e = tid; e < MQ; e += kChunkThreads) {
             const int r = e >> 6, j = e & 63;
-            if (j >= r) Am[e] = 0.f;
             if (j > r) DP[e] = 0.f;
-        }
-        __syncthreads();
-        // T = (I + Diag(beta) A)^{-1} in shared memory: eight threads per column, rows in order
-        {
-            float* Ns = gsm;                // Diag(beta) A [64][65]
-            float* Ts = gsm + C * (C + 1);  // T [64][65]
-            for (int e = tid; e < MQ; e += kChunkThreads) Ns[(e >> 6) * (C + 1) + (e & 63)] = bs[e >> 6] * Am[e];
-            __syncthreads();
-            const int j = tid >> 3, part = tid & 7;
-            for (int r = 0; r < C; ++r) {
-                float a = 0.f;
-                for (int i = j + part; i < r; i += 8) a += Ns[r * (C + 1) + i] * Ts[i * (C + 1) + j];
-                a += __shfl_xor_sync(0xffffffffu, a, 1);
-                a += __shfl_xor_sync(0xffffffffu, a, 2);
-                a += __shfl_xor_sync(0xffffffffu, a, 4);
-                if (part == 0) Ts[r * (C + 1) + j] = r == j ? 1.f : (r < j ? 0.f : -a);
-                __syncwarp();
-            }
-            __syncthreads();
-            for (int e = tid; e < MQ; e += kChunkThreads) Tm[e] = Ts[(e >> 6) * (C + 1) + (e & 63)];
         }
         // dT = [dW | dU] [Diag(beta) X | Diag(beta) v]^T;  [dBk | dBv] = T^T [dW | dU];
         // dM = -T^T dT T^T
-        cta_gemm<C, C, 2 * D>(DT, C, DWU, 2 * D, false, XVB, 2 * D, true, 1.f, false, gsm);
-        cta_gemm<C, 2 * D, C>(DBKV, 2 * D, Tm, C, true, DWU, 2 * D, false, 1.f, false, gsm);
-        cta_gemm<C, C, C>(TMP, C, DT, C, false, Tm, C, true, 1.f, false, gsm);
-        cta_gemm<C, C, C>(DM, C, Tm, C, true, TMP, C, false, -1.f, false, gsm);
+        for (int hk = 0; hk < 2 && !t.failed; ++hk)
+            tc_round<C, 1, false, false>(
+                t, D, hk > 0,
+                [&](uint8_t* hi, uint8_t* lo) {
+                    stage_op<C, D, true>(DWU + hk * D, 2 * D, hi, lo, D, 0);
+                    zero_rows(hi, lo, D, C);
+                },
+                [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, D, true>(XVB + hk * D, 2 * D, hi, lo, D, 0); });
+        if (t.failed) break;
+        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DT + r * C + c0, x, 1.f, false); });
+        tc_round<2 * D, 1, true, true>(
+            t, C, false,
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
+            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, 2 * D, false>(DWU, 2 * D, hi, lo, C, 0); });
+        if (t.failed) break;
+        tc_epi<2 * D, 1>(t, C, OneVariant{},
+                         [&](int r, int c0, const float* x) { put16(DBKV + r * 2 * D + c0, x, 1.f, false); });
+        tc_round<C, 1, false, false>(
+            t, C, false,
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, true>(DT, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
+            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, C, true>(Tm, C, hi, lo, C, 0); });
+        if (t.failed) break;
+        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(TMP + r * C + c0, x, 1.f, false); });
+        tc_round<C, 1, true, true>(
+            t, C, false,
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
+            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, C, false>(TMP, C, hi, lo, C, 0); });
+        if (t.failed) break;
+        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DM + r * C + c0, x, -1.f, false); });
         for (int e = tid; e < MQ; e += kChunkThreads) {
             const int r = e >> 6, j = e & 63;
             DA[e] = j < r ? bs[r] * DM[e] : 0.f;
@@ -644,26 +749,61 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         // the gated back-products: GB = (dA k e^{G_m - G_j}) per row block, GF the same with
         // dP (both times e^{G_r - G_m} later); GC = the transposed ones with kL and qL (times
         // 1 / pre_j later)
-        gated_rows(GB, DA, K_, PRE, ptot, gsm);
-        gated_rows(GF, DP, K_, PRE, ptot, gsm);
-        gated_cols(GC, DA, KL, ptot, false, gsm);
-        gated_cols(GC, DP, QL, ptot, true, gsm);
+        tc_round<D, 4, false, true>(
+            t, C, false,
+            [&](uint8_t* hi, uint8_t* lo) {
+                stage_op<C, C, true>(DA, C, hi, lo, C, 0);
+                stage_op<C, C, true>(DP, C, hi, lo, C, C);
+            },
+            [&](uint8_t* hi, uint8_t* lo, int b) {
+                stage_op<C, D, false>(K_, D, hi, lo, C, 0, 0, 0, Krf{PRE, ptot, b});
+            });
+        if (t.failed) break;
+        tc_epi<D, 4>(t, 2 * C, [](int r) { return (r & 63) >> 4; }, [&](int r, int c0, const float* x) {
+            put16((r < C ? GB + r * D : GF + (r - C) * D) + c0, x, 1.f, false);
+        });
+        for (int part = 0; part < 2 && !t.failed; ++part)
+            tc_round<D, 4, true, true>(
+                t, C, part > 0,
+                [&](uint8_t* hi, uint8_t* lo) {
+                    stage_op<C, C, false>(part == 0 ? DA : DP, C, hi, lo, C, 0);
+                    zero_rows(hi, lo, C, C);
+                },
+                [&](uint8_t* hi, uint8_t* lo, int b) {
+                    stage_op<C, D, false>(part == 0 ? KL : QL, D, hi, lo, C, 0, 0, 0, Alp{ptot, b});
+                });
+        if (t.failed) break;
+        tc_epi<D, 4>(t, C, [](int r) { return r >> 4; },
+                     [&](int r, int c0, const float* x) { put16(GC + r * D + c0, x, 1.f, false); });
 
         // ---- dq, dk, dG ----------------------------------------------------------------------
-        for (int e = tid; e < MR; e += kChunkThreads) {
-            const int r = e >> 7, c = e & 127, B = r >> 4;
-            const float pr = PRE[e], ea = EA[e], kk = K_[e], qq = Q_[e];
-            const float kbf = ptot[(B * 4 + 3) * D + c] * tot[3 * D + c] / pr;   // e^{G_C - G_r}
-            const float dxe = bs[r] * DBKV[r * 2 * D + c] * ea + GB[e] * pr;  // dX e^G
-            const float dye = GC[e] / pr;                                       // dY e^{-G}
-            const float dqq = DXQ[e] * ea + GF[e] * pr;                         // dXq e^G
-            const float dkb = DKB[e];
-            gsm[e] = kk * dxe - kk * dye + qq * dqq - dkb * kk * kbf;   // dG
-            gsm[MR + e] = dkb * kk * kbf;                              // dKb Kb
+        // (four consecutive channels per item, the items' loads unrolled together)
+#pragma unroll 2
+        for (int u = tid; u < MR / 4; u += kChunkThreads) {
+            const int e = 4 * u, r = e >> 7, c = e & 127, B = r >> 4;
+            float pr[4], ea[4], kk[4], qq[4], xb[4], gb[4], gc[4], dx[4], gf[4], kb[4], pt[4], t3[4];
+            ld4(PRE + e, pr); ld4(EA + e, ea); ld4(K_ + e, kk); ld4(Q_ + e, qq);
+            ld4(DBKV + r * 2 * D + c, xb); ld4(GB + e, gb); ld4(GC + e, gc); ld4(DXQ + e, dx);
+            ld4(GF + e, gf); ld4(DKB + e, kb); ld4(ptot + (B * 4 + 3) * D + c, pt); ld4(tot + 3 * D + c, t3);
+            const float br = bs[r];
+            float dG[4], dKbKb[4], dqv[4], dkv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float kbf = pt[i] * t3[i] / pr[i];          // e^{G_C - G_r}
+                const float dxe = br * xb[i] * ea[i] + gb[i] * pr[i];  // dX e^G
+                const float dye = gc[i] / pr[i];                   // dY e^{-G}
+                const float dqq = dx[i] * ea[i] + gf[i] * pr[i];      // dXq e^G
+                dG[i] = kk[i] * dxe - kk[i] * dye + qq[i] * dqq - kb[i] * kk[i] * kbf;
+                dKbKb[i] = kb[i] * kk[i] * kbf;
+                dqv[i] = dqq;
+                dkv[i] = dxe + dye + kb[i] * kbf;
+            }
+            *reinterpret_cast<float4*>(gsm + e) = make_float4(dG[0], dG[1], dG[2], dG[3]);
+            *reinterpret_cast<float4*>(gsm + MR + e) = make_float4(dKbKb[0], dKbKb[1], dKbKb[2], dKbKb[3]);
             if (r < L) {
                 const int64_t o = ((c0 + r) * H + h) * D + c;
-                dq[o] = dqq;
-                dk[o] = dxe + dye + dkb * kbf;
+                *reinterpret_cast<float4*>(dq + o) = make_float4(dqv[0], dqv[1], dqv[2], dqv[3]);
+                *reinterpret_cast<float4*>(dk + o) = make_float4(dkv[0], dkv[1], dkv[2], dkv[3]);
             }
         }
         __syncthreads();
@@ -680,12 +820,23 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             }
         }
     }
+    // a wait that gave up: report it; MMAs it left running complete before TMEM is released
+    if (t.failed && tid == 0) report_timeout(pl);
+    if ((tid >> 5) == 0) {
+        tc::commit_w(bar_fin);
+        if ((tid & 31) == 0) tc::bar_wait(bar_fin, 0, 1u << 26);
+        __syncwarp();
+    }
+    tc::fence_before();
+    __syncthreads();
+    if ((tid >> 5) == 0) tc::tmem_dealloc(t.tm, 512);
 }
 
 // Workspace of the chunked backward: the forward's (bookkeeping and slots), o as
-// bf16, then per (chunk slot, head) the entering state, dS' and dU.
+// bf16, then per (chunk slot, head) the entering state, A and T, dS' and dU, then
+// the chunk kernel's per-CTA scratch.
 struct BwdLayout {
-    size_t fwd, o, states, dsp, du, scratch, total;
+    size_t fwd, o, states, at, dsp, du, scratch, total;
 };
 BwdLayout bwd_layout(int B, int T, int H, int N, bool packed) {
     BwdLayout l{};
@@ -695,10 +846,11 @@ BwdLayout bwd_layout(int B, int T, int H, int N, bool packed) {
     l.fwd = (chunk_tc_workspace(B, T, H, N, packed) + 255) & ~size_t(255);
     l.o = (((size_t)B * (size_t)T * (size_t)H * D * 2) + 255) & ~size_t(255);
     l.states = slots * D * D * 4;
+    l.at = slots * 2 * C * C * 4;
     l.dsp = l.states;
     l.du = slots * C * D * 4;
     l.scratch = (size_t)kBwdCtas * SC_TOTAL * 4;
-    l.total = (int64_t)N * H == 0 ? 0 : l.fwd + l.o + l.states + l.dsp + l.du + l.scratch;
+    l.total = (int64_t)N * H == 0 ? 0 : l.fwd + l.o + l.states + l.at + l.dsp + l.du + l.scratch;
     return l;
 }
 
@@ -721,14 +873,15 @@ cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, f
     uint8_t* fwd = base;
     void* o = base + lo.fwd;
     float* states = reinterpret_cast<float*>(base + lo.fwd + lo.o);
-    float* dsp = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states);
-    float* du = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.dsp);
-    float* scratch = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.dsp + lo.du);
+    float* at = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states);
+    float* dsp = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at);
+    float* du = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.dsp);
+    float* scratch = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.dsp + lo.du);
     ChunkParams fp = p;
     fp.o = o;
     fp.final_state = nullptr;
     Plan pl{};
-    cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, &pl, status, st);
+    cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, at, &pl, status, st);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BC_TOTAL);
     if (e != cudaSuccess) return e;
@@ -743,7 +896,8 @@ cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, f
         bwd_chunk_kernel<<<grid, kChunkThreads, BK_TOTAL, st>>>(
             pl, static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
             static_cast<const __nv_bfloat16*>(p.v), static_cast<const __nv_bfloat16*>(p.g),
-            static_cast<const __nv_bfloat16*>(p.beta), p.scale, dO, states, dsp, du, scratch, dq, dk, dv, dg, dbeta);
+            static_cast<const __nv_bfloat16*>(p.beta), p.scale, dO, states, at, dsp, du, scratch, dq, dk,
+            dv, dg, dbeta);
         e = cudaGetLastError();
     }
     return e;

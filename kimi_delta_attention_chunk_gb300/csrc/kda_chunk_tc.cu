@@ -727,6 +727,8 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             }
             tc::tmem_ld_wait();
             const float br = beta_s[r];
+            // (for the backward: A itself, without beta)
+            float* ao = pl.at_out != nullptr ? pl.at_out + ((int64_t)cur.gc * H + h) * (2 * C * C) + r * C : nullptr;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
                 if (R == 0 && g8 == 1) break;
@@ -736,6 +738,17 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     const int j = j0 + 8 * g8 + u;
                     const float xv = __uint_as_float(a[8 * g8 + u]);
                     v[u] = is_q ? (j <= r ? scale * xv : 0.f) : (j < r ? br * xv : 0.f);
+                }
+                if (!is_q && ao != nullptr) {
+                    float w[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) w[u] = j0 + 8 * g8 + u < r ? __uint_as_float(a[8 * g8 + u]) : 0.f;
+                    *reinterpret_cast<float4*>(ao + j0 + 8 * g8) = make_float4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<float4*>(ao + j0 + 8 * g8 + 4) = make_float4(w[4], w[5], w[6], w[7]);
+                    if (R == 0) {
+                        *reinterpret_cast<float4*>(ao + 32 + j0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4*>(ao + 32 + j0 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
                 if (is_q) {
                     uint4 hi, lo;
@@ -922,7 +935,15 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const float4 b = *reinterpret_cast<const float4*>(T + r * MAT_LD + 8 * jg + 4);
                 t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) t[u] = (8 * jg + u > r) ? 0.f : t[u] * beta_s[8 * jg + u];
+                for (int u = 0; u < 8; ++u) t[u] = (8 * jg + u > r) ? 0.f : t[u];
+                if (pl.at_out != nullptr) {
+                    // (for the backward: T itself)
+                    float* to = pl.at_out + ((int64_t)cur.gc * H + h) * (2 * C * C) + C * C + r * C + 8 * jg;
+                    *reinterpret_cast<float4*>(to) = make_float4(t[0], t[1], t[2], t[3]);
+                    *reinterpret_cast<float4*>(to + 4) = make_float4(t[4], t[5], t[6], t[7]);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t[u] *= beta_s[8 * jg + u];
                 uint4 hi, lo;
                 tc::split8(t, hi, lo);
                 *reinterpret_cast<uint4*>(smem + SM_TB + tc::kmaj(r, 8 * jg, C)) = hi;
@@ -1528,11 +1549,12 @@ Layout layout(int B, int T, int H, int N, bool packed) {
 }
 
 // The prefill's kernels on a caller-owned workspace of ws_bytes.  With states_out the
-// state kernel also writes the state entering every chunk there; plan_out receives
-// the work plan (both for the backward).
+// state kernel also writes the state entering every chunk there, with at_out the
+// local kernel each chunk's A and T; plan_out receives the work plan (all for the
+// backward).
 template <typename TOut>
 cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws_bytes, int32_t* status,
-                      bool fused, float* states_out = nullptr, Plan* plan_out = nullptr) {
+                      bool fused, float* states_out = nullptr, Plan* plan_out = nullptr, float* at_out = nullptr) {
     cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
     g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
     cudaError_t e = cudaSuccess;
@@ -1561,6 +1583,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws
     pl.inject = g_inject;
     g_inject = 0;
     pl.states_out = states_out;
+    pl.at_out = at_out;
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
     pl.slots = reinterpret_cast<uint8_t*>(ws) + lo.hdr_bytes;
     trace_record(trace[0], st);
@@ -1671,8 +1694,8 @@ cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, void* ws, siz
 }
 
 cudaError_t chunk_tc_forward_states(const ChunkParams& p, void* ws, size_t ws_bytes, float* states_out,
-                                    cplan::Plan* plan_out, int32_t* status, cudaStream_t st) {
-    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false, states_out, plan_out);
+                                    float* at_out, cplan::Plan* plan_out, int32_t* status, cudaStream_t st) {
+    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false, states_out, plan_out, at_out);
 }
 
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {

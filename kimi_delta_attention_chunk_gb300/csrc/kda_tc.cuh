@@ -41,11 +41,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16 with bf16 operands and fp32 accumulation.
-// b_mn: B operand stored MN-major (N contiguous) instead of K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool neg_a = false, bool b_mn = false) {
+// a_mn / b_mn: the A / B operand stored MN-major (M / N contiguous) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool neg_a = false, bool b_mn = false,
+                                                  bool a_mn = false) {
     return (1u << 4)                      // D = f32
            | (1u << 7) | (1u << 10)       // A, B = bf16
            | ((neg_a ? 1u : 0u) << 13)    // negate A
+           | ((a_mn ? 1u : 0u) << 15)     // A major-ness
            | ((b_mn ? 1u : 0u) << 16)     // B major-ness
            | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
