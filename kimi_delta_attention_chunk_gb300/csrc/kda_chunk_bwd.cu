@@ -548,18 +548,30 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         __syncthreads();   // the previous task is done with the scratch and the tables
 
         // ---- inputs (0 past the sequence end), U~ and dU, prefix products, -W ----------
-        for (int u = tid; u < MR / 8; u += kChunkThreads) {
+        // (every loop below has a fixed count per thread and is unrolled, so that its
+        // loads are in flight together)
+        constexpr int NKV = MR / 8 / kChunkThreads;
+        uint4 kr[NKV], qr[NKV], vr[NKV];
+#pragma unroll
+        for (int it = 0; it < NKV; ++it) {
+            const int u = tid + it * kChunkThreads;
             const int r = u >> 4, c = 8 * (u & 15);
             const int64_t ti = ((c0 + r) * H + h) * D + c;
-            float kx[8], qx[8], vx[8];
+            kr[it] = qr[it] = vr[it] = make_uint4(0u, 0u, 0u, 0u);
             if (r < L) {
-                tc::unpack8(*reinterpret_cast<const uint4*>(k + ti), kx);
-                tc::unpack8(*reinterpret_cast<const uint4*>(q + ti), qx);
-                tc::unpack8(*reinterpret_cast<const uint4*>(v + ti), vx);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kx[e] = qx[e] = vx[e] = 0.f;
+                kr[it] = *reinterpret_cast<const uint4*>(k + ti);
+                qr[it] = *reinterpret_cast<const uint4*>(q + ti);
+                vr[it] = *reinterpret_cast<const uint4*>(v + ti);
             }
+        }
+#pragma unroll
+        for (int it = 0; it < NKV; ++it) {
+            const int u = tid + it * kChunkThreads;
+            const int r = u >> 4, c = 8 * (u & 15);
+            float kx[8], qx[8], vx[8];
+            tc::unpack8(kr[it], kx);
+            tc::unpack8(qr[it], qx);
+            tc::unpack8(vr[it], vx);
             const int o = r * D + c;
             *reinterpret_cast<float4*>(K_ + o) = make_float4(kx[0], kx[1], kx[2], kx[3]);
             *reinterpret_cast<float4*>(K_ + o + 4) = make_float4(kx[4], kx[5], kx[6], kx[7]);
@@ -568,14 +580,27 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             *reinterpret_cast<float4*>(V_ + o) = make_float4(vx[0], vx[1], vx[2], vx[3]);
             *reinterpret_cast<float4*>(V_ + o + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
         }
-        for (int u = tid; u < MR / 4; u += kChunkThreads) {
-            const int r = u >> 5, c = 4 * (u & 31);
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < L) x = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c);
-            *reinterpret_cast<float4*>(DO_ + r * D + c) = x;
-            *reinterpret_cast<float4*>(U + r * D + c) =
-                *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(slot + SLOT_UT) + r * D + c);
-            *reinterpret_cast<float4*>(DWU + r * 2 * D + D + c) = *reinterpret_cast<const float4*>(DU + r * D + c);
+        {
+            // (all loads first: the slot is not known not to alias the scratch)
+            constexpr int NI = MR / 4 / kChunkThreads;
+            float4 xo[NI], xu[NI], xd[NI];
+#pragma unroll
+            for (int it = 0; it < NI; ++it) {
+                const int u = tid + it * kChunkThreads;
+                const int r = u >> 5, c = 4 * (u & 31);
+                xo[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < L) xo[it] = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c);
+                xu[it] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(slot + SLOT_UT) + r * D + c);
+                xd[it] = *reinterpret_cast<const float4*>(DU + r * D + c);
+            }
+#pragma unroll
+            for (int it = 0; it < NI; ++it) {
+                const int u = tid + it * kChunkThreads;
+                const int r = u >> 5, c = 4 * (u & 31);
+                *reinterpret_cast<float4*>(DO_ + r * D + c) = xo[it];
+                *reinterpret_cast<float4*>(U + r * D + c) = xu[it];
+                *reinterpret_cast<float4*>(DWU + r * 2 * D + D + c) = xd[it];
+            }
         }
         if (tid < C) bs[tid] = tid < L ? ld_in(beta + (c0 + tid) * H + h) : 0.f;
         {
@@ -595,12 +620,25 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             }
             tot[J * D + c] = run;
         }
-        for (int u = tid; u < 8 * D; u += kChunkThreads) {
-            const int c = u & 127, ng = u >> 7;
-            float x[8];
-            hilo8(slot + SLOT_WQH + u * 16, slot + SLOT_WQL + u * 16, x);
+        {
+            constexpr int NI = 8 * D / kChunkThreads;
+            uint4 wh[NI], wl[NI];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) WN[(8 * ng + e) * D + c] = x[e];
+            for (int it = 0; it < NI; ++it) {
+                const int u = tid + it * kChunkThreads;
+                wh[it] = *reinterpret_cast<const uint4*>(slot + SLOT_WQH + u * 16);
+                wl[it] = *reinterpret_cast<const uint4*>(slot + SLOT_WQL + u * 16);
+            }
+#pragma unroll
+            for (int it = 0; it < NI; ++it) {
+                const int u = tid + it * kChunkThreads;
+                const int c = u & 127, ng = u >> 7;
+                float a[8], b[8];
+                tc::unpack8(wh[it], a);
+                tc::unpack8(wl[it], b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) WN[(8 * ng + e) * D + c] = a[e] + b[e];
+            }
         }
         __syncthreads();
         if (tid < D) {
@@ -726,18 +764,37 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             DA[e] = j < r ? bs[r] * DM[e] : 0.f;
         }
         // dbeta = rowsum(dM A) + rowsum(dBk X) + rowsum(dBv v);  dv = Diag(beta) dBv
+        // (eight threads per row, each over 8 contiguous j and 16 contiguous c)
         {
             const int r = tid >> 3, part = tid & 7;
+            float m4[8], a4[8], xb[16], kx[16], ea[16], vb[16], vx[16];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                ld4(DM + r * C + 8 * part + 4 * i, m4 + 4 * i);
+                ld4(Am + r * C + 8 * part + 4 * i, a4 + 4 * i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = 16 * part + 4 * i;
+                ld4(DBKV + r * 2 * D + c, xb + 4 * i);
+                ld4(K_ + r * D + c, kx + 4 * i);
+                ld4(EA + r * D + c, ea + 4 * i);
+                ld4(DBKV + r * 2 * D + D + c, vb + 4 * i);
+                ld4(V_ + r * D + c, vx + 4 * i);
+            }
             float a = 0.f;
-            for (int j = part; j < C; j += 8) a += DM[r * C + j] * Am[r * C + j];
-            for (int c = part; c < D; c += 8)
-                a += DBKV[r * 2 * D + c] * K_[r * D + c] * EA[r * D + c] + DBKV[r * 2 * D + D + c] * V_[r * D + c];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a += m4[i] * a4[i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a += xb[i] * kx[i] * ea[i] + vb[i] * vx[i];
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             a += __shfl_xor_sync(0xffffffffu, a, 4);
             if (part == 0 && r < L) dbeta[(c0 + r) * H + h] = a;
         }
-        for (int u = tid; u < MR / 4; u += kChunkThreads) {
+#pragma unroll
+        for (int it = 0; it < MR / 4 / kChunkThreads; ++it) {
+            const int u = tid + it * kChunkThreads;
             const int r = u >> 5, c = 4 * (u & 31);
             if (r < L) {
                 const float4 x = *reinterpret_cast<const float4*>(DBKV + r * 2 * D + D + c);
