@@ -23,8 +23,8 @@
 //       state entering every chunk and each chunk's A and T; its workspace slots keep
 //       W, Qs = scale Xq, Kb, scale P, U~ and e^{G_C} per (chunk, head);
 //   bwd_chain_kernel: one CTA per (sequence, head) carries dS backwards through the
-//       chunks (the first two lines above, fp32 on the CUDA cores, operands read
-//       from the slots) and stores dS' and dU of every chunk;
+//       chunks (the first two lines above) with dS'^T in tensor memory, tcgen05
+//       rounds on the slots' operand images, and stores dS' and dU of every chunk;
 //   bwd_chunk_kernel: one CTA per (chunk, head) task forms dq, dk, dv, dg, dbeta; its
 //       products are tensor-core rounds (tcgen05, operands split hi | lo into bf16,
 //       fp32 accumulators in tensor memory) on operands staged from a per-CTA scratch.
@@ -37,188 +37,6 @@ namespace kda {
 namespace {
 
 using namespace cplan;
-
-constexpr int kChainThreads = 512;
-constexpr int LDX = D + 4;   // fp32 rows of 128 values, padded
-constexpr int LDR = C + 4;   // fp32 rows of 64 values, padded
-
-// bf16 hi + lo at the same offset of two images -> 8 floats
-__device__ __forceinline__ void hilo8(const uint8_t* hi, const uint8_t* lo, float* x) {
-    float a[8], b[8];
-    tc::unpack8(*reinterpret_cast<const uint4*>(hi), a);
-    tc::unpack8(*reinterpret_cast<const uint4*>(lo), b);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = a[i] + b[i];
-}
-
-// ---- reverse chain --------------------------------------------------------------
-// Shared memory (fp32): dSp [128][LDX] (the gradient of the state after the chunk),
-// dO, dU, Wn = -W, Qs [64][LDX] each (Qs over KbT once dU is formed), P [64][LDR],
-// KbT [128][LDR] (Kb transposed), e^{G_C} [128].
-constexpr uint32_t BC_DSP = 0;
-constexpr uint32_t BC_DO = BC_DSP + D * LDX * 4;
-constexpr uint32_t BC_DU = BC_DO + C * LDX * 4;
-constexpr uint32_t BC_WN = BC_DU + C * LDX * 4;
-constexpr uint32_t BC_P = BC_WN + C * LDX * 4;
-constexpr uint32_t BC_KB = BC_P + C * LDR * 4;   // KbT [128][LDR], later Qs [64][LDX]
-constexpr uint32_t BC_EGC = BC_KB + D * LDR * 4;
-constexpr uint32_t BC_TOTAL = BC_EGC + D * 4;
-static_assert(C * LDX <= D * LDR, "Qs fits the KbT region");
-static_assert(BC_TOTAL <= 232448, "shared memory of the chain kernel");
-
-__global__ void __launch_bounds__(kChainThreads, 1)
-bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __restrict__ dST,
-                 float* __restrict__ dS0, float* __restrict__ dsp_out, float* __restrict__ du_out) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    float* dSp = reinterpret_cast<float*>(smem + BC_DSP);
-    float* dOs = reinterpret_cast<float*>(smem + BC_DO);
-    float* dUs = reinterpret_cast<float*>(smem + BC_DU);
-    float* Wn = reinterpret_cast<float*>(smem + BC_WN);
-    float* Ps = reinterpret_cast<float*>(smem + BC_P);
-    float* KbT = reinterpret_cast<float*>(smem + BC_KB);
-    float* Qs = KbT;
-    float* egc = reinterpret_cast<float*>(smem + BC_EGC);
-    const int tid = threadIdx.x;
-    const Chain chn = chain_of(pl, blockIdx.x);
-    const int H = pl.H, h = chn.h;
-    const int64_t sbase = ((int64_t)chn.n * H + h) * D * D;
-
-    for (int e = tid; e < D * D; e += kChainThreads)
-        dSp[(e >> 7) * LDX + (e & 127)] = dST != nullptr ? dST[sbase + e] : 0.f;
-
-    for (int64_t i = chn.nchunks - 1; i >= 0; --i) {
-        const int64_t c0 = chn.bos + i * C;
-        const int L = (chn.eos - c0 < (int64_t)C) ? (int)(chn.eos - c0) : C;
-        const int64_t task = (chn.g0 + i) * H + h;
-        const uint8_t* slot = pl.slots + task * (int64_t)SLOT_BYTES;
-        __syncthreads();   // the previous chunk's readers are done
-        // dO rows of the chunk (0 past the sequence end)
-        for (int f = tid; f < C * (D / 4); f += kChainThreads) {
-            const int r = f >> 5, x4 = (f & 31) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < L) v = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + x4);
-            *reinterpret_cast<float4*>(dOs + r * LDX + x4) = v;
-        }
-        // scale P [r][j] (K-major [64 r][64 j]): one 16-byte unit = 8 consecutive j of a row
-        for (int u = tid; u < C * 8; u += kChainThreads) {
-            const int r = ((u >> 6) << 3) | (u & 7), jg = (u >> 3) & 7;
-            float x[8];
-            hilo8(slot + SLOT_P + u * 16, slot + SLOT_P + 8192 + u * 16, x);
-            *reinterpret_cast<float4*>(Ps + r * LDR + 8 * jg) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4*>(Ps + r * LDR + 8 * jg + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        }
-        // Kb (K-major [128 c][64 r]): a unit = 8 consecutive r of a channel c -> KbT[c][r]
-        for (int u = tid; u < D * 8; u += kChainThreads) {
-            const int c = ((u >> 6) << 3) | (u & 7), rg = (u >> 3) & 7;
-            float x[8];
-            hilo8(slot + SLOT_KH + u * 16, slot + SLOT_KL + u * 16, x);
-            *reinterpret_cast<float4*>(KbT + c * LDR + 8 * rg) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4*>(KbT + c * LDR + 8 * rg + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        }
-        // -W (the first half of the merged image, n-group major: a unit = 8 consecutive
-        // rows r of a channel c)
-        for (int u = tid; u < 8 * D; u += kChainThreads) {
-            const int c = u & 127, ng = u >> 7;
-            float x[8];
-            hilo8(slot + SLOT_WQH + u * 16, slot + SLOT_WQL + u * 16, x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Wn[(8 * ng + e) * LDX + c] = x[e];
-        }
-        if (tid < D) egc[tid] = reinterpret_cast<const float*>(slot + SLOT_EGC)[tid];
-        __syncthreads();
-
-        // the gradient of the state after this chunk, for the chunk's own gradients
-        {
-            float* dst = dsp_out + task * (int64_t)(D * D);
-            for (int f = tid; f < D * (D / 4); f += kChainThreads) {
-                const int c = f >> 5, x4 = (f & 31) * 4;
-                *reinterpret_cast<float4*>(dst + c * D + x4) = *reinterpret_cast<const float4*>(dSp + c * LDX + x4);
-            }
-        }
-        // dU = (scale P)^T dO + Kb dSp: rows 4 rg.., columns 4 cg..
-        {
-            const int rg = tid >> 5, cg = tid & 31;
-            float acc[4][4] = {};
-#pragma unroll 4
-            for (int j = 0; j < C; ++j) {
-                const float4 a = *reinterpret_cast<const float4*>(Ps + j * LDR + 4 * rg);
-                const float4 b = *reinterpret_cast<const float4*>(dOs + j * LDX + 4 * cg);
-                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[p][q] += av[p] * bv[q];
-            }
-#pragma unroll 4
-            for (int c = 0; c < D; ++c) {
-                const float4 a = *reinterpret_cast<const float4*>(KbT + c * LDR + 4 * rg);
-                const float4 b = *reinterpret_cast<const float4*>(dSp + c * LDX + 4 * cg);
-                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[p][q] += av[p] * bv[q];
-            }
-            float* gdu = du_out + task * (int64_t)(C * D);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const float4 v = make_float4(acc[p][0], acc[p][1], acc[p][2], acc[p][3]);
-                *reinterpret_cast<float4*>(dUs + (4 * rg + p) * LDX + 4 * cg) = v;
-                *reinterpret_cast<float4*>(gdu + (4 * rg + p) * D + 4 * cg) = v;
-            }
-        }
-        __syncthreads();   // KbT is read; dU is complete
-        // Qs = scale Xq (the second half of the merged image) over KbT
-        for (int u = tid; u < 8 * D; u += kChainThreads) {
-            const int c = u & 127, ng = u >> 7;
-            float x[8];
-            hilo8(slot + SLOT_WQH + 16384 + u * 16, slot + SLOT_WQL + 16384 + u * 16, x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Qs[(8 * ng + e) * LDX + c] = x[e];
-        }
-        __syncthreads();
-        // dSp <- Diag(e^{G_C}) dSp + Qs^T dO + (-W)^T dU: rows c = 4 rg.., columns x = 8 cg..
-        {
-            const int rg = tid >> 4, cg = tid & 15;
-            float acc[4][8];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const float e = egc[4 * rg + p];
-                const float4 s0 = *reinterpret_cast<const float4*>(dSp + (4 * rg + p) * LDX + 8 * cg);
-                const float4 s1 = *reinterpret_cast<const float4*>(dSp + (4 * rg + p) * LDX + 8 * cg + 4);
-                acc[p][0] = e * s0.x; acc[p][1] = e * s0.y; acc[p][2] = e * s0.z; acc[p][3] = e * s0.w;
-                acc[p][4] = e * s1.x; acc[p][5] = e * s1.y; acc[p][6] = e * s1.z; acc[p][7] = e * s1.w;
-            }
-#pragma unroll 2
-            for (int r = 0; r < C; ++r) {
-                const float4 a = *reinterpret_cast<const float4*>(Qs + r * LDX + 4 * rg);
-                const float4 b0 = *reinterpret_cast<const float4*>(dOs + r * LDX + 8 * cg);
-                const float4 b1 = *reinterpret_cast<const float4*>(dOs + r * LDX + 8 * cg + 4);
-                const float4 w = *reinterpret_cast<const float4*>(Wn + r * LDX + 4 * rg);
-                const float4 u0 = *reinterpret_cast<const float4*>(dUs + r * LDX + 8 * cg);
-                const float4 u1 = *reinterpret_cast<const float4*>(dUs + r * LDX + 8 * cg + 4);
-                const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w.x, w.y, w.z, w.w};
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[p][q] += av[p] * bv[q] + wv[p] * uv[q];
-            }
-            // (each thread reads and writes only its own elements of dSp here)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                *reinterpret_cast<float4*>(dSp + (4 * rg + p) * LDX + 8 * cg) =
-                    make_float4(acc[p][0], acc[p][1], acc[p][2], acc[p][3]);
-                *reinterpret_cast<float4*>(dSp + (4 * rg + p) * LDX + 8 * cg + 4) =
-                    make_float4(acc[p][4], acc[p][5], acc[p][6], acc[p][7]);
-            }
-        }
-    }
-    __syncthreads();
-    if (dS0 != nullptr)
-        for (int e = tid; e < D * D; e += kChainThreads) dS0[sbase + e] = dSp[(e >> 7) * LDX + (e & 127)];
-}
 
 // ---- chunk-parallel gradients ------------------------------------------------------
 constexpr int kChunkThreads = 512;
@@ -470,6 +288,267 @@ struct Alp {
         x.x *= pt[0]; x.y *= pt[1]; x.z *= pt[2]; x.w *= pt[3];
     }
 };
+
+// ---- reverse chain (tensor cores) ----------------------------------------------------
+// One CTA per (sequence, head).  The gradient of the state after the chunk, dS', lives
+// in tensor memory as dS'^T (lane = value column x, column = key channel c, fp32) for
+// the whole sequence; per chunk, last to first:
+//   store dS' (for the chunk kernel), split it hi | lo into TMEM, scale it by e^{G_C}
+//   (columns c), then
+//   dU^T  = dO^T (scale P)^T + dS'^T Kb^T              (M = 128 x, N = 64 r)
+//   store dU, split it hi | lo into TMEM, and
+//   dS^T += dO^T (Qs)^T + dU^T (-W)^T                   (M = 128 x, N = 128 c)
+// The forward's slot images serve as the B operands in place: P and Kb (K-major
+// images of P and Kb^T) are read MN-major as P^T and Kb^T... with their core-matrix
+// groups along k 1024 bytes apart; -W and Qs (the n-group-major image of [-W | Qs]
+// over c) are read K-major with k (= r) groups 2048 bytes apart.  dO^T is staged from
+// global memory as an MN-major image.  Operands split hi | lo, three MMA terms each.
+constexpr int kChainThreads = 256;
+constexpr uint32_t CS_IMG = 0;                        // [-W | Qs] hi, lo, e^{G_C} (the slot's first SLOT_IMG bytes)
+constexpr uint32_t CS_KBP = SLOT_IMG;                 // Kb hi, lo, P hi, lo (SLOT_KBP bytes from SLOT_KH)
+constexpr uint32_t CS_DO = CS_KBP + SLOT_KBP;         // dO^T hi | lo, MN-major [128 x][64 r]
+constexpr uint32_t CS_BAR = CS_DO + 2 * D * C * 2;    // barriers, TMEM base
+constexpr uint32_t CS_TOTAL = CS_BAR + 64;
+static_assert(CS_KBP % 16 == 0 && CS_DO % 16 == 0 && CS_TOTAL <= 232448, "chain kernel shared memory");
+static_assert(SLOT_KL == SLOT_KH + 16384 && SLOT_P == SLOT_KH + 32768, "Kb and P contiguous in the slot");
+// tensor memory (columns)
+constexpr uint32_t CT_S = 0;      // dS'^T fp32 [128 x][128 c]
+constexpr uint32_t CT_SH = 128;   // dS'^T hi (bf16 pairs over c) [128 x][64]
+constexpr uint32_t CT_SL = 192;   // its lo
+constexpr uint32_t CT_U = 256;    // dU^T accumulator fp32 [128 x][64 r]
+constexpr uint32_t CT_UH = 320;   // dU^T hi (bf16 pairs over r) [128 x][32]
+constexpr uint32_t CT_UL = 352;   // its lo
+
+__global__ void __launch_bounds__(kChainThreads, 1)
+bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __restrict__ dST,
+                 float* __restrict__ dS0, float* __restrict__ dsp_out, float* __restrict__ du_out) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(smem + CS_BAR);
+    uint64_t* bar_u = bar_ld + 1;
+    uint64_t* bar_s = bar_ld + 2;
+    uint64_t* bar_fin = bar_ld + 3;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_ld + 4);
+    const Chain chn = chain_of(pl, blockIdx.x);
+    const int H = pl.H, h = chn.h;
+    const int64_t sbase = ((int64_t)chn.n * H + h) * D * D;
+    if (warp == 0) tc::tmem_alloc(tmem_base_s, 512);
+    if (tid == 0) {
+        tc::bar_init(bar_ld, 1);
+        tc::bar_init(bar_u, 1);
+        tc::bar_init(bar_s, 1);
+        tc::bar_init(bar_fin, 1);
+        tc::bar_init_fence();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tmem_base_s;
+    // thread -> TMEM lane x (value column) and a half of the columns
+    const int x = (warp & 3) * 32 + lane, half = warp >> 2;
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+
+    uint32_t ph_ld = 0, ph_u = 0, ph_s = 0;
+    bool failed = false;
+    auto wait = [&](uint64_t* bar, uint32_t& phase) {
+        bool ok = true;
+        if (tid == 0) ok = tc::bar_wait(bar, phase, pl.wait_iter);
+        const bool gave_up = __syncthreads_or(!ok) != 0;
+        if (!gave_up) phase ^= 1;
+        failed = failed || gave_up;
+        tc::fence_after();
+        return !gave_up;
+    };
+    auto issue_loads = [&](int64_t i) {
+        if (tid == 0) {
+            const uint8_t* slot = pl.slots + ((chn.g0 + i) * H + h) * (int64_t)SLOT_BYTES;
+            tc::bar_expect_tx(bar_ld, SLOT_IMG + SLOT_KBP);
+            tc::bulk_load(smem + CS_IMG, slot, 32768, bar_ld);
+            tc::bulk_load(smem + CS_IMG + 32768, slot + 32768, 32768, bar_ld);
+            tc::bulk_load(smem + CS_IMG + 65536, slot + 65536, SLOT_IMG - 65536, bar_ld);
+            tc::bulk_load(smem + CS_KBP, slot + SLOT_KH, 32768, bar_ld);
+            tc::bulk_load(smem + CS_KBP + 32768, slot + SLOT_KH + 32768, SLOT_KBP - 32768, bar_ld);
+        }
+    };
+    bool ld_pending = false;
+
+    // dS'^T of the last chunk: the caller's dS_T (or zero), column x of dS_T [c][x]
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(dST != nullptr ? dST[sbase + (int64_t)(c0 + e) * D + x] : 0.f);
+        tc::tmem_st16(tm + lanes + CT_S + c0, v);
+    }
+    tc::tmem_st_wait();
+    if (chn.nchunks > 0) {
+        issue_loads(chn.nchunks - 1);
+        ld_pending = true;
+    }
+
+    const uint32_t id_u1 = tc::idesc_bf16(128, C, false, true, true);     // A dO^T (MN), B P^T (MN)
+    const uint32_t id_u2 = tc::idesc_bf16(128, C, false, true, false);    // A dS'^T (TMEM), B Kb^T (MN)
+    const uint32_t id_s1 = tc::idesc_bf16(128, D, false, false, true);    // A dO^T (MN), B Qs^T (K-major)
+    const uint32_t id_s2 = tc::idesc_bf16(128, D, false, false, false);   // A dU^T (TMEM), B (-W)^T (K-major)
+    for (int64_t i = chn.nchunks - 1; i >= 0 && !failed; --i) {
+        const int64_t c0t = chn.bos + i * C;
+        const int L = (chn.eos - c0t < (int64_t)C) ? (int)(chn.eos - c0t) : C;
+        const int64_t task = (chn.g0 + i) * H + h;
+        // dO^T of the chunk as an MN-major image (rows past the sequence end are zero):
+        // thread -> 8 rows r of 4 consecutive columns x, eight float4 in flight
+        {
+            uint8_t* hi = smem + CS_DO;
+            uint8_t* lo = hi + D * C * 2;
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + u * kChainThreads;   // 2048 units of [64 r][32 x4]
+                const int r = ((idx >> 8) << 3) | (idx & 7), xg = (idx >> 3) & 31;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < L) v[u] = *reinterpret_cast<const float4*>(dO + ((c0t + r) * H + h) * D + 4 * xg);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = tid + u * kChainThreads;
+                const int r = ((idx >> 8) << 3) | (idx & 7), xg = (idx >> 3) & 31;
+                uint2 hv, lv;
+                tc::split2(v[u].x, v[u].y, hv.x, lv.x);
+                tc::split2(v[u].z, v[u].w, hv.y, lv.y);
+                const uint32_t o = op_off(4 * xg, r, C, true);
+                *reinterpret_cast<uint2*>(hi + o) = hv;
+                *reinterpret_cast<uint2*>(lo + o) = lv;
+            }
+        }
+        if (!wait(bar_ld, ph_ld)) break;
+        ld_pending = false;
+        // dS': store it, split it, scale it by e^{G_C}
+        {
+            const float* egc = reinterpret_cast<const float*>(smem + CS_IMG + SLOT_EGC);
+            float* dst = dsp_out + task * (int64_t)(D * D) + x;
+            for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
+                uint32_t v[16];
+                tc::tmem_ld16(tm + lanes + CT_S + c0, v);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    f[e] = __uint_as_float(v[e]);
+                    dst[(int64_t)(c0 + e) * D] = f[e];
+                }
+                uint32_t hv[8], lv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tc::split2(f[2 * e], f[2 * e + 1], hv[e], lv[e]);
+                tc::tmem_st8(tm + lanes + CT_SH + c0 / 2, hv);
+                tc::tmem_st8(tm + lanes + CT_SL + c0 / 2, lv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(f[e] * egc[c0 + e]);
+                tc::tmem_st16(tm + lanes + CT_S + c0, v);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        // dU^T = dO^T (scale P)^T + dS'^T Kb^T
+        if (warp == 0) {
+            const uint32_t doh = tc::smem_u32(smem + CS_DO), dol = doh + D * C * 2;
+            const uint32_t kbh = tc::smem_u32(smem + CS_KBP), kbl = kbh + 16384;
+            const uint32_t phh = kbh + 32768, phl = kbh + 40960;
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                const uint64_t ah = tc::sdesc(doh + ks * 256, 128, C * 16), al = tc::sdesc(dol + ks * 256, 128, C * 16);
+                const uint64_t bh = tc::sdesc(phh + ks * 2048, 1024, 128), bl = tc::sdesc(phl + ks * 2048, 1024, 128);
+                tc::mma_ss_w(tm + CT_U, ah, bh, id_u1, ks > 0 ? 1u : 0u);
+                tc::mma_ss_w(tm + CT_U, ah, bl, id_u1, 1u);
+                tc::mma_ss_w(tm + CT_U, al, bh, id_u1, 1u);
+            }
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t bh = tc::sdesc(kbh + ks * 2048, 1024, 128), bl = tc::sdesc(kbl + ks * 2048, 1024, 128);
+                tc::mma_ts_w(tm + CT_U, tm + CT_SH + ks * 8, bh, id_u2, 1u);
+                tc::mma_ts_w(tm + CT_U, tm + CT_SH + ks * 8, bl, id_u2, 1u);
+                tc::mma_ts_w(tm + CT_U, tm + CT_SL + ks * 8, bh, id_u2, 1u);
+            }
+            tc::commit_w(bar_u);
+        }
+        if (!wait(bar_u, ph_u)) break;
+        // dU: store it, split it
+        {
+            float* dst = du_out + task * (int64_t)(C * D) + x;
+            for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 16) {
+                uint32_t v[16];
+                tc::tmem_ld16(tm + lanes + CT_U + r0, v);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    f[e] = __uint_as_float(v[e]);
+                    dst[(int64_t)(r0 + e) * D] = f[e];
+                }
+                uint32_t hv[8], lv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tc::split2(f[2 * e], f[2 * e + 1], hv[e], lv[e]);
+                tc::tmem_st8(tm + lanes + CT_UH + r0 / 2, hv);
+                tc::tmem_st8(tm + lanes + CT_UL + r0 / 2, lv);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        // dS^T += dO^T Qs^T + dU^T (-W)^T
+        if (warp == 0) {
+            const uint32_t doh = tc::smem_u32(smem + CS_DO), dol = doh + D * C * 2;
+            const uint32_t wh = tc::smem_u32(smem + CS_IMG + SLOT_WQH), wl = tc::smem_u32(smem + CS_IMG + SLOT_WQL);
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                const uint64_t ah = tc::sdesc(doh + ks * 256, 128, C * 16), al = tc::sdesc(dol + ks * 256, 128, C * 16);
+                const uint64_t bh = tc::sdesc(wh + 16384 + ks * 4096, 2048, 128);
+                const uint64_t bl = tc::sdesc(wl + 16384 + ks * 4096, 2048, 128);
+                tc::mma_ss_w(tm + CT_S, ah, bh, id_s1, 1u);
+                tc::mma_ss_w(tm + CT_S, ah, bl, id_s1, 1u);
+                tc::mma_ss_w(tm + CT_S, al, bh, id_s1, 1u);
+            }
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                const uint64_t bh = tc::sdesc(wh + ks * 4096, 2048, 128), bl = tc::sdesc(wl + ks * 4096, 2048, 128);
+                tc::mma_ts_w(tm + CT_S, tm + CT_UH + ks * 8, bh, id_s2, 1u);
+                tc::mma_ts_w(tm + CT_S, tm + CT_UH + ks * 8, bl, id_s2, 1u);
+                tc::mma_ts_w(tm + CT_S, tm + CT_UL + ks * 8, bh, id_s2, 1u);
+            }
+            tc::commit_w(bar_s);
+        }
+        if (!wait(bar_s, ph_s)) break;
+        // the slot buffers and dO^T are free: the previous chunk's loads
+        if (i > 0) {
+            issue_loads(i - 1);
+            ld_pending = true;
+        }
+    }
+    if (failed) {
+        if (tid == 0) {
+            report_timeout(pl);
+            if (ld_pending) tc::bar_wait(bar_ld, ph_ld, 1u << 26);
+        }
+    } else if (dS0 != nullptr) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 16) {
+            uint32_t v[16];
+            tc::tmem_ld16(tm + lanes + CT_S + c0, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dS0[sbase + (int64_t)(c0 + e) * D + x] = __uint_as_float(v[e]);
+        }
+    }
+    // MMAs that a wait gave up on may still run: they complete before TMEM is released
+    if (warp == 0) {
+        tc::commit_w(bar_fin);
+        if (lane == 0) tc::bar_wait(bar_fin, 0, 1u << 26);
+        __syncwarp();
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
 
 // One (chunk, head) task per CTA at a time: the chunk's dq, dk, dv, dg, dbeta from the
 // entering state S, the gradient dS' of the state after it, dU and dO, plus the
@@ -940,9 +1019,9 @@ cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, f
     Plan pl{};
     cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, at, &pl, status, st);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BC_TOTAL);
+    e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CS_TOTAL);
     if (e != cudaSuccess) return e;
-    bwd_chain_kernel<<<(unsigned)((int64_t)p.N * p.H), kChainThreads, BC_TOTAL, st>>>(pl, dO, dST, dS0, dsp, du);
+    bwd_chain_kernel<<<(unsigned)((int64_t)p.N * p.H), kChainThreads, CS_TOTAL, st>>>(pl, dO, dST, dS0, dsp, du);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t tasks = pl.max_chunks * p.H;
