@@ -306,6 +306,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    bf16_peak = float(peaks.get("bf16_tflops") or 1900.0)
     w = synth.WORKLOADS["prefill"]
     H, K, V, T = w.H, w.K, w.V, w.T
     host = synth.direct_inputs(T, H, K, V, w.dtype, w.seed + 1000 * rank)
@@ -501,7 +502,7 @@ def run_ours(args, world, rank, local):
                                       "trips through the workspace (split partial sums and y)"}}
     del gp_in, gp_gx, gp_beta, gp_ws
 
-    # ---- the backward of the 4096-token prefill (token by token, fp32); a
+    # ---- the backward of the 4096-token prefill (chunked, tensor cores); a
     # failure here is reported in its own line and does not stop the others
     dO = torch.randn((1, T, H, V), generator=torch.Generator(device=dev).manual_seed(11 + rank), device=dev)
     del ws
@@ -521,26 +522,27 @@ def run_ours(args, world, rank, local):
         nb = 3
         bw_ms, bwper = time_launches(bwstep, nb, stream)
         bw_ms = max_over_ranks(bw_ms, world) / nb
+        # algorithmic bytes: q, k, v, g (bf16), beta, dO (fp32) in; dq, dk, dv, dg, dbeta (fp32) out
         bw_bytes = T * H * ((3 * K + V) * 2 + 2 + 4 * V + (3 * K + V) * 4 + 4)
         bw_call = sum(bwper) / len(bwper)
         bw_gbs = bw_bytes / (bw_call * 1e-3) / 1e9
-        # fp32 multiply-adds of the chunked backward's CUDA-core kernels per (64-token chunk, head):
-        # the reverse chain (dU, dS) and the chunk kernel (its 17 products), as launched
+        # the method's multiply-adds of the backward's own products per (64-token chunk, head), one
+        # term each (the hi|lo split runs three): the reverse chain's dU and dS, and the chunk kernel's
+        # U, dO S^T, dU S^T, dO U^T, U dS'^T, dT, [dBk | dBv], T-products, and the gated back-products
         chunks = (T + 63) // 64 * H
-        bw_flops = 2 * chunks * (64 * 128 * 192 + 2 * 128 * 128 * 64 + 9961472)
-        # fp32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the sampled maximum SM clock
-        alu_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * (
-            clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+        bw_flops = 2 * chunks * (3670016 + 9437184)
         bw_tf = bw_flops / (bw_call * 1e-3) / 1e12
         backward = {"value": world * T / (bw_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": bw_ms,
                     "workload": "backward of the 4096-token prefill (dq, dk, dv, dg, dbeta, dS0): the "
-                                "tensor-core prefill again keeping every chunk's state, a reverse chain "
-                                "carrying dS, chunk-parallel gradients (fp32 CUDA cores)",
+                                "tensor-core prefill again keeping every chunk's state, A and T, a reverse "
+                                "tcgen05 chain carrying dS, chunk-parallel tcgen05 gradients",
                     "gpu_launches": 4 * nb,
-                    "roofline": {"bound": "alu", "achieved": bw_tf, "peak": alu_peak, "unit": "TFLOP/s",
-                                 "frac": bw_tf / alu_peak, "traffic": None, "algorithmic_flops": bw_flops,
-                                 "peak_kind": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
-                                 "algorithmic_bytes": bw_bytes, "hbm_gbs": bw_gbs, "hbm_frac": bw_gbs / hbm}}
+                    "roofline": {"bound": "hbm", "achieved": bw_gbs, "peak": hbm, "unit": "GB/s",
+                                 "frac": bw_gbs / hbm, "traffic": None, "algorithmic_bytes": bw_bytes,
+                                 "tensor_tflops": bw_tf, "tensor_frac": bw_tf / bf16_peak,
+                                 "algorithmic_flops": bw_flops,
+                                 "note": "the chunk kernel dominates and is bound by the latency of its "
+                                         "per-CTA scratch round trips, neither by HBM nor by the tensor pipe"}}
     else:
         backward = {"error": bw_err or "failed on another rank"}
     del dO, bws
