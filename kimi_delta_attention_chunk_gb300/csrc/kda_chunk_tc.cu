@@ -150,8 +150,10 @@ __device__ __forceinline__ float lg2_approx(float x) {
 // the prologue runs on them first and leaves q, k as bf16 hi (in the q, k tiles)
 // plus lo (in the v, g tiles), v as hi/lo in TMEM and g folded into pass 1.
 // SILU: the convolution is followed by SiLU (a separate instance, so that the
-// other never evaluates it).
-template <bool FUSED, bool SILU = false>
+// other never evaluates it).  AT: also write each chunk's A and T to pl.at_out
+// (for the backward; an instance of its own so that the prefill carries no trace
+// of it).
+template <bool FUSED, bool SILU = false, bool AT = false>
 __global__ void __launch_bounds__(NT, 1)
 chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
@@ -728,7 +730,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc::tmem_ld_wait();
             const float br = beta_s[r];
             // (for the backward: A itself, without beta)
-            float* ao = pl.at_out != nullptr ? pl.at_out + ((int64_t)cur.gc * H + h) * (2 * C * C) + r * C : nullptr;
+            float* ao = AT ? pl.at_out + ((int64_t)cur.gc * H + h) * (2 * C * C) + r * C : nullptr;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
                 if (R == 0 && g8 == 1) break;
@@ -739,7 +741,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     const float xv = __uint_as_float(a[8 * g8 + u]);
                     v[u] = is_q ? (j <= r ? scale * xv : 0.f) : (j < r ? br * xv : 0.f);
                 }
-                if (!is_q && ao != nullptr) {
+                if (AT && !is_q) {
                     float w[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) w[u] = j0 + 8 * g8 + u < r ? __uint_as_float(a[8 * g8 + u]) : 0.f;
@@ -936,7 +938,7 @@ chunk_local_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) t[u] = (8 * jg + u > r) ? 0.f : t[u];
-                if (pl.at_out != nullptr) {
+                if constexpr (AT) {
                     // (for the backward: T itself)
                     float* to = pl.at_out + ((int64_t)cur.gc * H + h) * (2 * C * C) + C * C + r * C + 8 * jg;
                     *reinterpret_cast<float4*>(to) = make_float4(t[0], t[1], t[2], t[3]);
@@ -1615,7 +1617,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws
         pro.conv_q = p.conv_q; pro.conv_k = p.conv_k; pro.conv_v = p.conv_v;
         pro.A_log = p.A_log; pro.dt_bias = p.dt_bias;
         pro.lower_bound = p.lower_bound; pro.l2_eps = p.l2_eps;
-        auto kern = !fused ? chunk_local_kernel<false>
+        auto kern = !fused ? (at_out != nullptr ? chunk_local_kernel<false, false, true> : chunk_local_kernel<false>)
                            : (p.conv_act == 1 ? chunk_local_kernel<true, true> : chunk_local_kernel<true, false>);
         const int smem_bytes = (int)(fused ? SM_LOCAL_TOTAL_FUSED : SM_LOCAL_TOTAL) + 1024;  // + alignment slack
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
