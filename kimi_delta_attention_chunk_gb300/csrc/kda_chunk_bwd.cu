@@ -82,6 +82,7 @@ __device__ __forceinline__ void unit_rc(int i, int& r, int& c) {
 struct Ident {
     __device__ __forceinline__ void operator()(int, int, float4&) const {}
 };
+constexpr int kStageInFlight = 8;   // float4 loads in flight per thread while staging an operand
 struct OneVariant {
     __device__ __forceinline__ int operator()(int) const { return 0; }
 };
@@ -103,16 +104,17 @@ __device__ __forceinline__ uint32_t op_off(int row, int k, int Kd, bool mn) {
 // float4 passed through f(r + r_off, c + c_off, v) first (its coordinates in the
 // whole matrix).  KROW: the matrix rows are operand rows row0 + r and its columns
 // are k (K-major image); else its rows are k and its columns operand rows row0 + c
-// (MN-major image).  Four float4 loads in flight per thread.
+// (MN-major image).  kStageInFlight float4 loads in flight per thread.
 template <int R, int CO, bool KROW, typename F = Ident>
 __device__ __forceinline__ void stage_op(const float* src, int ld, uint8_t* hi, uint8_t* lo, int Kd, int row0,
                                          int r_off = 0, int c_off = 0, F f = F()) {
     static_assert(R % 8 == 0 && CO % 4 == 0, "operand tile");
     constexpr int NV = R * (CO / 4);
-    for (int i0 = threadIdx.x; i0 < NV; i0 += 4 * kChunkThreads) {
-        float4 v[4];
+    constexpr int IF = kStageInFlight;
+    for (int i0 = threadIdx.x; i0 < NV; i0 += IF * kChunkThreads) {
+        float4 v[IF];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < IF; ++u) {
             const int i = i0 + u * kChunkThreads;
             if (i < NV) {
                 int r, c;
@@ -121,7 +123,7 @@ __device__ __forceinline__ void stage_op(const float* src, int ld, uint8_t* hi, 
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < IF; ++u) {
             const int i = i0 + u * kChunkThreads;
             if (i >= NV) break;
             int r, c;
