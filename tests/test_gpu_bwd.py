@@ -91,3 +91,15 @@ def test_fp32_two_dense_rows_no_initial_state():
     d = synth.direct_inputs(65, 2, 128, 64, torch.float32, seed=113, B=2)
     dO = torch.randn(2, 65, 2, 64, generator=torch.Generator().manual_seed(3))
     check(d, dO, None, TOL_F32)
+
+
+def test_bf16_chunked_all_heads():
+    # every one of the 96 heads at 512 tokens (768 (chunk, head) tasks over the chunk
+    # kernel's persistent CTAs, several per CTA), with an initial state and a
+    # final-state gradient: a mistake in the task-to-head mapping would show here
+    T, H = 512, 96
+    d = synth.direct_inputs(T, H, 128, 128, torch.bfloat16, seed=117, init_state=True)
+    gen = torch.Generator().manual_seed(7)
+    dO = torch.randn(1, T, H, 128, generator=gen)
+    dST = torch.randn(1, H, 128, 128, generator=gen)
+    check(d, dO, dST, TOL_BF16)
