@@ -80,6 +80,7 @@ gate_proj_xa_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
     const int s = blockIdx.y;
     const int kb0 = s * nk_per;
     const int nkb = min(nk, kb0 + nk_per) - kb0;   // >= 1: the host leaves no range empty
+    tc::grid_dep_launch();   // (the finishing kernel waits for this grid before it reads)
 
     if (warp == 0) tc::tmem_alloc(tmem_base_s, 256);
     if (tid == 0) {
@@ -181,6 +182,8 @@ gate_proj_finish_kernel(const float* __restrict__ part, int S, int rows, int R, 
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int row = r0 + lane;
     constexpr int kCols = kFinCols / (kThreadsFin / 32);   // columns per warp
+    tc::grid_dep_launch();   // (the second product waits for this grid before it reads y)
+    tc::grid_dep_wait();     // the partial sums are complete
     float v[kCols][kMaxSplit];
 #pragma unroll
     for (int q = 0; q < kCols; ++q) {
@@ -222,6 +225,25 @@ gate_proj_finish_kernel(const float* __restrict__ part, int S, int rows, int R, 
 // One CTA: the 128-token tile blockIdx.x and the channel tiles [t0, t0 + nt) of GN2 each.
 // Shared memory: A hi | A lo ([128][R] each: R/64 swizzle atoms of 16 KB), a ring of
 // kRingB f_b tiles ([128][R]), two output stagings ([128][128] bf16 as two 16 KB atoms).
+// A launch that may begin while the previous grid on the stream still runs
+// (programmatic stream serialization): the kernel waits for that grid with
+// grid_dep_wait() before it reads what the grid wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 __host__ __device__ __forceinline__ uint32_t fb_smem_bytes(int R) {
     return (uint32_t)(R / GK) * kTileA * 2 + (uint32_t)kRingB * (uint32_t)(R / GK) * kTileA + 2u * 2u * kTileA;
 }
@@ -272,18 +294,25 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
     auto wait = [&](uint64_t* bar, uint32_t parity) { return tc::bar_wait_or_abort(bar, parity, wait_iter, abort_s); };
 
     if (warp == 0) {
-        // ---- TMA producer: y hi|lo once, then the f_b tiles through the ring ------
+        // ---- TMA producer: the first f_b tiles, then y hi|lo once the kernel that
+        //      writes it has completed, then the rest of the f_b tiles through the ring
         if (lane == 0) {
-            tc::bar_expect_tx(a_full, 2u * na * kTileA);
-            for (int a = 0; a < na; ++a) {
-                tc::tma_load_2d(ah + a * kTileA, &myh, a * GK, m0, a_full);
-                tc::tma_load_2d(al + a * kTileA, &myl, a * GK, m0, a_full);
-            }
+            bool y_issued = false;
+            auto issue_y = [&]() {
+                tc::grid_dep_wait();
+                tc::bar_expect_tx(a_full, 2u * na * kTileA);
+                for (int a = 0; a < na; ++a) {
+                    tc::tma_load_2d(ah + a * kTileA, &myh, a * GK, m0, a_full);
+                    tc::tma_load_2d(al + a * kTileA, &myl, a * GK, m0, a_full);
+                }
+                y_issued = true;
+            };
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < nt; ++i) {
                 const int st = i % kRingB;
                 if (i >= kRingB) {
+                    if (!y_issued) issue_y();
                     ok = wait(b_empty + st, (uint32_t)(((i / kRingB) - 1) & 1));
                     if (!ok) break;
                 }
@@ -292,6 +321,7 @@ gate_proj_fb_kernel(const __grid_constant__ CUtensorMap myh, const __grid_consta
                     tc::tma_load_2d(bring + (st * na + a) * kTileA, &mfb, a * GK, (t0 + i) * GN2, b_full + st);
                 issued = i + 1;
             }
+            if (!y_issued) issue_y();
             if (!ok) report(status);
             // every load issued lands before the CTA exits
             tc::bar_wait(a_full, 0, kWaitDefault);
@@ -485,9 +515,8 @@ cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const voi
     }
     {
         const dim3 grid((unsigned)((rows + kFinRows - 1) / kFinRows), (unsigned)(N1 / kFinCols));
-        gate_proj_finish_kernel<<<grid, kThreadsFin, 0, st>>>(part, S, (int)rows, R, NH, yh, yl,
-                                                              reinterpret_cast<__nv_bfloat16*>(beta));
-        e = cudaGetLastError();
+        e = launch_dependent(gate_proj_finish_kernel, grid, dim3(kThreadsFin), 0, st, (const float*)part, S,
+                             (int)rows, R, NH, yh, yl, reinterpret_cast<__nv_bfloat16*>(beta));
         if (e != cudaSuccess) return e;
     }
     {
@@ -502,9 +531,8 @@ cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const voi
                       "shared memory of the second product");
         e = cudaFuncSetAttribute(gate_proj_fb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        gate_proj_fb_kernel<<<dim3(mt, (unsigned)ng), kThreadsFB, smem, st>>>(myh, myl, mfb, mout, R, ntiles, per_cta,
-                                                                            status, wait_iter);
-        e = cudaGetLastError();
+        e = launch_dependent(gate_proj_fb_kernel, dim3(mt, (unsigned)ng), dim3(kThreadsFB), (size_t)smem, st, myh, myl,
+                             mfb, mout, R, ntiles, per_cta, status, wait_iter);
     }
     return e;
 }

@@ -196,6 +196,15 @@ __device__ __forceinline__ bool bar_wait_or_abort(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// A grid launched with programmatic stream serialization may start while the grid
+// before it on the stream still runs: grid_dep_wait() blocks the calling thread until
+// that grid has completed and its memory operations are visible; grid_dep_launch()
+// lets the next such grid start (every CTA of this grid must have called it or
+// exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- named barriers (ids 1..15; count a multiple of 32) ----------------------
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
