@@ -225,25 +225,6 @@ gate_proj_finish_kernel(const float* __restrict__ part, int S, int rows, int R, 
 // One CTA: the 128-token tile blockIdx.x and the channel tiles [t0, t0 + nt) of GN2 each.
 // Shared memory: A hi | A lo ([128][R] each: R/64 swizzle atoms of 16 KB), a ring of
 // kRingB f_b tiles ([128][R]), two output stagings ([128][128] bf16 as two 16 KB atoms).
-// A launch that may begin while the previous grid on the stream still runs
-// (programmatic stream serialization): the kernel waits for that grid with
-// grid_dep_wait() before it reads what the grid wrote.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                             Args... args) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
-
 __host__ __device__ __forceinline__ uint32_t fb_smem_bytes(int R) {
     return (uint32_t)(R / GK) * kTileA * 2 + (uint32_t)kRingB * (uint32_t)(R / GK) * kTileA + 2u * 2u * kTileA;
 }
@@ -515,7 +496,7 @@ cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const voi
     }
     {
         const dim3 grid((unsigned)((rows + kFinRows - 1) / kFinRows), (unsigned)(N1 / kFinCols));
-        e = launch_dependent(gate_proj_finish_kernel, grid, dim3(kThreadsFin), 0, st, (const float*)part, S,
+        e = tc::launch_dependent(gate_proj_finish_kernel, grid, dim3(kThreadsFin), 0, st, (const float*)part, S,
                              (int)rows, R, NH, yh, yl, reinterpret_cast<__nv_bfloat16*>(beta));
         if (e != cudaSuccess) return e;
     }
@@ -531,7 +512,7 @@ cudaError_t gate_proj(const void* x, const void* f_a, const void* f_b, const voi
                       "shared memory of the second product");
         e = cudaFuncSetAttribute(gate_proj_fb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        e = launch_dependent(gate_proj_fb_kernel, dim3(mt, (unsigned)ng), dim3(kThreadsFB), (size_t)smem, st, myh, myl,
+        e = tc::launch_dependent(gate_proj_fb_kernel, dim3(mt, (unsigned)ng), dim3(kThreadsFB), (size_t)smem, st, myh, myl,
                              mfb, mout, R, ntiles, per_cta, status, wait_iter);
     }
     return e;
