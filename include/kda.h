@@ -243,10 +243,11 @@ KDA_API void kda_set_wait_limit(uint32_t iterations);
 
 /*
  * kda_inject_wait_timeout -- testing hook: the next kda_chunk_fwd,
- * kda_chunk_fwd_fused or kda_chunk_fwd_noalloc call made by the calling host
- * thread on the tensor-core path makes the first wait of one of its kernels
- * (kernel = 1: the chunk-local kernel, in every CTA; 2: the state kernel's MMA
- * issuer, in every CTA) a wait on an mbarrier that nothing arrives on.  That
+ * kda_chunk_fwd_fused, kda_chunk_fwd_noalloc or kda_chunk_bwd call made by the
+ * calling host thread on the tensor-core path makes the first wait of one of its
+ * kernels (kernel = 1: the chunk-local kernel, in every CTA; 2: the state
+ * kernel's MMA issuer, in every CTA; 3: the chunked backward's chain kernel, 4:
+ * its chunk kernel, in every CTA) a wait on an mbarrier that nothing arrives on.  That
  * wait runs out after the kda_set_wait_limit polls, records KDA_ERR_TIMEOUT in
  * the call's status word and the kernels take their give-up path (no fault, no
  * trap).  The call consumes the setting; another kernel value clears it.

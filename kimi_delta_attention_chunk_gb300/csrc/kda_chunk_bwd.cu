@@ -155,6 +155,8 @@ struct Tc {
     uint32_t phase;
     uint32_t wait_iter;
     bool failed;
+    uint64_t* never;    // testing: an mbarrier that nothing arrives on
+    bool inject;        // testing: the next wait is on it
 };
 
 // One round: D_b (+)= A B_b^T for the NB variants b (TMEM columns [b N, b N + N)),
@@ -194,7 +196,8 @@ __device__ __forceinline__ bool tc_round(Tc& t, int Kd, bool acc, SA sa, SB sb) 
         tc::commit_w(t.bar);
     }
     bool ok = true;
-    if (warp == 0) ok = tc::bar_wait(t.bar, t.phase, t.wait_iter);
+    if (warp == 0) ok = t.inject ? tc::bar_wait(t.never, 0, t.wait_iter) : tc::bar_wait(t.bar, t.phase, t.wait_iter);
+    t.inject = false;
     const bool gave_up = __syncthreads_or(!ok) != 0;
     if (!gave_up) t.phase ^= 1;
     t.failed = t.failed || gave_up;
@@ -331,6 +334,7 @@ bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __res
     uint64_t* bar_s = bar_ld + 2;
     uint64_t* bar_fin = bar_ld + 3;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_ld + 4);
+    uint64_t* bar_never = bar_ld + 5;   // testing: nothing arrives on it
     const Chain chn = chain_of(pl, blockIdx.x);
     const int H = pl.H, h = chn.h;
     const int64_t sbase = ((int64_t)chn.n * H + h) * D * D;
@@ -340,6 +344,7 @@ bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __res
         tc::bar_init(bar_u, 1);
         tc::bar_init(bar_s, 1);
         tc::bar_init(bar_fin, 1);
+        tc::bar_init(bar_never, 1);
         tc::bar_init_fence();
     }
     tc::fence_before();
@@ -352,9 +357,11 @@ bwd_chain_kernel(const Plan pl, const float* __restrict__ dO, const float* __res
 
     uint32_t ph_ld = 0, ph_u = 0, ph_s = 0;
     bool failed = false;
+    bool inject = pl.inject == 3;
     auto wait = [&](uint64_t* bar, uint32_t& phase) {
         bool ok = true;
-        if (tid == 0) ok = tc::bar_wait(bar, phase, pl.wait_iter);
+        if (tid == 0) ok = tc::bar_wait(inject ? bar_never : bar, inject ? 0u : phase, pl.wait_iter);
+        inject = false;
         const bool gave_up = __syncthreads_or(!ok) != 0;
         if (!gave_up) phase ^= 1;
         failed = failed || gave_up;
@@ -576,18 +583,20 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     uint64_t* bar_mma = reinterpret_cast<uint64_t*>(smem + BK_BAR);
     uint64_t* bar_fin = bar_mma + 1;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_mma + 2);
+    uint64_t* bar_never = bar_mma + 3;   // testing: nothing arrives on it
     const int tid = threadIdx.x;
     const int H = pl.H;
     if ((tid >> 5) == 0) tc::tmem_alloc(tmem_base_s, 512);
     if (tid == 0) {
         tc::bar_init(bar_mma, 1);
         tc::bar_init(bar_fin, 1);
+        tc::bar_init(bar_never, 1);
         tc::bar_init_fence();
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    Tc t{smem, *tmem_base_s, bar_mma, 0u, pl.wait_iter, false};
+    Tc t{smem, *tmem_base_s, bar_mma, 0u, pl.wait_iter, false, bar_never, pl.inject == 4};
     float* sc = scratch + (int64_t)blockIdx.x * SC_TOTAL;
     float* K_ = sc + SC_K;
     float* Q_ = sc + SC_Q;

@@ -43,7 +43,8 @@ struct Plan {
     uint8_t* slots;
     int32_t* status;           // device status word (KDA_ERR_TIMEOUT on a wait that gave up), or null
     uint32_t wait_iter;        // polls before a wait gives up
-    int inject;                // testing: 1 = the chunk-local kernel's, 2 = the state kernel's first wait
+    int inject;                // testing: 1 = the chunk-local kernel's, 2 = the state kernel's, 3 = the
+                               //   backward chain kernel's, 4 = the backward chunk kernel's first wait
                                //   is on an mbarrier that nothing arrives on (0 = none)
     float* states_out;         // or null: the state entering every chunk, fp32 [slot][K][V] (for the backward)
     float* at_out;             // or null: per slot A (strictly lower, without beta) and T = (I + Diag(beta) A)^{-1},

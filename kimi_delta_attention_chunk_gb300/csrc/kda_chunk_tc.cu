@@ -1681,7 +1681,7 @@ void trace_set(void* begin, void* split, void* end) {
 
 void set_wait_limit(uint32_t iterations) { g_wait_limit.store(iterations, std::memory_order_relaxed); }
 
-void inject_wait_timeout(int kernel) { g_inject = (kernel == 1 || kernel == 2) ? kernel : 0; }
+void inject_wait_timeout(int kernel) { g_inject = (kernel >= 1 && kernel <= 4) ? kernel : 0; }
 
 cudaError_t chunk_tc(kda_dtype out_dt, const ChunkParams& p, void* ws, size_t ws_bytes, int32_t* status,
                      cudaStream_t st) {

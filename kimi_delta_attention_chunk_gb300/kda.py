@@ -153,9 +153,10 @@ def set_wait_limit(iterations: int = 0):
 
 
 def inject_wait_timeout(kernel: int):
-    """Testing hook: the next tensor-core prefill call on this thread makes the
-    first wait of its chunk-local (1) or state (2) kernel one that nothing
-    completes, so that it gives up and reports KDA_ERR_TIMEOUT."""
+    """Testing hook: the next tensor-core prefill or chunked backward call on this
+    thread makes the first wait of its chunk-local (1), state (2), backward chain
+    (3) or backward chunk (4) kernel one that nothing completes, so that it gives
+    up and reports KDA_ERR_TIMEOUT."""
     load_library().kda_inject_wait_timeout(int(kernel))
 
 

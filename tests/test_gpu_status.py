@@ -109,3 +109,35 @@ def test_backward_skipping_a_malformed_sequence_reports_range():
     kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO.cuda(), scale=d["scale"], status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == KDA_OK
+
+
+@pytest.mark.parametrize("kernel", [3, 4])
+def test_backward_wait_that_gives_up_reports_timeout_and_the_context_stays_usable(kernel):
+    """kernel 3: the chunked backward's chain kernel, kernel 4: its chunk kernel,
+    first waits (in every CTA) on an mbarrier that nothing arrives on."""
+    T, H = 200, 3
+    inp = synth.direct_inputs(T, H, 128, 128, torch.bfloat16, seed=76, init_state=True)
+    d = to_dev(inp)
+    rng = np.random.default_rng(77)
+    dO = torch.from_numpy(rng.standard_normal((1, T, H, 128)).astype(np.float32))
+    st = status_word()
+    kda.set_wait_limit(2000)
+    kda.inject_wait_timeout(kernel)
+    try:
+        kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO.cuda(), scale=d["scale"],
+                      initial_state=d["initial_state"], status=st)
+        torch.cuda.synchronize()
+    finally:
+        kda.set_wait_limit(0)
+        kda.inject_wait_timeout(0)
+    assert int(st.item()) == KDA_ERR_TIMEOUT
+    # the kernels exited cleanly: the same call with the default limit succeeds
+    st = status_word()
+    got = kda.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO.cuda(), scale=d["scale"],
+                        initial_state=d["initial_state"], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == KDA_OK
+    ref = oracle.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dO, scale=inp["scale"],
+                              initial_state=inp["initial_state"])
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "dS0"):
+        assert rel_err(got[key], ref[key]) <= TOL_BF16, key
