@@ -49,13 +49,12 @@ enum : int {
     SC_K = 0, SC_Q = SC_K + MR, SC_V = SC_Q + MR, SC_DO = SC_V + MR, SC_WN = SC_DO + MR,
     SC_PRE = SC_WN + MR, SC_EA = SC_PRE + MR, SC_KL = SC_EA + MR, SC_QL = SC_KL + MR,
     SC_U = SC_QL + MR, SC_DXQ = SC_U + MR, SC_DWU = SC_DXQ + MR, SC_DKB = SC_DWU + 2 * MR,
-    SC_DBKV = SC_DKB + MR, SC_XVB = SC_DBKV + 2 * MR, SC_GB = SC_XVB + 2 * MR, SC_GF = SC_GB + MR,
+    SC_DBKV = SC_DKB + MR, SC_GB = SC_DBKV + 2 * MR, SC_GF = SC_GB + MR,
     SC_GC = SC_GF + MR,
-    SC_DP = SC_GC + MR, SC_DT = SC_DP + MQ, SC_TMP = SC_DT + MQ,
-    SC_DM = SC_TMP + MQ, SC_DA = SC_DM + MQ,
+    SC_DP = SC_GC + MR, SC_DM = SC_DP + MQ, SC_DA = SC_DM + MQ,
     SC_TOTAL = SC_DA + MQ
 };
-static_assert(SC_TOTAL * 4 == 770048, "the per-CTA scratch size stated in kda.h");
+static_assert(SC_TOTAL * 4 == 671744, "the per-CTA scratch size stated in kda.h");
 // Shared memory of the chunk kernel: the operand images of one tensor-core round
 // (bf16 hi | lo), then small tables and the MMA barriers.
 constexpr uint32_t OP_BYTES = 160 * 1024;               // the largest round: A 128 x 64 + 4 B variants 128 x 64
@@ -83,6 +82,11 @@ struct Ident {
     __device__ __forceinline__ void operator()(int, int, float4&) const {}
 };
 constexpr int kStageInFlight = 8;   // float4 loads in flight per thread while staging an operand
+struct Neg {
+    __device__ __forceinline__ void operator()(int, int, float4& x) const {
+        x.x = -x.x; x.y = -x.y; x.z = -x.z; x.w = -x.w;
+    }
+};
 struct OneVariant {
     __device__ __forceinline__ int operator()(int) const { return 0; }
 };
@@ -612,13 +616,10 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* DWU = sc + SC_DWU;    // [dW | dU] [64][256]
     float* DKB = sc + SC_DKB;
     float* DBKV = sc + SC_DBKV;  // [dBk | dBv] [64][256]
-    float* XVB = sc + SC_XVB;    // [Diag(beta) X | Diag(beta) v] [64][256]
     float* GB = sc + SC_GB;
     float* GF = sc + SC_GF;
     float* GC = sc + SC_GC;
     float* DP = sc + SC_DP;
-    float* DT = sc + SC_DT;
-    float* TMP = sc + SC_TMP;
     float* DM = sc + SC_DM;
     float* DA = sc + SC_DA;
     const int64_t ntasks = pl.max_chunks * H;
@@ -742,7 +743,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
                 }
             }
         }
-        // derived operands: e^{G_r}, a e^{G_r - G_m(b(r))}, Diag(beta) X, Diag(beta) v
+        // derived operands: e^{G_r}, a e^{G_r - G_m(b(r))}
         for (int u = tid; u < MR / 4; u += kChunkThreads) {
             const int r = u >> 5, c = 4 * (u & 31), B = r >> 4;
             const float4 pr = *reinterpret_cast<const float4*>(PRE + r * D + c);
@@ -754,13 +755,9 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
                 bf.x *= tot[b * D + c]; bf.y *= tot[b * D + c + 1]; bf.z *= tot[b * D + c + 2]; bf.w *= tot[b * D + c + 3];
             }
             const float4 ea = make_float4(bf.x * pr.x, bf.y * pr.y, bf.z * pr.z, bf.w * pr.w);
-            const float br = bs[r];
             *reinterpret_cast<float4*>(EA + r * D + c) = ea;
             *reinterpret_cast<float4*>(KL + r * D + c) = make_float4(kx.x * pr.x, kx.y * pr.y, kx.z * pr.z, kx.w * pr.w);
             *reinterpret_cast<float4*>(QL + r * D + c) = make_float4(qx.x * pr.x, qx.y * pr.y, qx.z * pr.z, qx.w * pr.w);
-            *reinterpret_cast<float4*>(XVB + r * 2 * D + c) =
-                make_float4(br * kx.x * ea.x, br * kx.y * ea.y, br * kx.z * ea.z, br * kx.w * ea.w);
-            *reinterpret_cast<float4*>(XVB + r * 2 * D + D + c) = make_float4(br * vx.x, br * vx.y, br * vx.z, br * vx.w);
         }
 
         // ---- the products with S, dS', U (tensor-core rounds) ----------------------------
@@ -818,18 +815,9 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             const int r = e >> 6, j = e & 63;
             if (j > r) DP[e] = 0.f;
         }
-        // dT = [dW | dU] [Diag(beta) X | Diag(beta) v]^T;  [dBk | dBv] = T^T [dW | dU];
-        // dM = -T^T dT T^T
-        for (int hk = 0; hk < 2 && !t.failed; ++hk)
-            tc_round<C, 1, false, false>(
-                t, D, hk > 0,
-                [&](uint8_t* hi, uint8_t* lo) {
-                    stage_op<C, D, true>(DWU + hk * D, 2 * D, hi, lo, D, 0);
-                    zero_rows(hi, lo, D, C);
-                },
-                [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, D, true>(XVB + hk * D, 2 * D, hi, lo, D, 0); });
-        if (t.failed) break;
-        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DT + r * C + c0, x, 1.f, false); });
+        // [dBk | dBv] = T^T [dW | dU];  dM = -T^T dT T^T with dT = [dW | dU] (Diag(beta)
+        // [X | v])^T, and since T Diag(beta) [X | v] = [W | U~] (the forward's own
+        // products):  dM = -[dBk | dBv] [W | U~]^T = dBk (-W)^T + dBv (-U~)^T
         tc_round<2 * D, 1, true, true>(
             t, C, false,
             [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
@@ -837,18 +825,20 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         if (t.failed) break;
         tc_epi<2 * D, 1>(t, C, OneVariant{},
                          [&](int r, int c0, const float* x) { put16(DBKV + r * 2 * D + c0, x, 1.f, false); });
-        tc_round<C, 1, false, false>(
-            t, C, false,
-            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, true>(DT, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
-            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, C, true>(Tm, C, hi, lo, C, 0); });
+        for (int hk = 0; hk < 2 && !t.failed; ++hk)
+            tc_round<C, 1, false, false>(
+                t, D, hk > 0,
+                [&](uint8_t* hi, uint8_t* lo) {
+                    stage_op<C, D, true>(DBKV + hk * D, 2 * D, hi, lo, D, 0);
+                    zero_rows(hi, lo, D, C);
+                },
+                [&](uint8_t* hi, uint8_t* lo, int) {
+                    if (hk == 0) stage_op<C, D, true>(WN, D, hi, lo, D, 0);
+                    else stage_op<C, D, true>(reinterpret_cast<const float*>(slot + SLOT_UT), D, hi, lo, D, 0, 0, 0,
+                                              Neg{});
+                });
         if (t.failed) break;
-        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(TMP + r * C + c0, x, 1.f, false); });
-        tc_round<C, 1, true, true>(
-            t, C, false,
-            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
-            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, C, false>(TMP, C, hi, lo, C, 0); });
-        if (t.failed) break;
-        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DM + r * C + c0, x, -1.f, false); });
+        tc_epi<C, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DM + r * C + c0, x, 1.f, false); });
         for (int e = tid; e < MQ; e += kChunkThreads) {
             const int r = e >> 6, j = e & 63;
             DA[e] = j < r ? bs[r] * DM[e] : 0.f;
