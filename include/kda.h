@@ -451,9 +451,9 @@ KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v
  * Arguments, outputs and rules as kda_recurrent_bwd.  The caller passes a device
  * workspace of at least kda_chunk_bwd_workspace_size bytes (16-byte aligned): for
  * the chunked path kda_chunk_fwd_workspace_size + 2 B T H V (o, bf16), each rounded
- * up to 256 bytes, + 4 slots (K V + 2 * 64 * 64 + K V + 64 V) with slots =
- * max_chunks * H (the entering state, A and T, dS' and dU of every chunk) + a
- * scratch of 152 * 671744 bytes (one area per CTA of the gradient kernel); for the
+ * up to 256 bytes, + 4 slots (K V + 2 * 64 * 64 + 64 V + K V + 64 V) with slots =
+ * max_chunks * H (the entering state, A and T, U, dS' and dU of every chunk) + a
+ * scratch of 152 * 638976 bytes (one area per CTA of the gradient kernel); for the
  * other sizes kda_recurrent_bwd_workspace_size.  status: optional device word, KDA_ERR_TIMEOUT
  * if a bounded wait of the forward's kernels gave up (the gradients are then
  * unspecified).

@@ -48,13 +48,13 @@ constexpr int MQ = C * C;       // floats of a [64][64] matrix
 enum : int {
     SC_K = 0, SC_Q = SC_K + MR, SC_V = SC_Q + MR, SC_DO = SC_V + MR, SC_WN = SC_DO + MR,
     SC_PRE = SC_WN + MR, SC_EA = SC_PRE + MR, SC_KL = SC_EA + MR, SC_QL = SC_KL + MR,
-    SC_U = SC_QL + MR, SC_DXQ = SC_U + MR, SC_DWU = SC_DXQ + MR, SC_DKB = SC_DWU + 2 * MR,
+    SC_DXQ = SC_QL + MR, SC_DWU = SC_DXQ + MR, SC_DKB = SC_DWU + 2 * MR,
     SC_DBKV = SC_DKB + MR, SC_GB = SC_DBKV + 2 * MR, SC_GF = SC_GB + MR,
     SC_GC = SC_GF + MR,
     SC_DP = SC_GC + MR, SC_DM = SC_DP + MQ, SC_DA = SC_DM + MQ,
     SC_TOTAL = SC_DA + MQ
 };
-static_assert(SC_TOTAL * 4 == 671744, "the per-CTA scratch size stated in kda.h");
+static_assert(SC_TOTAL * 4 == 638976, "the per-CTA scratch size stated in kda.h");
 // Shared memory of the chunk kernel: the operand images of one tensor-core round
 // (bf16 hi | lo), then small tables and the MMA barriers.
 constexpr uint32_t OP_BYTES = 160 * 1024;               // the largest round: A 128 x 64 + 4 B variants 128 x 64
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
                  const __nv_bfloat16* __restrict__ beta, float scale, const float* __restrict__ dO,
-                 const float* __restrict__ states, const float* __restrict__ at, const float* __restrict__ dsp,
-                 const float* __restrict__ du,
+                 const float* __restrict__ states, const float* __restrict__ at, const float* __restrict__ uu,
+                 const float* __restrict__ dsp, const float* __restrict__ du,
                  float* __restrict__ scratch, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                  float* __restrict__ dg, float* __restrict__ dbeta) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -611,7 +611,6 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
     float* EA = sc + SC_EA;
     float* KL = sc + SC_KL;
     float* QL = sc + SC_QL;
-    float* U = sc + SC_U;
     float* DXQ = sc + SC_DXQ;
     float* DWU = sc + SC_DWU;    // [dW | dU] [64][256]
     float* DKB = sc + SC_DKB;
@@ -636,9 +635,10 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         const float* DU = du + task * (int64_t)(C * D);
         const float* Am = at + task * (int64_t)(2 * MQ);   // A (strictly lower), from the forward
         const float* Tm = Am + MQ;                          // T, from the forward
+        const float* U = uu + task * (int64_t)(C * D);     // U = U~ - W S, from the forward
         __syncthreads();   // the previous task is done with the scratch and the tables
 
-        // ---- inputs (0 past the sequence end), U~ and dU, prefix products, -W ----------
+        // ---- inputs (0 past the sequence end), dU, prefix products, -W ---------------
         // (every loop below has a fixed count per thread and is unrolled, so that its
         // loads are in flight together)
         constexpr int NKV = MR / 8 / kChunkThreads;
@@ -672,16 +672,15 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             *reinterpret_cast<float4*>(V_ + o + 4) = make_float4(vx[4], vx[5], vx[6], vx[7]);
         }
         {
-            // (all loads first: the slot is not known not to alias the scratch)
+            // (all loads first)
             constexpr int NI = MR / 4 / kChunkThreads;
-            float4 xo[NI], xu[NI], xd[NI];
+            float4 xo[NI], xd[NI];
 #pragma unroll
             for (int it = 0; it < NI; ++it) {
                 const int u = tid + it * kChunkThreads;
                 const int r = u >> 5, c = 4 * (u & 31);
                 xo[it] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (r < L) xo[it] = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c);
-                xu[it] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(slot + SLOT_UT) + r * D + c);
                 xd[it] = *reinterpret_cast<const float4*>(DU + r * D + c);
             }
 #pragma unroll
@@ -689,7 +688,6 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
                 const int u = tid + it * kChunkThreads;
                 const int r = u >> 5, c = 4 * (u & 31);
                 *reinterpret_cast<float4*>(DO_ + r * D + c) = xo[it];
-                *reinterpret_cast<float4*>(U + r * D + c) = xu[it];
                 *reinterpret_cast<float4*>(DWU + r * 2 * D + D + c) = xd[it];
             }
         }
@@ -761,13 +759,6 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         }
 
         // ---- the products with S, dS', U (tensor-core rounds) ----------------------------
-        // U = U~ + (-W) S
-        tc_round<D, 1, false, true>(
-            t, D, false,
-            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, D, true>(WN, D, hi, lo, D, 0); zero_rows(hi, lo, D, C); },
-            [&](uint8_t* hi, uint8_t* lo, int) { stage_op<D, D, false>(S, D, hi, lo, D, 0); });
-        if (t.failed) break;
-        tc_epi<D, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(U + r * D + c0, x, 1.f, true); });
         // [dO; dU] [S; U]^T: scale dO S^T, dW = -dU S^T, scale dO U^T (dU U^T unused)
         tc_round<D + C, 1, false, false>(
             t, D, false,
@@ -970,10 +961,10 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
 }
 
 // Workspace of the chunked backward: the forward's (bookkeeping and slots), o as
-// bf16, then per (chunk slot, head) the entering state, A and T, dS' and dU, then
-// the chunk kernel's per-CTA scratch.
+// bf16, then per (chunk slot, head) the entering state, A and T, U, dS' and dU,
+// then the chunk kernel's per-CTA scratch.
 struct BwdLayout {
-    size_t fwd, o, states, at, dsp, du, scratch, total;
+    size_t fwd, o, states, at, u, dsp, du, scratch, total;
 };
 BwdLayout bwd_layout(int B, int T, int H, int N, bool packed) {
     BwdLayout l{};
@@ -984,10 +975,11 @@ BwdLayout bwd_layout(int B, int T, int H, int N, bool packed) {
     l.o = (((size_t)B * (size_t)T * (size_t)H * D * 2) + 255) & ~size_t(255);
     l.states = slots * D * D * 4;
     l.at = slots * 2 * C * C * 4;
+    l.u = slots * C * D * 4;
     l.dsp = l.states;
     l.du = slots * C * D * 4;
     l.scratch = (size_t)kBwdCtas * SC_TOTAL * 4;
-    l.total = (int64_t)N * H == 0 ? 0 : l.fwd + l.o + l.states + l.at + l.dsp + l.du + l.scratch;
+    l.total = (int64_t)N * H == 0 ? 0 : l.fwd + l.o + l.states + l.at + l.u + l.dsp + l.du + l.scratch;
     return l;
 }
 
@@ -1011,14 +1003,15 @@ cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, f
     void* o = base + lo.fwd;
     float* states = reinterpret_cast<float*>(base + lo.fwd + lo.o);
     float* at = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states);
-    float* dsp = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at);
-    float* du = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.dsp);
-    float* scratch = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.dsp + lo.du);
+    float* uu = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at);
+    float* dsp = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.u);
+    float* du = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.u + lo.dsp);
+    float* scratch = reinterpret_cast<float*>(base + lo.fwd + lo.o + lo.states + lo.at + lo.u + lo.dsp + lo.du);
     ChunkParams fp = p;
     fp.o = o;
     fp.final_state = nullptr;
     Plan pl{};
-    cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, at, &pl, status, st);
+    cudaError_t e = chunk_tc_forward_states(fp, fwd, lo.fwd, states, at, uu, &pl, status, st);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CS_TOTAL);
     if (e != cudaSuccess) return e;
@@ -1033,8 +1026,8 @@ cudaError_t chunk_bwd(const ChunkParams& p, const float* dO, const float* dST, f
         bwd_chunk_kernel<<<grid, kChunkThreads, BK_TOTAL, st>>>(
             pl, static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
             static_cast<const __nv_bfloat16*>(p.v), static_cast<const __nv_bfloat16*>(p.g),
-            static_cast<const __nv_bfloat16*>(p.beta), p.scale, dO, states, at, dsp, du, scratch, dq, dk,
-            dv, dg, dbeta);
+            static_cast<const __nv_bfloat16*>(p.beta), p.scale, dO, states, at, uu, dsp, du, scratch,
+            dq, dk, dv, dg, dbeta);
         e = cudaGetLastError();
     }
     return e;

@@ -49,6 +49,7 @@ struct Plan {
     float* states_out;         // or null: the state entering every chunk, fp32 [slot][K][V] (for the backward)
     float* at_out;             // or null: per slot A (strictly lower, without beta) and T = (I + Diag(beta) A)^{-1},
                                //   fp32 [slot][2][C][C] (for the backward)
+    float* u_out;              // with states_out: per slot U = U~ - W S, fp32 [slot][C][V] (for the backward)
 };
 
 __device__ __forceinline__ void report_timeout(const Plan& pl) {
@@ -127,8 +128,10 @@ struct ChunkParams;
 // The tensor-core prefill (bf16 inputs, K = V = 128, no prologue) for the backward:
 // o goes to p.o as bf16 (scratch), the state entering every chunk to states_out
 // (fp32 [max_chunks * H][K][V]), each chunk's A and T to at_out (fp32 [max_chunks *
-// H][2][C][C]), and *plan_out receives the work plan, whose slots (in ws) hold the
-// forward's per-chunk operands.  Workspace as for chunk_tc.
+// H][2][C][C]) and its U = U~ - W S to u_out (fp32 [max_chunks * H][C][V]), and
+// *plan_out receives the work plan, whose slots (in ws) hold the forward's per-chunk
+// operands.  Workspace as for chunk_tc.
 cudaError_t chunk_tc_forward_states(const ChunkParams& p, void* ws, size_t ws_bytes, float* states_out,
-                                    float* at_out, cplan::Plan* plan_out, int32_t* status, cudaStream_t st);
+                                    float* at_out, float* u_out, cplan::Plan* plan_out, int32_t* status,
+                                    cudaStream_t st);
 }  // namespace kda

@@ -1141,7 +1141,8 @@ constexpr uint32_t TS_UH = 384;   // U^T hi (bf16 pairs) [128 v][32]
 constexpr uint32_t TS_UL = 416;   // U^T lo
 constexpr uint32_t TS_COLS = 512;
 
-// STATES: also write the state entering every chunk to pl.states_out (for the backward).
+// STATES: also write the state entering every chunk to pl.states_out and every chunk's
+// U = U~ - W S to pl.u_out (for the backward).
 template <typename TOut, bool STATES = false>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restrict__ initial_state,
@@ -1396,10 +1397,17 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mo, const float* __restri
                 tc::tmem_ld16(tm + lane_base(warp) + TS_AU + rb, a);
                 tc::tmem_ld_wait();
                 uint32_t hi[8], lo[8];
+                float u[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    tc::split2(ut_s[(rb + 2 * j) * D + x] + __uint_as_float(a[2 * j]),
-                               ut_s[(rb + 2 * j + 1) * D + x] + __uint_as_float(a[2 * j + 1]), hi[j], lo[j]);
+                for (int j = 0; j < 16; ++j) u[j] = ut_s[(rb + j) * D + x] + __uint_as_float(a[j]);
+                if constexpr (STATES) {
+                    // U of this chunk, U[r][x] (a warp's 32 lanes are 32 consecutive x)
+                    float* uo = pl.u_out + ((g0 + i) * H + h) * (int64_t)(C * D) + x;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) uo[(int64_t)(rb + j) * D] = u[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tc::split2(u[2 * j], u[2 * j + 1], hi[j], lo[j]);
                 tc::tmem_st8(tm + lane_base(warp) + TS_UH + rb / 2, hi);
                 tc::tmem_st8(tm + lane_base(warp) + TS_UL + rb / 2, lo);
                 tc::tmem_st_wait();
@@ -1556,7 +1564,8 @@ Layout layout(int B, int T, int H, int N, bool packed) {
 // backward).
 template <typename TOut>
 cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws_bytes, int32_t* status,
-                      bool fused, float* states_out = nullptr, Plan* plan_out = nullptr, float* at_out = nullptr) {
+                      bool fused, float* states_out = nullptr, Plan* plan_out = nullptr, float* at_out = nullptr,
+                      float* u_out = nullptr) {
     cudaEvent_t trace[3] = {g_trace[0], g_trace[1], g_trace[2]};
     g_trace[0] = g_trace[1] = g_trace[2] = nullptr;
     cudaError_t e = cudaSuccess;
@@ -1586,6 +1595,7 @@ cudaError_t launch_tc(const ChunkParams& p, cudaStream_t st, void* ws, size_t ws
     g_inject = 0;
     pl.states_out = states_out;
     pl.at_out = at_out;
+    pl.u_out = u_out;
     int32_t* hdr = reinterpret_cast<int32_t*>(ws);
     pl.slots = reinterpret_cast<uint8_t*>(ws) + lo.hdr_bytes;
     trace_record(trace[0], st);
@@ -1696,8 +1706,9 @@ cudaError_t chunk_tc_fused(kda_dtype out_dt, const ChunkParams& p, void* ws, siz
 }
 
 cudaError_t chunk_tc_forward_states(const ChunkParams& p, void* ws, size_t ws_bytes, float* states_out,
-                                    float* at_out, cplan::Plan* plan_out, int32_t* status, cudaStream_t st) {
-    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false, states_out, plan_out, at_out);
+                                    float* at_out, float* u_out, cplan::Plan* plan_out, int32_t* status,
+                                    cudaStream_t st) {
+    return launch_tc<__nv_bfloat16>(p, st, ws, ws_bytes, status, false, states_out, plan_out, at_out, u_out);
 }
 
 cudaError_t chunk_tc_fixed_scratch(kda_dtype out_dt, const ChunkParams& p, cudaStream_t st) {
