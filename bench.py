@@ -528,9 +528,10 @@ def run_ours(args, world, rank, local):
         bw_gbs = bw_bytes / (bw_call * 1e-3) / 1e9
         # the method's multiply-adds of the backward's own products per (64-token chunk, head), one
         # term each (the hi|lo split runs three): the reverse chain's dU and dS, and the chunk kernel's
-        # U, dO S^T, dU S^T, dO U^T, U dS'^T, [dBk | dBv], dM, and the gated back-products
+        # dO S^T, dU S^T, dO U^T, U dS'^T, [dBk | dBv], dM, and the gated back-products (U itself
+        # comes from the forward's state kernel)
         chunks = (T + 63) // 64 * H
-        bw_flops = 2 * chunks * (3670016 + 8912896)
+        bw_flops = 2 * chunks * (3670016 + 7864320)
         bw_tf = bw_flops / (bw_call * 1e-3) / 1e12
         backward = {"value": world * T / (bw_ms * 1e-3), "unit": "tokens/s", "ms_per_launch": bw_ms,
                     "workload": "backward of the 4096-token prefill (dq, dk, dv, dg, dbeta, dS0): the "
