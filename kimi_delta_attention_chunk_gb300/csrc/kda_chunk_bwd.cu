@@ -20,8 +20,9 @@
 //
 // Kernels, on the caller's stream:
 //   the forward (chunk_tc_forward_states): the tensor-core prefill, also writing the
-//       state entering every chunk and each chunk's A and T; its workspace slots keep
-//       W, Qs = scale Xq, Kb, scale P, U~ and e^{G_C} per (chunk, head);
+//       state S entering every chunk, each chunk's U = U~ - W S (its state kernel
+//       forms it anyway) and each chunk's A and T; its workspace slots keep W,
+//       Qs = scale Xq, Kb, scale P, U~ and e^{G_C} per (chunk, head);
 //   bwd_chain_kernel: one CTA per (sequence, head) carries dS backwards through the
 //       chunks (the first two lines above) with dS'^T in tensor memory, tcgen05
 //       rounds on the slots' operand images, and stores dS' and dU of every chunk;
