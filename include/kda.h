@@ -445,8 +445,11 @@ KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v
  *
  *     dU = scale P^T dO + Kb dS',   dS = scale (q e^G)^T dO + Diag(e^{G_C}) dS' - W^T dU,
  *
- * and forms every chunk's dq, dk, dv, dg, dbeta in parallel from (S, dU, dS', dO)
- * (fp32 on the CUDA cores).  Other dtypes and head sizes take kda_recurrent_bwd.
+ * and forms every chunk's dq, dk, dv, dg, dbeta in parallel from (S, U, dU, dS',
+ * dO) and the chunk's A and T.  The products of both steps run on the tensor cores
+ * (operands split hi + lo into bf16, three MMA terms, fp32 accumulation); the
+ * elementwise passes in fp32 on the CUDA cores.  Other dtypes and head sizes take
+ * kda_recurrent_bwd.
  *
  * Arguments, outputs and rules as kda_recurrent_bwd.  The caller passes a device
  * workspace of at least kda_chunk_bwd_workspace_size bytes (16-byte aligned): for
@@ -454,9 +457,11 @@ KDA_API kda_status kda_recurrent_bwd(const void *q, const void *k, const void *v
  * up to 256 bytes, + 4 slots (K V + 2 * 64 * 64 + 64 V + K V + 64 V) with slots =
  * max_chunks * H (the entering state, A and T, U, dS' and dU of every chunk) + a
  * scratch of 152 * 638976 bytes (one area per CTA of the gradient kernel); for the
- * other sizes kda_recurrent_bwd_workspace_size.  status: optional device word, KDA_ERR_TIMEOUT
- * if a bounded wait of the forward's kernels gave up (the gradients are then
- * unspecified).
+ * other sizes kda_recurrent_bwd_workspace_size.  status: optional device word,
+ * KDA_ERR_TIMEOUT if a bounded wait of the forward's kernels, of the backward chain
+ * or of the gradient kernel gave up (the kernels then drain their work in flight
+ * and return; the gradients are unspecified), KDA_ERR_RANGE as kda_recurrent_bwd
+ * on the other sizes.
  */
 KDA_API size_t kda_chunk_bwd_workspace_size(kda_dtype in_dtype, int B, int T, int H, int K, int V, int N,
                                             int packed);
