@@ -645,6 +645,9 @@ def profile_case(args):
             kda.gate_proj(gp["x"], gp["f_a"], gp["f_b"], gp["b_proj"])
     elif args.profile_case == "bwd":
         d = synth.device_inputs("prefill", dev)
+        if args.profile_bwd_H < d["q"].shape[2]:  # the first heads of the 4096-token workload
+            d = {k: (v[:, :, :args.profile_bwd_H].contiguous() if k in ("q", "k", "v", "g", "beta") else v)
+                 for k, v in d.items()}
         dO = torch.randn(d["q"].shape[:3] + (d["v"].shape[-1],), device=dev,
                          generator=torch.Generator(device=dev).manual_seed(11))
         for _ in range(args.profile_reps):
@@ -673,6 +676,8 @@ def main():
     ap.add_argument("--profile-T", type=int, default=2048)
     ap.add_argument("--profile-H", type=int, default=16)
     ap.add_argument("--profile-reps", type=int, default=2)
+    ap.add_argument("--profile-bwd-H", type=int, default=96,
+                    help="bwd case: heads of the 4096-token workload to run (default all 96)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
