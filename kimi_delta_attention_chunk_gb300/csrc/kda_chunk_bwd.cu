@@ -109,8 +109,10 @@ __device__ __forceinline__ uint32_t op_off(int row, int k, int Kd, bool mn) {
 // float4 passed through f(r + r_off, c + c_off, v) first (its coordinates in the
 // whole matrix).  KROW: the matrix rows are operand rows row0 + r and its columns
 // are k (K-major image); else its rows are k and its columns operand rows row0 + c
-// (MN-major image).  kStageInFlight float4 loads in flight per thread.
-template <int R, int CO, bool KROW, typename F = Ident>
+// (MN-major image).  kStageInFlight float4 loads in flight per thread.  ONCE: the
+// source's last read in the task, loaded with the streaming hint (first out of L2),
+// so that the per-CTA scratch, read again round after round, keeps its place.
+template <int R, int CO, bool KROW, bool ONCE = false, typename F = Ident>
 __device__ __forceinline__ void stage_op(const float* src, int ld, uint8_t* hi, uint8_t* lo, int Kd, int row0,
                                          int r_off = 0, int c_off = 0, F f = F()) {
     static_assert(R % 8 == 0 && CO % 4 == 0, "operand tile");
@@ -124,7 +126,8 @@ __device__ __forceinline__ void stage_op(const float* src, int ld, uint8_t* hi, 
             if (i < NV) {
                 int r, c;
                 unit_rc<R, CO>(i, r, c);
-                v[u] = *reinterpret_cast<const float4*>(src + (int64_t)r * ld + c);
+                const float4* a = reinterpret_cast<const float4*>(src + (int64_t)r * ld + c);
+                v[u] = ONCE ? __ldcs(a) : *a;
             }
         }
 #pragma unroll
@@ -263,6 +266,11 @@ template <typename TIn>
 __device__ __forceinline__ float ld_in(const TIn* p) { return to_f32<TIn>(*p); }
 __device__ __forceinline__ void ld4(const float* p, float* x) {
     const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+// (a source's last read in the task: streaming hint)
+__device__ __forceinline__ void ld4_once(const float* p, float* x) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(p));
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
 }
 
@@ -651,9 +659,9 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             const int64_t ti = ((c0 + r) * H + h) * D + c;
             kr[it] = qr[it] = vr[it] = make_uint4(0u, 0u, 0u, 0u);
             if (r < L) {
-                kr[it] = *reinterpret_cast<const uint4*>(k + ti);
-                qr[it] = *reinterpret_cast<const uint4*>(q + ti);
-                vr[it] = *reinterpret_cast<const uint4*>(v + ti);
+                kr[it] = __ldcs(reinterpret_cast<const uint4*>(k + ti));
+                qr[it] = __ldcs(reinterpret_cast<const uint4*>(q + ti));
+                vr[it] = __ldcs(reinterpret_cast<const uint4*>(v + ti));
             }
         }
 #pragma unroll
@@ -681,7 +689,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
                 const int u = tid + it * kChunkThreads;
                 const int r = u >> 5, c = 4 * (u & 31);
                 xo[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r < L) xo[it] = *reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c);
+                if (r < L) xo[it] = __ldcs(reinterpret_cast<const float4*>(dO + ((c0 + r) * H + h) * D + c));
                 xd[it] = *reinterpret_cast<const float4*>(DU + r * D + c);
             }
 #pragma unroll
@@ -716,8 +724,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
 #pragma unroll
             for (int it = 0; it < NI; ++it) {
                 const int u = tid + it * kChunkThreads;
-                wh[it] = *reinterpret_cast<const uint4*>(slot + SLOT_WQH + u * 16);
-                wl[it] = *reinterpret_cast<const uint4*>(slot + SLOT_WQL + u * 16);
+                wh[it] = __ldcs(reinterpret_cast<const uint4*>(slot + SLOT_WQH + u * 16));
+                wl[it] = __ldcs(reinterpret_cast<const uint4*>(slot + SLOT_WQL + u * 16));
             }
 #pragma unroll
             for (int it = 0; it < NI; ++it) {
@@ -765,7 +773,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             t, D, false,
             [&](uint8_t* hi, uint8_t* lo) {
                 stage_op<C, D, true>(DO_, D, hi, lo, D, 0);
-                stage_op<C, D, true>(DU, D, hi, lo, D, C);
+                stage_op<C, D, true, true>(DU, D, hi, lo, D, C);
             },
             [&](uint8_t* hi, uint8_t* lo, int) {
                 stage_op<D, D, true>(S, D, hi, lo, D, 0);
@@ -783,7 +791,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         // U dS'^T
         tc_round<D, 1, false, false>(
             t, D, false,
-            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, D, true>(U, D, hi, lo, D, 0); zero_rows(hi, lo, D, C); },
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, D, true, true>(U, D, hi, lo, D, 0); zero_rows(hi, lo, D, C); },
             [&](uint8_t* hi, uint8_t* lo, int) { stage_op<D, D, true>(DSP, D, hi, lo, D, 0); });
         if (t.failed) break;
         tc_epi<D, 1>(t, C, OneVariant{}, [&](int r, int c0, const float* x) { put16(DKB + r * D + c0, x, 1.f, false); });
@@ -793,8 +801,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             float4 a4[8], b4[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                a4[i] = *reinterpret_cast<const float4*>(DSP + c * D + part * 32 + 4 * i);
-                b4[i] = *reinterpret_cast<const float4*>(S + c * D + part * 32 + 4 * i);
+                a4[i] = __ldcs(reinterpret_cast<const float4*>(DSP + c * D + part * 32 + 4 * i));
+                b4[i] = __ldcs(reinterpret_cast<const float4*>(S + c * D + part * 32 + 4 * i));
             }
             float a = 0.f;
 #pragma unroll
@@ -812,7 +820,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
         // products):  dM = -[dBk | dBv] [W | U~]^T = dBk (-W)^T + dBv (-U~)^T
         tc_round<2 * D, 1, true, true>(
             t, C, false,
-            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
+            [&](uint8_t* hi, uint8_t* lo) { stage_op<C, C, false, true>(Tm, C, hi, lo, C, 0); zero_rows(hi, lo, C, C); },
             [&](uint8_t* hi, uint8_t* lo, int) { stage_op<C, 2 * D, false>(DWU, 2 * D, hi, lo, C, 0); });
         if (t.failed) break;
         tc_epi<2 * D, 1>(t, C, OneVariant{},
@@ -826,7 +834,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
                 },
                 [&](uint8_t* hi, uint8_t* lo, int) {
                     if (hk == 0) stage_op<C, D, true>(WN, D, hi, lo, D, 0);
-                    else stage_op<C, D, true>(reinterpret_cast<const float*>(slot + SLOT_UT), D, hi, lo, D, 0, 0, 0,
+                    else stage_op<C, D, true, true>(reinterpret_cast<const float*>(slot + SLOT_UT), D, hi, lo, D, 0, 0, 0,
                                               Neg{});
                 });
         if (t.failed) break;
@@ -843,7 +851,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 ld4(DM + r * C + 8 * part + 4 * i, m4 + 4 * i);
-                ld4(Am + r * C + 8 * part + 4 * i, a4 + 4 * i);
+                ld4_once(Am + r * C + 8 * part + 4 * i, a4 + 4 * i);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -862,7 +870,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             a += __shfl_xor_sync(0xffffffffu, a, 1);
             a += __shfl_xor_sync(0xffffffffu, a, 2);
             a += __shfl_xor_sync(0xffffffffu, a, 4);
-            if (part == 0 && r < L) dbeta[(c0 + r) * H + h] = a;
+            if (part == 0 && r < L) __stcs(dbeta + (c0 + r) * H + h, a);
         }
 #pragma unroll
         for (int it = 0; it < MR / 4 / kChunkThreads; ++it) {
@@ -871,8 +879,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             if (r < L) {
                 const float4 x = *reinterpret_cast<const float4*>(DBKV + r * 2 * D + D + c);
                 const float br = bs[r];
-                *reinterpret_cast<float4*>(dv + ((c0 + r) * H + h) * D + c) =
-                    make_float4(br * x.x, br * x.y, br * x.z, br * x.w);
+                __stcs(reinterpret_cast<float4*>(dv + ((c0 + r) * H + h) * D + c),
+                       make_float4(br * x.x, br * x.y, br * x.z, br * x.w));
             }
         }
         // the gated back-products: GB = (dA k e^{G_m - G_j}) per row block, GF the same with
@@ -931,8 +939,8 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             *reinterpret_cast<float4*>(gsm + MR + e) = make_float4(dKbKb[0], dKbKb[1], dKbKb[2], dKbKb[3]);
             if (r < L) {
                 const int64_t o = ((c0 + r) * H + h) * D + c;
-                *reinterpret_cast<float4*>(dq + o) = make_float4(dqv[0], dqv[1], dqv[2], dqv[3]);
-                *reinterpret_cast<float4*>(dk + o) = make_float4(dkv[0], dkv[1], dkv[2], dkv[3]);
+                __stcs(reinterpret_cast<float4*>(dq + o), make_float4(dqv[0], dqv[1], dqv[2], dqv[3]));
+                __stcs(reinterpret_cast<float4*>(dk + o), make_float4(dkv[0], dkv[1], dkv[2], dkv[3]));
             }
         }
         __syncthreads();
@@ -945,7 +953,7 @@ bwd_chunk_kernel(const Plan pl, const __nv_bfloat16* __restrict__ q, const __nv_
             float acc = dec[c] * ec[c] + colsum;
             for (int r = C - 1; r >= 0; --r) {
                 acc += gsm[r * D + c];
-                if (r < L) dg[((c0 + r) * H + h) * D + c] = acc;
+                if (r < L) __stcs(dg + ((c0 + r) * H + h) * D + c, acc);
             }
         }
     }
